@@ -1,0 +1,223 @@
+"""fp64 CPU oracle for D = alpha*A*B + beta*C -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of
+``bench.py`` may import this package.  The GPU library never loads it and
+shares no code with it: the arithmetic lives in ``mp_oracle.c`` (plain C,
+fp64, no fused multiply-add), and this module only marshals numpy arrays.
+
+Operands: A and B are bf16 bit patterns (numpy ``uint16``), row-major with
+leading dimensions; C is ``float32`` (ignored when beta == 0).  Every result is
+``float64``.
+
+What each routine follows (page titles and sections):
+  * ``gemm_naive``  -- MikPoly summary, section 1.2: the plain i-j-k nest,
+    then the BOLT summary's epilogue ``alpha*A*W + beta*C``.
+  * ``gemm_tiled``  -- MikPoly summary, section 1.2: the TILE_SIZE 32 nest
+    (zeroed output, edges clamped).
+  * ``gemm_rows``   -- the same definition in i-k-j order over OpenMP rows.
+  * ``gemm_entries`` / ``magnitude`` / ``freivalds`` -- the same definition
+    evaluated at chosen entries, its element-wise magnitude, and a
+    matrix-vector probe for outputs too large to recompute.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mp_oracle.c")
+_LIB = os.path.join(_HERE, "libmp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile mp_oracle.c into libmp_oracle.so with gcc (OpenMP, fp-contract off)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            gemm_args = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _dbl, _dbl, _vp, _i64]
+            for name in ("oracle_gemm_naive", "oracle_gemm_tiled"):
+                f = getattr(lib, name)
+                f.argtypes = gemm_args
+                f.restype = None
+            lib.oracle_gemm_rows.argtypes = gemm_args + [ctypes.c_int]
+            lib.oracle_gemm_rows.restype = ctypes.c_int
+            lib.oracle_gemm_entries.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                                _dbl, _dbl, _i64, _vp, _vp, _vp, _vp]
+            lib.oracle_gemm_entries.restype = None
+            lib.oracle_gemm_magnitude.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp,
+                                                  _i64, _dbl, _vp, _i64]
+            lib.oracle_gemm_magnitude.restype = None
+            lib.oracle_freivalds.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                             _dbl, _dbl, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
+            lib.oracle_freivalds.restype = None
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data
+
+
+def _operands(A, B, C, beta):
+    A = np.ascontiguousarray(A, dtype=np.uint16) if A.dtype != np.uint16 else A
+    B = np.ascontiguousarray(B, dtype=np.uint16) if B.dtype != np.uint16 else B
+    if beta != 0.0:
+        if C is None:
+            raise ValueError("beta != 0 needs C")
+        if C.dtype != np.float32:
+            raise TypeError("C must be float32")
+    else:
+        C = None
+    for X in (A, B) + ((C,) if C is not None else ()):
+        if X.ndim != 2 or (X.size and X.shape[1] > 1 and X.strides[1] != X.itemsize):
+            raise ValueError("operands must be 2-D with unit column stride")
+    return A, B, C
+
+
+def _ld(X):
+    if X is None:
+        return 0
+    if X.size == 0 or X.shape[0] == 1:
+        return max(1, X.shape[1])
+    return X.strides[0] // X.itemsize
+
+
+def _shape(A, B):
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner sizes differ: A is {A.shape}, B is {B.shape}")
+    return M, N, K
+
+
+def _gemm(name, A, B, C, alpha, beta, threads=None):
+    lib = _load()
+    A, B, C = _operands(A, B, C, beta)
+    M, N, K = _shape(A, B)
+    D = np.empty((M, N), dtype=np.float64)
+    args = [M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+            float(alpha), float(beta), _ptr(D), N]
+    if threads is None:
+        getattr(lib, name)(*args)
+        return D
+    used = lib.oracle_gemm_rows(*args, int(threads))
+    return D, used
+
+
+def gemm_naive(A, B, C=None, alpha=1.0, beta=0.0) -> np.ndarray:
+    """Plain i-j-k nest (MikPoly summary, section 1.2) with the alpha/beta epilogue."""
+    return _gemm("oracle_gemm_naive", A, B, C, alpha, beta)
+
+
+def gemm_tiled(A, B, C=None, alpha=1.0, beta=0.0) -> np.ndarray:
+    """Loop-tiled nest, TILE_SIZE 32 (MikPoly summary, section 1.2), edges clamped."""
+    return _gemm("oracle_gemm_tiled", A, B, C, alpha, beta)
+
+
+def gemm_rows(A, B, C=None, alpha=1.0, beta=0.0, threads: int = 0):
+    """Same definition, i-k-j order, OpenMP over rows.  Returns (D, threads_used)."""
+    return _gemm("oracle_gemm_rows", A, B, C, alpha, beta, threads=threads)
+
+
+def gemm(A, B, C=None, alpha=1.0, beta=0.0) -> np.ndarray:
+    """The oracle's default full evaluation (row-parallel)."""
+    return gemm_rows(A, B, C, alpha, beta)[0]
+
+
+def gemm_entries(A, B, C, alpha, beta, rows, cols):
+    """Entries (rows[t], cols[t]) of the definition and their magnitudes."""
+    lib = _load()
+    A, B, C = _operands(A, B, C, beta)
+    M, N, K = _shape(A, B)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    if rows.size and (rows.min() < 0 or rows.max() >= M or cols.min() < 0 or cols.max() >= N):
+        raise IndexError("entry outside the output")
+    out = np.empty(rows.size, dtype=np.float64)
+    mag = np.empty(rows.size, dtype=np.float64)
+    lib.oracle_gemm_entries(M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+                            float(alpha), float(beta), rows.size, _ptr(rows), _ptr(cols),
+                            _ptr(out), _ptr(mag))
+    return out, mag
+
+
+def magnitude(A, B, C=None, beta=0.0) -> np.ndarray:
+    """sum_k |A_ik||B_kj| + |beta*C_ij| for every entry (the tolerance scale)."""
+    lib = _load()
+    A, B, C = _operands(A, B, C, beta)
+    M, N, K = _shape(A, B)
+    G = np.empty((M, N), dtype=np.float64)
+    lib.oracle_gemm_magnitude(M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+                              float(beta), _ptr(G), N)
+    return G
+
+
+def freivalds(A, B, C, alpha, beta, D, x):
+    """Residual y = D x - (alpha A (B x) + beta C x) and its row magnitudes."""
+    lib = _load()
+    A, B, C = _operands(A, B, C, beta)
+    M, N, K = _shape(A, B)
+    D = np.ascontiguousarray(D, dtype=np.float32)
+    if D.shape != (M, N):
+        raise ValueError("D has the wrong shape")
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    bx = np.empty(K, dtype=np.float64)
+    abx = np.empty(K, dtype=np.float64)
+    y = np.empty(M, dtype=np.float64)
+    ymag = np.empty(M, dtype=np.float64)
+    lib.oracle_freivalds(M, N, K, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C),
+                         float(alpha), float(beta), _ptr(D), N, _ptr(x), _ptr(bx), _ptr(abx),
+                         _ptr(y), _ptr(ymag))
+    return y, ymag
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (high half of an fp32 word) to fp64."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# The parity bound stated for bf16 inputs with fp32 accumulation and fp32 output:
+#   |D - D_ref| <= 2e-3 * (sum_k |A_ik||B_kj| + |beta*C_ij|)
+PARITY_RTOL = 2e-3
+
+
+def within_bound(D, Dref, mag, rtol: float = PARITY_RTOL):
+    """Element-wise check of the parity bound; returns (ok, worst ratio)."""
+    D = np.asarray(D, dtype=np.float64)
+    err = np.abs(D - Dref)
+    lim = rtol * mag
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(lim > 0, err / np.where(lim > 0, lim, 1.0), np.where(err > 0, np.inf, 0.0))
+    ok = bool(np.all(np.isfinite(D)) and np.all(err <= lim))
+    return ok, float(ratio.max()) if ratio.size else 0.0

@@ -1,0 +1,335 @@
+"""Pins for the fp64 oracle, checked against what the pages and mathematics fix.
+
+Each pin is written as a function of a GEMM callable so that the same checks
+can be run against deliberately broken copies of the oracle (planted mistakes:
+a dropped term, a wrong sign, a wrong index, a transposed operand, an
+off-by-one loop) and shown to reject every one of them.
+"""
+import fractions
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from micro_polymerization_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32_to_bf16_bits(x):
+    """Round fp32 values to bf16 (nearest even) and return the bit patterns."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u >> 16) & 1) + 0x7FFF
+    return ((u + r) >> 16).astype(np.uint16)
+
+
+def rand_bits(rng, shape):
+    return f32_to_bf16_bits(rng.uniform(-1, 1, size=shape).astype(np.float32))
+
+
+def int_bits(rng, shape, lo=-4, hi=4):
+    return f32_to_bf16_bits(rng.integers(lo, hi + 1, size=shape).astype(np.float32))
+
+
+def exact_gemm(A, B, C, alpha, beta):
+    """Exact rational D via fractions (independent of any float arithmetic)."""
+    Af = [[fractions.Fraction(float(v)) for v in row] for row in oracle.bf16_bits_to_f64(A)]
+    Bf = [[fractions.Fraction(float(v)) for v in row] for row in oracle.bf16_bits_to_f64(B)]
+    M, K = A.shape
+    N = B.shape[1]
+    a, b = fractions.Fraction(alpha), fractions.Fraction(beta)
+    D = [[None] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = sum((Af[i][k] * Bf[k][j] for k in range(K)), fractions.Fraction(0))
+            c = fractions.Fraction(float(C[i, j])) if beta != 0 else 0
+            D[i][j] = a * s + b * c
+    return D
+
+
+# ----------------------------------------------------------------------------
+# Pins (each takes a callable gemm(A_bits, B_bits, C, alpha, beta) -> fp64 D)
+# ----------------------------------------------------------------------------
+
+def pin_widening():
+    table = {0x3F80: 1.0, 0xC000: -2.0, 0x0000: 0.0, 0x8000: -0.0, 0x3F00: 0.5,
+             0x0001: 2.0 ** -133, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127, 0x4049: 3.140625}
+    got = oracle.bf16_bits_to_f64(np.array(list(table), dtype=np.uint16))
+    return np.array_equal(got, np.array(list(table.values())))
+
+
+def pin_closed_form_ones(gemm):
+    """A = 1, B = 1:  D = alpha*K + beta*C  exactly (ragged and odd sizes)."""
+    rng = np.random.default_rng(5)
+    for (M, N, K) in [(3, 5, 7), (33, 17, 65), (1, 1, 1), (2, 70, 129)]:
+        A = np.full((M, K), 0x3F80, dtype=np.uint16)
+        B = np.full((K, N), 0x3F80, dtype=np.uint16)
+        C = rng.integers(-8, 9, size=(M, N)).astype(np.float32)
+        for alpha, beta in [(1.0, 0.0), (1.5, 0.5), (-2.0, 1.0), (0.25, -3.0)]:
+            D = gemm(A, B, C, alpha, beta)
+            want = alpha * K + beta * C.astype(np.float64)
+            if not np.array_equal(D, want):
+                return False
+    return True
+
+
+def pin_identity_permutation(gemm):
+    """B = I gives alpha*A + beta*C; B = P (a permutation) permutes A's columns."""
+    rng = np.random.default_rng(6)
+    M, K = 9, 13
+    A = rand_bits(rng, (M, K))
+    Af = oracle.bf16_bits_to_f64(A)
+    C = rng.uniform(-1, 1, size=(M, K)).astype(np.float32)
+    eye = np.where(np.eye(K, dtype=bool), 0x3F80, 0).astype(np.uint16)
+    D = gemm(A, eye, C, 1.0, 0.5)
+    if not np.array_equal(D, Af + 0.5 * C.astype(np.float64)):
+        return False
+    perm = rng.permutation(K)
+    P = np.zeros((K, K), dtype=np.uint16)
+    P[perm, np.arange(K)] = 0x3F80  # column j of P selects row perm[j] of ... A[:, perm[j]]
+    D = gemm(A, P, C, 1.0, 0.0)
+    return np.array_equal(D, Af[:, perm])
+
+
+def pin_bruteforce_exact(gemm):
+    """Tiny non-square shapes vs the exact rational result, within fp64 rounding."""
+    rng = np.random.default_rng(7)
+    for (M, N, K) in [(1, 1, 1), (2, 3, 4), (4, 3, 2), (5, 1, 3), (3, 4, 5), (6, 2, 7)]:
+        A = rand_bits(rng, (M, K))
+        B = rand_bits(rng, (K, N))
+        C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
+        for alpha, beta in [(1.0, 0.0), (1.5, 0.5), (-0.75, 2.0)]:
+            D = gemm(A, B, C, alpha, beta)
+            E = exact_gemm(A, B, C, alpha, beta)
+            mag = (abs(alpha) * (np.abs(oracle.bf16_bits_to_f64(A)) @ np.abs(oracle.bf16_bits_to_f64(B)))
+                   + abs(beta) * np.abs(C.astype(np.float64)))
+            for i in range(M):
+                for j in range(N):
+                    err = abs(fractions.Fraction(float(D[i, j])) - E[i][j])
+                    if err > fractions.Fraction((K + 4) * 2.0 ** -52 * mag[i, j]):
+                        return False
+    return True
+
+
+def pin_integer_exact(gemm):
+    """Integer-valued operands: every partial sum is exact, so D is exact."""
+    rng = np.random.default_rng(8)
+    for (M, N, K) in [(64, 96, 32), (37, 45, 70), (1, 33, 65)]:
+        A = int_bits(rng, (M, K))
+        B = int_bits(rng, (K, N))
+        C = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+        want = (oracle.bf16_bits_to_f64(A).astype(np.int64) @ oracle.bf16_bits_to_f64(B).astype(np.int64)
+                ).astype(np.float64) * 2.0 + 3.0 * C
+        if not np.array_equal(gemm(A, B, C, 2.0, 3.0), want):
+            return False
+    return True
+
+
+def pin_fp64_cancellation(gemm):
+    """1 + 2^-30 - 1 = 2^-30 holds in fp64 (the oracle's precision) but not in
+    fp32: the accumulation must be carried in fp64."""
+    A = np.array([[0x3F80, 0x3080, 0xBF80]], dtype=np.uint16)  # 1, 2^-30, -1
+    B = np.full((3, 2), 0x3F80, dtype=np.uint16)
+    D = gemm(A, B, None, 1.0, 0.0)
+    return np.array_equal(D, np.full((1, 2), 2.0 ** -30))
+
+
+ORACLE_FORMS = {
+    "naive": lambda A, B, C, a, b: oracle.gemm_naive(A, B, C, a, b),
+    "tiled": lambda A, B, C, a, b: oracle.gemm_tiled(A, B, C, a, b),
+    "rows": lambda A, B, C, a, b: oracle.gemm(A, B, C, a, b),
+}
+
+
+def _entries_form(A, B, C, a, b):
+    M, N = A.shape[0], B.shape[1]
+    r, c = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    out, _ = oracle.gemm_entries(A, B, C, a, b, r.ravel(), c.ravel())
+    return out.reshape(M, N)
+
+
+ORACLE_FORMS["entries"] = _entries_form
+PINS = [pin_closed_form_ones, pin_identity_permutation, pin_bruteforce_exact, pin_integer_exact,
+        pin_fp64_cancellation]
+
+
+def test_bf16_widening():
+    assert pin_widening()
+
+
+@pytest.mark.parametrize("form", sorted(ORACLE_FORMS))
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_pins(form, pin):
+    assert pin(ORACLE_FORMS[form])
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 64, 64), (96, 32, 128), (37, 45, 70), (33, 1, 31), (1, 65, 97)])
+def test_naive_equals_tiled_bitwise(M, N, K):
+    """The two printed nests (MikPoly summary, section 1.2) agree exactly on
+    integer data, for tile-multiple and ragged sizes."""
+    rng = np.random.default_rng(M * 1000 + N * 10 + K)
+    A, B = int_bits(rng, (M, K)), int_bits(rng, (K, N))
+    C = rng.integers(-4, 5, size=(M, N)).astype(np.float32)
+    Dn = oracle.gemm_naive(A, B, C, 1.0, 1.0)
+    Dt = oracle.gemm_tiled(A, B, C, 1.0, 1.0)
+    Dr = oracle.gemm(A, B, C, 1.0, 1.0)
+    assert np.array_equal(Dn, Dt) and np.array_equal(Dn, Dr)
+
+
+def test_forms_agree_on_random_data():
+    """Same k order in every form: naive, rows and entries are bitwise equal;
+    the tiled nest sums the same terms in the same order as well."""
+    rng = np.random.default_rng(11)
+    A, B = rand_bits(rng, (21, 40)), rand_bits(rng, (40, 19))
+    C = rng.uniform(-1, 1, size=(21, 19)).astype(np.float32)
+    ref = oracle.gemm_naive(A, B, C, 1.5, 0.5)
+    for name, f in ORACLE_FORMS.items():
+        assert np.array_equal(f(A, B, C, 1.5, 0.5), ref), name
+
+
+def test_beta_zero_never_reads_c():
+    rng = np.random.default_rng(12)
+    A, B = rand_bits(rng, (4, 5)), rand_bits(rng, (5, 6))
+    C = np.full((4, 6), np.nan, dtype=np.float32)
+    for f in ORACLE_FORMS.values():
+        assert np.all(np.isfinite(f(A, B, C, 1.0, 0.0)))
+
+
+def test_k_zero_gives_beta_c():
+    rng = np.random.default_rng(13)
+    A = np.zeros((3, 0), dtype=np.uint16)
+    B = np.zeros((0, 4), dtype=np.uint16)
+    C = rng.uniform(-1, 1, size=(3, 4)).astype(np.float32)
+    for f in ORACLE_FORMS.values():
+        assert np.array_equal(f(A, B, C, 2.0, 0.5), 0.5 * C.astype(np.float64))
+
+
+def test_leading_dimensions():
+    """Padded leading dimensions address the same logical matrices."""
+    rng = np.random.default_rng(14)
+    A, B = rand_bits(rng, (7, 9)), rand_bits(rng, (9, 5))
+    C = rng.uniform(-1, 1, size=(7, 5)).astype(np.float32)
+    Ap = np.zeros((7, 16), np.uint16); Ap[:, :9] = A
+    Bp = np.zeros((9, 11), np.uint16); Bp[:, :5] = B
+    Cp = np.zeros((7, 8), np.float32); Cp[:, :5] = C
+    ref = oracle.gemm_naive(A, B, C, 1.0, 1.0)
+    for f in ORACLE_FORMS.values():
+        assert np.array_equal(f(Ap[:, :9], Bp[:, :5], Cp[:, :5], 1.0, 1.0), ref)
+
+
+def test_magnitude_closed_form():
+    A = np.full((3, 10), 0xBF80, dtype=np.uint16)  # -1
+    B = np.full((10, 4), 0x4000, dtype=np.uint16)  # 2
+    C = np.full((3, 4), -3.0, dtype=np.float32)
+    G = oracle.magnitude(A, B, C, beta=0.5)
+    assert np.array_equal(G, np.full((3, 4), 20.0 + 1.5))
+
+
+def test_freivalds_separates_right_from_wrong():
+    rng = np.random.default_rng(15)
+    M, N, K = 40, 30, 50
+    A, B = rand_bits(rng, (M, K)), rand_bits(rng, (K, N))
+    C = rng.uniform(-1, 1, size=(M, N)).astype(np.float32)
+    D = oracle.gemm(A, B, C, 1.5, 0.5).astype(np.float32)
+    x = rng.choice([-1.0, 1.0], size=N)
+    y, ymag = oracle.freivalds(A, B, C, 1.5, 0.5, D, x)
+    assert np.all(np.abs(y) <= 1e-5 * ymag + 1e-12)
+    D2 = D.copy()
+    D2[17, 3] += 0.05
+    y, ymag = oracle.freivalds(A, B, C, 1.5, 0.5, D2, x)
+    assert np.abs(y[17]) > 1e-5 * ymag[17] and np.all(np.abs(np.delete(y, 17)) <= 1e-5 * np.delete(ymag, 17))
+
+
+def test_within_bound_semantics():
+    ok, r = oracle.within_bound(np.array([1.0, 2.0]), np.array([1.0, 2.001]), np.array([1.0, 1.0]))
+    assert ok and 0.4 < r < 0.6
+    ok, _ = oracle.within_bound(np.array([1.0]), np.array([1.003]), np.array([1.0]))
+    assert not ok
+    ok, _ = oracle.within_bound(np.array([np.nan]), np.array([0.0]), np.array([1.0]))
+    assert not ok
+    ok, _ = oracle.within_bound(np.array([0.0]), np.array([1e-30]), np.array([0.0]))
+    assert not ok
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: broken copies of the definition (numpy, fp64) must each
+# fail at least one pin.  The mistakes live here, on the CPU, never in the
+# oracle's sources.
+# ----------------------------------------------------------------------------
+
+def _f(bits):
+    return oracle.bf16_bits_to_f64(bits)
+
+
+def _c(C, beta, shape):
+    return beta * C.astype(np.float64) if beta != 0 else np.zeros(shape)
+
+
+MUTANTS = {
+    "dropped_beta_term": lambda A, B, C, a, b: a * (_f(A) @ _f(B)),
+    "wrong_beta_sign": lambda A, B, C, a, b: a * (_f(A) @ _f(B)) - _c(C, b, (A.shape[0], B.shape[1])),
+    "alpha_on_c": lambda A, B, C, a, b: a * (_f(A) @ _f(B) + _c(C, b, (A.shape[0], B.shape[1]))),
+    "k_off_by_one": lambda A, B, C, a, b: a * (_f(A)[:, :-1] @ _f(B)[:-1, :]) + _c(C, b, (A.shape[0], B.shape[1])),
+    "b_transposed": lambda A, B, C, a, b: (a * (_f(A) @ _f(B).T.reshape(B.shape))
+                                            + _c(C, b, (A.shape[0], B.shape[1]))),
+    "a_rows_reversed": lambda A, B, C, a, b: a * (_f(A)[::-1] @ _f(B)) + _c(C, b, (A.shape[0], B.shape[1])),
+    "products_in_fp32": lambda A, B, C, a, b: (a * (_f(A).astype(np.float32) @ _f(B).astype(np.float32))
+                                                .astype(np.float64) + _c(C, b, (A.shape[0], B.shape[1]))),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_mistakes(name):
+    mutant = MUTANTS[name]
+
+    def safe(pin):
+        try:
+            return pin(mutant)
+        except Exception:
+            return False
+
+    assert not all(safe(p) for p in PINS), f"no pin caught {name}"
+
+
+def test_correct_numpy_restatement_passes_pins():
+    """Control for the planted-mistake test: an independent fp64 numpy
+    statement of the definition passes the same pins."""
+    good = lambda A, B, C, a, b: a * (_f(A) @ _f(B)) + _c(C, b, (A.shape[0], B.shape[1]))
+    assert pin_closed_form_ones(good) and pin_identity_permutation(good) and pin_integer_exact(good)
+
+
+# ----------------------------------------------------------------------------
+# Workload recipe sanity (shared generator module; no arithmetic of the method)
+# ----------------------------------------------------------------------------
+
+def test_workload_shapes_follow_their_recipes():
+    seq = wl.dynamic_sequence()
+    assert len(seq) == 64 and all(g.M % 8 == 0 and 8 <= g.M <= 4096 for g in seq)
+    assert [(g.N, g.K) for g in seq[:4]] == wl.SEQ_NK
+    conv = wl.dynamic_resolution()
+    assert all(g.N in (64, 128, 256, 512) and g.K == 9 * g.N for g in conv)
+    qkv = wl.merged_qkv()
+    assert all(g.N == 3072 and g.K == 1024 and 1 <= g.M <= 4096 for g in qkv)
+    bat = wl.merged_batched()
+    assert all(g.batch == 12 and g.K == 64 and g.M == g.N and 16 <= g.M <= 512 for g in bat)
+    st = wl.stress()
+    assert len(st) == 1001 and st[-1].M == st[-1].N == st[-1].K == 4096
+    assert all(1 <= d <= 16384 for g in st for d in (g.M, g.N, g.K))
+    assert wl.single_skinny()[0].M == 105
+
+
+def test_generator_is_seeded_and_in_range():
+    g = wl.Gemm(17, 9, 33, alpha=1.5, beta=0.5, seed=42)
+    A1, B1, C1 = wl.make_operands(g)
+    A2, B2, C2 = wl.make_operands(g)
+    assert np.array_equal(wl.bf16_bits(A1), wl.bf16_bits(A2))
+    assert np.array_equal(C1.numpy(), C2.numpy())
+    for T in (A1.float(), B1.float(), C1):
+        assert float(T.min()) >= -1.0 and float(T.max()) <= 1.0
+    # torch's bf16 rounding agrees with round-to-nearest-even of the fp32 draw
+    x = np.random.default_rng(0).uniform(-1, 1, 1000).astype(np.float32)
+    import torch
+    assert np.array_equal(wl.bf16_bits(torch.from_numpy(x).to(torch.bfloat16)), f32_to_bf16_bits(x))
