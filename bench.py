@@ -1,0 +1,488 @@
+"""Benchmark: dynamic-shape GEMM throughput (TFLOPS, device-timed, planning
+included) and the fraction of each shape's roofline.
+
+One step = the whole hot path over one batch of synthetic input: 64 GEMMs of
+the dynamic-sequence-length workload (M = 8 * seq, seq uniform on [1, 512];
+(N, K) cycling over a Transformer layer's four projections; beta = 0), each
+planned and launched through the C ABI (mp_gemm) back to back on one stream.
+Every GEMM has its own operand buffers, 1.4 GB in all -- larger than the
+129 MB L2 -- so no operand is still cached when it is read again.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mp|reference]
+                    [--workload NAME] [--sweep]
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.  ``--sweep`` also writes one
+summary line per workload to stderr.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "dynamic-shape GEMM TFLOPS (device-timed, incl. planning) and % of per-shape roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of the persistent kernel from one ncu capture (bytes per
+# algorithmic byte, i.e. dram read+write / (2MK+2KN+4MN)), valid only for the
+# kernel source it was taken on; see profiles/.
+TRAFFIC_RECORD = {"kernel_sha1": None, "dram_bytes_per_alg_byte": None}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_sha1():
+    p = os.path.join(ROOT, "micro_polymerization_gb300", "csrc", "mp_gemm.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def roofline_us(g, peaks):
+    t_flop = g.flops / (peaks["bf16_tflops"] * 1e6)
+    t_mem = g.min_bytes() / (peaks["hbm_gbs"] * 1e3)
+    return max(t_flop, t_mem), ("tensor" if t_flop >= t_mem else "hbm")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mp_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_workload(name: str, rank: int):
+    """Each rank runs its own copy of the workload (weak scaling): same shapes,
+    operands seeded per rank."""
+    from micro_polymerization_gb300 import workloads as wl
+    gs = wl.workload(name)
+    if rank == 0:
+        return gs
+    import dataclasses
+    return [dataclasses.replace(g, seed=g.seed + 1_000_003 * rank) for g in gs]
+
+
+def needs_repack(ptr: int, ld: int) -> bool:
+    return ptr % 16 != 0 or (ld * 2) % 16 != 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_mp(args):
+    import torch
+    import micro_polymerization_gb300 as mp
+    from micro_polymerization_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    h = mp.mp_init(local)
+    lib = mp.library()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    gs = rank_workload(args.workload, rank)
+    ops = []
+    launches_per_step = 0
+    for g in gs:
+        A, B, C = wl.make_operands(g, device=dev)
+        D = torch.empty((g.batch, g.M, g.N) if g.batch > 1 else (g.M, g.N), device=dev)
+        ops.append((g, A, B, C, D))
+        launches_per_step += 1 + int(needs_repack(A.data_ptr(), g.K)) + int(needs_repack(B.data_ptr(), g.N))
+    torch.cuda.synchronize()
+
+    # Pre-marshalled C-ABI argument tuples (the call itself plans and launches).
+    calls = []
+    for g, A, B, C, D in ops:
+        cp = C.data_ptr() if C is not None else None
+        if g.batch > 1:
+            calls.append((lib.mp_gemm_batched, (h.ptr, g.batch, g.M, g.N, g.K, A.data_ptr(), g.K, g.M * g.K,
+                                                B.data_ptr(), g.N, g.K * g.N, cp, g.N, g.M * g.N,
+                                                D.data_ptr(), g.N, g.M * g.N, g.alpha, g.beta, sp)))
+        else:
+            calls.append((lib.mp_gemm, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
+                                        cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, sp)))
+
+    def step(evs=None):
+        for i, (fn, a) in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            st = fn(*a)
+            if st != 0:
+                raise mp.MPError(st, "mp_gemm")
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    torch.cuda.synchronize()
+
+    # Per-launch device time of every GEMM (events around each call).
+    n = len(calls)
+    per_launch = np.zeros(n)
+    reps = max(1, min(args.steps, 20))
+    for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        step(evs)
+        torch.cuda.synchronize()
+        per_launch += np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+    per_launch /= reps
+
+    # The timed region: K whole steps, barrier + synchronize on both sides.
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = mp.mp_check(h)
+    if status != 0:
+        raise RuntimeError(f"device status word set in the timed region: {status}")
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    ms_per_step = elapsed_ms / args.steps
+    flops_step = sum(g.flops for g in gs)
+    value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # Per-shape roofline fractions (from the per-launch times).
+    troof = np.array([roofline_us(g, peaks)[0] for g in gs])
+    bounds = [roofline_us(g, peaks)[1] for g in gs]
+    flops = np.array([g.flops for g in gs], dtype=np.float64)
+    frac_shape = troof / per_launch
+    flop_weighted = float(np.sum(flops * frac_shape) / np.sum(flops))
+    time_ratio = float(troof.sum() / per_launch.sum())
+
+    # Dominant kernel: the persistent GEMM kernel (one launch per GEMM).  Its
+    # bound is the one that dominates the summed roofline time.
+    t_hbm = sum(t for t, b in zip(troof, bounds) if b == "hbm")
+    t_ten = sum(t for t, b in zip(troof, bounds) if b == "tensor")
+    if t_hbm >= t_ten:
+        sel = [i for i, b in enumerate(bounds) if b == "hbm"]
+        work = sum(gs[i].min_bytes() for i in sel)
+        achieved = work / (per_launch[sel].sum() * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit, bound = "GB/s", "hbm"
+    else:
+        sel = [i for i, b in enumerate(bounds) if b == "tensor"]
+        work = sum(gs[i].flops for i in sel)
+        achieved = work / (per_launch[sel].sum() * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit, bound = "TFLOP/s", "tensor"
+    traffic = None
+    if TRAFFIC_RECORD["kernel_sha1"] == kernel_sha1() and TRAFFIC_RECORD["dram_bytes_per_alg_byte"]:
+        alg = sum(gs[i].min_bytes() for i in sel) / max(1, len(sel))
+        traffic = TRAFFIC_RECORD["dram_bytes_per_alg_byte"] * alg
+
+    # End to end: pinned host inputs copied in, outputs read back, every step.
+    e2e = None
+    if not args.no_e2e:
+        host_in = []
+        for g, A, B, C, D in ops:
+            hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True); hA.copy_(A)
+            hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True); hB.copy_(B)
+            hC = None
+            if C is not None:
+                hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True); hC.copy_(C)
+            hD = torch.empty(D.shape, dtype=D.dtype, pin_memory=True)
+            host_in.append((hA, hB, hC, hD))
+        h2d = sum(x.numel() * x.element_size() for t in host_in for x in t[:3] if x is not None)
+        d2h = sum(t[3].numel() * t[3].element_size() for t in host_in)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for (g, A, B, C, D), (hA, hB, hC, hD), (fn, a) in zip(ops, host_in, calls):
+                A.copy_(hA, non_blocking=True)
+                B.copy_(hB, non_blocking=True)
+                if C is not None:
+                    C.copy_(hC, non_blocking=True)
+                st = fn(*a)
+                if st != 0:
+                    raise mp.MPError(st, "mp_gemm")
+                hD.copy_(D, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": round(flops_step * world * e2e_steps / t_e2e / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    # Planner latency on the host (search, cache bypassed by fresh shapes).
+    plan_us = None
+    if rank == 0:
+        h2 = mp.mp_init_host(mp.mp_get_hw(h)[0])
+        shapes = [(g.M + 1, g.N, g.K) for g in gs]
+        t0 = time.perf_counter()
+        for s in shapes:
+            mp.mp_plan(h2, *s)
+        plan_us = (time.perf_counter() - t0) / len(shapes) * 1e6
+        h2.close()
+
+    cpu = cpu_baseline(args, gs) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if args.sweep and rank == 0:
+        sweep(args, h, peaks, dev)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(args.workload), "gemms_per_step": len(gs),
+                       "flops_per_step": int(flops_step), "l2": "inputs larger than L2 "
+                       f"({sum(g.min_bytes() for g in gs) / 1e9:.2f} GB of distinct operands per step)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
+                                   "sum_troof_over_sum_t": round(time_ratio, 4),
+                                   "peaks": peak_src},
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "launches": len(sel), "kernel": "k_poly_gemm", "peak_source": peak_src},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "plan_us": round(plan_us, 3) if plan_us is not None else None,
+            "clocks": clocks.summary(), "impl": "mp",
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def workload_desc(name):
+    return {
+        "dynamic_sequence": "dynamic sequence length: 64 GEMMs, M = 8*seq (seq uniform [1,512]), "
+                            "(N,K) cycling (2304,768),(768,768),(3072,768),(768,3072), bf16 A,B, beta=0",
+        "single_skinny": "single GEMM (105,1024,12544), alpha=1, beta=1",
+        "dynamic_resolution": "conv-as-GEMM, 64 draws of ResNet-50-like 3x3 layers",
+        "merged_qkv": "A x concat(Wq,Wk,Wv), K=1024, N=3072, M uniform [1,4096], 64 draws",
+        "merged_batched": "batched 12 x (seq,seq,64), seq uniform [16,512], 64 draws",
+        "stress": "1000 log-uniform shapes in [1,16384]^3 plus 4096^3, alpha=1.5, beta=0.5",
+    }[name]
+
+
+def sweep(args, h, peaks, dev):
+    """One summary line per workload on stderr (per-shape events, L2 flushed)."""
+    import torch
+    import micro_polymerization_gb300 as mp
+    from micro_polymerization_gb300 import workloads as wl
+    flush = torch.empty(int(512 * 2 ** 20), dtype=torch.uint8, device=dev)
+    for name in wl.WORKLOADS:
+        gs = wl.workload(name)
+        ts, trs, fl = [], [], []
+        for g in gs:
+            A, B, C = wl.make_operands(g, device=dev)
+            D = torch.empty((g.batch, g.M, g.N) if g.batch > 1 else (g.M, g.N), device=dev)
+            fn = (lambda: mp.mp_gemm_batched(h, A, B, C, D, g.alpha, g.beta)) if g.batch > 1 else \
+                 (lambda: mp.mp_gemm(h, A, B, C, D, g.alpha, g.beta))
+            for _ in range(3):
+                fn()
+            best = []
+            for _ in range(5):
+                flush.random_(0, 255)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                best.append(e0.elapsed_time(e1) * 1e3)
+            t = statistics.median(best)
+            ts.append(t); trs.append(roofline_us(g, peaks)[0]); fl.append(g.flops)
+            del A, B, C, D
+        ts, trs, fl = map(np.array, (ts, trs, fl))
+        frac = trs / ts
+        sys.stderr.write(json.dumps({
+            "workload": name, "gemms": len(gs), "tflops": round(fl.sum() / (ts.sum() * 1e-6) / 1e12, 2),
+            "flop_weighted_roofline_frac": round(float((fl * frac).sum() / fl.sum()), 4),
+            "sum_troof_over_sum_t": round(float(trs.sum() / ts.sum()), 4),
+            "median_frac": round(float(np.median(frac)), 4), "min_frac": round(float(frac.min()), 4),
+        }) + "\n")
+        sys.stderr.flush()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle, timed on a bounded sample of the same workload
+# ---------------------------------------------------------------------------
+def cpu_baseline(args, gs, budget_s=None):
+    import torch
+    import oracle
+    from micro_polymerization_gb300 import workloads as wl
+    budget_s = budget_s or args.cpu_seconds
+    flops = 0.0
+    used = 0
+    t_total = 0.0
+    done = 0
+    for g in gs:
+        A, B, C = wl.make_operands(g)
+        if g.batch > 1:
+            A, B = A[0], B[0]
+            C = C[0] if C is not None else None
+        rows = min(g.M, 256)
+        Ab = wl.bf16_bits(A[:rows])
+        Bb = wl.bf16_bits(B)
+        Cn = C[:rows].numpy() if C is not None else None
+        t0 = time.perf_counter()
+        _, used = oracle.gemm_rows(Ab, Bb, Cn, g.alpha, g.beta)
+        t_total += time.perf_counter() - t0
+        flops += 2.0 * rows * g.N * g.K
+        done += 1
+        if t_total >= budget_s:
+            break
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(used), "kind": "oracle",
+            "sample": f"first {min(256, 'M')} rows of each of the first {done} GEMMs of the workload "
+                      f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)".replace("'M'", "M")}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    gs = rank_workload(args.workload, 0)
+    import oracle  # noqa: F401
+    for _ in range(args.warmup):
+        cpu_baseline(args, gs[:1], budget_s=0.01)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    vals = []
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(args, gs, budget_s=per_step))
+    v = statistics.median(x["value"] for x in vals)
+    line = {
+        "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload)},
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "impl": "reference",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["mp", "reference"], default="mp")
+    ap.add_argument("--workload", default="dynamic_sequence")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "mp":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mp(args)
+
+
+if __name__ == "__main__":
+    main()

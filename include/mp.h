@@ -1,0 +1,249 @@
+/*
+ * mp.h -- dynamic-shape GEMM with epilogue for NVIDIA GB300 (sm_103a).
+ *
+ *     D = alpha * A * B + beta * C
+ *
+ * A [M x K] and B [K x N] are bf16, C and D [M x N] are fp32, products are
+ * accumulated in fp32.  All matrices are row-major with a leading dimension
+ * (elements between the starts of consecutive rows).  The shape (M, N, K) is
+ * known only at run time: every call plans its own "polymerization" -- the
+ * output is cut into up to four rectangular regions, each covered by one
+ * fixed-size micro-kernel with a split-K factor -- and runs the whole plan in
+ * one persistent kernel launch.
+ *
+ * Sources (page titles and sections):
+ *   [MP]    "Optimizing Dynamic-Shape Neural Networks on Accelerators via
+ *           On-the-Fly Micro-Kernel Polymerization" (MikPoly summary):
+ *           section 3 (multi-level accelerator abstraction H, micro-kernel
+ *           performance model g_predict, polymerization patterns, cost model
+ *           Cost(S,H) = sum_i f_wave * f_pipe, pruned heuristic search),
+ *           section 4 (GPU: Patterns I and II; offsets and loop counts passed
+ *           as run-time scalars), section 6 (case study (4096,1024,4096)).
+ *   [BOLT]  BOLT summary, "Persistent kernel (GEMM/Conv) fusion": the
+ *           epilogue form D = alpha*A*W + beta*C.
+ *   [DISC]  BladeDISC v0.2.0 release notes, "GEMM merge": shared-operand
+ *           merge A x concat(B, C) and same-shape batched GEMM.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns A, B, C, D and the stream; the library owns the handle
+ *     and everything it allocates at mp_init (split-K workspace, tile
+ *     counters, an operand staging area, the device status word).  mp_gemm and
+ *     mp_gemm_batched never allocate.
+ *   - Errors are returned as mp_status codes; nothing aborts, throws or falls
+ *     back to the CPU.
+ *   - A handle serves one host thread and one stream at a time: two calls that
+ *     overlap on the device share the split-K workspace and would race.
+ */
+#ifndef MP_H_
+#define MP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mp_handle_s* mp_handle;
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef void* mp_stream;
+
+typedef enum {
+    MP_OK = 0,
+    MP_ERR_INVALID_ARG = -1,     /* bad size, pointer, leading dimension or overlap */
+    MP_ERR_UNSUPPORTED = -2,     /* valid request this build cannot run (e.g. no sm_103 device) */
+    MP_ERR_CUDA = -3,            /* a CUDA runtime/driver call failed */
+    MP_ERR_PLAN = -4,            /* the planner produced no valid plan */
+    MP_ERR_DEVICE_TIMEOUT = -5,  /* a device-side wait gave up (reported by mp_check) */
+    MP_ERR_NO_MEMORY = -6        /* allocation at mp_init failed */
+} mp_status;
+
+#define MP_MAX_REGIONS 4
+#define MP_MAX_KERNELS 16
+
+/*
+ * Hardware description H [MP section 3, "multi-level accelerator
+ * abstraction"]: the number of processing engines, each PE's local memory,
+ * and the memory shared by all PEs; plus the rates the cost model uses.
+ */
+typedef struct {
+    int32_t num_pe;            /* processing engines (SMs)                      */
+    int32_t warps_per_wave;    /* warps resident at once over all PEs; a task
+                                  of w warps gets warps_per_wave / w slots     */
+    int64_t local_mem_bytes;   /* per-PE local memory (shared memory)           */
+    int64_t shared_mem_bytes;  /* memory shared by the PEs (L2)                 */
+    double hbm_gbs;            /* global-memory bandwidth, GB/s                 */
+    double l2_gbs;             /* shared-memory (L2) to PE bandwidth, GB/s      */
+    double mma_tflops;         /* dense bf16 tensor throughput, TFLOP/s         */
+} mp_hw;
+
+/*
+ * One micro-kernel: a fixed output tile (um x un) with a fixed K step uk
+ * [MP section 3, "micro-kernel generation"], and its performance model
+ * g_predict(t) = fixed_us + per_step_us * t for a pipeline task of t
+ * micro-kernel instances [MP section 3, "micro-kernel performance model"].
+ * swap = 1 marks the transposed form (D^T = B^T A^T) used for short M.
+ */
+typedef struct {
+    int32_t um, un, uk;
+    int32_t warps;             /* warps per task, for wave counting            */
+    int32_t swap;
+    double fixed_us;           /* per-task time that does not scale with t     */
+    double per_step_us;        /* time per micro-kernel instance (one uk step) */
+} mp_kernel_desc;
+
+/* One region R_i of a plan and its cost terms [MP section 3, cost model]. */
+typedef struct {
+    int32_t kernel;            /* index into the handle's micro-kernel set     */
+    int32_t um, un, uk, swap;
+    int64_t m0, n0;            /* origin of the region in D                    */
+    int64_t m_ext, n_ext;      /* extent of the region                         */
+    int32_t splits;            /* split-K factor: K~_i = ceil(K / splits)      */
+    int32_t f_num;             /* micro-kernel instances per task              */
+    int64_t f_parallel;        /* pipeline tasks = tiles * splits              */
+    int64_t f_wave;            /* ceil(f_parallel / slots)                     */
+    double f_pipe_us;          /* g_predict(f_num) (+ split-K reduction)       */
+} mp_region_info;
+
+typedef struct {
+    int32_t pattern;           /* 1: one region; 2: two regions along M or N;
+                                  4: body / right / bottom / corner            */
+    int32_t num_regions;
+    mp_region_info region[MP_MAX_REGIONS];
+    double cost_us;            /* Cost(S, H) of the chosen strategy            */
+    int64_t total_tasks;
+    int32_t evaluated;         /* strategies whose cost was computed           */
+    int32_t pruned;            /* strategies skipped by the running best       */
+    int64_t workspace_bytes;   /* split-K partials the plan needs              */
+} mp_plan_info;
+
+/*
+ * Create a handle on CUDA device `device` (must be an sm_103 GB300-class
+ * GPU).  Reads the device's SM count and memory sizes into H, allocates the
+ * library-owned device memory, and loads a micro-kernel timing table from
+ * `calib_path` when it is non-NULL and readable; otherwise the analytic
+ * default model is used.  The table is plain text, one micro-kernel per line:
+ * "um un uk swap fixed_us per_step_us" ('#' starts a comment); lines that
+ * name no kernel of the set are ignored.  The rates in H default to GB300
+ * figures and can be overridden with the environment variables MP_HBM_GBS,
+ * MP_L2_GBS and MP_MMA_TFLOPS.
+ * Errors: MP_ERR_INVALID_ARG (out NULL or bad device), MP_ERR_UNSUPPORTED
+ * (not sm_103), MP_ERR_NO_MEMORY, MP_ERR_CUDA.
+ */
+mp_status mp_init(mp_handle* out, int device, const char* calib_path);
+
+/*
+ * Create a planning-only handle from an explicit H and micro-kernel set (no
+ * GPU is touched; mp_gemm on it returns MP_ERR_UNSUPPORTED).  Used to check
+ * the planner against the pages' worked example.  kernels[0..num_kernels) is
+ * copied; num_kernels <= MP_MAX_KERNELS.
+ */
+mp_status mp_init_host(mp_handle* out, const mp_hw* hw,
+                       const mp_kernel_desc* kernels, int32_t num_kernels);
+
+/* Release the handle and all library-owned memory.  NULL is accepted. */
+mp_status mp_destroy(mp_handle h);
+
+/*
+ * Plan (M, N, K) without running it [MP section 3, "polymerization" and
+ * "heuristic search"; section 4, Patterns I and II]: evaluate Cost(S,H) over
+ * the strategies the search visits and return the cheapest in *out
+ * (optional).  Host only; never touches the device.
+ * Errors: MP_ERR_INVALID_ARG (negative size), MP_ERR_PLAN.
+ */
+mp_status mp_plan(mp_handle h, int64_t M, int64_t N, int64_t K, mp_plan_info* out);
+
+/* Same, for `batch` independent problems of one shape run in one launch. */
+mp_status mp_plan_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          mp_plan_info* out);
+
+/*
+ * Cost of a given strategy under the handle's model [MP section 3, cost
+ * model]: the caller fills num_regions and, per region, kernel, m0, n0,
+ * m_ext, n_ext and splits; the call fills every other field and cost_us.
+ * Used to evaluate the pages' worked example and for exhaustive search.
+ * Errors: MP_ERR_INVALID_ARG (unknown kernel), MP_ERR_PLAN (the regions do
+ * not tile the output exactly once).
+ */
+mp_status mp_evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                           mp_plan_info* inout);
+
+/*
+ * D = alpha * A * B + beta * C, asynchronously on `stream`.  Plans the shape
+ * (as mp_plan) and issues one persistent kernel launch [MP section 4:
+ * offsets and loop counts are run-time scalars of fixed-size micro-kernels;
+ * BOLT: the alpha/beta epilogue is fused].
+ *   A: device pointer, M x K bf16, row-major, lda >= max(1, K)
+ *   B: device pointer, K x N bf16, row-major, ldb >= max(1, N)
+ *   C: device pointer, M x N fp32, row-major, ldc >= max(1, N); not read and
+ *      may be NULL when beta == 0
+ *   D: device pointer, M x N fp32, row-major, ldd >= max(1, N)
+ * Any element-aligned pointer and leading dimension is accepted; operands
+ * whose rows are not 16-byte aligned are first repacked into the handle's
+ * staging area by the library's own kernel.  M == 0 or N == 0 is a no-op;
+ * K == 0 gives D = beta * C.  D may equal C only with ldc == ldd; any other
+ * overlap of D with A, B or C is MP_ERR_INVALID_ARG.  Repeated calls with the
+ * same plan give bitwise-identical D (split-K partials are reduced in a fixed
+ * order).
+ * Errors: MP_ERR_INVALID_ARG, MP_ERR_UNSUPPORTED (host-only handle or size
+ * beyond the staging area), MP_ERR_PLAN, MP_ERR_CUDA (launch failure).
+ */
+mp_status mp_gemm(mp_handle h, int64_t M, int64_t N, int64_t K,
+                  const void* A, int64_t lda,
+                  const void* B, int64_t ldb,
+                  const float* C, int64_t ldc,
+                  float* D, int64_t ldd,
+                  float alpha, float beta, mp_stream stream);
+
+/*
+ * `batch` same-shape problems in one launch [DISC, "GEMM merge" 2]: problem
+ * b uses A + b*strideA, B + b*strideB, C + b*strideC, D + b*strideD (strides
+ * in elements, >= 0).  Per-problem rules are those of mp_gemm; the D blocks
+ * of different problems must not overlap.  batch == 0 is a no-op.
+ */
+mp_status mp_gemm_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, int64_t strideA,
+                          const void* B, int64_t ldb, int64_t strideB,
+                          const float* C, int64_t ldc, int64_t strideC,
+                          float* D, int64_t ldd, int64_t strideD,
+                          float alpha, float beta, mp_stream stream);
+
+/*
+ * Synchronize `stream` and read the device status word: MP_OK, or
+ * MP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * check (the word is then cleared), or MP_ERR_CUDA.
+ */
+mp_status mp_check(mp_handle h, mp_stream stream);
+
+/*
+ * Test and ablation hook: pin every later plan to micro-kernel `kernel`
+ * (-1: free choice) and split-K factor `splits` (0: free choice), Pattern I.
+ */
+mp_status mp_force_plan(mp_handle h, int32_t kernel, int32_t splits);
+
+/*
+ * Test hook for failure detection: with enable != 0 the next launch on this
+ * handle withholds one shared-memory stage of its first work unit, so the
+ * consumer's bounded wait runs out after limit_ns nanoseconds (0 keeps the
+ * handle's limit, 1 s by default; a positive value also becomes the limit of
+ * later launches).  The kernel then stops cleanly and mp_check reports
+ * MP_ERR_DEVICE_TIMEOUT.  Nothing faults, traps or hangs.
+ */
+mp_status mp_inject_wait_timeout(mp_handle h, int32_t enable, int64_t limit_ns);
+
+/* Copy the handle's H and micro-kernel set (either pointer may be NULL). */
+mp_status mp_get_hw(mp_handle h, mp_hw* hw, mp_kernel_desc* kernels, int32_t* num_kernels);
+
+/*
+ * Replace micro-kernel k's performance model (g_predict) with measured
+ * values; used by calibration.  The plan cache is cleared.
+ */
+mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us);
+
+/* Static text for a status code. */
+const char* mp_status_string(mp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MP_H_ */

@@ -1,0 +1,284 @@
+"""Python binding of the mp C ABI (dynamic-shape GEMM D = alpha*A*B + beta*C on GB300).
+
+Argument marshalling only: every function here forwards to the entry point of
+the same name in ``libmp.so`` (declared in ``include/mp.h``); the planning and
+every step of the GEMM run in that library and its CUDA kernels.  Torch
+tensors supply device memory and streams.  A missing or unloadable library is
+an error -- there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import _build
+
+__all__ = [
+    "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched",
+    "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
+    "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library",
+    "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
+]
+
+MP_MAX_REGIONS = 4
+MP_MAX_KERNELS = 16
+
+MP_OK = 0
+MP_ERR_INVALID_ARG = -1
+MP_ERR_UNSUPPORTED = -2
+MP_ERR_CUDA = -3
+MP_ERR_PLAN = -4
+MP_ERR_DEVICE_TIMEOUT = -5
+MP_ERR_NO_MEMORY = -6
+
+
+class MpHw(ctypes.Structure):
+    _fields_ = [("num_pe", ctypes.c_int32), ("warps_per_wave", ctypes.c_int32),
+                ("local_mem_bytes", ctypes.c_int64), ("shared_mem_bytes", ctypes.c_int64),
+                ("hbm_gbs", ctypes.c_double), ("l2_gbs", ctypes.c_double),
+                ("mma_tflops", ctypes.c_double)]
+
+
+class MpKernelDesc(ctypes.Structure):
+    _fields_ = [("um", ctypes.c_int32), ("un", ctypes.c_int32), ("uk", ctypes.c_int32),
+                ("warps", ctypes.c_int32), ("swap", ctypes.c_int32),
+                ("fixed_us", ctypes.c_double), ("per_step_us", ctypes.c_double)]
+
+
+class MpRegionInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("um", ctypes.c_int32), ("un", ctypes.c_int32),
+                ("uk", ctypes.c_int32), ("swap", ctypes.c_int32),
+                ("m0", ctypes.c_int64), ("n0", ctypes.c_int64),
+                ("m_ext", ctypes.c_int64), ("n_ext", ctypes.c_int64),
+                ("splits", ctypes.c_int32), ("f_num", ctypes.c_int32),
+                ("f_parallel", ctypes.c_int64), ("f_wave", ctypes.c_int64),
+                ("f_pipe_us", ctypes.c_double)]
+
+
+class MpPlanInfo(ctypes.Structure):
+    _fields_ = [("pattern", ctypes.c_int32), ("num_regions", ctypes.c_int32),
+                ("region", MpRegionInfo * MP_MAX_REGIONS), ("cost_us", ctypes.c_double),
+                ("total_tasks", ctypes.c_int64), ("evaluated", ctypes.c_int32),
+                ("pruned", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+
+    def regions(self):
+        return [self.region[i] for i in range(self.num_regions)]
+
+
+class MPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mp_status_string(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+_f = ctypes.c_float
+
+
+def library(build: bool = True) -> ctypes.CDLL:
+    """Load libmp.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build:
+                path = _build.build()
+            if not os.path.exists(path):
+                raise OSError(f"libmp.so not built at {path}")
+            lib = ctypes.CDLL(path)
+            sig = {
+                "mp_init": ([ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_char_p], ctypes.c_int),
+                "mp_init_host": ([ctypes.POINTER(_vp), ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
+                                  _i32], ctypes.c_int),
+                "mp_destroy": ([_vp], ctypes.c_int),
+                "mp_plan": ([_vp, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
+                "mp_plan_batched": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
+                "mp_evaluate_plan": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
+                "mp_gemm": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                             _f, _f, _vp], ctypes.c_int),
+                "mp_gemm_batched": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
+                                     _vp, _i64, _i64, _vp, _i64, _i64, _f, _f, _vp], ctypes.c_int),
+                "mp_check": ([_vp, _vp], ctypes.c_int),
+                "mp_force_plan": ([_vp, _i32, _i32], ctypes.c_int),
+                "mp_get_hw": ([_vp, ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
+                               ctypes.POINTER(_i32)], ctypes.c_int),
+                "mp_set_kernel_model": ([_vp, _i32, ctypes.c_double, ctypes.c_double], ctypes.c_int),
+                "mp_inject_wait_timeout": ([_vp, _i32, _i64], ctypes.c_int),
+                "mp_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def mp_status_string(status: int) -> str:
+    return library().mp_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MP_OK:
+        raise MPError(status, where)
+
+
+class Handle:
+    """Owns one mp_handle; destroyed with mp_destroy when closed or collected."""
+
+    def __init__(self, ptr: int, device: Optional[int]):
+        self.ptr = ptr
+        self.device = device
+
+    def close(self) -> None:
+        if self.ptr:
+            library().mp_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):  # pragma: no cover - best effort at interpreter exit
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def mp_init(device: int = 0, calib_path: Optional[str] = None) -> Handle:
+    out = _vp()
+    _check(library().mp_init(ctypes.byref(out), int(device),
+                             calib_path.encode() if calib_path else None), "mp_init")
+    return Handle(out.value, device)
+
+
+def mp_init_host(hw: MpHw, kernels=None) -> Handle:
+    out = _vp()
+    if kernels:
+        arr = (MpKernelDesc * len(kernels))(*kernels)
+        st = library().mp_init_host(ctypes.byref(out), ctypes.byref(hw), arr, len(kernels))
+    else:
+        st = library().mp_init_host(ctypes.byref(out), ctypes.byref(hw), None, 0)
+    _check(st, "mp_init_host")
+    return Handle(out.value, None)
+
+
+def mp_destroy(h: Handle) -> None:
+    h.close()
+
+
+def mp_plan(h: Handle, M: int, N: int, K: int) -> MpPlanInfo:
+    info = MpPlanInfo()
+    _check(library().mp_plan(h.ptr, M, N, K, ctypes.byref(info)), "mp_plan")
+    return info
+
+
+def mp_plan_batched(h: Handle, batch: int, M: int, N: int, K: int) -> MpPlanInfo:
+    info = MpPlanInfo()
+    _check(library().mp_plan_batched(h.ptr, batch, M, N, K, ctypes.byref(info)), "mp_plan_batched")
+    return info
+
+
+def mp_evaluate_plan(h: Handle, batch: int, M: int, N: int, K: int, regions) -> MpPlanInfo:
+    """regions: list of dicts with kernel, m0, n0, m_ext, n_ext, splits."""
+    info = MpPlanInfo()
+    info.num_regions = len(regions)
+    for i, r in enumerate(regions):
+        g = info.region[i]
+        g.kernel, g.m0, g.n0 = r["kernel"], r["m0"], r["n0"]
+        g.m_ext, g.n_ext, g.splits = r["m_ext"], r["n_ext"], r.get("splits", 1)
+    _check(library().mp_evaluate_plan(h.ptr, batch, M, N, K, ctypes.byref(info)), "mp_evaluate_plan")
+    return info
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ld(t, name: str) -> int:
+    if t.dim() < 2:
+        raise ValueError(f"{name} must have at least 2 dimensions")
+    if t.size(-1) > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have unit stride along its last dimension")
+    return t.stride(-2) if t.size(-2) > 1 else max(1, t.size(-1))
+
+
+def mp_gemm(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """D = alpha*A@B + beta*C with torch CUDA tensors (A, B bf16; C, D fp32)."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or D.dtype != torch.float32:
+        raise TypeError("A and B must be bfloat16, D float32")
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-1]
+    if B.shape[-2] != K or D.shape[-2:] != (M, N):
+        raise ValueError("shape mismatch")
+    c_ptr, ldc = None, 0
+    if beta != 0.0:
+        if C is None or C.dtype != torch.float32 or C.shape[-2:] != (M, N):
+            raise ValueError("beta != 0 needs an fp32 C of D's shape")
+        c_ptr, ldc = C.data_ptr(), _ld(C, "C")
+    st = library().mp_gemm(h.ptr, M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+                           c_ptr, ldc, D.data_ptr(), _ld(D, "D"), float(alpha), float(beta),
+                           _stream_ptr(stream))
+    _check(st, "mp_gemm")
+
+
+def mp_gemm_batched(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """Batched form on 3-D tensors [batch, rows, cols]; a batch stride of 0 shares an operand."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or D.dtype != torch.float32:
+        raise TypeError("A and B must be bfloat16, D float32")
+    if A.dim() != 3 or B.dim() != 3 or D.dim() != 3:
+        raise ValueError("batched operands are 3-D")
+    batch = D.shape[0]
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-1]
+    sa = A.stride(0) if A.shape[0] > 1 else 0
+    sb = B.stride(0) if B.shape[0] > 1 else 0
+    c_ptr, ldc, sc = None, 0, 0
+    if beta != 0.0:
+        c_ptr, ldc = C.data_ptr(), _ld(C, "C")
+        sc = C.stride(0) if C.shape[0] > 1 else 0
+    st = library().mp_gemm_batched(h.ptr, batch, M, N, K, A.data_ptr(), _ld(A, "A"), sa,
+                                   B.data_ptr(), _ld(B, "B"), sb, c_ptr, ldc, sc,
+                                   D.data_ptr(), _ld(D, "D"), D.stride(0),
+                                   float(alpha), float(beta), _stream_ptr(stream))
+    _check(st, "mp_gemm_batched")
+
+
+def mp_check(h: Handle, stream=None) -> int:
+    """Synchronize and return the device status (MP_OK or MP_ERR_DEVICE_TIMEOUT)."""
+    return int(library().mp_check(h.ptr, _stream_ptr(stream)))
+
+
+def mp_force_plan(h: Handle, kernel: int = -1, splits: int = 0) -> None:
+    _check(library().mp_force_plan(h.ptr, kernel, splits), "mp_force_plan")
+
+
+def mp_get_hw(h: Handle):
+    hw = MpHw()
+    ks = (MpKernelDesc * MP_MAX_KERNELS)()
+    n = _i32()
+    _check(library().mp_get_hw(h.ptr, ctypes.byref(hw), ks, ctypes.byref(n)), "mp_get_hw")
+    return hw, [ks[i] for i in range(n.value)]
+
+
+def mp_set_kernel_model(h: Handle, k: int, fixed_us: float, per_step_us: float) -> None:
+    _check(library().mp_set_kernel_model(h.ptr, k, fixed_us, per_step_us), "mp_set_kernel_model")
+
+
+def mp_inject_wait_timeout(h: Handle, enable: bool = True, limit_ns: int = 0) -> None:
+    _check(library().mp_inject_wait_timeout(h.ptr, 1 if enable else 0, int(limit_ns)),
+           "mp_inject_wait_timeout")

@@ -1,0 +1,259 @@
+// The C ABI: handle lifecycle, argument checking and dispatch to the planner
+// and the device code.  Every entry point returns an mp_status; nothing here
+// throws across the boundary or falls back to host arithmetic.
+#include <cerrno>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "mp_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;  // sizes and offsets fit int32 on the device
+
+double env_double(const char* name, double dflt) {
+    const char* v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    char* end = nullptr;
+    double x = std::strtod(v, &end);
+    return (end && end != v && x > 0) ? x : dflt;
+}
+
+// Calibration table: "um un uk swap fixed_us per_step_us" per line.
+void load_calibration(mp_handle h, const char* path) {
+    if (!path || !*path) return;
+    FILE* f = std::fopen(path, "r");
+    if (!f) return;
+    char line[512];
+    while (std::fgets(line, sizeof line, f)) {
+        char* hash = std::strchr(line, '#');
+        if (hash) *hash = 0;
+        int um, un, uk, swap;
+        double fixed, step;
+        if (std::sscanf(line, "%d %d %d %d %lf %lf", &um, &un, &uk, &swap, &fixed, &step) != 6) continue;
+        if (!(fixed >= 0) || !(step > 0)) continue;
+        for (int k = 0; k < h->num_kernels; k++) {
+            mp_kernel_desc& d = h->kernels[k];
+            if (d.um == um && d.un == un && d.uk == uk && d.swap == swap) {
+                d.fixed_us = fixed;
+                d.per_step_us = step;
+            }
+        }
+    }
+    std::fclose(f);
+}
+
+mp_handle new_handle() {
+    mp_handle h = new (std::nothrow) mp_handle_s();
+    if (!h) return nullptr;
+    try {
+        h->cache.resize(4096);
+    } catch (...) {
+        delete h;
+        return nullptr;
+    }
+    return h;
+}
+
+// Byte extent [lo, hi) of a row-major matrix block.
+struct Span {
+    uintptr_t lo, hi;
+};
+
+Span span_of(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t elem, int64_t batch,
+             int64_t stride) {
+    uintptr_t lo = (uintptr_t)p;
+    int64_t last = (rows - 1) * ld + cols;  // elements from the first to one past the last
+    if (batch > 1) last += (batch - 1) * stride;
+    return Span{lo, lo + (uintptr_t)(last * elem)};
+}
+
+bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+mp_status check_args(const mp::GemmArgs& a) {
+    const int64_t batch = a.batch, M = a.M, N = a.N, K = a.K;
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return MP_ERR_INVALID_ARG;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || batch >= kMaxDim) return MP_ERR_INVALID_ARG;
+    if (batch == 0 || M == 0 || N == 0) return MP_OK;
+    if (!a.D) return MP_ERR_INVALID_ARG;
+    if (a.ldd < (N > 1 ? N : 1)) return MP_ERR_INVALID_ARG;
+    if (((uintptr_t)a.D & 3) != 0) return MP_ERR_INVALID_ARG;
+    if (a.strideA < 0 || a.strideB < 0 || a.strideC < 0 || a.strideD < 0) return MP_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!a.A || !a.B) return MP_ERR_INVALID_ARG;
+        if (a.lda < K || a.ldb < (N > 1 ? N : 1)) return MP_ERR_INVALID_ARG;
+        if (((uintptr_t)a.A & 1) != 0 || ((uintptr_t)a.B & 1) != 0) return MP_ERR_INVALID_ARG;
+    }
+    const bool read_c = a.beta != 0.0f;
+    if (read_c) {
+        if (!a.C || a.ldc < (N > 1 ? N : 1)) return MP_ERR_INVALID_ARG;
+        if (((uintptr_t)a.C & 3) != 0) return MP_ERR_INVALID_ARG;
+    }
+    // Distinct problems of a batch must write disjoint D blocks.
+    if (batch > 1 && a.strideD < (M - 1) * a.ldd + N) return MP_ERR_INVALID_ARG;
+    const Span d = span_of(a.D, M, N, a.ldd, 4, batch, a.strideD);
+    if (K > 0) {
+        if (overlap(d, span_of(a.A, M, K, a.lda, 2, batch, a.strideA))) return MP_ERR_INVALID_ARG;
+        if (overlap(d, span_of(a.B, K, N, a.ldb, 2, batch, a.strideB))) return MP_ERR_INVALID_ARG;
+    }
+    if (read_c) {
+        const bool in_place = a.C == a.D && a.ldc == a.ldd && (batch == 1 || a.strideC == a.strideD);
+        if (!in_place && overlap(d, span_of(a.C, M, N, a.ldc, 4, batch, a.strideC)))
+            return MP_ERR_INVALID_ARG;
+    }
+    return MP_OK;
+}
+
+mp_status run(mp_handle h, const mp::GemmArgs& a) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    mp_status st = check_args(a);
+    if (st != MP_OK) return st;
+    if (a.batch == 0 || a.M == 0 || a.N == 0) return MP_OK;
+    if (h->host_only) return MP_ERR_UNSUPPORTED;
+    mp_plan_info plan;
+    st = mp::plan_shape(h, a.batch, a.M, a.N, a.K, &plan);
+    if (st != MP_OK) return st;
+    return mp::device_run(h, plan, a);
+}
+
+}  // namespace
+
+extern "C" {
+
+mp_status mp_init(mp_handle* out, int device, const char* calib_path) {
+    if (!out) return MP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (device < 0) return MP_ERR_INVALID_ARG;
+    mp_handle h = new_handle();
+    if (!h) return MP_ERR_NO_MEMORY;
+    h->host_only = false;
+    h->device = device;
+    mp_status st = mp::device_init(h, device);  // fills H and allocates device state
+    if (st != MP_OK) {
+        mp::device_destroy(h);
+        delete h;
+        return st;
+    }
+    h->hw.hbm_gbs = env_double("MP_HBM_GBS", h->hw.hbm_gbs);
+    h->hw.l2_gbs = env_double("MP_L2_GBS", h->hw.l2_gbs);
+    h->hw.mma_tflops = env_double("MP_MMA_TFLOPS", h->hw.mma_tflops);
+    mp::default_gb300_kernels(h->hw, h->kernels, &h->num_kernels);
+    load_calibration(h, calib_path);
+    *out = h;
+    return MP_OK;
+}
+
+mp_status mp_init_host(mp_handle* out, const mp_hw* hw, const mp_kernel_desc* kernels,
+                       int32_t num_kernels) {
+    if (!out) return MP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!hw || hw->num_pe < 1 || hw->warps_per_wave < 1) return MP_ERR_INVALID_ARG;
+    if (num_kernels < 0 || num_kernels > MP_MAX_KERNELS || (num_kernels > 0 && !kernels))
+        return MP_ERR_INVALID_ARG;
+    for (int32_t k = 0; k < num_kernels; k++) {
+        const mp_kernel_desc& d = kernels[k];
+        if (d.um < 1 || d.un < 1 || d.uk < 1 || d.warps < 1 || d.fixed_us < 0 || d.per_step_us < 0)
+            return MP_ERR_INVALID_ARG;
+    }
+    mp_handle h = new_handle();
+    if (!h) return MP_ERR_NO_MEMORY;
+    h->hw = *hw;
+    if (num_kernels == 0) {
+        mp::default_gb300_kernels(h->hw, h->kernels, &h->num_kernels);
+    } else {
+        std::memcpy(h->kernels, kernels, sizeof(mp_kernel_desc) * (size_t)num_kernels);
+        h->num_kernels = num_kernels;
+    }
+    *out = h;
+    return MP_OK;
+}
+
+mp_status mp_destroy(mp_handle h) {
+    if (!h) return MP_OK;
+    mp::device_destroy(h);
+    delete h;
+    return MP_OK;
+}
+
+mp_status mp_plan(mp_handle h, int64_t M, int64_t N, int64_t K, mp_plan_info* out) {
+    return mp_plan_batched(h, 1, M, N, K, out);
+}
+
+mp_status mp_plan_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          mp_plan_info* out) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return MP_ERR_INVALID_ARG;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || batch >= kMaxDim) return MP_ERR_INVALID_ARG;
+    mp_plan_info tmp;
+    return mp::plan_shape(h, batch, M, N, K, out ? out : &tmp);
+}
+
+mp_status mp_evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                           mp_plan_info* inout) {
+    return mp::evaluate_plan(h, batch, M, N, K, inout);
+}
+
+mp_status mp_gemm(mp_handle h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                  const void* B, int64_t ldb, const float* C, int64_t ldc, float* D, int64_t ldd,
+                  float alpha, float beta, mp_stream stream) {
+    mp::GemmArgs a{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, stream};
+    return run(h, a);
+}
+
+mp_status mp_gemm_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda, int64_t strideA, const void* B, int64_t ldb,
+                          int64_t strideB, const float* C, int64_t ldc, int64_t strideC, float* D,
+                          int64_t ldd, int64_t strideD, float alpha, float beta, mp_stream stream) {
+    mp::GemmArgs a{batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
+                   D, ldd, strideD, alpha, beta, stream};
+    return run(h, a);
+}
+
+mp_status mp_check(mp_handle h, mp_stream stream) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    if (h->host_only) return MP_OK;
+    return mp::device_check(h, stream);
+}
+
+mp_status mp_force_plan(mp_handle h, int32_t kernel, int32_t splits) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    if (kernel < -1 || kernel >= h->num_kernels || splits < 0) return MP_ERR_INVALID_ARG;
+    h->force_kernel = kernel;
+    h->force_splits = splits;
+    mp::clear_plan_cache(h);
+    return MP_OK;
+}
+
+mp_status mp_get_hw(mp_handle h, mp_hw* hw, mp_kernel_desc* kernels, int32_t* num_kernels) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    if (hw) *hw = h->hw;
+    if (kernels) std::memcpy(kernels, h->kernels, sizeof(mp_kernel_desc) * (size_t)h->num_kernels);
+    if (num_kernels) *num_kernels = h->num_kernels;
+    return MP_OK;
+}
+
+mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us) {
+    if (!h || k < 0 || k >= h->num_kernels || !(fixed_us >= 0) || !(per_step_us > 0))
+        return MP_ERR_INVALID_ARG;
+    h->kernels[k].fixed_us = fixed_us;
+    h->kernels[k].per_step_us = per_step_us;
+    mp::clear_plan_cache(h);
+    return MP_OK;
+}
+
+const char* mp_status_string(mp_status s) {
+    switch (s) {
+        case MP_OK: return "ok";
+        case MP_ERR_INVALID_ARG: return "invalid argument";
+        case MP_ERR_UNSUPPORTED: return "unsupported";
+        case MP_ERR_CUDA: return "CUDA error";
+        case MP_ERR_PLAN: return "no valid plan";
+        case MP_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MP_ERR_NO_MEMORY: return "out of memory";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

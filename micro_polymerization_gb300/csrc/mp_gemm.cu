@@ -1,0 +1,884 @@
+// Device side: one persistent kernel that runs a whole polymerization plan.
+//
+// Each CTA (one per SM) walks the plan's work units -- (region, tile, split)
+// triples -- in a static round-robin.  Every unit is a pipeline task in the
+// sense of the MikPoly summary, section 3 ("micro-kernel performance
+// model"): its K loop is serial on one PE and runs in three stages,
+//   (1) load the operand tiles into the PE's local memory  -> TMA producer warp
+//   (2) run the micro-kernel on them                       -> tcgen05.mma issuer
+//   (3) write the result back                              -> epilogue warps
+// overlapped through an mbarrier ring of shared-memory stages and two TMEM
+// accumulator buffers.  Offsets and loop counts of the fixed-size
+// micro-kernels arrive as run-time scalars (MikPoly summary, section 4).  The
+// epilogue applies D = alpha*acc + beta*C (BOLT summary, persistent kernel
+// fusion) with masking at the region edges, so any (M, N, K) runs in one
+// launch without per-shape compilation.
+//
+// Micro-kernel forms (both with a 128-lane fp32 accumulator in TMEM):
+//   normal:  acc[128 x bn] = A_tile[128 x K] * B_tile[K x bn]
+//            A is K-major (row-major A), B is MN-major (row-major B).
+//   swapped: acc[128 x bn] = B_tile^T[128 x K] * A_tile^T[K x bn], i.e. the
+//            transpose of a bn x 128 block of D, for short M: the UMMA M runs
+//            over N and bn (16..128) over M.
+// Operand tiles use the 128-byte swizzle: one swizzle row holds 64 bf16, so
+// a stage carries 64 elements of K.
+//
+// Warp roles (192 threads):  warp 0 = TMA producer, warp 1 = TMEM owner and
+// MMA issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Every wait is bounded: on expiry the CTA records an error code in the
+// handle's status word, tells its other roles to stop, waits (bounded) for
+// its own copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "mp_internal.h"
+
+namespace mp {
+namespace dev {
+
+constexpr int kStages = 4;
+constexpr int kXBytes = 128 * 64 * 2;   // 128 rows (or 128 columns of B^T) x 64 K, bf16
+constexpr int kYBytes = 256 * 64 * 2;   // up to 256 columns x 64 K, bf16
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;          // two accumulator buffers of 256 columns
+constexpr int kAccStride = 256;
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = kStages * (kXBytes + kYBytes) + kBarBytes + 1024;
+
+// Error codes written to the status word (first writer wins).
+constexpr int kErrWaitEmpty = 1;
+constexpr int kErrWaitFull = 2;
+constexpr int kErrWaitAccEmpty = 3;
+constexpr int kErrWaitAccFull = 4;
+constexpr int kErrDrain = 5;
+
+struct Region {
+    int m0, n0, m_end, n_end;   // region bounds in D
+    int tiles_m, tiles_n;
+    int bn;                     // UMMA N (normal: columns of D; swapped: rows of D)
+    int swap;
+    int splits, kb_per_split;
+    int unit_begin, units;
+    long long ws_begin;         // first fp32 of this region's split-K partials
+    int cnt_begin;              // first tile counter
+    int pad_;
+};
+
+struct alignas(128) Params {
+    CUtensorMap tmA;     // A viewed as [batch][M][K] bf16, box {64 (K), 128 rows}
+    CUtensorMap tmA16;   // same tensor, box {64 (K), 16 rows}
+    CUtensorMap tmB;     // B viewed as [batch][K][N] bf16, box {64 (N), 64 rows of K}
+    const float* C;
+    float* D;
+    long long ldc, ldd, strideC, strideD;
+    float alpha, beta;
+    int num_kb;          // ceil(K / 64)
+    int a_bstep, b_bstep;
+    int total_units;
+    int num_regions;
+    int inject_timeout;  // test hook: withhold the first stage of the first unit
+    unsigned long long wait_limit_ns;
+    Region reg[MP_MAX_REGIONS];
+    float* ws;
+    unsigned int* cnt;
+    int* err;
+};
+
+struct Work {
+    int b, split, splits;
+    int m_t0, n_t0, m_end, n_end;
+    int bn, swap;
+    int kb0, kb1;
+    long long ws_tile;   // split 0 of this tile's partials
+    int cnt;
+};
+
+__device__ __forceinline__ Work decode(const Params& p, int u) {
+    int r = 0;
+#pragma unroll
+    for (int i = 1; i < MP_MAX_REGIONS; i++)
+        if (i < p.num_regions && u >= p.reg[i].unit_begin) r = i;
+    const Region& g = p.reg[r];
+    const int local = u - g.unit_begin;
+    const int tiles = g.tiles_m * g.tiles_n;
+    const int per_b = tiles * g.splits;
+    Work w;
+    w.b = local / per_b;
+    const int rem = local - w.b * per_b;
+    const int tile = rem / g.splits;
+    w.split = rem - tile * g.splits;
+    w.splits = g.splits;
+    const int tm = tile / g.tiles_n;
+    const int tn = tile - tm * g.tiles_n;
+    w.swap = g.swap;
+    w.bn = g.bn;
+    if (!g.swap) {
+        w.m_t0 = g.m0 + tm * 128;
+        w.n_t0 = g.n0 + tn * g.bn;
+    } else {
+        w.m_t0 = g.m0 + tm * g.bn;
+        w.n_t0 = g.n0 + tn * 128;
+    }
+    w.m_end = g.m_end;
+    w.n_end = g.n_end;
+    w.kb0 = w.split * g.kb_per_split;
+    w.kb1 = min(w.kb0 + g.kb_per_split, p.num_kb);
+    const long long tile_id = (long long)w.b * tiles + tile;
+    w.ws_tile = g.ws_begin + tile_id * g.splits * (128ll * g.bn);
+    w.cnt = g.cnt_begin + (int)tile_id;
+    return w;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of parity `parity` of `bar` to complete, for at most
+// `limit_ns`.  With `honor_abort`, also give up as soon as another role of
+// the CTA has aborted.  On expiry, raise the CTA's abort flag and record
+// `code` in the status word.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code, uint64_t limit_ns, bool honor_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honor_abort && *abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicCAS(err, 0, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 16 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    // The wait names the registers so that no use is scheduled above it.
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// K-major operand: rows of 64 bf16 (128 B) with 8-row swizzle atoms 1024 B
+// apart; one UMMA K step (16 elements) advances 32 B inside the row.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kstep) {
+    return smem_desc(tile + 32u * kstep, 16u, 1024u);
+}
+
+// MN-major operand: atoms of 64 MN elements x 8 K rows (1024 B); K groups of
+// 8 rows 1024 B apart, 64-wide MN blocks 8192 B apart (one TMA box each); one
+// UMMA K step (16 rows) advances 2048 B.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kstep) {
+    return smem_desc(tile + 2048u * kstep, 8192u, 1024u);
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue store of 16 accumulator columns of one TMEM lane
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, int c, const float* v) {
+    const float alpha = p.alpha, beta = p.beta;
+    if (!w.swap) {
+        // lane = row of D, columns = columns of D
+        const int m = w.m_t0 + tl;
+        if (m >= w.m_end) return;
+        float* d = p.D + (long long)w.b * p.strideD + (long long)m * p.ldd;
+        const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc;
+        const int n0 = w.n_t0 + c;
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const int n = n0 + j;
+            if (n < w.n_end) {
+                float r = alpha * v[j];
+                if (beta != 0.0f) r = fmaf(beta, cr[n], r);
+                d[n] = r;
+            }
+        }
+    } else {
+        // lane = column of D, columns = rows of D
+        const int n = w.n_t0 + tl;
+        if (n >= w.n_end) return;
+        const long long bd = (long long)w.b * p.strideD + n;
+        const long long bc = (long long)w.b * p.strideC + n;
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const int m = w.m_t0 + c + j;
+            if (m < w.m_end) {
+                float r = alpha * v[j];
+                if (beta != 0.0f) r = fmaf(beta, p.C[bc + (long long)m * p.ldc], r);
+                p.D[bd + (long long)m * p.ldd] = r;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The persistent kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t xs0 = base;
+    const uint32_t ys0 = base + kStages * kXBytes;
+    const uint32_t bar0 = ys0 + kStages * kYBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + (bar0 - base));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accf = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto acce = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+    const uint64_t limit = p.wait_limit_ns;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; s++) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(accf(b), 1);
+            mbar_init(acce(b), 4);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        *s_last = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_map(&p.tmA);
+        tma_prefetch_map(&p.tmA16);
+        tma_prefetch_map(&p.tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer ---------------------
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t armed_mask = 0, armed_ph = 0;
+            bool withhold = p.inject_timeout != 0;
+            for (int u = blockIdx.x; u < p.total_units && !*abort_flag; u += gridDim.x) {
+                const Work w = decode(p, u);
+                const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bounded(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit, true))
+                        goto producer_out;
+                    if (!withhold) {
+                        const uint32_t xs = xs0 + stage * kXBytes, ys = ys0 + stage * kYBytes;
+                        const int kc = kb * 64;
+                        mbar_arrive_expect_tx(full(stage), (uint32_t)(kXBytes + w.bn * 128));
+                        if (!w.swap) {
+                            tma_load_3d(xs, &p.tmA, full(stage), kc, w.m_t0, ab);
+                            for (int c = 0; c < w.bn / 64; ++c)
+                                tma_load_3d(ys + c * 8192, &p.tmB, full(stage), w.n_t0 + 64 * c, kc, bb);
+                        } else {
+                            tma_load_3d(xs, &p.tmB, full(stage), w.n_t0, kc, bb);
+                            tma_load_3d(xs + 8192, &p.tmB, full(stage), w.n_t0 + 64, kc, bb);
+                            for (int c = 0; c < w.bn / 16; ++c)
+                                tma_load_3d(ys + c * 2048, &p.tmA16, full(stage), kc, w.m_t0 + 16 * c, ab);
+                        }
+                        armed_mask |= 1u << stage;
+                        armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    }
+                    withhold = false;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        producer_out:
+            if (*abort_flag) {
+                // Let every copy this thread started land before the CTA exits.
+                for (int s = 0; s < kStages; s++)
+                    if (armed_mask & (1u << s))
+                        wait_bounded(full(s), (armed_ph >> s) & 1u, abort_flag, p.err, kErrDrain, limit, false);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------ MMA issuer -----------------------
+            int stage = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+                const Work w = decode(p, u);
+                if (!wait_bounded(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit, true))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
+                const uint32_t idesc = w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true);
+                bool ok = true;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!wait_bounded(full(stage), ph, abort_flag, p.err, kErrWaitFull, limit, true)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = xs0 + stage * kXBytes, ys = ys0 + stage * kYBytes;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint64_t ad, bd;
+                        if (!w.swap) {
+                            ad = desc_kmajor(xs, k);
+                            bd = desc_mnmajor(ys, k);
+                        } else {
+                            ad = desc_mnmajor(xs, k);
+                            bd = desc_kmajor(ys, k);
+                        }
+                        umma_bf16(d, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(accf(acc));
+                acc ^= 1;
+                if (acc == 0) aph ^= 1u;
+            }
+            // Every MMA this thread issued has completed once `done_bar` flips.
+            umma_commit(done_bar);
+            wait_bounded(done_bar, 0, abort_flag, p.err, kErrDrain, limit, false);
+        }
+    } else {
+        // ------------------------------ epilogue (128 threads) ----------------
+        const int q = warp & 3;        // TMEM lane quarter this warp may access
+        const int tl = q * 32 + lane;  // accumulator lane held by this thread
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+            const Work w = decode(p, u);
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_bounded(accf(acc), aph, abort_flag, p.err, kErrWaitAccFull, limit, true) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
+            const bool has_k = w.kb1 > w.kb0;
+            if (w.splits == 1) {
+                for (int c = 0; c < w.bn; c += 16) {
+                    float v[16];
+                    if (has_k) {
+                        tmem_ld16(t + c, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; j++) v[j] = 0.0f;
+                    }
+                    store16(p, w, tl, c, v);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce(acc));
+            } else {
+                // Split-K: park this split's partial, column-major per tile
+                // (128 lanes contiguous), then the last split to arrive sums
+                // all partials in split order and runs the epilogue.
+                float* part = p.ws + w.ws_tile + (long long)w.split * (128ll * w.bn);
+                for (int c = 0; c < w.bn; c += 16) {
+                    float v[16];
+                    tmem_ld16(t + c, v);
+#pragma unroll
+                    for (int j = 0; j < 16; j++) __stcg(part + (c + j) * 128 + tl, v[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce(acc));  // TMEM buffer free for the next unit
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 64) {
+                    const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
+                    *s_last = (old == (unsigned)(w.splits - 1)) ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                if (*s_last) {
+                    __threadfence();
+                    const float* tile_ws = p.ws + w.ws_tile;
+                    for (int c = 0; c < w.bn; c += 16) {
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j++) v[j] = 0.0f;
+                        for (int s = 0; s < w.splits; s++) {
+                            const float* ps = tile_ws + (long long)s * (128ll * w.bn);
+#pragma unroll
+                            for (int j = 0; j < 16; j++) v[j] += __ldcg(ps + (c + j) * 128 + tl);
+                        }
+                        store16(p, w, tl, c, v);
+                    }
+                    if (threadIdx.x == 64) p.cnt[w.cnt] = 0u;  // ready for the next launch
+                }
+            }
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Copy a (batch x rows x cols) bf16 operand whose rows are not 16-byte
+// aligned into a staging buffer with rows padded to a multiple of 8 elements
+// (zero-filled), so that TMA can address it.
+__global__ void k_repack_bf16(const uint16_t* __restrict__ src, long long ld_src, long long stride_src,
+                              uint16_t* __restrict__ dst, long long ld_dst, long long stride_dst, int rows,
+                              int cols, int batch) {
+    const long long chunks = ld_dst / 8;
+    const long long total = (long long)batch * rows * chunks;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long ch = i % chunks;
+        const long long rb = i / chunks;
+        const int r = (int)(rb % rows);
+        const int b = (int)(rb / rows);
+        const uint16_t* s = src + b * stride_src + r * ld_src + ch * 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const long long c0 = ch * 8 + 2 * j;
+            const uint32_t lo = c0 < cols ? s[2 * j] : 0u;
+            const uint32_t hi = c0 + 1 < cols ? s[2 * j + 1] : 0u;
+            w[j] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + b * stride_dst + r * ld_dst + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+}  // namespace dev
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    int device = -1;
+    int num_sms = 0;
+    float* ws = nullptr;
+    unsigned int* cnt = nullptr;
+    int* err = nullptr;
+    uint8_t* staging = nullptr;
+    int64_t staging_bytes = 0;
+    EncodeTiledFn encode = nullptr;
+    bool log = false;
+    int inject_timeout = 0;
+    uint64_t wait_limit_ns = 1000000000ull;  // 1 s
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_ok(const void* p, int64_t ld, int64_t batch, int64_t stride) {
+    if (((uintptr_t)p & 15u) != 0) return false;
+    if ((ld * 2) % 16 != 0) return false;
+    if (batch > 1 && stride != 0 && (stride * 2) % 16 != 0) return false;
+    return true;
+}
+
+void log_plan(const mp_plan_info& plan, const GemmArgs& a, int grid) {
+    std::fprintf(stderr, "[mp] batch=%lld M=%lld N=%lld K=%lld pattern=%d regions=%d tasks=%lld grid=%d cost=%.2fus\n",
+                 (long long)a.batch, (long long)a.M, (long long)a.N, (long long)a.K, plan.pattern,
+                 plan.num_regions, (long long)plan.total_tasks, grid, plan.cost_us);
+    for (int i = 0; i < plan.num_regions; i++) {
+        const mp_region_info& r = plan.region[i];
+        std::fprintf(stderr, "[mp]   R%d [%lld+%lld, %lld+%lld] kernel=%d (%dx%d%s) splits=%d f_num=%d waves=%lld pipe=%.2fus\n",
+                     i, (long long)r.m0, (long long)r.m_ext, (long long)r.n0, (long long)r.n_ext, r.kernel, r.um,
+                     r.un, r.swap ? " swapped" : "", r.splits, r.f_num, (long long)r.f_wave, r.f_pipe_us);
+    }
+}
+
+}  // namespace
+
+mp_status device_init(mp_handle h, int device) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) return MP_ERR_UNSUPPORTED;
+    if (device >= count) return MP_ERR_INVALID_ARG;
+    DeviceGuard g(device);
+    if (!g.ok) return MP_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MP_ERR_UNSUPPORTED;  // sm_103 only
+
+    DeviceState* s = new DeviceState();
+    h->dev = s;
+    s->device = device;
+    s->num_sms = prop.multiProcessorCount;
+    s->log = std::getenv("MP_LOG") != nullptr;
+    if (const char* v = std::getenv("MP_STAGING_BYTES")) s->staging_bytes = std::atoll(v);
+    if (s->staging_bytes <= 0) s->staging_bytes = kDefaultStagingBytes;
+
+    h->hw.num_pe = prop.multiProcessorCount;
+    h->hw.warps_per_wave = prop.multiProcessorCount * (dev::kThreads / 32);
+    h->hw.local_mem_bytes = (int64_t)prop.sharedMemPerBlockOptin;
+    h->hw.shared_mem_bytes = (int64_t)prop.l2CacheSize;
+    h->hw.hbm_gbs = 6684.0;    // measured STREAM-style copy on GB300
+    h->hw.l2_gbs = 20000.0;    // L2 -> SM operand rate assumed by the model
+    h->hw.mma_tflops = 1974.0; // measured dense bf16 on GB300
+
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return MP_ERR_CUDA;
+    s->encode = reinterpret_cast<EncodeTiledFn>(fn);
+
+    if (cudaMalloc(&s->ws, sizeof(float) * (size_t)h->workspace_floats) != cudaSuccess) return MP_ERR_NO_MEMORY;
+    if (cudaMalloc(&s->cnt, sizeof(unsigned) * (size_t)kMaxCounters) != cudaSuccess) return MP_ERR_NO_MEMORY;
+    if (cudaMalloc(&s->err, sizeof(int)) != cudaSuccess) return MP_ERR_NO_MEMORY;
+    if (cudaMalloc(&s->staging, (size_t)s->staging_bytes) != cudaSuccess) return MP_ERR_NO_MEMORY;
+    if (cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)kMaxCounters) != cudaSuccess) return MP_ERR_CUDA;
+    if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
+    if (cudaFuncSetAttribute(dev::k_poly_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+        cudaSuccess)
+        return MP_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
+    return MP_OK;
+}
+
+void device_destroy(mp_handle h) {
+    DeviceState* s = h->dev;
+    if (!s) return;
+    {
+        DeviceGuard g(s->device);
+        cudaDeviceSynchronize();
+        cudaFree(s->ws);
+        cudaFree(s->cnt);
+        cudaFree(s->err);
+        cudaFree(s->staging);
+    }
+    delete s;
+    h->dev = nullptr;
+}
+
+mp_status device_check(mp_handle h, void* stream) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    DeviceGuard g(s->device);
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MP_ERR_CUDA;
+    int e = 0;
+    if (cudaMemcpy(&e, s->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MP_ERR_CUDA;
+    if (e != 0) {
+        // An aborted launch may leave split-K counters mid-count: clear them.
+        cudaMemset(s->err, 0, sizeof(int));
+        cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)kMaxCounters);
+        if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
+        return MP_ERR_DEVICE_TIMEOUT;
+    }
+    return MP_OK;
+}
+
+mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    cudaStream_t stream = (cudaStream_t)a.stream;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return MP_ERR_CUDA;
+    DeviceGuard g(s->device);  // no-op when already current
+
+    dev::Params p;
+    std::memset(&p, 0, sizeof(p));
+    const int64_t batch = a.batch, M = a.M, N = a.N, K = a.K;
+
+    // ---- operands: TMA views, repacked when rows are not 16-byte aligned ----
+    const void* A = a.A;
+    const void* B = a.B;
+    int64_t lda = a.lda, ldb = a.ldb, sA = a.strideA, sB = a.strideB;
+    int64_t bA = (batch > 1 && a.strideA != 0) ? batch : 1;
+    int64_t bB = (batch > 1 && a.strideB != 0) ? batch : 1;
+    if (K > 0) {
+        int64_t used = 0;
+        if (!tma_ok(A, lda, batch, sA)) {
+            const int64_t ld2 = round_up(K, 8), st2 = M * ld2;
+            const int64_t bytes = round_up(2 * bA * st2, 256);
+            if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
+            const int64_t chunks = bA * M * (ld2 / 8);
+            const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
+            dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(A), lda, sA, dst, ld2,
+                                                           st2, (int)M, (int)K, (int)bA);
+            if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+            A = dst;
+            lda = ld2;
+            sA = st2;
+            used += bytes;
+        }
+        if (!tma_ok(B, ldb, batch, sB)) {
+            const int64_t ld2 = round_up(N, 8), st2 = K * ld2;
+            const int64_t bytes = round_up(2 * bB * st2, 256);
+            if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
+            uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
+            const int64_t chunks = bB * K * (ld2 / 8);
+            const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
+            dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(B), ldb, sB, dst, ld2,
+                                                           st2, (int)K, (int)N, (int)bB);
+            if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+            B = dst;
+            ldb = ld2;
+            sB = st2;
+            used += bytes;
+        }
+        const uint64_t a_s2 = bA > 1 ? (uint64_t)sA * 2 : (uint64_t)round_up(M * lda * 2, 16);
+        const uint64_t b_s2 = bB > 1 ? (uint64_t)sB * 2 : (uint64_t)round_up(K * ldb * 2, 16);
+        if (!encode_3d(s->encode, &p.tmA, A, K, M, bA, lda * 2, a_s2, 64, 128) ||
+            !encode_3d(s->encode, &p.tmA16, A, K, M, bA, lda * 2, a_s2, 64, 16) ||
+            !encode_3d(s->encode, &p.tmB, B, N, K, bB, ldb * 2, b_s2, 64, 64))
+            return MP_ERR_CUDA;
+    } else {
+        // K == 0: no operand is read; the maps only have to be well formed.
+        if (!encode_3d(s->encode, &p.tmA, s->staging, 64, 128, 1, 128, 128 * 128, 64, 128) ||
+            !encode_3d(s->encode, &p.tmA16, s->staging, 64, 128, 1, 128, 128 * 128, 64, 16) ||
+            !encode_3d(s->encode, &p.tmB, s->staging, 64, 128, 1, 128, 128 * 128, 64, 64))
+            return MP_ERR_CUDA;
+    }
+    p.a_bstep = bA > 1 ? 1 : 0;
+    p.b_bstep = bB > 1 ? 1 : 0;
+
+    p.C = a.beta != 0.0f ? a.C : nullptr;
+    p.D = a.D;
+    p.ldc = a.ldc;
+    p.ldd = a.ldd;
+    p.strideC = a.strideC;
+    p.strideD = a.strideD;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.num_kb = (int)cdiv(K, kUk);
+    p.ws = s->ws;
+    p.cnt = s->cnt;
+    p.err = s->err;
+    p.inject_timeout = s->inject_timeout;
+    s->inject_timeout = 0;
+    p.wait_limit_ns = s->wait_limit_ns;
+
+    // ---- regions -> device work list ----------------------------------------
+    int64_t units = 0, ws_floats = 0, counters = 0;
+    p.num_regions = plan.num_regions;
+    for (int i = 0; i < plan.num_regions; i++) {
+        const mp_region_info& r = plan.region[i];
+        dev::Region& d = p.reg[i];
+        const int bn = r.swap ? r.um : r.un;
+        if (r.uk != kUk || bn < 16 || bn > kMaxBn || bn % 16 != 0 || (!r.swap && (r.um != 128 || bn % 64 != 0)) ||
+            (r.swap && r.un != 128))
+            return MP_ERR_PLAN;
+        d.m0 = (int)r.m0;
+        d.n0 = (int)r.n0;
+        d.m_end = (int)(r.m0 + r.m_ext);
+        d.n_end = (int)(r.n0 + r.n_ext);
+        d.tiles_m = (int)cdiv(r.m_ext, r.um);
+        d.tiles_n = (int)cdiv(r.n_ext, r.un);
+        d.bn = bn;
+        d.swap = r.swap;
+        d.splits = r.splits;
+        d.kb_per_split = K > 0 ? (int)cdiv(p.num_kb, r.splits) : 0;
+        if (K > 0 && cdiv(p.num_kb, d.kb_per_split) != r.splits) return MP_ERR_PLAN;
+        const int64_t tiles = (int64_t)d.tiles_m * d.tiles_n * batch;
+        d.unit_begin = (int)units;
+        d.units = (int)(tiles * r.splits);
+        units += tiles * r.splits;
+        d.ws_begin = ws_floats;
+        d.cnt_begin = (int)counters;
+        if (r.splits > 1) {
+            ws_floats += tiles * r.splits * 128 * bn;
+            counters += tiles;
+        }
+    }
+    if (units >= ((int64_t)1 << 31) || ws_floats > h->workspace_floats || counters > kMaxCounters)
+        return MP_ERR_PLAN;
+    p.total_units = (int)units;
+    if (units == 0) return MP_OK;
+
+    const int grid = (int)std::min<int64_t>(units, s->num_sms);
+    if (s->log) log_plan(plan, a, grid);
+    dev::k_poly_gemm<<<grid, dev::kThreads, dev::kSmemBytes, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+    return MP_OK;
+}
+
+}  // namespace mp
+
+// Test hook for the bounded waits: the next launch withholds one stage so
+// that the consumer's wait runs out after `limit_ns`; mp_check then reports
+// MP_ERR_DEVICE_TIMEOUT.  limit_ns == 0 keeps the current limit.
+extern "C" mp_status mp_inject_wait_timeout(mp_handle h, int32_t enable, int64_t limit_ns) {
+    if (!h || !h->dev || limit_ns < 0) return MP_ERR_INVALID_ARG;
+    h->dev->inject_timeout = enable ? 1 : 0;
+    if (limit_ns > 0) h->dev->wait_limit_ns = (uint64_t)limit_ns;
+    return MP_OK;
+}

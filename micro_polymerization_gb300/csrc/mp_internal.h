@@ -1,0 +1,87 @@
+// Internal declarations shared by the host planner, the C ABI and the launch
+// code.  Nothing here is exported.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mp.h"
+
+namespace mp {
+
+// Micro-kernel geometry fixed by the device code: UMMA M = 128 rows of
+// accumulator lanes, one 128-byte swizzle row of bf16 (64 elements) per K step.
+constexpr int kUmmaM = 128;
+constexpr int kUk = 64;
+constexpr int kMaxBn = 256;
+
+// Limits of the device-side bookkeeping (allocated once per handle).
+constexpr int64_t kMaxCounters = 1 << 16;          // split-K tile counters
+constexpr int64_t kDefaultWorkspaceFloats = 16ll << 20;  // 64 MiB of fp32 partials
+constexpr int64_t kDefaultStagingBytes = 1ll << 30;      // repack area for unaligned operands
+
+struct PlanKey {
+    int64_t batch, M, N, K;
+    bool operator==(const PlanKey& o) const {
+        return batch == o.batch && M == o.M && N == o.N && K == o.K;
+    }
+};
+
+struct PlanCacheEntry {
+    PlanKey key{-1, -1, -1, -1};
+    mp_plan_info plan{};
+};
+
+struct DeviceState;  // defined in the CUDA translation unit
+
+}  // namespace mp
+
+struct mp_handle_s {
+    bool host_only = true;
+    int device = -1;
+    mp_hw hw{};
+    mp_kernel_desc kernels[MP_MAX_KERNELS]{};
+    int32_t num_kernels = 0;
+
+    // Test / ablation hook (mp_force_plan).
+    int32_t force_kernel = -1;
+    int32_t force_splits = 0;
+
+    // Plan cache: shapes repeat in dynamic workloads; a hit skips the search.
+    std::vector<mp::PlanCacheEntry> cache;
+    int64_t workspace_floats = mp::kDefaultWorkspaceFloats;
+
+    mp::DeviceState* dev = nullptr;
+};
+
+namespace mp {
+
+// Planner (mp_planner.cpp).
+mp_status plan_shape(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                     mp_plan_info* out);
+void clear_plan_cache(mp_handle h);
+mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                        mp_plan_info* p);
+void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n);
+// Checks that the regions of a plan tile the M x N output exactly once and
+// satisfy the device code's alignment rules.  Returns MP_OK or MP_ERR_PLAN.
+mp_status validate_plan(const mp_plan_info& p, int64_t M, int64_t N, int64_t K);
+
+// Device side (mp_gemm.cu).
+mp_status device_init(mp_handle h, int device);
+void device_destroy(mp_handle h);
+struct GemmArgs {
+    int64_t batch, M, N, K;
+    const void* A; int64_t lda, strideA;
+    const void* B; int64_t ldb, strideB;
+    const float* C; int64_t ldc, strideC;
+    float* D; int64_t ldd, strideD;
+    float alpha, beta;
+    void* stream;
+};
+mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a);
+mp_status device_check(mp_handle h, void* stream);
+
+}  // namespace mp

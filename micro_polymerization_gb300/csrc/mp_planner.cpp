@@ -1,0 +1,428 @@
+// The polymerizer: per-shape choice of regions, micro-kernels and split-K
+// factors under the cost model of the MikPoly summary, section 3
+// ("polymerization cost model", "heuristic search").
+//
+//   Cost(S, H) = sum over regions (R_i, K~_i) of  f_wave * f_pipe
+//   f_wave     = ceil(f_parallel(R_i, K~_i) / |P_multi|)
+//   f_pipe     = g_predict(f_num(R_i, K~_i))
+//
+// f_parallel is the number of pipeline tasks of region i (its tiles times its
+// split-K factor), |P_multi| the number of tasks the machine runs at once
+// (warps per wave divided by the micro-kernel's warps), f_num the number of
+// micro-kernel instances (K steps) in one task, and g_predict the
+// micro-kernel's measured (or modelled) time for a task of f_num instances.
+//
+// Patterns (MikPoly summary, section 4: a GPU uses Patterns I and II):
+//   I   one region, the whole output, one micro-kernel;
+//   II  two regions cut along M (top / bottom) or N (left / right), each with
+//       its own micro-kernel; the first region's cut is placed so that its
+//       tasks fill whole waves, or so that it holds only full tiles.
+// The search visits strategies in a fixed order and skips a strategy as soon
+// as its running cost exceeds the best found so far.
+//
+// GB300 additions (readings, see the design notes): f_pipe also carries the
+// split-K reduction traffic, and the total is floored by the algorithmic
+// bytes over HBM bandwidth ("HBM bytes versus MMA cycles").
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+
+#include "mp_internal.h"
+
+namespace mp {
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct RegionEval {
+    int32_t kernel = -1;
+    int32_t splits = 1;
+    int32_t f_num = 0;
+    int64_t f_parallel = 0;
+    int64_t f_wave = 0;
+    double f_pipe = 0.0;
+    double cost = 0.0;
+    int64_t ws_floats = 0;
+    bool ok = false;
+};
+
+inline int64_t slots_for(const mp_handle_s* h, const mp_kernel_desc& u) {
+    int64_t s = h->hw.warps_per_wave / std::max(1, u.warps);
+    return std::max<int64_t>(1, s);
+}
+
+// g_predict(f_num) plus the split-K reduction: every task of a split tile
+// writes an fp32 partial and the last task of the tile reads all of them.
+inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f_num, int64_t splits) {
+    double t = u.fixed_us + u.per_step_us * (double)f_num;
+    if (splits > 1 && h->hw.l2_gbs > 0 && h->hw.num_pe > 0) {
+        double tile_bytes = 4.0 * u.um * u.un;
+        double pe_gbs = h->hw.l2_gbs / h->hw.num_pe;
+        t += 2.0 * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
+    }
+    return t;
+}
+
+RegionEval eval_region(const mp_handle_s* h, int32_t k, int64_t m_ext, int64_t n_ext, int64_t K,
+                       int64_t batch, int32_t splits_req) {
+    RegionEval r;
+    const mp_kernel_desc& u = h->kernels[k];
+    int64_t tiles = cdiv(m_ext, u.um) * cdiv(n_ext, u.un) * batch;
+    int64_t kb = cdiv(K, u.uk);
+    int64_t splits = 1, f_num = kb;
+    if (kb > 0 && splits_req > 1) {
+        f_num = cdiv(kb, std::min<int64_t>(splits_req, kb));
+        splits = cdiv(kb, f_num);  // no empty split
+    }
+    r.kernel = k;
+    r.splits = (int32_t)splits;
+    r.f_num = (int32_t)f_num;
+    r.f_parallel = tiles * splits;
+    r.f_wave = cdiv(r.f_parallel, slots_for(h, u));
+    r.f_pipe = f_pipe_of(h, u, f_num, splits);
+    r.cost = (double)r.f_wave * r.f_pipe;
+    r.ws_floats = splits > 1 ? tiles * splits * (int64_t)u.um * u.un : 0;
+    r.ok = splits == 1 || (r.ws_floats <= h->workspace_floats && tiles <= kMaxCounters);
+    return r;
+}
+
+// Split-K candidates for a region of `tiles` tiles: none, and the factors
+// that bring the task count to about one or two waves.
+int split_candidates(const mp_handle_s* h, const mp_kernel_desc& u, int64_t tiles, int64_t kb,
+                     int32_t* out) {
+    int n = 0;
+    out[n++] = 1;
+    if (kb <= 1 || tiles <= 0) return n;
+    int64_t slots = slots_for(h, u);
+    if (tiles >= slots) return n;
+    static const int32_t kFactors[] = {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64};
+    for (int32_t s : kFactors) {
+        if (s > kb) break;
+        if (tiles * s > 2 * slots) break;
+        out[n++] = s;
+    }
+    int64_t fill = std::min<int64_t>(kb, std::max<int64_t>(1, slots / tiles));
+    if (fill > 1) out[n++] = (int32_t)fill;
+    return n;
+}
+
+struct Strategy {
+    int32_t pattern = 0;
+    int32_t nreg = 0;
+    int64_t m0[2], n0[2], m_ext[2], n_ext[2];
+    RegionEval ev[2];
+    double sum = 0.0;   // sum of f_wave * f_pipe
+    double cost = 0.0;  // max(sum, HBM floor)
+};
+
+inline double tile_area(const mp_handle_s* h, const Strategy& s) {
+    double a = 0.0;
+    for (int i = 0; i < s.nreg; i++) {
+        const mp_kernel_desc& u = h->kernels[s.ev[i].kernel];
+        a += (double)u.um * u.un * (double)(s.m_ext[i] * s.n_ext[i]);
+    }
+    return a;
+}
+
+// Is `c` better than `b`?  Costs within 0.5% tie; ties go to fewer regions,
+// then to the smaller work sum (more slack under the HBM floor), then to
+// larger tiles, then to less split-K.
+bool better(const mp_handle_s* h, const Strategy& c, const Strategy& b) {
+    if (b.nreg == 0) return true;
+    double tol = 0.005 * std::max(c.cost, b.cost);
+    if (c.cost < b.cost - tol) return true;
+    if (c.cost > b.cost + tol) return false;
+    if (c.nreg != b.nreg) return c.nreg < b.nreg;
+    if (std::fabs(c.sum - b.sum) > 0.005 * std::max(c.sum, b.sum)) return c.sum < b.sum;
+    double ta = tile_area(h, c), tb = tile_area(h, b);
+    if (ta != tb) return ta > tb;
+    int sc = 0, sb = 0;
+    for (int i = 0; i < c.nreg; i++) sc += c.ev[i].splits;
+    for (int i = 0; i < b.nreg; i++) sb += b.ev[i].splits;
+    return sc < sb;
+}
+
+double hbm_floor_us(const mp_handle_s* h, int64_t batch, int64_t M, int64_t N, int64_t K, bool beta_c) {
+    if (h->hw.hbm_gbs <= 0) return 0.0;
+    double bytes = 2.0 * M * K + 2.0 * K * N + 4.0 * M * N + (beta_c ? 4.0 * M * N : 0.0);
+    return bytes * (double)batch / (h->hw.hbm_gbs * 1e3);
+}
+
+void fill_info(const mp_handle_s* h, const Strategy& s, int64_t K, mp_plan_info* out, int evaluated,
+               int pruned) {
+    std::memset(out, 0, sizeof(*out));
+    out->pattern = s.pattern;
+    out->num_regions = s.nreg;
+    out->cost_us = s.cost;
+    out->evaluated = evaluated;
+    out->pruned = pruned;
+    for (int i = 0; i < s.nreg; i++) {
+        const RegionEval& e = s.ev[i];
+        const mp_kernel_desc& u = h->kernels[e.kernel];
+        mp_region_info& r = out->region[i];
+        r.kernel = e.kernel;
+        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap;
+        r.m0 = s.m0[i]; r.n0 = s.n0[i]; r.m_ext = s.m_ext[i]; r.n_ext = s.n_ext[i];
+        r.splits = e.splits;
+        r.f_num = e.f_num;
+        r.f_parallel = e.f_parallel;
+        r.f_wave = e.f_wave;
+        r.f_pipe_us = e.f_pipe;
+        out->total_tasks += e.f_parallel;
+        out->workspace_bytes += 4 * e.ws_floats;
+    }
+    (void)K;
+}
+
+mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp_plan_info* out) {
+    const double floor_us = hbm_floor_us(h, batch, M, N, K, false);
+    Strategy best;
+    int evaluated = 0, pruned = 0;
+    auto finish = [&](Strategy& s) {
+        s.sum = 0.0;
+        for (int i = 0; i < s.nreg; i++) s.sum += s.ev[i].cost;
+        s.cost = std::max(s.sum, floor_us);
+        evaluated++;
+        if (better(h, s, best)) best = s;
+    };
+
+    // ---- Pattern I: one micro-kernel over the whole output -------------------
+    double single_cost[MP_MAX_KERNELS];
+    for (int32_t k = 0; k < h->num_kernels; k++) {
+        single_cost[k] = INFINITY;
+        if (h->force_kernel >= 0 && k != h->force_kernel) continue;
+        const mp_kernel_desc& u = h->kernels[k];
+        int64_t tiles = cdiv(M, u.um) * cdiv(N, u.un) * batch;
+        int32_t cands[16];
+        int nc;
+        if (h->force_splits > 0) {
+            cands[0] = h->force_splits;
+            nc = 1;
+        } else {
+            nc = split_candidates(h, u, tiles, cdiv(K, u.uk), cands);
+        }
+        for (int c = 0; c < nc; c++) {
+            RegionEval e = eval_region(h, k, M, N, K, batch, cands[c]);
+            if (!e.ok) { pruned++; continue; }
+            Strategy s;
+            s.pattern = 1;
+            s.nreg = 1;
+            s.m0[0] = 0; s.n0[0] = 0; s.m_ext[0] = M; s.n_ext[0] = N;
+            s.ev[0] = e;
+            finish(s);
+            single_cost[k] = std::min(single_cost[k], e.cost);
+        }
+    }
+    if (h->force_kernel >= 0 || h->force_splits > 0) {
+        if (best.nreg == 0) return MP_ERR_PLAN;
+        fill_info(h, best, K, out, evaluated, pruned);
+        return MP_OK;
+    }
+
+    // ---- Pattern II: two regions cut along M or along N ----------------------
+    // First-region kernels: the three best single-kernel choices.
+    int32_t order[MP_MAX_KERNELS];
+    for (int32_t k = 0; k < h->num_kernels; k++) order[k] = k;
+    std::sort(order, order + h->num_kernels,
+              [&](int32_t a, int32_t b) { return single_cost[a] < single_cost[b]; });
+    const int n_first = std::min<int32_t>(3, h->num_kernels);
+
+    for (int dir = 0; dir < 2; dir++) {  // 0: cut along M, 1: cut along N
+        const int64_t along = dir == 0 ? M : N;
+        const int64_t across = dir == 0 ? N : M;
+        for (int ia = 0; ia < n_first; ia++) {
+            const int32_t a = order[ia];
+            if (!std::isfinite(single_cost[a])) continue;
+            const mp_kernel_desc& ua = h->kernels[a];
+            const int64_t step = dir == 0 ? ua.um : ua.un;
+            const int64_t blocks_across = cdiv(across, dir == 0 ? ua.un : ua.um) * batch;
+            const int64_t slots = slots_for(h, ua);
+            const int64_t total_blocks = cdiv(along, step);
+            // Cut candidates (in blocks of the first kernel): whole waves, and
+            // the largest cut that keeps only full tiles in the first region.
+            int64_t cuts[8];
+            int ncut = 0;
+            const int64_t waves = cdiv(total_blocks * blocks_across, slots);
+            for (int64_t w = 1; w < waves && ncut < 6; w++) {
+                int64_t blocks = (w * slots) / blocks_across;
+                if (blocks >= 1 && blocks < total_blocks) cuts[ncut++] = blocks;
+            }
+            if (along % step != 0 && along / step >= 1) cuts[ncut++] = along / step;
+            for (int ic = 0; ic < ncut; ic++) {
+                const int64_t cut = cuts[ic] * step;
+                if (cut <= 0 || cut >= along) continue;
+                // First region: no split (its tasks fill whole waves).
+                RegionEval ea = dir == 0 ? eval_region(h, a, cut, N, K, batch, 1)
+                                         : eval_region(h, a, M, cut, K, batch, 1);
+                if (!ea.ok) continue;
+                if (std::max(ea.cost, floor_us) > best.cost * 1.005) { pruned++; continue; }
+                const int64_t rest = along - cut;
+                for (int32_t b = 0; b < h->num_kernels; b++) {
+                    const mp_kernel_desc& ub = h->kernels[b];
+                    if (dir == 1 && ub.un % 8 != 0) continue;
+                    int64_t rm = dir == 0 ? rest : M, rn = dir == 0 ? N : rest;
+                    int64_t tiles_b = cdiv(rm, ub.um) * cdiv(rn, ub.un) * batch;
+                    int64_t kb = cdiv(K, ub.uk);
+                    int32_t sb[2] = {1, 1};
+                    int nsb = 1;
+                    int64_t sl = slots_for(h, ub);
+                    if (tiles_b < sl && kb > 1) {
+                        sb[1] = (int32_t)std::min<int64_t>(kb, std::max<int64_t>(1, sl / tiles_b));
+                        if (sb[1] > 1) nsb = 2;
+                    }
+                    for (int is = 0; is < nsb; is++) {
+                        RegionEval eb = eval_region(h, b, rm, rn, K, batch, sb[is]);
+                        if (!eb.ok) { pruned++; continue; }
+                        if (std::max(ea.cost + eb.cost, floor_us) > best.cost * 1.005) {
+                            pruned++;
+                            continue;
+                        }
+                        Strategy s;
+                        s.pattern = 2;
+                        s.nreg = 2;
+                        if (dir == 0) {
+                            s.m0[0] = 0; s.n0[0] = 0; s.m_ext[0] = cut; s.n_ext[0] = N;
+                            s.m0[1] = cut; s.n0[1] = 0; s.m_ext[1] = rest; s.n_ext[1] = N;
+                        } else {
+                            s.m0[0] = 0; s.n0[0] = 0; s.m_ext[0] = M; s.n_ext[0] = cut;
+                            s.m0[1] = 0; s.n0[1] = cut; s.m_ext[1] = M; s.n_ext[1] = rest;
+                        }
+                        s.ev[0] = ea;
+                        s.ev[1] = eb;
+                        finish(s);
+                    }
+                }
+            }
+        }
+    }
+    if (best.nreg == 0) return MP_ERR_PLAN;
+    fill_info(h, best, K, out, evaluated, pruned);
+    return MP_OK;
+}
+
+inline size_t cache_slot(const PlanKey& k, size_t n) {
+    uint64_t x = (uint64_t)k.M * 0x9E3779B97F4A7C15ull ^ (uint64_t)k.N * 0xC2B2AE3D27D4EB4Full ^
+                 (uint64_t)k.K * 0x165667B19E3779F9ull ^ (uint64_t)k.batch * 0x27D4EB2F165667C5ull;
+    x ^= x >> 29;
+    return (size_t)(x % n);
+}
+
+}  // namespace
+
+void clear_plan_cache(mp_handle h) {
+    for (auto& e : h->cache) e.key = PlanKey{-1, -1, -1, -1};
+}
+
+mp_status plan_shape(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp_plan_info* out) {
+    if (!h || !out) return MP_ERR_INVALID_ARG;
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return MP_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || batch == 0) {
+        std::memset(out, 0, sizeof(*out));
+        out->pattern = 1;
+        return MP_OK;
+    }
+    PlanKey key{batch, M, N, K};
+    if (!h->cache.empty()) {
+        PlanCacheEntry& e = h->cache[cache_slot(key, h->cache.size())];
+        if (e.key == key) {
+            *out = e.plan;
+            return MP_OK;
+        }
+    }
+    mp_status st = search(h, batch, M, N, K, out);
+    if (st != MP_OK) return st;
+    st = validate_plan(*out, M, N, K);
+    if (st != MP_OK) return st;
+    if (!h->cache.empty()) {
+        PlanCacheEntry& e = h->cache[cache_slot(key, h->cache.size())];
+        e.key = key;
+        e.plan = *out;
+    }
+    return MP_OK;
+}
+
+mp_status validate_plan(const mp_plan_info& p, int64_t M, int64_t N, int64_t K) {
+    (void)K;
+    if (p.num_regions < 1 || p.num_regions > MP_MAX_REGIONS) return MP_ERR_PLAN;
+    int64_t area = 0;
+    for (int i = 0; i < p.num_regions; i++) {
+        const mp_region_info& r = p.region[i];
+        if (r.m_ext <= 0 || r.n_ext <= 0 || r.m0 < 0 || r.n0 < 0) return MP_ERR_PLAN;
+        if (r.m0 + r.m_ext > M || r.n0 + r.n_ext > N) return MP_ERR_PLAN;
+        if (r.n0 % 8 != 0) return MP_ERR_PLAN;  // TMA x coordinate rule on B
+        if (r.splits < 1) return MP_ERR_PLAN;
+        area += r.m_ext * r.n_ext;
+        for (int j = 0; j < i; j++) {
+            const mp_region_info& q = p.region[j];
+            bool apart = r.m0 >= q.m0 + q.m_ext || q.m0 >= r.m0 + r.m_ext ||
+                         r.n0 >= q.n0 + q.n_ext || q.n0 >= r.n0 + r.n_ext;
+            if (!apart) return MP_ERR_PLAN;
+        }
+    }
+    return area == M * N ? MP_OK : MP_ERR_PLAN;
+}
+
+mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                        mp_plan_info* p) {
+    if (!h || !p || batch < 1 || M < 1 || N < 1 || K < 0) return MP_ERR_INVALID_ARG;
+    if (p->num_regions < 1 || p->num_regions > MP_MAX_REGIONS) return MP_ERR_INVALID_ARG;
+    double sum = 0.0;
+    p->total_tasks = 0;
+    p->workspace_bytes = 0;
+    for (int i = 0; i < p->num_regions; i++) {
+        mp_region_info& r = p->region[i];
+        if (r.kernel < 0 || r.kernel >= h->num_kernels) return MP_ERR_INVALID_ARG;
+        RegionEval e = eval_region(h, r.kernel, r.m_ext, r.n_ext, K, batch, std::max(1, r.splits));
+        const mp_kernel_desc& u = h->kernels[r.kernel];
+        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap;
+        r.splits = e.splits;
+        r.f_num = e.f_num;
+        r.f_parallel = e.f_parallel;
+        r.f_wave = e.f_wave;
+        r.f_pipe_us = e.f_pipe;
+        sum += e.cost;
+        p->total_tasks += e.f_parallel;
+        p->workspace_bytes += 4 * e.ws_floats;
+    }
+    p->cost_us = std::max(sum, hbm_floor_us(h, batch, M, N, K, false));
+    if (p->pattern == 0) p->pattern = p->num_regions == 1 ? 1 : 2;
+    return validate_plan(*p, M, N, K);
+}
+
+// The GB300 micro-kernel set and its analytic g_predict (used until a
+// calibration table replaces it).  Normal kernels: a 128-row accumulator
+// (UMMA M = 128) against un = 64..256 columns of B.  Swapped kernels compute
+// D^T = B^T A^T: the UMMA M = 128 runs over N and the short M becomes the
+// UMMA N (16..128), so a skinny M wastes no tensor-core rows.
+void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
+    struct G { int um, un, swap; };
+    static const G kSet[] = {
+        {128, 256, 0}, {128, 192, 0}, {128, 128, 0}, {128, 64, 0},
+        {16, 128, 1},  {32, 128, 1},  {64, 128, 1},  {128, 128, 1},
+    };
+    const double pe = std::max(1, hw.num_pe);
+    const double mma_pe = hw.mma_tflops > 0 ? hw.mma_tflops / pe : 13.0;   // TFLOP/s per PE
+    const double l2_pe = hw.l2_gbs > 0 ? hw.l2_gbs / pe : 120.0;          // GB/s per PE
+    const double hbm_pe = hw.hbm_gbs > 0 ? hw.hbm_gbs / pe : 45.0;
+    int32_t c = 0;
+    for (const G& g : kSet) {
+        mp_kernel_desc& d = out[c++];
+        d.um = g.um;
+        d.un = g.un;
+        d.uk = kUk;
+        d.warps = 6;  // one CTA of 6 warps per SM: one task slot per PE
+        d.swap = g.swap;
+        const double n_umma = g.swap ? g.um : g.un;
+        const double flops = 2.0 * kUmmaM * std::max(32.0, n_umma) * kUk;
+        const double mma_us = flops / (mma_pe * 1e6);
+        const double bytes = (kUmmaM + n_umma) * kUk * 2.0;
+        const double load_us = bytes / (l2_pe * 1e3);
+        d.per_step_us = std::max(mma_us, load_us);
+        const double epi_bytes = 4.0 * g.um * g.un;
+        d.fixed_us = 0.6 + 0.5 * epi_bytes / (hbm_pe * 1e3);
+    }
+    *n = c;
+}
+
+}  // namespace mp

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every symbol include/mp.h declares, and
+rejects bad arguments with status codes (no GPU needed: a planning-only
+handle checks arguments before it would launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import micro_polymerization_gb300 as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:mp_status|const char\*)\s+(mp_\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mp_init", "mp_destroy", "mp_plan", "mp_gemm", "mp_gemm_batched", "mp_status_string"):
+        assert required in names
+
+
+@pytest.mark.parametrize("name", declared_functions())
+def test_library_exports_every_declared_symbol(name):
+    lib = mp.library()
+    assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code in range(0, -7, -1):
+        s = mp.mp_status_string(code)
+        assert s and s != "unknown status"
+    assert mp.mp_status_string(-99) == "unknown status"
+
+
+def _host():
+    hw = mp.MpHw(num_pe=148, warps_per_wave=888, local_mem_bytes=232448, shared_mem_bytes=1 << 27,
+                 hbm_gbs=6684.0, l2_gbs=20000.0, mma_tflops=1974.0)
+    return mp.mp_init_host(hw)
+
+
+def test_argument_checks_before_launch():
+    lib = mp.library()
+    h = _host()
+    A, B, C, D = 0x10000, 0x20000000, 0x30000000, 0x40000000  # never dereferenced
+    g = lambda *a: lib.mp_gemm(h.ptr, *a)
+    # valid request on a planning-only handle: unsupported, not invalid
+    assert g(64, 64, 64, A, 64, B, 64, C, 64, D, 64, 1.0, 1.0, None) == mp.MP_ERR_UNSUPPORTED
+    assert g(-1, 64, 64, A, 64, B, 64, C, 64, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    assert g(64, 64, 64, A, 63, B, 64, C, 64, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG  # lda < K
+    assert g(64, 64, 64, A, 64, B, 63, C, 64, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG  # ldb < N
+    assert g(64, 64, 64, A, 64, B, 64, C, 64, D, 63, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG  # ldd < N
+    assert g(64, 64, 64, A, 64, B, 64, None, 64, D, 64, 1.0, 0.5, None) == mp.MP_ERR_INVALID_ARG  # beta, no C
+    assert g(64, 64, 64, None, 64, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    assert g(64, 64, 64, A, 64, B, 64, None, 0, None, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    assert g(64, 64, 64, A + 1, 64, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG  # odd bf16
+    assert g(64, 64, 64, A, 64, B, 64, None, 0, D + 2, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG  # fp32 align
+    # D overlapping A
+    assert g(64, 64, 64, A, 64, B, 64, None, 0, A + 64, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    # D == C in place is fine (only with ldc == ldd)
+    assert g(64, 64, 64, A, 64, B, 64, D, 64, D, 64, 1.0, 1.0, None) == mp.MP_ERR_UNSUPPORTED
+    assert g(64, 64, 64, A, 64, B, 64, D, 80, D, 64, 1.0, 1.0, None) == mp.MP_ERR_INVALID_ARG
+    # beta == 0 never needs C; empty problems are no-ops even here
+    assert g(0, 64, 64, A, 64, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_OK
+    assert g(64, 0, 64, A, 64, B, 1, None, 0, D, 1, 1.0, 0.0, None) == mp.MP_OK
+    # batched: overlapping D blocks are rejected
+    gb = lambda *a: lib.mp_gemm_batched(h.ptr, *a)
+    assert gb(3, 8, 8, 8, A, 8, 64, B, 8, 64, None, 0, 0, D, 8, 32, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    assert gb(3, 8, 8, 8, A, 8, 64, B, 8, 64, None, 0, 0, D, 8, 64, 1.0, 0.0, None) == mp.MP_ERR_UNSUPPORTED
+    assert gb(3, 8, 8, 8, A, 8, -1, B, 8, 64, None, 0, 0, D, 8, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    h.close()
+
+
+def test_null_handle_and_host_init_errors():
+    lib = mp.library()
+    assert lib.mp_plan(None, 1, 1, 1, None) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_destroy(None) == mp.MP_OK
+    out = ctypes.c_void_p()
+    assert lib.mp_init_host(ctypes.byref(out), None, None, 0) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_init(None, 0, None) == mp.MP_ERR_INVALID_ARG
+
+
+def test_mp_init_without_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    out = ctypes.c_void_p()
+    st = mp.library().mp_init(ctypes.byref(out), 0, None)
+    assert st in (mp.MP_ERR_UNSUPPORTED, mp.MP_ERR_CUDA) and not out.value

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bound (bf16 inputs, fp32 accumulation, fp32 output), element by element:
+    |D - D_ref| <= 2e-3 * (sum_k |A_ik||B_kj| + |beta*C_ij|)
+Integer-valued inputs make every fp32 partial sum exact, so there the GPU
+result must equal the oracle bit for bit, whatever the tile order or split-K.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import micro_polymerization_gb300 as mp
+from micro_polymerization_gb300 import workloads as wl
+
+from gpu_util import assert_parity, assert_sampled_parity, handle, oracle_full, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+def rand_problem(M, N, K, seed, beta=0.0):
+    g = wl.Gemm(M, N, K, alpha=1.0, beta=beta, seed=seed)
+    return wl.make_operands(g)
+
+
+# --------------------------------------------------------------------------
+# small shapes: brute force over every combination of tiny sizes
+# --------------------------------------------------------------------------
+TINY = [1, 2, 3, 5, 8, 9]
+
+
+def test_tiny_shapes_bruteforce():
+    for M, N, K in itertools.product(TINY, TINY, TINY):
+        A, B, C = rand_problem(M, N, K, seed=M * 100 + N * 10 + K, beta=0.5)
+        D = run_gemm(A, B, C, 1.5, 0.5)
+        assert_parity(D, A, B, C, 1.5, 0.5, what=f"{(M, N, K)}")
+
+
+EDGE = [1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 257]
+
+
+@pytest.mark.parametrize("M", EDGE)
+def test_edge_shapes_integer_exact(M):
+    """Tile edges in M, N and K with integer data: bitwise equal to the oracle."""
+    rng = np.random.default_rng(M)
+    for N in rng.choice(EDGE, 4, replace=False):
+        for K in rng.choice([1, 63, 64, 65, 128, 129, 300], 2, replace=False):
+            A, B, C = wl.integer_operands(M, int(N), int(K), seed=int(M * 7 + N * 3 + K))
+            D = run_gemm(A, B, C, 1.0, 1.0)
+            Dref, _ = oracle_full(A, B, C, 1.0, 1.0)
+            assert np.array_equal(D.numpy().astype(np.float64), Dref), (M, N, K)
+
+
+def test_identity_b_gives_a_exactly():
+    for M, K in [(1, 64), (100, 128), (129, 200), (300, 72)]:
+        A, _, _ = rand_problem(M, K, K, seed=M + K)
+        eye = torch.eye(K, dtype=torch.bfloat16)
+        D = run_gemm(A, eye, None, 1.0, 0.0)
+        assert torch.equal(D, A.float()), (M, K)
+
+
+def test_permutation_b_permutes_columns():
+    M, K = 77, 136
+    A, _, _ = rand_problem(M, K, K, seed=3)
+    perm = torch.randperm(K, generator=torch.Generator().manual_seed(1))
+    P = torch.zeros(K, K, dtype=torch.bfloat16)
+    P[perm, torch.arange(K)] = 1
+    D = run_gemm(A, P, None, 1.0, 0.0)
+    assert torch.equal(D, A.float()[:, perm])
+
+
+def test_closed_form_ones():
+    for M, N, K in [(33, 70, 129), (5, 300, 1000), (200, 17, 64)]:
+        A = torch.ones(M, K, dtype=torch.bfloat16)
+        B = torch.ones(K, N, dtype=torch.bfloat16)
+        C = torch.arange(M * N, dtype=torch.float32).reshape(M, N) % 7
+        D = run_gemm(A, B, C, 1.5, 0.5)
+        assert torch.equal(D, 1.5 * K + 0.5 * C), (M, N, K)
+
+
+# --------------------------------------------------------------------------
+# every micro-kernel of the set, with and without split-K
+# --------------------------------------------------------------------------
+def _kernels():
+    hw, ks = mp.mp_get_hw(handle())
+    return ks
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_each_micro_kernel(splits):
+    h = handle()
+    ks = _kernels()
+    try:
+        for k, desc in enumerate(ks):
+            for (M, N, K) in [(200, 300, 500), (37, 520, 130), (130, 129, 64)]:
+                mp.mp_force_plan(h, k, splits)
+                A, B, C = rand_problem(M, N, K, seed=k * 31 + M, beta=0.5)
+                D = run_gemm(A, B, C, 1.5, 0.5)
+                assert_parity(D, A, B, C, 1.5, 0.5,
+                              what=f"kernel {k} ({desc.um}x{desc.un} swap={desc.swap}) splits={splits} {(M, N, K)}")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
+def test_split_k_integer_exact_and_deterministic():
+    h = handle()
+    A, B, C = wl.integer_operands(105, 1024, 4000, seed=9)
+    try:
+        for k in range(len(_kernels())):
+            mp.mp_force_plan(h, k, 7)
+            D1 = run_gemm(A, B, C, 1.0, 1.0)
+            D2 = run_gemm(A, B, C, 1.0, 1.0)
+            Dref, _ = oracle_full(A, B, C, 1.0, 1.0)
+            assert np.array_equal(D1.numpy().astype(np.float64), Dref), k
+            assert torch.equal(D1, D2)
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
+def test_repeat_runs_bitwise_equal():
+    A, B, C = rand_problem(105, 1024, 12544, seed=1000, beta=1.0)
+    D1 = run_gemm(A, B, C, 1.0, 1.0)
+    D2 = run_gemm(A, B, C, 1.0, 1.0)
+    assert torch.equal(D1, D2)
+
+
+# --------------------------------------------------------------------------
+# layouts: padded and unaligned leading dimensions, offset pointers, in place
+# --------------------------------------------------------------------------
+def test_padded_leading_dimensions():
+    dev = torch.device("cuda", 0)
+    M, N, K = 150, 200, 260
+    A, B, C = rand_problem(M, N, K, seed=11, beta=0.5)
+    Ap = torch.zeros(M, K + 24, dtype=torch.bfloat16); Ap[:, :K] = A
+    Bp = torch.zeros(K, N + 40, dtype=torch.bfloat16); Bp[:, :N] = B
+    Cp = torch.zeros(M, N + 8); Cp[:, :N] = C
+    Dp = torch.full((M, N + 12), 7.0, device=dev)
+    mp.mp_gemm(handle(), Ap.to(dev)[:, :K], Bp.to(dev)[:, :N], Cp.to(dev)[:, :N], Dp[:, :N], 1.5, 0.5)
+    torch.cuda.synchronize()
+    Dp = Dp.cpu()
+    assert torch.all(Dp[:, N:] == 7.0), "write past the row end"
+    assert_parity(Dp[:, :N].contiguous(), A, B, C, 1.5, 0.5, what="padded ld")
+
+
+@pytest.mark.parametrize("M,N,K", [(31, 45, 77), (130, 257, 1001), (5, 1023, 333), (300, 9, 12001)])
+def test_unaligned_rows_are_repacked(M, N, K):
+    """Dense odd leading dimensions (rows not 16-byte aligned)."""
+    A, B, C = rand_problem(M, N, K, seed=M + N + K, beta=0.5)
+    D = run_gemm(A, B, C, 1.5, 0.5)
+    assert_parity(D, A, B, C, 1.5, 0.5, what=f"unaligned {(M, N, K)}")
+
+
+def test_offset_base_pointers():
+    dev = torch.device("cuda", 0)
+    M, N, K = 70, 96, 128
+    A, B, C = rand_problem(M, N, K, seed=5, beta=0.5)
+    Abuf = torch.zeros(M * K + 3, dtype=torch.bfloat16, device=dev)
+    Bbuf = torch.zeros(K * N + 5, dtype=torch.bfloat16, device=dev)
+    Aview = Abuf[1:1 + M * K].view(M, K); Aview.copy_(A.to(dev))
+    Bview = Bbuf[3:3 + K * N].view(K, N); Bview.copy_(B.to(dev))
+    D = torch.empty(M, N, device=dev)
+    mp.mp_gemm(handle(), Aview, Bview, C.to(dev), D, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert_parity(D.cpu(), A, B, C, 1.5, 0.5, what="offset pointers")
+
+
+def test_in_place_c_equals_d():
+    dev = torch.device("cuda", 0)
+    A, B, C = rand_problem(129, 140, 200, seed=8, beta=0.5)
+    CD = C.to(dev).clone()
+    mp.mp_gemm(handle(), A.to(dev), B.to(dev), CD, CD, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert_parity(CD.cpu(), A, B, C, 1.5, 0.5, what="in place")
+
+
+def test_k_zero_and_empty():
+    dev = torch.device("cuda", 0)
+    C = torch.randn(33, 65)
+    A = torch.empty(33, 0, dtype=torch.bfloat16)
+    B = torch.empty(0, 65, dtype=torch.bfloat16)
+    D = torch.full((33, 65), float("nan"), device=dev)
+    mp.mp_gemm(handle(), A.to(dev), B.to(dev), C.to(dev), D, 2.0, 0.5)
+    torch.cuda.synchronize()
+    assert torch.equal(D.cpu(), 0.5 * C)
+    E = torch.full((0, 5), 1.0, device=dev)
+    mp.mp_gemm(handle(), torch.empty(0, 7, dtype=torch.bfloat16, device=dev),
+               torch.empty(7, 5, dtype=torch.bfloat16, device=dev), None, E, 1.0, 0.0)
+
+
+def test_output_guard_bands():
+    """Nothing is written outside D: canaries before, after and between rows."""
+    dev = torch.device("cuda", 0)
+    M, N, K, pad = 133, 250, 96, 64
+    A, B, _ = rand_problem(M, N, K, seed=12)
+    buf = torch.full((pad + M * (N + 3) + pad,), -12345.0, device=dev)
+    D = buf[pad:pad + M * (N + 3)].view(M, N + 3)[:, :N]
+    for k in range(len(_kernels())):
+        mp.mp_force_plan(handle(), k, 2)
+        mp.mp_gemm(handle(), A.to(dev), B.to(dev), None, D, 1.0, 0.0)
+    mp.mp_force_plan(handle(), -1, 0)
+    torch.cuda.synchronize()
+    b = buf.cpu()
+    assert torch.all(b[:pad] == -12345.0) and torch.all(b[-pad:] == -12345.0)
+    assert torch.all(b[pad:pad + M * (N + 3)].view(M, N + 3)[:, N:] == -12345.0)
+
+
+# --------------------------------------------------------------------------
+# merged GEMMs (shared operand concat; same-shape batch)
+# --------------------------------------------------------------------------
+def test_shared_operand_merge_equals_separate():
+    """A x concat(Wq, Wk, Wv) == concat(A Wq, A Wk, A Wv), bitwise on integers."""
+    A, B, _ = wl.integer_operands(257, 3 * 320, 256, seed=21)
+    merged = run_gemm(A, B, None, 1.0, 0.0)
+    parts = [run_gemm(A, B[:, i * 320:(i + 1) * 320].contiguous(), None, 1.0, 0.0) for i in range(3)]
+    assert torch.equal(merged, torch.cat(parts, dim=1))
+
+
+@pytest.mark.parametrize("seq", [16, 100, 257])
+def test_batched_equals_loop(seq):
+    dev = torch.device("cuda", 0)
+    g = wl.Gemm(seq, seq, 64, batch=12, seed=seq)
+    A, B, _ = wl.make_operands(g)
+    D = torch.empty(12, seq, seq, device=dev)
+    mp.mp_gemm_batched(handle(), A.to(dev), B.to(dev), None, D, 1.0, 0.0)
+    torch.cuda.synchronize()
+    D = D.cpu()
+    for b in range(12):
+        assert_parity(D[b], A[b], B[b], None, 1.0, 0.0, what=f"batch {b}")
+    Ai, Bi, _ = wl.integer_operands(seq, seq, 64, seed=seq)
+    Ab = torch.stack([Ai] * 3); Bb = torch.stack([Bi, -Bi, Bi])
+    Db = torch.empty(3, seq, seq, device=dev)
+    mp.mp_gemm_batched(handle(), Ab.to(dev), Bb.to(dev), None, Db, 1.0, 0.0)
+    torch.cuda.synchronize()
+    single = run_gemm(Ai, Bi, None, 1.0, 0.0)
+    assert torch.equal(Db[0].cpu(), single) and torch.equal(Db[1].cpu(), -single)
+
+
+def test_batched_shared_operand_stride_zero():
+    dev = torch.device("cuda", 0)
+    A, B, _ = rand_problem(64, 80, 96, seed=4)
+    Bs = torch.stack([B, 2 * B, -B])
+    D = torch.empty(3, 64, 80, device=dev)
+    mp.mp_gemm_batched(handle(), A.to(dev).unsqueeze(0), Bs.to(dev), None, D, 1.0, 0.0)
+    torch.cuda.synchronize()
+    for b in range(3):
+        assert_parity(D[b].cpu(), A, Bs[b], None, 1.0, 0.0, what=f"shared A, batch {b}")
+
+
+# --------------------------------------------------------------------------
+# the workloads at full size (sampled where the oracle cannot do all of it)
+# --------------------------------------------------------------------------
+def test_single_skinny_full_oracle():
+    g = wl.single_skinny()[0]
+    A, B, C = wl.make_operands(g)
+    D = run_gemm(A, B, C, g.alpha, g.beta)
+    assert_parity(D, A, B, C, g.alpha, g.beta, what="(105,1024,12544)")
+
+
+@pytest.mark.parametrize("name,count", [("dynamic_sequence", 6), ("dynamic_resolution", 4),
+                                        ("merged_qkv", 4), ("stress", 12)])
+def test_workload_samples_full_size(name, count):
+    rng = np.random.default_rng(len(name))
+    shapes = wl.workload(name)
+    picks = [shapes[i] for i in rng.choice(len(shapes), count, replace=False)]
+    if name == "stress":
+        picks.append(shapes[-1])  # 4096^3
+    dev = torch.device("cuda", 0)
+    for g in picks:
+        A, B, C = wl.make_operands(g, device=dev)
+        D = torch.empty(g.M, g.N, device=dev)
+        mp.mp_gemm(handle(), A, B, C, D, g.alpha, g.beta)
+        torch.cuda.synchronize()
+        assert_sampled_parity(D.cpu(), A.cpu(), B.cpu(), C.cpu() if C is not None else None,
+                              g.alpha, g.beta, rng, what=f"{name} {(g.M, g.N, g.K)}")
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """A withheld pipeline stage makes the consumer's bounded wait expire; the
+    kernel stops cleanly, mp_check reports it, and the next call is correct."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    A, B, C = rand_problem(256, 256, 512, seed=2, beta=0.5)
+    D = torch.empty(256, 256, device=dev)
+    mp.mp_inject_wait_timeout(h, True, 50_000_000)  # 50 ms
+    mp.mp_gemm(h, A.to(dev), B.to(dev), C.to(dev), D, 1.0, 0.5)
+    assert mp.mp_check(h) == mp.MP_ERR_DEVICE_TIMEOUT
+    mp.mp_inject_wait_timeout(h, False, 1_000_000_000)
+    assert mp.mp_check(h) == mp.MP_OK
+    D2 = run_gemm(A, B, C, 1.0, 0.5)
+    assert_parity(D2, A, B, C, 1.0, 0.5, what="after timeout")

@@ -1,0 +1,158 @@
+"""Host-side tests of the polymerizer (no GPU): the pages' worked example, the
+cost formula's wave arithmetic, and the structural invariants of every plan."""
+import ctypes
+import json
+import os
+
+import numpy as np
+import pytest
+
+import micro_polymerization_gb300 as mp
+from micro_polymerization_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "case_study_4096_1024_4096.json")
+
+
+def a100_handle(Ta, Tb):
+    """H and micro-kernels of the case study: 108 SMs, 864 warps per wave;
+    GEMM-A (256,128,32) with 8 warps, GEMM-B (64,64,64) with 4 warps.  Ta and
+    Tb are the pipeline-task times at K = 4096 (f_num = 128 and 64)."""
+    hw = mp.MpHw(num_pe=108, warps_per_wave=864, local_mem_bytes=164 * 1024,
+                 shared_mem_bytes=40 * 2 ** 20, hbm_gbs=0.0, l2_gbs=0.0, mma_tflops=0.0)
+    ka = mp.MpKernelDesc(um=256, un=128, uk=32, warps=8, swap=0, fixed_us=0.0, per_step_us=Ta / 128)
+    kb = mp.MpKernelDesc(um=64, un=64, uk=64, warps=4, swap=0, fixed_us=0.0, per_step_us=Tb / 64)
+    return mp.mp_init_host(hw, [ka, kb])
+
+
+def test_case_study_wave_arithmetic():
+    gold = json.load(open(GOLDEN))
+    M, N, K = gold["shape"]
+    Ta, Tb = 10.0, 3.0
+    h = a100_handle(Ta, Tb)
+    single = mp.mp_evaluate_plan(h, 1, M, N, K, [dict(kernel=0, m0=0, n0=0, m_ext=M, n_ext=N)])
+    r = single.region[0]
+    assert r.f_parallel == gold["single_A"]["tasks"]
+    assert r.f_parallel * 8 == gold["single_A"]["warps"]
+    assert r.f_wave == gold["single_A"]["waves"]
+    assert r.f_num == 128
+    assert single.cost_us == pytest.approx(2 * Ta)
+
+    cut = gold["polymerized"]["cut_rows"]
+    poly = mp.mp_evaluate_plan(h, 1, M, N, K, [dict(kernel=0, m0=0, n0=0, m_ext=cut, n_ext=N),
+                                               dict(kernel=1, m0=cut, n0=0, m_ext=M - cut, n_ext=N)])
+    ra, rb = poly.region[0], poly.region[1]
+    assert ra.f_parallel == gold["polymerized"]["region_A"]["tasks"]
+    assert rb.f_parallel == gold["polymerized"]["region_B"]["tasks"]
+    assert ra.f_parallel * 8 == gold["polymerized"]["region_A"]["warps"]
+    assert rb.f_parallel * 4 == gold["polymerized"]["region_B"]["warps"]
+    assert ra.f_parallel * 8 + rb.f_parallel * 4 == gold["polymerized"]["total_warps"]
+    assert (ra.f_wave, rb.f_wave) == (1, 2)
+    assert ra.f_wave + rb.f_wave == gold["polymerized"]["total_waves"]
+    assert poly.cost_us == pytest.approx(Ta + 2 * Tb)
+    # The page's conclusion: polymerization wins exactly when Ta > 2 Tb.
+    assert (poly.cost_us < single.cost_us) == (Ta > 2 * Tb)
+    h.close()
+
+
+@pytest.mark.parametrize("Ta,Tb", [(10.0, 3.0), (10.0, 6.0), (10.0, 4.99), (10.0, 5.01), (8.0, 1.0)])
+def test_search_is_never_worse_than_the_pages_strategies(Ta, Tb):
+    h = a100_handle(Ta, Tb)
+    p = mp.mp_plan(h, 4096, 1024, 4096)
+    assert p.cost_us <= min(2 * Ta, Ta + 2 * Tb) + 1e-9
+    assert p.evaluated >= 2
+    h.close()
+
+
+def test_split_k_factor_and_f_num():
+    """K~ = K / splits: f_num = ceil(K~ / uk) and no split is empty."""
+    h = a100_handle(10.0, 3.0)
+    for K, splits in [(4096, 3), (100, 7), (64, 64), (65, 2)]:
+        p = mp.mp_evaluate_plan(h, 1, 256, 128, K, [dict(kernel=0, m0=0, n0=0, m_ext=256, n_ext=128,
+                                                         splits=splits)])
+        r = p.region[0]
+        kb = -(-K // 32)
+        assert r.f_num == -(-kb // splits) or r.splits < splits
+        assert (r.splits - 1) * r.f_num < kb <= r.splits * r.f_num
+        assert r.f_parallel == r.splits
+    h.close()
+
+
+def gb300_handle():
+    hw = mp.MpHw(num_pe=148, warps_per_wave=148 * 6, local_mem_bytes=232448,
+                 shared_mem_bytes=126 * 2 ** 20, hbm_gbs=6684.0, l2_gbs=20000.0, mma_tflops=1974.0)
+    return mp.mp_init_host(hw)
+
+
+def check_tiling(p, M, N):
+    cover = np.zeros((M, N), dtype=np.int32) if M * N <= 4_000_000 else None
+    area = 0
+    for r in p.regions():
+        assert r.m_ext > 0 and r.n_ext > 0 and r.m0 >= 0 and r.n0 >= 0
+        assert r.m0 + r.m_ext <= M and r.n0 + r.n_ext <= N
+        assert r.n0 % 8 == 0 and r.splits >= 1
+        area += r.m_ext * r.n_ext
+        if cover is not None:
+            cover[r.m0:r.m0 + r.m_ext, r.n0:r.n0 + r.n_ext] += 1
+    assert area == M * N
+    if cover is not None:
+        assert np.all(cover == 1)
+
+
+def test_plans_tile_the_output_exactly_once():
+    h = gb300_handle()
+    shapes = [(g.M, g.N, g.K) for name in ("stress", "dynamic_sequence", "dynamic_resolution", "merged_qkv")
+              for g in wl.workload(name)]
+    shapes += [(m, n, k) for m in (1, 7, 128, 129, 4095) for n in (1, 8, 200, 3072) for k in (0, 1, 64, 4097)]
+    for (M, N, K) in shapes:
+        p = mp.mp_plan(h, M, N, K)
+        assert p.num_regions in (1, 2)
+        check_tiling(p, M, N)
+        assert p.cost_us > 0
+    h.close()
+
+
+def test_plan_cache_returns_the_same_plan():
+    h = gb300_handle()
+    p1 = mp.mp_plan(h, 777, 3072, 1024)
+    p2 = mp.mp_plan(h, 777, 3072, 1024)
+    assert bytes(p1) == bytes(p2)
+    h.close()
+
+
+def test_skinny_huge_k_gets_split():
+    """(105, 1024, 12544): 8 tiles of 128x128 cannot fill 148 SMs without split-K."""
+    h = gb300_handle()
+    p = mp.mp_plan(h, 105, 1024, 12544)
+    assert sum(r.f_parallel for r in p.regions()) >= 72
+    assert any(r.splits > 1 for r in p.regions())
+    h.close()
+
+
+def test_forced_plan_and_errors():
+    h = gb300_handle()
+    _, ks = mp.mp_get_hw(h)
+    for k in range(len(ks)):
+        mp.mp_force_plan(h, k, 3)
+        p = mp.mp_plan(h, 300, 500, 700)
+        assert p.num_regions == 1 and p.region[0].kernel == k and p.region[0].splits == 3
+    mp.mp_force_plan(h, -1, 0)
+    with pytest.raises(mp.MPError):
+        mp.mp_force_plan(h, len(ks), 0)
+    with pytest.raises(mp.MPError):
+        mp.mp_plan(h, -1, 5, 5)
+    bad = mp.MpPlanInfo()
+    bad.num_regions = 2
+    for i, (m0, me) in enumerate([(0, 60), (50, 50)]):  # overlapping rows
+        bad.region[i].kernel, bad.region[i].m0, bad.region[i].m_ext = 0, m0, me
+        bad.region[i].n0, bad.region[i].n_ext, bad.region[i].splits = 0, 64, 1
+    st = mp.library().mp_evaluate_plan(h.ptr, 1, 100, 64, 64, ctypes.byref(bad))
+    assert st == mp.MP_ERR_PLAN
+    h.close()
+
+
+def test_empty_shapes_plan_to_nothing():
+    h = gb300_handle()
+    for M, N in [(0, 5), (5, 0), (0, 0)]:
+        p = mp.mp_plan(h, M, N, 10)
+        assert p.num_regions == 0 and p.total_tasks == 0
+    h.close()
