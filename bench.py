@@ -433,8 +433,8 @@ def cpu_baseline(args, gs, budget_s=None):
         if t_total >= budget_s:
             break
     return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(used), "kind": "oracle",
-            "sample": f"first {min(256, 'M')} rows of each of the first {done} GEMMs of the workload "
-                      f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)".replace("'M'", "M")}
+            "sample": f"first min(M, 256) rows of each of the first {done} GEMMs of the workload "
+                      f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)"}
 
 
 def run_reference(args):

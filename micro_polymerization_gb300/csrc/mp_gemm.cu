@@ -47,8 +47,9 @@ constexpr int kYBytes = 256 * 64 * 2;   // up to 256 columns x 64 K, bf16
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;          // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
+constexpr int kStageBytesEpi = 4 * 32 * 16 * 4;  // per epilogue warp: 32 rows x 16 fp32
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = kStages * (kXBytes + kYBytes) + kBarBytes + 1024;
+constexpr int kSmemBytes = kStages * (kXBytes + kYBytes) + kStageBytesEpi + kBarBytes + 1024;
 
 // Error codes written to the status word (first writer wins).
 constexpr int kErrWaitEmpty = 1;
@@ -82,6 +83,7 @@ struct alignas(128) Params {
     int total_units;
     int num_regions;
     int inject_timeout;  // test hook: withhold the first stage of the first unit
+    int vec_c, vec_d;    // C / D rows allow 16-byte vector access
     unsigned long long wait_limit_ns;
     Region reg[MP_MAX_REGIONS];
     float* ws;
@@ -340,6 +342,70 @@ __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, 
     }
 }
 
+// Four consecutive columns n..n+3 of row m of D (vector access when allowed).
+// Same arithmetic as store16: alpha*acc, then fma with beta*C.
+__device__ __forceinline__ void store4(const Params& p, const Work& w, int m, int n, float4 x) {
+    if (n >= w.n_end) return;
+    const float alpha = p.alpha, beta = p.beta;
+    float* d = p.D + (long long)w.b * p.strideD + (long long)m * p.ldd + n;
+    const float* cp = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + n;
+    float o[4] = {alpha * x.x, alpha * x.y, alpha * x.z, alpha * x.w};
+    if (p.vec_d && n + 3 < w.n_end) {
+        if (beta != 0.0f) {
+            float4 cv;
+            if (p.vec_c) {
+                cv = *reinterpret_cast<const float4*>(cp);
+            } else {
+                cv = make_float4(cp[0], cp[1], cp[2], cp[3]);
+            }
+            o[0] = fmaf(beta, cv.x, o[0]);
+            o[1] = fmaf(beta, cv.y, o[1]);
+            o[2] = fmaf(beta, cv.z, o[2]);
+            o[3] = fmaf(beta, cv.w, o[3]);
+        }
+        *reinterpret_cast<float4*>(d) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            if (n + e < w.n_end) {
+                float r = o[e];
+                if (beta != 0.0f) r = fmaf(beta, cp[e], r);
+                d[e] = r;
+            }
+        }
+    }
+}
+
+// Write accumulator columns [c, c+16) of this thread's TMEM lane to D.
+//   normal tiles (lane = row of D): the warp's 32 x 16 block is staged in
+//   shared memory -- rows of 64 B, 16-byte groups XOR-swizzled so that both
+//   the row-wise writes and the transposed reads are free of bank conflicts
+//   -- and read back so that each store instruction covers 8 rows x 64
+//   contiguous bytes instead of 32 scattered rows.
+//   swapped tiles (lane = column of D): each store already covers 32
+//   consecutive columns of one row.
+__device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
+                                       float4* stage) {
+    if (w.swap) {
+        store16(p, w, q * 32 + lane, c, v);
+        return;
+    }
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        stage[lane * 4 + (i ^ sw)] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    __syncwarp();
+    const int g = lane & 3;
+#pragma unroll
+    for (int it = 0; it < 4; it++) {
+        const int r = it * 8 + (lane >> 2);
+        const float4 x = stage[r * 4 + (g ^ ((r >> 1) & 3))];
+        const int m = w.m_t0 + q * 32 + r;
+        if (m < w.m_end) store4(p, w, m, w.n_t0 + c + 4 * g, x);
+    }
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // The persistent kernel
 // ---------------------------------------------------------------------------
@@ -350,11 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     uint8_t* gbase = smem_raw + (base - raw);
     const uint32_t xs0 = base;
     const uint32_t ys0 = base + kStages * kXBytes;
-    const uint32_t bar0 = ys0 + kStages * kYBytes;
+    const uint32_t epi0 = ys0 + kStages * kYBytes;
+    const uint32_t bar0 = epi0 + kStageBytesEpi;
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + (bar0 - base));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -378,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         mbar_init(done_bar, 1);
         *abort_flag = 0;
         *s_last = 0;
+        *epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_map(&p.tmA);
         tma_prefetch_map(&p.tmA16);
@@ -489,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         // ------------------------------ epilogue (128 threads) ----------------
         const int q = warp & 3;        // TMEM lane quarter this warp may access
         const int tl = q * 32 + lane;  // accumulator lane held by this thread
+        float4* stage = reinterpret_cast<float4*>(gbase + (epi0 - base)) + (warp - 2) * (32 * 4);
         int acc = 0;
         uint32_t aph = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -497,7 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             if (lane == 0)
                 ok = wait_bounded(accf(acc), aph, abort_flag, p.err, kErrWaitAccFull, limit, true) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            // The four epilogue warps decide together whether to stop, so that
+            // none of them is left alone at a later named barrier.  The flag
+            // is written only before the first barrier and read between the
+            // two, so no warp can see another iteration's value.
+            if (!ok && lane == 0) *epi_abort = 1;
+            named_bar_sync(1, 128);
+            const int stop = *epi_abort;
+            named_bar_sync(1, 128);
+            if (stop) break;
             tc_fence_after();
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
@@ -510,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 #pragma unroll
                         for (int j = 0; j < 16; j++) v[j] = 0.0f;
                     }
-                    store16(p, w, tl, c, v);
+                    emit16(p, w, q, lane, c, v, stage);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -548,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 #pragma unroll
                             for (int j = 0; j < 16; j++) v[j] += __ldcg(ps + (c + j) * 128 + tl);
                         }
-                        store16(p, w, tl, c, v);
+                        emit16(p, w, q, lane, c, v, stage);
                     }
                     if (threadIdx.x == 64) p.cnt[w.cnt] = 0u;  // ready for the next launch
                 }
@@ -812,6 +890,8 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     p.b_bstep = bB > 1 ? 1 : 0;
 
     p.C = a.beta != 0.0f ? a.C : nullptr;
+    p.vec_d = (((uintptr_t)a.D & 15u) == 0 && a.ldd % 4 == 0 && (batch == 1 || a.strideD % 4 == 0)) ? 1 : 0;
+    p.vec_c = (p.C && ((uintptr_t)a.C & 15u) == 0 && a.ldc % 4 == 0 && (batch == 1 || a.strideC % 4 == 0)) ? 1 : 0;
     p.D = a.D;
     p.ldc = a.ldc;
     p.ldd = a.ldd;
