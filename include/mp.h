@@ -208,6 +208,37 @@ mp_status mp_gemm_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
                           float alpha, float beta, mp_stream stream);
 
 /*
+ * D = alpha * A * B + beta * C without a handle and without allocating any
+ * device memory.  The pages have no counterpart to this call; it exists for
+ * callers that cannot call cudaMalloc: plugin interfaces of inference runtimes
+ * that own all device memory, processes that reserve device memory up front,
+ * and latency-critical loops where an allocation may synchronize the device.
+ *
+ * Same operands, layout rules and errors as mp_gemm (one problem, on the
+ * current device).  Its scratch is a fixed array inside the library, about
+ * 48 MiB on every GPU that loads the library, held until the process exits:
+ * 16 MiB of split-K partials (the planner never asks for more), 4096 tile
+ * counters, a status word, and a 32 MiB staging area for operands whose rows
+ * are not 16-byte aligned.  A request that would need more than that -- an
+ * unaligned operand above 32 MiB after padding its rows to 8 elements -- is
+ * rejected with MP_ERR_UNSUPPORTED before anything runs.
+ *
+ * The first call on a device finds the array's address and clears it with a
+ * synchronous cudaMemset; make that first call before any stream capture.
+ * Every call shares the array and starts from what the previous call left:
+ * the counters a call needs are cleared on `stream` before its kernel.  Calls
+ * whose kernels overlap on the GPU (other streams, other host threads) race
+ * on the array; issue them on one stream.  No cudaMalloc, cudaFree or other
+ * allocating routine is called.
+ */
+mp_status mp_gemm_noalloc(int64_t M, int64_t N, int64_t K,
+                          const void* A, int64_t lda,
+                          const void* B, int64_t ldb,
+                          const float* C, int64_t ldc,
+                          float* D, int64_t ldd,
+                          float alpha, float beta, mp_stream stream);
+
+/*
  * Synchronize `stream` and read the device status word: MP_OK, or
  * MP_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
  * check (the word is then cleared), or MP_ERR_CUDA.

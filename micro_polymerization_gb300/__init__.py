@@ -18,7 +18,7 @@ from . import _build
 __all__ = [
     "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched",
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
-    "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library",
+    "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
 ]
 
@@ -104,6 +104,8 @@ def library(build: bool = True) -> ctypes.CDLL:
                              _f, _f, _vp], ctypes.c_int),
                 "mp_gemm_batched": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
                                      _vp, _i64, _i64, _vp, _i64, _i64, _f, _f, _vp], ctypes.c_int),
+                "mp_gemm_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                     _f, _f, _vp], ctypes.c_int),
                 "mp_check": ([_vp, _vp], ctypes.c_int),
                 "mp_force_plan": ([_vp, _i32, _i32], ctypes.c_int),
                 "mp_get_hw": ([_vp, ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
@@ -256,6 +258,31 @@ def mp_gemm_batched(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0
                                    D.data_ptr(), _ld(D, "D"), D.stride(0),
                                    float(alpha), float(beta), _stream_ptr(stream))
     _check(st, "mp_gemm_batched")
+
+
+def mp_gemm_noalloc(A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """mp_gemm without a handle: for callers that cannot allocate device memory.
+
+    The library keeps this call's scratch in a fixed array it owns (about
+    48 MiB per GPU, held until exit); see mp_gemm_noalloc in include/mp.h.
+    Calls that overlap on the GPU share that array and race.
+    """
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or D.dtype != torch.float32:
+        raise TypeError("A and B must be bfloat16, D float32")
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-1]
+    if B.shape[-2] != K or D.shape[-2:] != (M, N):
+        raise ValueError("shape mismatch")
+    c_ptr, ldc = None, 0
+    if beta != 0.0:
+        if C is None or C.dtype != torch.float32 or C.shape[-2:] != (M, N):
+            raise ValueError("beta != 0 needs an fp32 C of D's shape")
+        c_ptr, ldc = C.data_ptr(), _ld(C, "C")
+    st = library().mp_gemm_noalloc(M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+                                   c_ptr, ldc, D.data_ptr(), _ld(D, "D"), float(alpha), float(beta),
+                                   _stream_ptr(stream))
+    _check(st, "mp_gemm_noalloc")
 
 
 def mp_check(h: Handle, stream=None) -> int:

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmp.so")
-SOURCES = ["mp_api.cpp", "mp_planner.cpp", "mp_gemm.cu"]
+SOURCES = ["mp_api.cpp", "mp_planner.cpp", "mp_gemm.cu", "mp_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "mp_internal.h"), os.path.join(ROOT, "include", "mp.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -120,6 +120,8 @@ mp_status run(mp_handle h, const mp::GemmArgs& a) {
 
 }  // namespace
 
+mp_status mp::validate_args(const mp::GemmArgs& a) { return check_args(a); }
+
 extern "C" {
 
 mp_status mp_init(mp_handle* out, int device, const char* calib_path) {

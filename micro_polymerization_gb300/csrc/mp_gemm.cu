@@ -791,6 +791,50 @@ mp_status device_init(mp_handle h, int device) {
     return MP_OK;
 }
 
+// Device state for the no-allocation entry point: the same kernels run over
+// memory the caller of this function already owns (a fixed array of the
+// library image), so nothing is allocated here.  One state per device,
+// kept in static storage; call with `device` current.
+mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_floats, unsigned int* cnt,
+                              int* err, uint8_t* staging, int64_t staging_bytes) {
+    static DeviceState fixed_states[kMaxFixedDevices];
+    if (device < 0 || device >= kMaxFixedDevices) return MP_ERR_UNSUPPORTED;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return MP_ERR_UNSUPPORTED;  // sm_103 only
+    DeviceState* s = &fixed_states[device];
+    s->device = device;
+    s->num_sms = prop.multiProcessorCount;
+    s->ws = ws;
+    s->cnt = cnt;
+    s->err = err;
+    s->staging = staging;
+    s->staging_bytes = staging_bytes;
+    s->log = std::getenv("MP_LOG") != nullptr;
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return MP_ERR_CUDA;
+    s->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (cudaFuncSetAttribute(dev::k_poly_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+        cudaSuccess)
+        return MP_ERR_CUDA;
+    h->host_only = false;
+    h->device = device;
+    h->hw.num_pe = prop.multiProcessorCount;
+    h->hw.warps_per_wave = prop.multiProcessorCount * (dev::kThreads / 32);
+    h->hw.local_mem_bytes = (int64_t)prop.sharedMemPerBlockOptin;
+    h->hw.shared_mem_bytes = (int64_t)prop.l2CacheSize;
+    h->hw.hbm_gbs = 6684.0;
+    h->hw.l2_gbs = 20000.0;
+    h->hw.mma_tflops = 1974.0;
+    h->workspace_floats = ws_floats;
+    h->dev = s;
+    return MP_OK;
+}
+
 void device_destroy(mp_handle h) {
     DeviceState* s = h->dev;
     if (!s) return;

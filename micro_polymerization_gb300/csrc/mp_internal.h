@@ -21,6 +21,7 @@ constexpr int kMaxBn = 256;
 constexpr int64_t kMaxCounters = 1 << 16;          // split-K tile counters
 constexpr int64_t kDefaultWorkspaceFloats = 16ll << 20;  // 64 MiB of fp32 partials
 constexpr int64_t kDefaultStagingBytes = 1ll << 30;      // repack area for unaligned operands
+constexpr int kMaxFixedDevices = 64;                      // devices served by the no-allocation entry point
 
 struct PlanKey {
     int64_t batch, M, N, K;
@@ -83,5 +84,9 @@ struct GemmArgs {
 };
 mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a);
 mp_status device_check(mp_handle h, void* stream);
+mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_floats, unsigned int* cnt,
+                              int* err, uint8_t* staging, int64_t staging_bytes);
+// Argument rules of mp_gemm (mp_api.cpp).
+mp_status validate_args(const GemmArgs& a);
 
 }  // namespace mp
