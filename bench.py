@@ -322,6 +322,18 @@ def run_mp(args):
         plan_us = (time.perf_counter() - t0) / len(shapes) * 1e6
         h2.close()
 
+    if args.dump and rank == 0:
+        with open(args.dump, "w") as f:
+            for g, t, tr, b in zip(gs, per_launch, troof, bounds):
+                p = mp.mp_plan_batched(h, g.batch, g.M, g.N, g.K)
+                f.write(json.dumps({
+                    "M": g.M, "N": g.N, "K": g.K, "batch": g.batch, "t_us": round(float(t), 3),
+                    "troof_us": round(float(tr), 3), "frac": round(float(tr / t), 4), "bound": b,
+                    "plan_cost_us": round(p.cost_us, 3), "regions": [
+                        {"um": r.um, "un": r.un, "swap": r.swap, "m_ext": r.m_ext, "n_ext": r.n_ext,
+                         "splits": r.splits, "tasks": r.f_parallel, "waves": r.f_wave}
+                        for r in p.regions()]}) + "\n")
+
     cpu = cpu_baseline(args, gs) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if args.sweep and rank == 0:
         sweep(args, h, peaks, dev)
@@ -471,6 +483,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mp", "reference"], default="mp")
     ap.add_argument("--workload", default="dynamic_sequence")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--dump", default=None, help="write per-GEMM time, roofline and plan (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)

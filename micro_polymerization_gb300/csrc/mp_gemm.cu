@@ -57,6 +57,7 @@ constexpr int kErrWaitFull = 2;
 constexpr int kErrWaitAccEmpty = 3;
 constexpr int kErrWaitAccFull = 4;
 constexpr int kErrDrain = 5;
+constexpr int kErrWaitSplits = 6;
 
 struct Region {
     int m0, n0, m_end, n_end;   // region bounds in D
@@ -384,12 +385,11 @@ __device__ __forceinline__ void store4(const Params& p, const Work& w, int m, in
 //   contiguous bytes instead of 32 scattered rows.
 //   swapped tiles (lane = column of D): each store already covers 32
 //   consecutive columns of one row.
-__device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
-                                       float4* stage) {
-    if (w.swap) {
-        store16(p, w, q * 32 + lane, c, v);
-        return;
-    }
+// Transpose a warp's 32 x 16 block (lane = row, v = its 16 columns) through
+// `stage` and hand it back as (row r, column group g, 4 values) so that the
+// 32 lanes of one call cover 8 rows x 4 groups.
+template <class Sink>
+__device__ __forceinline__ void transpose16(int lane, const float* v, float4* stage, Sink sink) {
     const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int i = 0; i < 4; i++)
@@ -399,11 +399,69 @@ __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, in
 #pragma unroll
     for (int it = 0; it < 4; it++) {
         const int r = it * 8 + (lane >> 2);
-        const float4 x = stage[r * 4 + (g ^ ((r >> 1) & 3))];
-        const int m = w.m_t0 + q * 32 + r;
-        if (m < w.m_end) store4(p, w, m, w.n_t0 + c + 4 * g, x);
+        sink(r, g, stage[r * 4 + (g ^ ((r >> 1) & 3))]);
     }
     __syncwarp();
+}
+
+__device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
+                                       float4* stage) {
+    if (w.swap) {
+        store16(p, w, q * 32 + lane, c, v);
+        return;
+    }
+    transpose16(lane, v, stage, [&](int r, int g, float4 x) {
+        const int m = w.m_t0 + q * 32 + r;
+        if (m < w.m_end) store4(p, w, m, w.n_t0 + c + 4 * g, x);
+    });
+}
+
+// Split-K partials are kept "D-row-major" per tile: a buffer of R rows x L
+// columns where element (r, l) belongs to D(m_t0 + r, n_t0 + l).  Normal
+// tiles: R = 128 (TMEM lanes), L = bn.  Swapped tiles: R = bn (TMEM
+// columns), L = 128 (TMEM lanes).
+__device__ __forceinline__ void park16(const Work& w, int q, int lane, int c, const float* v, float4* stage,
+                                       float* part) {
+    if (w.swap) {
+        // lane = column l of the buffer, v = rows c..c+15: 128 B per store.
+#pragma unroll
+        for (int j = 0; j < 16; j++) __stcg(part + (c + j) * 128 + q * 32 + lane, v[j]);
+        return;
+    }
+    transpose16(lane, v, stage, [&](int r, int g, float4 x) {
+        __stcg(reinterpret_cast<float4*>(part + (q * 32 + r) * w.bn + c + 4 * g), x);
+    });
+}
+
+// Rows [r0, r1) of a split tile: sum the S partials in split order and write
+// D.  Consecutive threads take consecutive 16-byte groups of a row.
+__device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, const float* tile_ws, int r0, int r1,
+                                            int tid) {
+    const int L = w.swap ? 128 : w.bn;
+    const int L4 = L / 4;
+    const long long part_floats = 128ll * w.bn;
+    const int total = (r1 - r0) * L4;
+    for (int i = tid; i < total; i += 128) {
+        const int r = r0 + i / L4;
+        const int l4 = i - (i / L4) * L4;
+        const float4* src = reinterpret_cast<const float4*>(tile_ws + (long long)r * L) + l4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < w.splits; s++) {
+            const float4 x = __ldcg(src + s * (part_floats / 4));
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+        }
+        const int m = w.m_t0 + r;
+        if (m < w.m_end) store4(p, w, m, w.n_t0 + 4 * l4, acc);
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -556,8 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         }
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
-        const int q = warp & 3;        // TMEM lane quarter this warp may access
-        const int tl = q * 32 + lane;  // accumulator lane held by this thread
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
         float4* stage = reinterpret_cast<float4*>(gbase + (epi0 - base)) + (warp - 2) * (32 * 4);
         int acc = 0;
         uint32_t aph = 0;
@@ -594,15 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce(acc));
             } else {
-                // Split-K: park this split's partial, column-major per tile
-                // (128 lanes contiguous), then the last split to arrive sums
-                // all partials in split order and runs the epilogue.
+                // Split-K: park this split's partial (D-row-major per tile),
+                // free the TMEM buffer, wait until every split of the tile
+                // has parked, then sum this split's 1/S slice of the tile's
+                // rows over all partials, in split order, and write D.
                 float* part = p.ws + w.ws_tile + (long long)w.split * (128ll * w.bn);
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
                     tmem_ld16(t + c, v);
-#pragma unroll
-                    for (int j = 0; j < 16; j++) __stcg(part + (c + j) * 128 + tl, v[j]);
+                    park16(w, q, lane, c, v, stage, part);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -610,25 +667,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (threadIdx.x == 64) {
-                    const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
-                    *s_last = (old == (unsigned)(w.splits - 1)) ? 1 : 0;
+                    unsigned int* cnt = p.cnt + w.cnt;
+                    atomicAdd(cnt, 1u);
+                    // Bounded wait for the other splits.  They are consecutive
+                    // work units on distinct CTAs, so none of them waits on
+                    // this CTA's later work.
+                    int arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits;
+                    if (!arrived) {
+                        const uint64_t t0 = globaltimer();
+                        while (!(arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits)) {
+                            if (*abort_flag) break;
+                            if (globaltimer() - t0 > limit) {
+                                *abort_flag = 1;
+                                atomicCAS(p.err, 0, kErrWaitSplits);
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    *s_last = arrived;
                 }
                 named_bar_sync(1, 128);
-                if (*s_last) {
+                const int arrived = *s_last;
+                named_bar_sync(1, 128);
+                if (arrived) {
                     __threadfence();
-                    const float* tile_ws = p.ws + w.ws_tile;
-                    for (int c = 0; c < w.bn; c += 16) {
-                        float v[16];
-#pragma unroll
-                        for (int j = 0; j < 16; j++) v[j] = 0.0f;
-                        for (int s = 0; s < w.splits; s++) {
-                            const float* ps = tile_ws + (long long)s * (128ll * w.bn);
-#pragma unroll
-                            for (int j = 0; j < 16; j++) v[j] += __ldcg(ps + (c + j) * 128 + tl);
-                        }
-                        emit16(p, w, q, lane, c, v, stage);
+                    const int R = w.swap ? w.bn : 128;
+                    const int r0 = (int)((long long)R * w.split / w.splits);
+                    const int r1 = (int)((long long)R * (w.split + 1) / w.splits);
+                    reduce_rows(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
+                    named_bar_sync(1, 128);
+                    if (threadIdx.x == 64) {
+                        // The last split to leave resets the counter for the next launch.
+                        const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
+                        if (old == 2u * (unsigned)w.splits - 1u) p.cnt[w.cnt] = 0u;
                     }
-                    if (threadIdx.x == 64) p.cnt[w.cnt] = 0u;  // ready for the next launch
+                } else if (lane == 0) {
+                    *epi_abort = 1;  // stop at the next unit (the flag is read between its barriers)
                 }
             }
             acc ^= 1;

@@ -35,6 +35,9 @@ namespace {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Latency of the split-K handshake (atomic arrive, acquire poll, barrier).
+constexpr double kSplitSyncUs = 1.0;
+
 struct RegionEval {
     int32_t kernel = -1;
     int32_t splits = 1;
@@ -53,13 +56,14 @@ inline int64_t slots_for(const mp_handle_s* h, const mp_kernel_desc& u) {
 }
 
 // g_predict(f_num) plus the split-K reduction: every task of a split tile
-// writes an fp32 partial and the last task of the tile reads all of them.
+// writes an fp32 partial, waits for the tile's other splits (a counter round
+// trip through L2), then reads 1/S of every partial -- one partial's worth.
 inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f_num, int64_t splits) {
     double t = u.fixed_us + u.per_step_us * (double)f_num;
     if (splits > 1 && h->hw.l2_gbs > 0 && h->hw.num_pe > 0) {
         double tile_bytes = 4.0 * u.um * u.un;
         double pe_gbs = h->hw.l2_gbs / h->hw.num_pe;
-        t += 2.0 * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
+        t += kSplitSyncUs + 2.0 * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
     }
     return t;
 }
