@@ -41,15 +41,19 @@
 namespace mp {
 namespace dev {
 
-constexpr int kStages = 4;
+// Shared-memory ring: each stage holds one X tile (16 KB) and one Y tile of
+// the plan's widest micro-kernel (bn x 64 bf16), so narrow plans get more
+// stages in flight: 4 at bn = 256, 6 at 128, 8 at 64, 10 at 16.
 constexpr int kXBytes = 128 * 64 * 2;   // 128 rows (or 128 columns of B^T) x 64 K, bf16
-constexpr int kYBytes = 256 * 64 * 2;   // up to 256 columns x 64 K, bf16
-constexpr int kThreads = 192;
+constexpr int kRingBytes = 4 * (kXBytes + 256 * 64 * 2);
+constexpr int kMaxStages = 12;
+constexpr int kThreads = 224;           // 7 warps: producer, MMA, 4 epilogue, producer
+constexpr int kProducer2Warp = 6;
 constexpr int kTmemCols = 512;          // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
 constexpr int kStageBytesEpi = 4 * 32 * 16 * 4;  // per epilogue warp: 32 rows x 16 fp32
-constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = kStages * (kXBytes + kYBytes) + kStageBytesEpi + kBarBytes + 1024;
+constexpr int kBarBytes = 512;
+constexpr int kSmemBytes = kRingBytes + kStageBytesEpi + kBarBytes + 1024;
 
 // Error codes written to the status word (first writer wins).
 constexpr int kErrWaitEmpty = 1;
@@ -73,8 +77,13 @@ struct Region {
 
 struct alignas(128) Params {
     CUtensorMap tmA;     // A viewed as [batch][M][K] bf16, box {64 (K), 128 rows}
-    CUtensorMap tmA16;   // same tensor, box {64 (K), 16 rows}
+    CUtensorMap tmAs;    // same tensor, box {64 (K), as_rows rows}: A of swapped tiles
     CUtensorMap tmB;     // B viewed as [batch][K][N] bf16, box {64 (N), 64 rows of K}
+    // B viewed as [batch][N/64 full blocks][K][64]: box {64, 64 (K), j+1 blocks}
+    // fetches j+1 adjacent 64-column blocks in one copy (encoded when used).
+    CUtensorMap tmB4[4];
+    int nb_full;         // floor(N / 64): blocks tmB4 may address
+    int as_rows;         // rows per A box of swapped tiles (divides every swapped bn)
     const float* C;
     float* D;
     long long ldc, ldd, strideC, strideD;
@@ -85,6 +94,8 @@ struct alignas(128) Params {
     int num_regions;
     int inject_timeout;  // test hook: withhold the first stage of the first unit
     int vec_c, vec_d;    // C / D rows allow 16-byte vector access
+    int num_stages;      // shared-memory ring depth for this plan
+    int stage_bytes;     // 16 KB X tile + the widest Y tile of the plan
     unsigned long long wait_limit_ns;
     Region reg[MP_MAX_REGIONS];
     float* ws;
@@ -194,12 +205,41 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Non-blocking probe of a phase (mbarrier.test_wait never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Inline fast path: one non-blocking probe, then the bounded slow path.
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int code, uint64_t limit_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort_flag, err, code, limit_ns, true);
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
                                             int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
 
@@ -472,28 +512,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t xs0 = base;
-    const uint32_t ys0 = base + kStages * kXBytes;
-    const uint32_t epi0 = ys0 + kStages * kYBytes;
+    const uint32_t ring0 = base;
+    const uint32_t epi0 = base + kRingBytes;
     const uint32_t bar0 = epi0 + kStageBytesEpi;
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + (bar0 - base));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
     volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
+    const int nst = p.num_stages;
+    const uint32_t stage_bytes = (uint32_t)p.stage_bytes;  // X tile, then Y tile
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto accf = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto acce = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 4);
+    auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+    auto accf = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
+    auto acce = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kMaxStages + 4);
     const uint64_t limit = p.wait_limit_ns;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; s++) {
+        for (int s = 0; s < nst; s++) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
@@ -507,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         *epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_map(&p.tmA);
-        tma_prefetch_map(&p.tmA16);
+        tma_prefetch_map(&p.tmAs);
         tma_prefetch_map(&p.tmB);
     }
     if (warp == 1) {
@@ -517,100 +558,135 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Programmatic dependent launch: everything above (barrier set-up, TMEM,
+    // descriptor prefetch) may overlap the previous kernel on this stream;
+    // nothing below runs before that kernel has finished and its writes are
+    // visible.  The next kernel may then start its own set-up on SMs as they
+    // free up.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------ TMA producer ---------------------
-            int stage = 0;
-            uint32_t ph = 0;
-            uint32_t armed_mask = 0, armed_ph = 0;
-            bool withhold = p.inject_timeout != 0;
-            for (int u = blockIdx.x; u < p.total_units && !*abort_flag; u += gridDim.x) {
-                const Work w = decode(p, u);
-                const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit, true))
-                        goto producer_out;
-                    if (!withhold) {
-                        const uint32_t xs = xs0 + stage * kXBytes, ys = ys0 + stage * kYBytes;
-                        const int kc = kb * 64;
-                        mbar_arrive_expect_tx(full(stage), (uint32_t)(kXBytes + w.bn * 128));
-                        if (!w.swap) {
-                            tma_load_3d(xs, &p.tmA, full(stage), kc, w.m_t0, ab);
-                            for (int c = 0; c < w.bn / 64; ++c)
-                                tma_load_3d(ys + c * 8192, &p.tmB, full(stage), w.n_t0 + 64 * c, kc, bb);
-                        } else {
-                            tma_load_3d(xs, &p.tmB, full(stage), w.n_t0, kc, bb);
-                            tma_load_3d(xs + 8192, &p.tmB, full(stage), w.n_t0 + 64, kc, bb);
-                            for (int c = 0; c < w.bn / 16; ++c)
-                                tma_load_3d(ys + c * 2048, &p.tmA16, full(stage), kc, w.m_t0 + 16 * c, ab);
+    if (warp == 0 || warp == kProducer2Warp) {
+        // ------------------------------ TMA producers (two warps) -------------
+        // Issuing a stage (probe the slot, copies, expect-tx) costs several
+        // hundred cycles of dependent latency, so two warps take alternate
+        // K steps of the CTA's global step sequence g: step g uses stage
+        // g % nst, phase (g / nst) & 1, and belongs to warp 0 when g is even.
+        // Within a warp, lane 0 probes the slot and arms it; the stage's
+        // copies (one to five boxes) go out from different lanes in one
+        // instruction, before the expect-tx (the transaction count may run
+        // negative until then; the phase cannot complete without the arrive).
+        //   normal tile:  lane 0 -> A box (128 rows), lanes 1.. -> B
+        //   swapped tile: lane 0.. -> B^T (128 columns), lanes 2.. -> A
+        // B comes in one box of all the tile's 64-column blocks when they
+        // are all full; a tile that reaches past the last full block loads
+        // its blocks one by one (zero-filled beyond N).
+        const uint32_t pid = warp == 0 ? 0u : 1u;
+        uint32_t g = 0;
+        uint32_t armed_mask = 0, armed_ph = 0;
+        bool withhold = pid == 0 && p.inject_timeout != 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+            const Work w = decode(p, u);
+            const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
+            const int blk0 = w.n_t0 >> 6;
+            const int nblk = w.swap ? 2 : (w.bn >> 6);
+            const bool whole_b = blk0 + nblk <= p.nb_full;
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+                if ((g & 1u) != pid) continue;
+                const int stage = (int)(g % (uint32_t)nst);
+                const uint32_t ph = (g / (uint32_t)nst) & 1u;
+                int ok = 1;
+                if (lane == 0) ok = wait_fast(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_out;
+                if (!withhold) {
+                    const uint32_t xs = ring0 + stage * stage_bytes, ys = xs + kXBytes;
+                    const uint32_t fb = full(stage);
+                    const int kc = kb * 64;
+                    if (!w.swap) {
+                        if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
+                        if (whole_b) {
+                            if (lane == 1) tma_load_4d(ys, &p.tmB4[nblk - 1], fb, 0, kc, blk0, bb);
+                        } else if (lane >= 1 && lane <= nblk) {
+                            const int c = lane - 1;
+                            tma_load_3d(ys + c * 8192, &p.tmB, fb, w.n_t0 + 64 * c, kc, bb);
                         }
-                        armed_mask |= 1u << stage;
-                        armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    } else {
+                        if (whole_b) {
+                            if (lane == 0) tma_load_4d(xs, &p.tmB4[1], fb, 0, kc, blk0, bb);
+                        } else if (lane < 2) {
+                            tma_load_3d(xs + lane * 8192, &p.tmB, fb, w.n_t0 + 64 * lane, kc, bb);
+                        }
+                        const int na = w.bn / p.as_rows;
+                        if (lane >= 2 && lane < 2 + na) {
+                            const int c = lane - 2;
+                            tma_load_3d(ys + c * p.as_rows * 128, &p.tmAs, fb, kc, w.m_t0 + c * p.as_rows, ab);
+                        }
                     }
-                    withhold = false;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(kXBytes + w.bn * 128));
+                    armed_mask |= 1u << stage;
+                    armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
                 }
-            }
-        producer_out:
-            if (*abort_flag) {
-                // Let every copy this thread started land before the CTA exits.
-                for (int s = 0; s < kStages; s++)
-                    if (armed_mask & (1u << s))
-                        wait_bounded(full(s), (armed_ph >> s) & 1u, abort_flag, p.err, kErrDrain, limit, false);
+                withhold = false;
             }
         }
+    producer_out:
+        if (lane == 0 && *abort_flag) {
+            // Let every copy this warp started land before the CTA exits.
+            for (int s = 0; s < nst; s++)
+                if (armed_mask & (1u << s))
+                    wait_bounded(full(s), (armed_ph >> s) & 1u, abort_flag, p.err, kErrDrain, limit, false);
+        }
+        __syncwarp();
     } else if (warp == 1) {
+        // ------------------------------ MMA issuer (lane 0) --------------------
+        // One thread waits, issues every MMA and every commit, so that each
+        // commit tracks exactly this thread's MMAs.
         if (lane == 0) {
-            // ------------------------------ MMA issuer -----------------------
-            int stage = 0;
-            uint32_t ph = 0;
-            int acc = 0;
-            uint32_t aph = 0;
-            for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-                const Work w = decode(p, u);
-                if (!wait_bounded(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit, true))
-                    break;
-                tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
-                const uint32_t idesc = w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true);
-                bool ok = true;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(full(stage), ph, abort_flag, p.err, kErrWaitFull, limit, true)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t xs = xs0 + stage * kXBytes, ys = ys0 + stage * kYBytes;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint64_t ad, bd;
-                        if (!w.swap) {
-                            ad = desc_kmajor(xs, k);
-                            bd = desc_mnmajor(ys, k);
-                        } else {
-                            ad = desc_mnmajor(xs, k);
-                            bd = desc_kmajor(ys, k);
-                        }
-                        umma_bf16(d, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(empty(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
-                }
+        int stage = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+            const Work w = decode(p, u);
+            bool ok = wait_fast(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
+            const uint32_t idesc = w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true);
+            // Descriptors of stage 0, K step 0.  Every later stage and K step
+            // only moves the start address (bits 0..13, in 16-byte units;
+            // shared addresses stay below 2^18, so the sums never carry out of
+            // the field): one 64-bit add per operand.
+            const uint64_t dx0 = w.swap ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
+            const uint64_t dy0 = w.swap ? desc_kmajor(ring0 + kXBytes, 0) : desc_mnmajor(ring0 + kXBytes, 0);
+            const uint32_t kx = w.swap ? (2048u >> 4) : (32u >> 4);
+            const uint32_t ky = w.swap ? (32u >> 4) : (2048u >> 4);
+            const uint32_t sstep = stage_bytes >> 4;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                ok = wait_fast(full(stage), ph, abort_flag, p.err, kErrWaitFull, limit);
                 if (!ok) break;
-                umma_commit(accf(acc));
-                acc ^= 1;
-                if (acc == 0) aph ^= 1u;
+                tc_fence_after();
+                const uint64_t ax = dx0 + (uint64_t)(stage * sstep);
+                const uint64_t by = dy0 + (uint64_t)(stage * sstep);
+                umma_bf16(d, ax, by, idesc, kb > w.kb0 ? 1u : 0u);
+                umma_bf16(d, ax + kx, by + ky, idesc, 1u);
+                umma_bf16(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
+                umma_bf16(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
+                umma_commit(empty(stage));
+                if (++stage == nst) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
             }
-            // Every MMA this thread issued has completed once `done_bar` flips.
-            umma_commit(done_bar);
-            wait_bounded(done_bar, 0, abort_flag, p.err, kErrDrain, limit, false);
+            if (!ok) break;
+            umma_commit(accf(acc));
+            acc ^= 1;
+            if (acc == 0) aph ^= 1u;
+        }
+        // Every MMA this thread issued has completed once `done_bar` flips.
+        umma_commit(done_bar);
+        wait_bounded(done_bar, 0, abort_flag, p.err, kErrDrain, limit, false);
         }
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
@@ -798,6 +874,18 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, 
     return r == CUDA_SUCCESS;
 }
 
+bool encode_4d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t d3, uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box0, uint32_t box1, uint32_t box2) {
+    cuuint64_t dims[4] = {d0, d1, d2, d3};
+    cuuint64_t strides[3] = {s1, s2, s3};
+    cuuint32_t box[4] = {box0, box1, box2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool tma_ok(const void* p, int64_t ld, int64_t batch, int64_t stride) {
     if (((uintptr_t)p & 15u) != 0) return false;
     if ((ld * 2) % 16 != 0) return false;
@@ -838,7 +926,7 @@ mp_status device_init(mp_handle h, int device) {
     if (s->staging_bytes <= 0) s->staging_bytes = kDefaultStagingBytes;
 
     h->hw.num_pe = prop.multiProcessorCount;
-    h->hw.warps_per_wave = prop.multiProcessorCount * (dev::kThreads / 32);
+    h->hw.warps_per_wave = prop.multiProcessorCount * kModelWarpsPerTask;
     h->hw.local_mem_bytes = (int64_t)prop.sharedMemPerBlockOptin;
     h->hw.shared_mem_bytes = (int64_t)prop.l2CacheSize;
     h->hw.hbm_gbs = 6684.0;    // measured STREAM-style copy on GB300
@@ -899,7 +987,7 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
     h->host_only = false;
     h->device = device;
     h->hw.num_pe = prop.multiProcessorCount;
-    h->hw.warps_per_wave = prop.multiProcessorCount * (dev::kThreads / 32);
+    h->hw.warps_per_wave = prop.multiProcessorCount * kModelWarpsPerTask;
     h->hw.local_mem_bytes = (int64_t)prop.sharedMemPerBlockOptin;
     h->hw.shared_mem_bytes = (int64_t)prop.l2CacheSize;
     h->hw.hbm_gbs = 6684.0;
@@ -992,16 +1080,46 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             sB = st2;
             used += bytes;
         }
+        // Box shapes the plan's regions use: rows per A box of swapped tiles
+        // (the smallest swapped bn divides the others: all are powers of 2),
+        // and the numbers of 64-column blocks a B copy covers.
+        int as_rows = 128;
+        bool need_b4[4] = {false, false, false, false};
+        for (int i = 0; i < plan.num_regions; i++) {
+            const mp_region_info& r = plan.region[i];
+            if (r.swap) {
+                as_rows = std::min(as_rows, (int)r.um);
+                need_b4[1] = true;
+            } else if (r.un >= 64 && r.un <= 256) {
+                need_b4[r.un / 64 - 1] = true;
+            }
+        }
+        p.as_rows = as_rows;
         const uint64_t a_s2 = bA > 1 ? (uint64_t)sA * 2 : (uint64_t)round_up(M * lda * 2, 16);
         const uint64_t b_s2 = bB > 1 ? (uint64_t)sB * 2 : (uint64_t)round_up(K * ldb * 2, 16);
         if (!encode_3d(s->encode, &p.tmA, A, K, M, bA, lda * 2, a_s2, 64, 128) ||
-            !encode_3d(s->encode, &p.tmA16, A, K, M, bA, lda * 2, a_s2, 64, 16) ||
+            !encode_3d(s->encode, &p.tmAs, A, K, M, bA, lda * 2, a_s2, 64, (uint32_t)as_rows) ||
             !encode_3d(s->encode, &p.tmB, B, N, K, bB, ldb * 2, b_s2, 64, 64))
             return MP_ERR_CUDA;
+        // Whole-tile B copies: B as [batch][N/64][K][64] (block stride 128 B).
+        // Only full 64-column blocks are addressable, so nothing past a row
+        // end is ever read; tiles reaching past the last full block load per
+        // block.  If a view cannot be encoded, every tile loads per block.
+        p.nb_full = (int)(N / 64);
+        for (int j = 0; j < 4 && p.nb_full > 0; j++) {
+            if (!need_b4[j]) continue;
+            if (!encode_4d(s->encode, &p.tmB4[j], B, 64, (uint64_t)K, (uint64_t)p.nb_full, (uint64_t)bB,
+                           (uint64_t)ldb * 2, 128, b_s2, 64, 64, (uint32_t)(j + 1))) {
+                p.nb_full = 0;
+                break;
+            }
+        }
     } else {
         // K == 0: no operand is read; the maps only have to be well formed.
+        p.as_rows = 16;
+        p.nb_full = 0;
         if (!encode_3d(s->encode, &p.tmA, s->staging, 64, 128, 1, 128, 128 * 128, 64, 128) ||
-            !encode_3d(s->encode, &p.tmA16, s->staging, 64, 128, 1, 128, 128 * 128, 64, 16) ||
+            !encode_3d(s->encode, &p.tmAs, s->staging, 64, 128, 1, 128, 128 * 128, 64, 16) ||
             !encode_3d(s->encode, &p.tmB, s->staging, 64, 128, 1, 128, 128 * 128, 64, 64))
             return MP_ERR_CUDA;
     }
@@ -1063,10 +1181,27 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     p.total_units = (int)units;
     if (units == 0) return MP_OK;
 
+    // Ring depth: stages sized for the widest Y tile of this plan.
+    int bn_max = 16;
+    for (int i = 0; i < p.num_regions; i++) bn_max = std::max(bn_max, p.reg[i].bn);
+    p.stage_bytes = dev::kXBytes + bn_max * 128;
+    p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
+
     const int grid = (int)std::min<int64_t>(units, s->num_sms);
     if (s->log) log_plan(plan, a, grid);
-    dev::k_poly_gemm<<<grid, dev::kThreads, dev::kSmemBytes, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+    // One CTA per SM; launched as a programmatic dependent of the previous
+    // kernel on the stream so that its set-up overlaps that kernel's tail.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(dev::kThreads);
+    cfg.dynamicSmemBytes = dev::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, dev::k_poly_gemm, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 

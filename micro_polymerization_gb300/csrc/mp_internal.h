@@ -7,7 +7,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/mp.h"
+#include "mp.h"  // include/ is on the compiler's include path
 
 namespace mp {
 
@@ -16,6 +16,9 @@ namespace mp {
 constexpr int kUmmaM = 128;
 constexpr int kUk = 64;
 constexpr int kMaxBn = 256;
+// Warps per task in the wave model of the GB300 kernel set (one CTA per SM,
+// so warps_per_wave = SMs * kModelWarpsPerTask gives one task slot per SM).
+constexpr int kModelWarpsPerTask = 6;
 
 // Limits of the device-side bookkeeping (allocated once per handle).
 constexpr int64_t kMaxCounters = 1 << 16;          // split-K tile counters

@@ -415,7 +415,7 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
         d.um = g.um;
         d.un = g.un;
         d.uk = kUk;
-        d.warps = 6;  // one CTA of 6 warps per SM: one task slot per PE
+        d.warps = kModelWarpsPerTask;  // one CTA per SM: one task slot per PE
         d.swap = g.swap;
         const double n_umma = g.swap ? g.um : g.un;
         const double flops = 2.0 * kUmmaM * std::max(32.0, n_umma) * kUk;
