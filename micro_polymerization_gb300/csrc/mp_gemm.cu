@@ -51,7 +51,10 @@ constexpr int kThreads = 224;           // 7 warps: producer, MMA, 4 epilogue, p
 constexpr int kProducer2Warp = 6;
 constexpr int kTmemCols = 512;          // two accumulator buffers of 256 columns
 constexpr int kAccStride = 256;
-constexpr int kStageBytesEpi = 4 * 32 * 16 * 4;  // per epilogue warp: 32 rows x 16 fp32
+// Epilogue staging, 8 KB per epilogue warp: two 32 x 32 fp32 slabs for bulk
+// tensor stores of D (the 16-column transposes use the first 2 KB).
+constexpr int kEpiWarpBytes = 2 * 32 * 32 * 4;
+constexpr int kStageBytesEpi = 4 * kEpiWarpBytes;
 constexpr int kBarBytes = 512;
 constexpr int kSmemBytes = kRingBytes + kStageBytesEpi + kBarBytes + 1024;
 
@@ -94,6 +97,8 @@ struct alignas(128) Params {
     int num_regions;
     int inject_timeout;  // test hook: withhold the first stage of the first unit
     int vec_c, vec_d;    // C / D rows allow 16-byte vector access
+    CUtensorMap tmD;     // D viewed as [batch][M][N] fp32, box {32 (N), 32 rows}, 128-byte swizzle
+    int tma_d;           // 1: normal tiles store D through tmD (beta == 0, rows 16-byte aligned)
     int num_stages;      // shared-memory ring depth for this plan
     int stage_bytes;     // 16 KB X tile + the widest Y tile of the plan
     unsigned long long wait_limit_ns;
@@ -243,6 +248,26 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Bulk tensor store of a shared-memory box to global memory (bulk-group
+// completion); rows and columns outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most one bulk group of this thread is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Generic-proxy writes to shared memory become visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -307,6 +332,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
                  : "memory");
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
@@ -454,6 +503,31 @@ __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, in
         const int m = w.m_t0 + q * 32 + r;
         if (m < w.m_end) store4(p, w, m, w.n_t0 + c + 4 * g, x);
     });
+}
+
+// Normal tile, beta == 0: write alpha * (32 accumulator columns of this
+// lane's row) into a 32 x 32 fp32 slab with the 128-byte swizzle (16-byte
+// group j of row r at r*128 + ((j ^ (r & 7)) << 4): conflict-free, and the
+// layout a swizzled tensor store expects), then one lane stores the slab to
+// D(m0 .. m0+31, n0 .. n0+31) with a bulk tensor copy.  Two slabs alternate;
+// before a slab is rewritten, the store that last read it must have finished
+// reading.
+__device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int lane, int m0, int n0,
+                                           const float* v, uint8_t* slab, uint32_t slab_s) {
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+    const float a = p.alpha;
+    uint8_t* row = slab + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+        *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+            make_float4(a * v[4 * j], a * v[4 * j + 1], a * v[4 * j + 2], a * v[4 * j + 3]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(&p.tmD, slab_s, n0, m0, w.b);
+        bulk_commit_group();
+    }
 }
 
 // Split-K partials are kept "D-row-major" per tile: a buffer of R rows x L
@@ -691,7 +765,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        float4* stage = reinterpret_cast<float4*>(gbase + (epi0 - base)) + (warp - 2) * (32 * 4);
+        uint8_t* epi_g = gbase + (epi0 - base) + (warp - 2) * kEpiWarpBytes;
+        const uint32_t epi_s = epi0 + (uint32_t)((warp - 2) * kEpiWarpBytes);
+        float4* stage = reinterpret_cast<float4*>(epi_g);
+        uint32_t slab = 0;  // running slab index of this warp's bulk stores
         int acc = 0;
         uint32_t aph = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -712,7 +789,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
-            if (w.splits == 1) {
+            if (w.splits == 1 && p.tma_d && !w.swap) {
+                for (int c = 0; c < w.bn; c += 32) {
+                    float v[32];
+                    if (has_k) {
+                        tmem_ld32(t + c, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] = 0.0f;
+                    }
+                    // A slab wholly past the region's last row or column has
+                    // nothing to store (and no store group, so the slab
+                    // alternation is kept by counting only real stores).
+                    const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
+                    if (m0 < w.m_end && n0 < w.n_end) {
+                        const uint32_t off = (slab & 1u) * 4096u;
+                        emit32_tma(p, w, lane, m0, n0, v, epi_g + off, epi_s + off);
+                        ++slab;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce(acc));
+            } else if (w.splits == 1) {
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
                     if (has_k) {
@@ -732,6 +831,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 // has parked, then sum this split's 1/S slice of the tile's
                 // rows over all partials, in split order, and write D.
                 float* part = p.ws + w.ws_tile + (long long)w.split * (128ll * w.bn);
+                // The transpose staging overlaps the first store slab: let
+                // every bulk store of this warp finish reading it first.
+                if (lane == 0) bulk_wait_all();
+                __syncwarp();
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
                     tmem_ld16(t + c, v);
@@ -785,6 +888,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
+        // Bulk stores still in flight must finish before the CTA exits.
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     __syncthreads();
@@ -869,6 +975,19 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, 
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// fp32 output view [d2][d1][d0] for bulk tensor stores, box {box0, box1, 1}.
+bool encode_3d_f32(EncodeTiledFn enc, CUtensorMap* m, void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1127,6 +1246,18 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     p.b_bstep = bB > 1 ? 1 : 0;
 
     p.C = a.beta != 0.0f ? a.C : nullptr;
+    // Bulk tensor stores of D for normal tiles when there is no C to combine
+    // and D's rows allow a tensor map (16-byte aligned base, row pitch and
+    // batch pitch).  Rows and columns past M and N are clipped by the map;
+    // region cuts fall on tile boundaries, so no tile reaches another region.
+    p.tma_d = 0;
+    if (a.beta == 0.0f && ((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0 &&
+        (batch == 1 || (a.strideD * 4) % 16 == 0)) {
+        const uint64_t d_s2 = batch > 1 ? (uint64_t)a.strideD * 4 : (uint64_t)round_up(M * a.ldd * 4, 16);
+        if (encode_3d_f32(s->encode, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch, (uint64_t)a.ldd * 4,
+                          d_s2, 32, 32))
+            p.tma_d = 1;
+    }
     p.vec_d = (((uintptr_t)a.D & 15u) == 0 && a.ldd % 4 == 0 && (batch == 1 || a.strideD % 4 == 0)) ? 1 : 0;
     p.vec_c = (p.C && ((uintptr_t)a.C & 15u) == 0 && a.ldc % 4 == 0 && (batch == 1 || a.strideC % 4 == 0)) ? 1 : 0;
     p.D = a.D;
