@@ -86,6 +86,7 @@ struct alignas(128) Params {
     // fetches j+1 adjacent 64-column blocks in one copy (encoded when used).
     CUtensorMap tmB4[4];
     int nb_full;         // floor(N / 64): blocks tmB4 may address
+    int b4_mask;         // bit j: tmB4[j] is encoded (prefetched at set-up)
     int as_rows;         // rows per A box of swapped tiles (divides every swapped bn)
     const float* C;
     float* D;
@@ -512,16 +513,59 @@ __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, in
 // D(m0 .. m0+31, n0 .. n0+31) with a bulk tensor copy.  Two slabs alternate;
 // before a slab is rewritten, the store that last read it must have finished
 // reading.
+// C for the same 32 x 32 block, one row per lane (zero outside the region);
+// issued before the TMEM load of the chunk so that both latencies overlap.
+__device__ __forceinline__ void load_c32(const Params& p, const Work& w, int lane, int m0, int n0, float* c) {
+    const int m = m0 + lane;
+    if (m < w.m_end) {
+        const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + n0;
+        if (p.vec_c && n0 + 32 <= w.n_end) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
+                c[4 * j] = x.x;
+                c[4 * j + 1] = x.y;
+                c[4 * j + 2] = x.z;
+                c[4 * j + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; j++) c[j] = n0 + j < w.n_end ? __ldg(cr + j) : 0.0f;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++) c[j] = 0.0f;
+    }
+}
+
+// Ask L2 for this lane's row of C over the whole tile (one 128-byte line per
+// 32 columns) before the accumulator is ready.
+__device__ __forceinline__ void prefetch_c_row(const Params& p, const Work& w, int m) {
+    if (m >= w.m_end) return;
+    const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + w.n_t0;
+    for (int c = 0; c < w.bn && w.n_t0 + c < w.n_end; c += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + c));
+}
+
 __device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int lane, int m0, int n0,
-                                           const float* v, uint8_t* slab, uint32_t slab_s) {
+                                           const float* v, const float* c, uint8_t* slab, uint32_t slab_s) {
     if (lane == 0) bulk_wait_read_1();
     __syncwarp();
-    const float a = p.alpha;
+    const float a = p.alpha, bt = p.beta;
     uint8_t* row = slab + lane * 128;
+    if (bt == 0.0f) {
 #pragma unroll
-    for (int j = 0; j < 8; j++)
-        *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
-            make_float4(a * v[4 * j], a * v[4 * j + 1], a * v[4 * j + 2], a * v[4 * j + 3]);
+        for (int j = 0; j < 8; j++)
+            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+                make_float4(a * v[4 * j], a * v[4 * j + 1], a * v[4 * j + 2], a * v[4 * j + 3]);
+    } else {
+        // Same arithmetic as the other epilogue paths: fma(beta, C, alpha*acc).
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+                make_float4(fmaf(bt, c[4 * j], a * v[4 * j]), fmaf(bt, c[4 * j + 1], a * v[4 * j + 1]),
+                            fmaf(bt, c[4 * j + 2], a * v[4 * j + 2]), fmaf(bt, c[4 * j + 3], a * v[4 * j + 3]));
+    }
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -621,9 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         *s_last = 0;
         *epi_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // Fetch every descriptor this launch uses while the previous kernel
+        // on the stream may still be running.
         tma_prefetch_map(&p.tmA);
         tma_prefetch_map(&p.tmAs);
         tma_prefetch_map(&p.tmB);
+        for (int j = 0; j < 4; j++)
+            if (p.b4_mask & (1 << j)) tma_prefetch_map(&p.tmB4[j]);
+        if (p.tma_d) tma_prefetch_map(&p.tmD);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -773,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t aph = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
             const Work w = decode(p, u);
+            if (p.tma_d && p.beta != 0.0f && w.splits == 1 && !w.swap) prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded(accf(acc), aph, abort_flag, p.err, kErrWaitAccFull, limit, true) ? 1 : 0;
@@ -790,7 +840,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
             if (w.splits == 1 && p.tma_d && !w.swap) {
+                const bool with_c = p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
+                    const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
+                    float cv[32];
+                    if (with_c) load_c32(p, w, lane, m0, n0, cv);
                     float v[32];
                     if (has_k) {
                         tmem_ld32(t + c, v);
@@ -801,10 +855,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     // A slab wholly past the region's last row or column has
                     // nothing to store (and no store group, so the slab
                     // alternation is kept by counting only real stores).
-                    const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
                     if (m0 < w.m_end && n0 < w.n_end) {
                         const uint32_t off = (slab & 1u) * 4096u;
-                        emit32_tma(p, w, lane, m0, n0, v, epi_g + off, epi_s + off);
+                        emit32_tma(p, w, lane, m0, n0, v, cv, epi_g + off, epi_s + off);
                         ++slab;
                     }
                 }
@@ -1230,8 +1283,10 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             if (!encode_4d(s->encode, &p.tmB4[j], B, 64, (uint64_t)K, (uint64_t)p.nb_full, (uint64_t)bB,
                            (uint64_t)ldb * 2, 128, b_s2, 64, 64, (uint32_t)(j + 1))) {
                 p.nb_full = 0;
+                p.b4_mask = 0;
                 break;
             }
+            p.b4_mask |= 1 << j;
         }
     } else {
         // K == 0: no operand is read; the maps only have to be well formed.
@@ -1246,12 +1301,13 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     p.b_bstep = bB > 1 ? 1 : 0;
 
     p.C = a.beta != 0.0f ? a.C : nullptr;
-    // Bulk tensor stores of D for normal tiles when there is no C to combine
-    // and D's rows allow a tensor map (16-byte aligned base, row pitch and
-    // batch pitch).  Rows and columns past M and N are clipped by the map;
-    // region cuts fall on tile boundaries, so no tile reaches another region.
+    // Bulk tensor stores of D for normal tiles when D's rows allow a tensor
+    // map (16-byte aligned base, row pitch and batch pitch).  Rows and columns
+    // past M and N are clipped by the map; region cuts fall on tile
+    // boundaries, so no tile reaches another region.  C (beta != 0) is read
+    // by the epilogue threads and fused before the store.
     p.tma_d = 0;
-    if (a.beta == 0.0f && ((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0 &&
+    if (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0 &&
         (batch == 1 || (a.strideD * 4) % 16 == 0)) {
         const uint64_t d_s2 = batch > 1 ? (uint64_t)a.strideD * 4 : (uint64_t)round_up(M * a.ldd * 4, 16);
         if (encode_3d_f32(s->encode, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch, (uint64_t)a.ldd * 4,
