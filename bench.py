@@ -143,9 +143,16 @@ def barrier(world: int):
 
 def rank_workload(name: str, rank: int):
     """Each rank runs its own copy of the workload (weak scaling): same shapes,
-    operands seeded per rank."""
+    operands seeded per rank.  ``shape:M,N,K[,beta]`` names a one-GEMM
+    workload (alpha = 1, C uniform when beta != 0), for profiling one shape."""
     from micro_polymerization_gb300 import workloads as wl
-    gs = wl.workload(name)
+    if name.startswith("shape:"):
+        vals = [float(x) for x in name[len("shape:"):].split(",")]
+        M, N, K = (int(v) for v in vals[:3])
+        beta = vals[3] if len(vals) > 3 else 0.0
+        gs = [wl.Gemm(M, N, K, alpha=1.0, beta=beta, seed=77)]
+    else:
+        gs = wl.workload(name)
     if rank == 0:
         return gs
     import dataclasses
@@ -171,7 +178,11 @@ def run_mp(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    h = mp.mp_init(local)
+    # The planner's g_predict table, measured once per machine by
+    # micro_polymerization_gb300/calibrate.py (analytic defaults if absent).
+    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
+    calib = calib if (os.path.exists(calib) and not args.no_calib) else None
+    h = mp.mp_init(local, calib)
     lib = mp.library()
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -345,8 +356,7 @@ def run_mp(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": workload_desc(args.workload), "gemms_per_step": len(gs),
-                       "flops_per_step": int(flops_step), "l2": "inputs larger than L2 "
-                       f"({sum(g.min_bytes() for g in gs) / 1e9:.2f} GB of distinct operands per step)",
+                       "flops_per_step": int(flops_step), "l2": l2_note(gs),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
                                    "sum_troof_over_sum_t": round(time_ratio, 4),
@@ -356,6 +366,7 @@ def run_mp(args):
                          "launches": len(sel), "kernel": "k_poly_gemm", "peak_source": peak_src},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "plan_us": round(plan_us, 3) if plan_us is not None else None,
+            "cost_model": "calibrated" if calib else "analytic",
             "clocks": clocks.summary(), "impl": "mp",
         }
         print(json.dumps(line), flush=True)
@@ -365,7 +376,22 @@ def run_mp(args):
         dist.destroy_process_group()
 
 
+L2_BYTES = 126 * 2 ** 20
+
+
+def l2_note(gs):
+    """How the timed region treats L2: the default workload touches far more
+    distinct operand bytes per step than L2 holds; a one-shape workload does
+    not, so its numbers are warm-L2 numbers (used for profiling only)."""
+    total = sum(g.min_bytes() for g in gs)
+    if total >= 2 * L2_BYTES:
+        return f"inputs larger than L2 ({total / 1e9:.2f} GB of distinct operands per step)"
+    return f"inputs smaller than L2 ({total / 1e9:.3f} GB per step, not flushed): warm-L2 numbers"
+
+
 def workload_desc(name):
+    if name.startswith("shape:"):
+        return f"single GEMM (M,N,K[,beta]) = ({name[len('shape:'):]}), alpha=1"
     return {
         "dynamic_sequence": "dynamic sequence length: 64 GEMMs, M = 8*seq (seq uniform [1,512]), "
                             "(N,K) cycling (2304,768),(768,768),(3072,768),(768,3072), bf16 A,B, beta=0",
@@ -385,6 +411,10 @@ def sweep(args, h, peaks, dev):
     flush = torch.empty(int(512 * 2 ** 20), dtype=torch.uint8, device=dev)
     for name in wl.WORKLOADS:
         gs = wl.workload(name)
+        if len(gs) > args.sweep_count:
+            # A seeded sample of the list (the stress sweep's 4096^3 is kept).
+            idx = np.random.default_rng(7).choice(len(gs) - 1, args.sweep_count - 1, replace=False)
+            gs = [gs[i] for i in sorted(idx)] + [gs[-1]]
         ts, trs, fl = [], [], []
         for g in gs:
             A, B, C = wl.make_operands(g, device=dev)
@@ -483,9 +513,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mp", "reference"], default="mp")
     ap.add_argument("--workload", default="dynamic_sequence")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-count", type=int, default=128, help="GEMMs per workload in the sweep (sampled)")
     ap.add_argument("--dump", default=None, help="write per-GEMM time, roofline and plan (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-calib", action="store_true", help="plan with the analytic cost model")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)

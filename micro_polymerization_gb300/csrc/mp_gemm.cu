@@ -55,7 +55,7 @@ constexpr int kAccStride = 256;
 // tensor stores of D (the 16-column transposes use the first 2 KB).
 constexpr int kEpiWarpBytes = 2 * 32 * 32 * 4;
 constexpr int kStageBytesEpi = 4 * kEpiWarpBytes;
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 1024;  // mbarriers, flags and the region table
 constexpr int kSmemBytes = kRingBytes + kStageBytesEpi + kBarBytes + 1024;
 
 // Error codes written to the status word (first writer wins).
@@ -99,6 +99,10 @@ struct alignas(128) Params {
     int inject_timeout;  // test hook: withhold the first stage of the first unit
     int vec_c, vec_d;    // C / D rows allow 16-byte vector access
     CUtensorMap tmD;     // D viewed as [batch][M][N] fp32, box {32 (N), 32 rows}, 128-byte swizzle
+    // Split-K partials of region i viewed as [tiles*splits*128 rows][bn] fp32,
+    // box {32, 32}, 128-byte swizzle (encoded for split regions of normal tiles).
+    CUtensorMap tmW[MP_MAX_REGIONS];
+    int w_mask;          // bit i: tmW[i] is encoded
     int tma_d;           // 1: normal tiles store D through tmD (beta == 0, rows 16-byte aligned)
     int num_stages;      // shared-memory ring depth for this plan
     int stage_bytes;     // 16 KB X tile + the widest Y tile of the plan
@@ -116,14 +120,17 @@ struct Work {
     int kb0, kb1;
     long long ws_tile;   // split 0 of this tile's partials
     int cnt;
+    int r;               // region index
+    int ws_row;          // first row of this split's partial in the region's [rows][bn] view
 };
 
-__device__ __forceinline__ Work decode(const Params& p, int u) {
+// `regs` is the shared-memory copy of p.reg made during set-up.
+__device__ __forceinline__ Work decode(const Params& p, const Region* regs, int u) {
     int r = 0;
 #pragma unroll
     for (int i = 1; i < MP_MAX_REGIONS; i++)
-        if (i < p.num_regions && u >= p.reg[i].unit_begin) r = i;
-    const Region& g = p.reg[r];
+        if (i < p.num_regions && u >= regs[i].unit_begin) r = i;
+    const Region& g = regs[r];
     const int local = u - g.unit_begin;
     const int tiles = g.tiles_m * g.tiles_n;
     const int per_b = tiles * g.splits;
@@ -151,6 +158,8 @@ __device__ __forceinline__ Work decode(const Params& p, int u) {
     const long long tile_id = (long long)w.b * tiles + tile;
     w.ws_tile = g.ws_begin + tile_id * g.splits * (128ll * g.bn);
     w.cnt = g.cnt_begin + (int)tile_id;
+    w.r = r;
+    w.ws_row = (int)((tile_id * g.splits + w.split) * 128);
     return w;
 }
 
@@ -599,20 +608,42 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
     const int L4 = L / 4;
     const long long part_floats = 128ll * w.bn;
     const int total = (r1 - r0) * L4;
-    for (int i = tid; i < total; i += 128) {
-        const int r = r0 + i / L4;
-        const int l4 = i - (i / L4) * L4;
-        const float4* src = reinterpret_cast<const float4*>(tile_ws + (long long)r * L) + l4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < w.splits; s++) {
-            const float4 x = __ldcg(src + s * (part_floats / 4));
-            acc.x += x.x;
-            acc.y += x.y;
-            acc.z += x.z;
-            acc.w += x.w;
+    const long long step4 = part_floats / 4;
+    // Each thread takes two outputs at a time and keeps 2 x 8 loads in
+    // flight; every output still adds its partials in split order.
+    for (int i0 = tid; i0 < total; i0 += 256) {
+        const int i1 = i0 + 128;
+        const bool two = i1 < total;
+        const float4* src0 = reinterpret_cast<const float4*>(tile_ws + (long long)(r0 + i0 / L4) * L) + (i0 % L4);
+        const float4* src1 =
+            two ? reinterpret_cast<const float4*>(tile_ws + (long long)(r0 + i1 / L4) * L) + (i1 % L4) : src0;
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+        int s = 0;
+        for (; s + 8 <= w.splits; s += 8) {
+            float4 x0[8], x1[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                x0[e] = __ldcg(src0 + (s + e) * step4);
+                x1[e] = __ldcg(src1 + (s + e) * step4);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                a0.x += x0[e].x; a0.y += x0[e].y; a0.z += x0[e].z; a0.w += x0[e].w;
+                a1.x += x1[e].x; a1.y += x1[e].y; a1.z += x1[e].z; a1.w += x1[e].w;
+            }
         }
-        const int m = w.m_t0 + r;
-        if (m < w.m_end) store4(p, w, m, w.n_t0 + 4 * l4, acc);
+        for (; s < w.splits; s++) {
+            const float4 x0 = __ldcg(src0 + s * step4);
+            const float4 x1 = __ldcg(src1 + s * step4);
+            a0.x += x0.x; a0.y += x0.y; a0.z += x0.z; a0.w += x0.w;
+            a1.x += x1.x; a1.y += x1.y; a1.z += x1.z; a1.w += x1.w;
+        }
+        const int m0 = w.m_t0 + r0 + i0 / L4;
+        if (m0 < w.m_end) store4(p, w, m0, w.n_t0 + 4 * (i0 % L4), a0);
+        if (two) {
+            const int m1 = w.m_t0 + r0 + i1 / L4;
+            if (m1 < w.m_end) store4(p, w, m1, w.n_t0 + 4 * (i1 % L4), a1);
+        }
     }
 }
 
@@ -638,6 +669,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
     volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 3);
+    // Region table copy: 512 bytes into the 1 KB barrier area (barriers and
+    // flags use the first ~250 bytes).
+    static_assert(sizeof(Region) * MP_MAX_REGIONS <= kBarBytes - 512, "region table does not fit");
+    static_assert((2 * kMaxStages + 5) * 8 + 16 <= 512, "barriers do not fit");
+    Region* regs_s = reinterpret_cast<Region*>(gbase + (bar0 - base) + 512);
 
     const int nst = p.num_stages;
     const uint32_t stage_bytes = (uint32_t)p.stage_bytes;  // X tile, then Y tile
@@ -673,7 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         for (int j = 0; j < 4; j++)
             if (p.b4_mask & (1 << j)) tma_prefetch_map(&p.tmB4[j]);
         if (p.tma_d) tma_prefetch_map(&p.tmD);
+        for (int i = 0; i < MP_MAX_REGIONS; i++)
+            if (p.w_mask & (1 << i)) tma_prefetch_map(&p.tmW[i]);
     }
+    // The region table goes to shared memory during set-up (ordinary member
+    // reads of the parameter), so that work-unit decoding after the
+    // dependency wait reads shared memory instead of cold parameter lines.
+    if (threadIdx.x < MP_MAX_REGIONS) regs_s[threadIdx.x] = p.reg[threadIdx.x];
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -709,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t armed_mask = 0, armed_ph = 0;
         bool withhold = pid == 0 && p.inject_timeout != 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, u);
+            const Work w = decode(p, regs_s, u);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
             const int blk0 = w.n_t0 >> 6;
             const int nblk = w.swap ? 2 : (w.bn >> 6);
@@ -771,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         int acc = 0;
         uint32_t aph = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, u);
+            const Work w = decode(p, regs_s, u);
             bool ok = wait_fast(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit);
             if (!ok) break;
             tc_fence_after();
@@ -821,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         int acc = 0;
         uint32_t aph = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, u);
+            const Work w = decode(p, regs_s, u);
             if (p.tma_d && p.beta != 0.0f && w.splits == 1 && !w.swap) prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
             int ok = 1;
             if (lane == 0)
@@ -884,14 +926,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 // has parked, then sum this split's 1/S slice of the tile's
                 // rows over all partials, in split order, and write D.
                 float* part = p.ws + w.ws_tile + (long long)w.split * (128ll * w.bn);
-                // The transpose staging overlaps the first store slab: let
-                // every bulk store of this warp finish reading it first.
-                if (lane == 0) bulk_wait_all();
-                __syncwarp();
-                for (int c = 0; c < w.bn; c += 16) {
-                    float v[16];
-                    tmem_ld16(t + c, v);
-                    park16(w, q, lane, c, v, stage, part);
+                if (w.swap) {
+                    // lane = buffer column: every store covers 128 contiguous bytes.
+                    for (int c = 0; c < w.bn; c += 16) {
+                        float v[16];
+                        tmem_ld16(t + c, v);
+                        park16(w, q, lane, c, v, stage, part);
+                    }
+                } else if (p.w_mask & (1 << w.r)) {
+                    // Bulk tensor stores of 32 x 32 slabs into the region's
+                    // row-major partial view; the stores must have landed
+                    // (not just left shared memory) before the tile counter
+                    // announces this split.
+                    for (int c = 0; c < w.bn; c += 32) {
+                        float v[32];
+                        tmem_ld32(t + c, v);
+                        const uint32_t off = (slab & 1u) * 4096u;
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
+                        uint8_t* row = epi_g + off + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&p.tmW[w.r], epi_s + off, c, w.ws_row + q * 32, 0);
+                            bulk_commit_group();
+                        }
+                        ++slab;
+                    }
+                    if (lane == 0) {
+                        bulk_wait_all();
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                    __syncwarp();
+                } else {
+                    // lane = buffer row: 32 columns are 128 contiguous bytes of it.
+                    float* prow = part + (long long)(q * 32 + lane) * w.bn;
+                    for (int c = 0; c < w.bn; c += 32) {
+                        float v[32];
+                        tmem_ld32(t + c, v);
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            __stcg(reinterpret_cast<float4*>(prow + c) + j,
+                                   make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1359,7 +1440,12 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         d.ws_begin = ws_floats;
         d.cnt_begin = (int)counters;
         if (r.splits > 1) {
-            ws_floats += tiles * r.splits * 128 * bn;
+            const int64_t rows = tiles * r.splits * 128;
+            if (!r.swap && ws_floats + rows * bn <= h->workspace_floats &&
+                encode_3d_f32(s->encode, &p.tmW[i], s->ws + ws_floats, (uint64_t)bn, (uint64_t)rows, 1,
+                              (uint64_t)bn * 4, (uint64_t)round_up(rows * bn * 4, 16), 32, 32))
+                p.w_mask |= 1 << i;
+            ws_floats += rows * bn;
             counters += tiles;
         }
     }
