@@ -1071,6 +1071,26 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                   CUtensorMapFloatOOBfill);
 
+// Encoded tensor maps keyed by every input of the encoding: dynamic-shape
+// callers reuse buffers (weights always, activations often), so most calls
+// find their maps here instead of re-encoding them.
+struct TmKey {
+    uint64_t ptr;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t box[4];
+    uint32_t dtype, rank;
+    bool operator==(const TmKey& o) const { return std::memcmp(this, &o, sizeof(TmKey)) == 0; }
+};
+
+struct alignas(128) TmEntry {
+    CUtensorMap map;
+    TmKey key;
+    bool valid;
+};
+
+constexpr int kTmCacheEntries = 256;
+
 struct DeviceState {
     int device = -1;
     int num_sms = 0;
@@ -1083,6 +1103,8 @@ struct DeviceState {
     bool log = false;
     int inject_timeout = 0;
     uint64_t wait_limit_ns = 1000000000ull;  // 1 s
+    // Tensor-map cache (only for handles, which serve one host thread).
+    TmEntry* tm_cache = nullptr;
 };
 
 namespace {
@@ -1102,41 +1124,77 @@ struct DeviceGuard {
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
-bool encode_3d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+// Tiled map, interleave none, 128-byte swizzle, zero fill, element strides 1.
+bool encode_tiled(DeviceState* s, CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* ptr,
+                  const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+    TmKey key;
+    std::memset(&key, 0, sizeof key);
+    key.ptr = (uint64_t)(uintptr_t)ptr;
+    key.dtype = (uint32_t)dt;
+    key.rank = rank;
+    for (uint32_t i = 0; i < rank; i++) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    TmEntry* e = nullptr;
+    if (s->tm_cache) {
+        uint64_t h = key.ptr * 0x9E3779B97F4A7C15ull;
+        for (uint32_t i = 0; i < rank; i++) h ^= (key.dims[i] + 0x632BE59BD9B4E019ull * (i + 1)) * 0xC2B2AE3D27D4EB4Full;
+        h ^= ((uint64_t)key.box[0] << 32 | key.box[1]) * 0x165667B19E3779F9ull ^ (uint64_t)key.box[2] << 7 ^ dt ^
+             (uint64_t)rank << 3;
+        for (uint32_t i = 0; i + 1 < rank; i++) h ^= key.strides[i] * (0x27D4EB2F165667C5ull + i);
+        h ^= h >> 31;
+        e = &s->tm_cache[h % kTmCacheEntries];
+        if (e->valid && e->key == key) {
+            std::memcpy(m, &e->map, sizeof(CUtensorMap));
+            return true;
+        }
+    }
+    cuuint64_t d[5];
+    cuuint64_t st[4];
+    cuuint32_t bx[5], es[5];
+    for (uint32_t i = 0; i < rank; i++) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = s->encode(m, dt, rank, const_cast<void*>(ptr), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    if (e) {
+        std::memcpy(&e->map, m, sizeof(CUtensorMap));
+        e->key = key;
+        e->valid = true;
+    }
+    return true;
+}
+
+bool encode_3d(DeviceState* s, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    cuuint32_t box[3] = {box0, box1, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const uint32_t box[3] = {box0, box1, 1};
+    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box);
 }
 
 // fp32 output view [d2][d1][d0] for bulk tensor stores, box {box0, box1, 1}.
-bool encode_3d_f32(EncodeTiledFn enc, CUtensorMap* m, void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+bool encode_3d_f32(DeviceState* s, CUtensorMap* m, void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    cuuint32_t box[3] = {box0, box1, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const uint32_t box[3] = {box0, box1, 1};
+    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box);
 }
 
-bool encode_4d(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+bool encode_4d(DeviceState* s, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t d3, uint64_t s1, uint64_t s2, uint64_t s3, uint32_t box0, uint32_t box1, uint32_t box2) {
-    cuuint64_t dims[4] = {d0, d1, d2, d3};
-    cuuint64_t strides[3] = {s1, s2, s3};
-    cuuint32_t box[4] = {box0, box1, box2, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[4] = {d0, d1, d2, d3};
+    const uint64_t strides[3] = {s1, s2, s3};
+    const uint32_t box[4] = {box0, box1, box2, 1};
+    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box);
 }
 
 bool tma_ok(const void* p, int64_t ld, int64_t batch, int64_t stride) {
@@ -1193,6 +1251,7 @@ mp_status device_init(mp_handle h, int device) {
         q != cudaDriverEntryPointSuccess || !fn)
         return MP_ERR_CUDA;
     s->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (!std::getenv("MP_NO_TMAP_CACHE")) s->tm_cache = new TmEntry[kTmCacheEntries]();
 
     if (cudaMalloc(&s->ws, sizeof(float) * (size_t)h->workspace_floats) != cudaSuccess) return MP_ERR_NO_MEMORY;
     if (cudaMalloc(&s->cnt, sizeof(unsigned) * (size_t)kMaxCounters) != cudaSuccess) return MP_ERR_NO_MEMORY;
@@ -1262,6 +1321,7 @@ void device_destroy(mp_handle h) {
         cudaFree(s->err);
         cudaFree(s->staging);
     }
+    delete[] s->tm_cache;
     delete s;
     h->dev = nullptr;
 }
@@ -1350,9 +1410,9 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         p.as_rows = as_rows;
         const uint64_t a_s2 = bA > 1 ? (uint64_t)sA * 2 : (uint64_t)round_up(M * lda * 2, 16);
         const uint64_t b_s2 = bB > 1 ? (uint64_t)sB * 2 : (uint64_t)round_up(K * ldb * 2, 16);
-        if (!encode_3d(s->encode, &p.tmA, A, K, M, bA, lda * 2, a_s2, 64, 128) ||
-            !encode_3d(s->encode, &p.tmAs, A, K, M, bA, lda * 2, a_s2, 64, (uint32_t)as_rows) ||
-            !encode_3d(s->encode, &p.tmB, B, N, K, bB, ldb * 2, b_s2, 64, 64))
+        if (!encode_3d(s, &p.tmA, A, K, M, bA, lda * 2, a_s2, 64, 128) ||
+            !encode_3d(s, &p.tmAs, A, K, M, bA, lda * 2, a_s2, 64, (uint32_t)as_rows) ||
+            !encode_3d(s, &p.tmB, B, N, K, bB, ldb * 2, b_s2, 64, 64))
             return MP_ERR_CUDA;
         // Whole-tile B copies: B as [batch][N/64][K][64] (block stride 128 B).
         // Only full 64-column blocks are addressable, so nothing past a row
@@ -1361,7 +1421,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         p.nb_full = (int)(N / 64);
         for (int j = 0; j < 4 && p.nb_full > 0; j++) {
             if (!need_b4[j]) continue;
-            if (!encode_4d(s->encode, &p.tmB4[j], B, 64, (uint64_t)K, (uint64_t)p.nb_full, (uint64_t)bB,
+            if (!encode_4d(s, &p.tmB4[j], B, 64, (uint64_t)K, (uint64_t)p.nb_full, (uint64_t)bB,
                            (uint64_t)ldb * 2, 128, b_s2, 64, 64, (uint32_t)(j + 1))) {
                 p.nb_full = 0;
                 p.b4_mask = 0;
@@ -1373,9 +1433,9 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         // K == 0: no operand is read; the maps only have to be well formed.
         p.as_rows = 16;
         p.nb_full = 0;
-        if (!encode_3d(s->encode, &p.tmA, s->staging, 64, 128, 1, 128, 128 * 128, 64, 128) ||
-            !encode_3d(s->encode, &p.tmAs, s->staging, 64, 128, 1, 128, 128 * 128, 64, 16) ||
-            !encode_3d(s->encode, &p.tmB, s->staging, 64, 128, 1, 128, 128 * 128, 64, 64))
+        if (!encode_3d(s, &p.tmA, s->staging, 64, 128, 1, 128, 128 * 128, 64, 128) ||
+            !encode_3d(s, &p.tmAs, s->staging, 64, 128, 1, 128, 128 * 128, 64, 16) ||
+            !encode_3d(s, &p.tmB, s->staging, 64, 128, 1, 128, 128 * 128, 64, 64))
             return MP_ERR_CUDA;
     }
     p.a_bstep = bA > 1 ? 1 : 0;
@@ -1391,7 +1451,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     if (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0 &&
         (batch == 1 || (a.strideD * 4) % 16 == 0)) {
         const uint64_t d_s2 = batch > 1 ? (uint64_t)a.strideD * 4 : (uint64_t)round_up(M * a.ldd * 4, 16);
-        if (encode_3d_f32(s->encode, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch, (uint64_t)a.ldd * 4,
+        if (encode_3d_f32(s, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch, (uint64_t)a.ldd * 4,
                           d_s2, 32, 32))
             p.tma_d = 1;
     }
@@ -1442,7 +1502,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         if (r.splits > 1) {
             const int64_t rows = tiles * r.splits * 128;
             if (!r.swap && ws_floats + rows * bn <= h->workspace_floats &&
-                encode_3d_f32(s->encode, &p.tmW[i], s->ws + ws_floats, (uint64_t)bn, (uint64_t)rows, 1,
+                encode_3d_f32(s, &p.tmW[i], s->ws + ws_floats, (uint64_t)bn, (uint64_t)rows, 1,
                               (uint64_t)bn * 4, (uint64_t)round_up(rows * bn * 4, 16), 32, 32))
                 p.w_mask |= 1 << i;
             ws_floats += rows * bn;
