@@ -647,6 +647,11 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
     }
 }
 
+// Wait until the previous kernel on the stream (programmatic dependent
+// launch) has completed and its memory operations are visible; returns at
+// once when there is none.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -723,12 +728,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Programmatic dependent launch: everything above (barrier set-up, TMEM,
-    // descriptor prefetch) may overlap the previous kernel on this stream;
-    // nothing below runs before that kernel has finished and its writes are
-    // visible.  The next kernel may then start its own set-up on SMs as they
-    // free up.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Programmatic dependent launch: set-up, work decoding and the first slot
+    // probes may overlap the previous kernel on this stream.  Each thread that
+    // touches global memory (the producers before their first copy, the
+    // epilogue before anything else) first waits until that kernel has
+    // finished and its writes are visible; every thread waits once more
+    // before exit, so this grid never completes ahead of its predecessor.
+    // The next kernel may start its own set-up on SMs as they free up.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || warp == kProducer2Warp) {
@@ -750,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t g = 0;
         uint32_t armed_mask = 0, armed_ph = 0;
         bool withhold = pid == 0 && p.inject_timeout != 0;
+        bool dep_done = false;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
             const Work w = decode(p, regs_s, u);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
@@ -763,6 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 int ok = 1;
                 if (lane == 0) ok = wait_fast(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_out;
+                if (!dep_done) {
+                    grid_dep_wait();
+                    dep_done = true;
+                }
                 if (!withhold) {
                     const uint32_t xs = ring0 + stage * stage_bytes, ys = xs + kXBytes;
                     const uint32_t fb = full(stage);
@@ -855,6 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         }
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        grid_dep_wait();
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t* epi_g = gbase + (epi0 - base) + (warp - 2) * kEpiWarpBytes;
         const uint32_t epi_s = epi0 + (uint32_t)((warp - 2) * kEpiWarpBytes);
@@ -1027,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         __syncwarp();
     }
 
+    grid_dep_wait();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
