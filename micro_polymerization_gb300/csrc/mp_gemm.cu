@@ -105,7 +105,9 @@ struct alignas(128) Params {
     int w_mask;          // bit i: tmW[i] is encoded
     int tma_d;           // 1: normal tiles store D through tmD (beta == 0, rows 16-byte aligned)
     int num_stages;      // shared-memory ring depth for this plan
-    int stage_bytes;     // 16 KB X tile + the widest Y tile of the plan
+    int sub_bytes;       // one 64-deep K step: 16 KB X tile + the widest Y tile of the plan
+    int kg;              // K steps per ring stage (1 or 2): one full/empty barrier pair per stage
+    int stage_bytes;     // kg * sub_bytes
     unsigned long long wait_limit_ns;
     Region reg[MP_MAX_REGIONS];
     float* ws;
@@ -681,7 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     Region* regs_s = reinterpret_cast<Region*>(gbase + (bar0 - base) + 512);
 
     const int nst = p.num_stages;
-    const uint32_t stage_bytes = (uint32_t)p.stage_bytes;  // X tile, then Y tile
+    const uint32_t stage_bytes = (uint32_t)p.stage_bytes;  // kg sub-stages of (X tile, then Y tile)
+    const uint32_t sub_bytes = (uint32_t)p.sub_bytes;
+    const int kg = p.kg;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
     auto accf = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
@@ -741,12 +745,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         // ------------------------------ TMA producers (two warps) -------------
         // Issuing a stage (probe the slot, copies, expect-tx) costs several
         // hundred cycles of dependent latency, so two warps take alternate
-        // K steps of the CTA's global step sequence g: step g uses stage
-        // g % nst, phase (g / nst) & 1, and belongs to warp 0 when g is even.
-        // Within a warp, lane 0 probes the slot and arms it; the stage's
-        // copies (one to five boxes) go out from different lanes in one
-        // instruction, before the expect-tx (the transaction count may run
-        // negative until then; the phase cannot complete without the arrive).
+        // stages of the CTA's global stage sequence g: a stage holds kg
+        // consecutive 64-deep K steps of one unit (fewer at the unit's end);
+        // stage g uses ring slot g % nst, phase (g / nst) & 1, and belongs to
+        // warp 0 when g is even.  Within a warp, lane 0 probes the slot and
+        // arms it; each K step's copies (one to five boxes) go out from
+        // different lanes in one instruction, before the expect-tx for the
+        // whole stage (the transaction count may run negative until then; the
+        // phase cannot complete without the arrive).
         //   normal tile:  lane 0 -> A box (128 rows), lanes 1.. -> B
         //   swapped tile: lane 0.. -> B^T (128 columns), lanes 2.. -> A
         // B comes in one box of all the tile's 64-column blocks when they
@@ -763,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const int blk0 = w.n_t0 >> 6;
             const int nblk = w.swap ? 2 : (w.bn >> 6);
             const bool whole_b = blk0 + nblk <= p.nb_full;
-            for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+            for (int kb = w.kb0; kb < w.kb1; kb += kg, ++g) {
                 if ((g & 1u) != pid) continue;
                 const int stage = (int)(g % (uint32_t)nst);
                 const uint32_t ph = (g / (uint32_t)nst) & 1u;
@@ -775,9 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     dep_done = true;
                 }
                 if (!withhold) {
-                    const uint32_t xs = ring0 + stage * stage_bytes, ys = xs + kXBytes;
                     const uint32_t fb = full(stage);
-                    const int kc = kb * 64;
+                    const int nsub = min(kg, w.kb1 - kb);
+                    for (int j = 0; j < nsub; j++) {
+                    const uint32_t xs = ring0 + stage * stage_bytes + j * sub_bytes, ys = xs + kXBytes;
+                    const int kc = (kb + j) * 64;
                     if (!w.swap) {
                         if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
                         if (whole_b) {
@@ -798,8 +806,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                             tma_load_3d(ys + c * p.as_rows * 128, &p.tmAs, fb, kc, w.m_t0 + c * p.as_rows, ab);
                         }
                     }
+                    }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(kXBytes + w.bn * 128));
+                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nsub * (kXBytes + w.bn * 128)));
                     armed_mask |= 1u << stage;
                     armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
                 }
@@ -838,17 +847,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const uint64_t dy0 = w.swap ? desc_kmajor(ring0 + kXBytes, 0) : desc_mnmajor(ring0 + kXBytes, 0);
             const uint32_t kx = w.swap ? (2048u >> 4) : (32u >> 4);
             const uint32_t ky = w.swap ? (32u >> 4) : (2048u >> 4);
-            const uint32_t sstep = stage_bytes >> 4;
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            const uint32_t sstep = stage_bytes >> 4, jstep = sub_bytes >> 4;
+            // One wait and one commit per stage of kg (1 or 2) K steps.
+            for (int kb = w.kb0; kb < w.kb1; kb += kg) {
                 ok = wait_fast(full(stage), ph, abort_flag, p.err, kErrWaitFull, limit);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t ax = dx0 + (uint64_t)(stage * sstep);
-                const uint64_t by = dy0 + (uint64_t)(stage * sstep);
+                uint64_t ax = dx0 + (uint64_t)(stage * sstep);
+                uint64_t by = dy0 + (uint64_t)(stage * sstep);
                 umma_bf16(d, ax, by, idesc, kb > w.kb0 ? 1u : 0u);
                 umma_bf16(d, ax + kx, by + ky, idesc, 1u);
                 umma_bf16(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
                 umma_bf16(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
+                if (kg > 1 && kb + 1 < w.kb1) {
+                    ax += jstep;
+                    by += jstep;
+                    umma_bf16(d, ax, by, idesc, 1u);
+                    umma_bf16(d, ax + kx, by + ky, idesc, 1u);
+                    umma_bf16(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
+                    umma_bf16(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
+                }
                 umma_commit(empty(stage));
                 if (++stage == nst) {
                     stage = 0;
@@ -1530,7 +1548,12 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // Ring depth: stages sized for the widest Y tile of this plan.
     int bn_max = 16;
     for (int i = 0; i < p.num_regions; i++) bn_max = std::max(bn_max, p.reg[i].bn);
-    p.stage_bytes = dev::kXBytes + bn_max * 128;
+    // The single MMA-issuing thread pays a fixed cost per stage (barrier
+    // wait, fence, commit) on top of each MMA; two K steps per stage halve
+    // that cost per MMA wherever the ring still holds at least three stages.
+    p.sub_bytes = dev::kXBytes + bn_max * 128;
+    p.kg = 3 * 2 * p.sub_bytes <= dev::kRingBytes ? 2 : 1;
+    p.stage_bytes = p.kg * p.sub_bytes;
     p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
 
     const int grid = (int)std::min<int64_t>(units, s->num_sms);
