@@ -82,11 +82,16 @@ typedef struct {
  * g_predict(t) = fixed_us + per_step_us * t for a pipeline task of t
  * micro-kernel instances [MP section 3, "micro-kernel performance model"].
  * swap = 1 marks the transposed form (D^T = B^T A^T) used for short M.
+ * pair = 1 marks a tile computed by a cluster of two CTAs on two SMs with the
+ * pair MMA (each CTA holds half of the tile's rows of A and D and half of its
+ * columns of B); such a kernel never splits K, and a plan uses either pair
+ * kernels only or none.
  */
 typedef struct {
     int32_t um, un, uk;
     int32_t warps;             /* warps per task, for wave counting            */
     int32_t swap;
+    int32_t pair;
     double fixed_us;           /* per-task time that does not scale with t     */
     double per_step_us;        /* time per micro-kernel instance (one uk step) */
 } mp_kernel_desc;
@@ -95,6 +100,7 @@ typedef struct {
 typedef struct {
     int32_t kernel;            /* index into the handle's micro-kernel set     */
     int32_t um, un, uk, swap;
+    int32_t pair;              /* tile computed by a CTA pair (see mp_kernel_desc) */
     int64_t m0, n0;            /* origin of the region in D                    */
     int64_t m_ext, n_ext;      /* extent of the region                         */
     int32_t splits;            /* split-K factor: K~_i = ceil(K / splits)      */
@@ -125,7 +131,10 @@ typedef struct {
  * "um un uk swap fixed_us per_step_us" ('#' starts a comment); lines that
  * name no kernel of the set are ignored.  The rates in H default to GB300
  * figures and can be overridden with the environment variables MP_HBM_GBS,
- * MP_L2_GBS and MP_MMA_TFLOPS.
+ * MP_L2_GBS and MP_MMA_TFLOPS.  The set holds the CTA-pair micro-kernels
+ * only when the device can keep two-CTA clusters of the kernel resident and
+ * MP_PAIR is not "0"; they come last, so the other kernels' indices do not
+ * depend on them.
  * Errors: MP_ERR_INVALID_ARG (out NULL or bad device), MP_ERR_UNSUPPORTED
  * (not sm_103), MP_ERR_NO_MEMORY, MP_ERR_CUDA.
  */

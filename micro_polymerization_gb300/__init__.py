@@ -43,13 +43,13 @@ class MpHw(ctypes.Structure):
 
 class MpKernelDesc(ctypes.Structure):
     _fields_ = [("um", ctypes.c_int32), ("un", ctypes.c_int32), ("uk", ctypes.c_int32),
-                ("warps", ctypes.c_int32), ("swap", ctypes.c_int32),
+                ("warps", ctypes.c_int32), ("swap", ctypes.c_int32), ("pair", ctypes.c_int32),
                 ("fixed_us", ctypes.c_double), ("per_step_us", ctypes.c_double)]
 
 
 class MpRegionInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("um", ctypes.c_int32), ("un", ctypes.c_int32),
-                ("uk", ctypes.c_int32), ("swap", ctypes.c_int32),
+                ("uk", ctypes.c_int32), ("swap", ctypes.c_int32), ("pair", ctypes.c_int32),
                 ("m0", ctypes.c_int64), ("n0", ctypes.c_int64),
                 ("m_ext", ctypes.c_int64), ("n_ext", ctypes.c_int64),
                 ("splits", ctypes.c_int32), ("f_num", ctypes.c_int32),

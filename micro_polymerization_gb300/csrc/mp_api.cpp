@@ -142,6 +142,7 @@ mp_status mp_init(mp_handle* out, int device, const char* calib_path) {
     h->hw.l2_gbs = env_double("MP_L2_GBS", h->hw.l2_gbs);
     h->hw.mma_tflops = env_double("MP_MMA_TFLOPS", h->hw.mma_tflops);
     mp::default_gb300_kernels(h->hw, h->kernels, &h->num_kernels);
+    mp::drop_unavailable_kernels(h);
     load_calibration(h, calib_path);
     *out = h;
     return MP_OK;

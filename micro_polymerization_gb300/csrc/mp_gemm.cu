@@ -31,6 +31,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -75,7 +77,10 @@ struct Region {
     int unit_begin, units;
     long long ws_begin;         // first fp32 of this region's split-K partials
     int cnt_begin;              // first tile counter
-    int pad_;
+    // Tile order: groups of `group` tile rows, column by column inside a
+    // group, so that the tiles in flight at once share their rows of A and
+    // columns of B in L2 (1: row by row).
+    int group;
 };
 
 struct alignas(128) Params {
@@ -108,6 +113,10 @@ struct alignas(128) Params {
     int sub_bytes;       // one 64-deep K step: 16 KB X tile + the widest Y tile of the plan
     int kg;              // K steps per ring stage (1 or 2): one full/empty barrier pair per stage
     int stage_bytes;     // kg * sub_bytes
+    // 1: clusters of two CTAs; a work unit is two vertically adjacent tiles
+    // (rank r takes tile row 2 t + r) that share their B tile, each CTA
+    // multicasting half of B's 64-column blocks into both shared memories.
+    int pair;
     unsigned long long wait_limit_ns;
     Region reg[MP_MAX_REGIONS];
     float* ws;
@@ -127,7 +136,8 @@ struct Work {
 };
 
 // `regs` is the shared-memory copy of p.reg made during set-up.
-__device__ __forceinline__ Work decode(const Params& p, const Region* regs, int u) {
+// In paired launches `u` counts tile pairs and `rank` picks the pair's tile.
+__device__ __forceinline__ Work decode(const Params& p, const Region* regs, int u, int rank) {
     int r = 0;
 #pragma unroll
     for (int i = 1; i < MP_MAX_REGIONS; i++)
@@ -142,12 +152,23 @@ __device__ __forceinline__ Work decode(const Params& p, const Region* regs, int 
     const int tile = rem / g.splits;
     w.split = rem - tile * g.splits;
     w.splits = g.splits;
-    const int tm = tile / g.tiles_n;
-    const int tn = tile - tm * g.tiles_n;
+    int tm, tn;
+    if (g.group > 1) {
+        const int per_group = g.group * g.tiles_n;
+        const int gi = tile / per_group;
+        const int first = gi * g.group;
+        const int rows = min(g.tiles_m - first, g.group);
+        const int in = tile - gi * per_group;
+        tn = in / rows;
+        tm = first + (in - tn * rows);
+    } else {
+        tm = tile / g.tiles_n;
+        tn = tile - tm * g.tiles_n;
+    }
     w.swap = g.swap;
     w.bn = g.bn;
     if (!g.swap) {
-        w.m_t0 = g.m0 + tm * 128;
+        w.m_t0 = g.m0 + (p.pair ? 2 * tm + rank : tm) * 128;
         w.n_t0 = g.n0 + tn * g.bn;
     } else {
         w.m_t0 = g.m0 + tm * g.bn;
@@ -260,6 +281,38 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Copies of the odd CTA of a pair: the box lands in this CTA's shared memory
+// and completes its bytes on the even CTA's barrier (`bar`, a cluster address
+// from mapa), where that CTA's MMA issuer waits for both halves.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Bulk tensor store of a shared-memory box to global memory (bulk-group
 // completion); rows and columns outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
@@ -284,19 +337,33 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// TMEM allocation.  CG = 1: one warp of the CTA; CG = 2: one warp of each
+// CTA of the pair, together (both receive the same address).  A kernel uses
+// one CTA group for all its tcgen05 operations.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                     : "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -308,14 +375,26 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], bf16 inputs, fp32 accumulate.
+// CG = 2: issued by the even CTA of a pair for both; each CTA holds its half
+// of A's rows and of B's columns at the same shared-memory offsets, and
+// receives its half of D's rows at the same TMEM address.
+template <int CG = 1>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
@@ -323,6 +402,29 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Pair version: arrive, once every tcgen05 operation issued so far by this
+// thread has completed, on the barrier at `bar`'s offset in every CTA of
+// `mask` (cluster ranks).
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on a barrier of another CTA of the cluster (address from mapa).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 16 consecutive accumulator columns of this thread's TMEM lane.
@@ -399,10 +501,11 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kstep) {
     return smem_desc(tile + 2048u * kstep, 8192u, 1024u);
 }
 
-// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, M = m (128, or
+// 256 for a CTA pair), N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn, int m = 128) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------
@@ -663,7 +766,11 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
 // ---------------------------------------------------------------------------
 // The persistent kernel
 // ---------------------------------------------------------------------------
+// CG = 1: one CTA per tile.  CG = 2: clusters of two CTAs on 256-row tile
+// pairs with the pair MMA (the even CTA issues for both; see umma_bf16).
+template <int CG>
 __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
+    constexpr bool kPair = CG == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -695,6 +802,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Pairs: a cluster of two CTAs works through tile pairs; rank 0 (the
+    // leader) waits for both CTAs' operands and issues the MMAs; its commits
+    // reach the barriers of both.
+    const int rank = kPair ? (int)cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int u0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int ustep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; s++) {
@@ -703,7 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(accf(b), 1);
-            mbar_init(acce(b), 4);
+            // The leader's accumulator is free once the epilogues of both
+            // CTAs have read their halves.
+            mbar_init(acce(b), kPair ? 8 : 4);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -726,10 +842,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     // dependency wait reads shared memory instead of cold parameter lines.
     if (threadIdx.x < MP_MAX_REGIONS) regs_s[threadIdx.x] = p.reg[threadIdx.x];
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish<CG>();
     }
     __syncthreads();
+    // Pairs: each CTA's copies, commits and arrivals also target the other's
+    // barriers, so both finish initialising them before either starts.
+    if (kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     // Programmatic dependent launch: set-up, work decoding and the first slot
@@ -763,8 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t armed_mask = 0, armed_ph = 0;
         bool withhold = pid == 0 && p.inject_timeout != 0;
         bool dep_done = false;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, regs_s, u);
+        for (int u = u0; u < p.total_units; u += ustep) {
+            const Work w = decode(p, regs_s, u, rank);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
             const int blk0 = w.n_t0 >> 6;
             const int nblk = w.swap ? 2 : (w.bn >> 6);
@@ -781,18 +900,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     dep_done = true;
                 }
                 if (!withhold) {
-                    const uint32_t fb = full(stage);
+                    // Pairs: the odd CTA's copies complete on the leader's barrier.
+                    const uint32_t fb = (kPair && !leader) ? mapa_shared(full(stage), 0) : full(stage);
                     const int nsub = min(kg, w.kb1 - kb);
                     for (int j = 0; j < nsub; j++) {
                     const uint32_t xs = ring0 + stage * stage_bytes + j * sub_bytes, ys = xs + kXBytes;
                     const int kc = (kb + j) * 64;
                     if (!w.swap) {
+                        if constexpr (kPair) {
+                            // This CTA's 128 rows of A and its half of B's
+                            // 64-column blocks (rank r: blocks [r h, r h + h)).
+                            const int h = nblk >> 1, first = rank * h;
+                            if (leader) {
+                                if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
+                                if (whole_b) {
+                                    if (lane == 1) tma_load_4d(ys, &p.tmB4[h - 1], fb, 0, kc, blk0 + first, bb);
+                                } else if (lane >= 1 && lane <= h) {
+                                    const int c = first + lane - 1;
+                                    tma_load_3d(ys + (lane - 1) * 8192, &p.tmB, fb, w.n_t0 + 64 * c, kc, bb);
+                                }
+                            } else {
+                                if (lane == 0) tma_load_3d_pair(xs, &p.tmA, fb, kc, w.m_t0, ab);
+                                if (whole_b) {
+                                    if (lane == 1) tma_load_4d_pair(ys, &p.tmB4[h - 1], fb, 0, kc, blk0 + first, bb);
+                                } else if (lane >= 1 && lane <= h) {
+                                    const int c = first + lane - 1;
+                                    tma_load_3d_pair(ys + (lane - 1) * 8192, &p.tmB, fb, w.n_t0 + 64 * c, kc, bb);
+                                }
+                            }
+                        } else {
                         if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
                         if (whole_b) {
                             if (lane == 1) tma_load_4d(ys, &p.tmB4[nblk - 1], fb, 0, kc, blk0, bb);
                         } else if (lane >= 1 && lane <= nblk) {
                             const int c = lane - 1;
                             tma_load_3d(ys + c * 8192, &p.tmB, fb, w.n_t0 + 64 * c, kc, bb);
+                        }
                         }
                     } else {
                         if (whole_b) {
@@ -808,9 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     }
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(nsub * (kXBytes + w.bn * 128)));
-                    armed_mask |= 1u << stage;
-                    armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    // The leader arms its barrier for both CTAs' bytes (A rows
+                    // and B halves of each); the odd CTA arms nothing.
+                    if (!kPair || leader) {
+                        const uint32_t bytes = kPair ? 2u * (kXBytes + (w.bn >> 1) * 128) : kXBytes + w.bn * 128;
+                        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)nsub * bytes);
+                        armed_mask |= 1u << stage;
+                        armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
+                    }
                 }
                 withhold = false;
             }
@@ -821,24 +969,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             for (int s = 0; s < nst; s++)
                 if (armed_mask & (1u << s))
                     wait_bounded(full(s), (armed_ph >> s) & 1u, abort_flag, p.err, kErrDrain, limit, false);
+        } else if (kPair && pid == 0 && lane == 0) {
+            // Pairs: the leader's MMA commits reach this CTA's empty barriers
+            // too; wait until the last use of every slot has been released,
+            // so that nothing arrives here after exit.
+            for (uint32_t s = 0; s < (uint32_t)nst && s < g; s++) {
+                const uint32_t k = (g - 1u - s) / (uint32_t)nst;
+                wait_bounded(empty((int)s), k & 1u, abort_flag, p.err, kErrDrain, limit, true);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------ MMA issuer (lane 0) --------------------
         // One thread waits, issues every MMA and every commit, so that each
-        // commit tracks exactly this thread's MMAs.
-        if (lane == 0) {
+        // commit tracks exactly this thread's MMAs.  Pairs: the leader's
+        // thread issues for both CTAs; the odd CTA's MMA warp only holds TMEM.
+        if (lane == 0 && (!kPair || leader)) {
         int stage = 0;
         uint32_t ph = 0;
         int acc = 0;
         uint32_t aph = 0;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, regs_s, u);
+        for (int u = u0; u < p.total_units; u += ustep) {
+            const Work w = decode(p, regs_s, u, rank);
             bool ok = wait_fast(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit);
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
-            const uint32_t idesc = w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true);
+            const uint32_t idesc =
+                w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
             // Descriptors of stage 0, K step 0.  Every later stage and K step
             // only moves the start address (bits 0..13, in 16-byte units;
             // shared addresses stay below 2^18, so the sums never carry out of
@@ -855,36 +1013,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_after();
                 uint64_t ax = dx0 + (uint64_t)(stage * sstep);
                 uint64_t by = dy0 + (uint64_t)(stage * sstep);
-                umma_bf16(d, ax, by, idesc, kb > w.kb0 ? 1u : 0u);
-                umma_bf16(d, ax + kx, by + ky, idesc, 1u);
-                umma_bf16(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
-                umma_bf16(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
+                umma_bf16<CG>(d, ax, by, idesc, kb > w.kb0 ? 1u : 0u);
+                umma_bf16<CG>(d, ax + kx, by + ky, idesc, 1u);
+                umma_bf16<CG>(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
+                umma_bf16<CG>(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
                 if (kg > 1 && kb + 1 < w.kb1) {
                     ax += jstep;
                     by += jstep;
-                    umma_bf16(d, ax, by, idesc, 1u);
-                    umma_bf16(d, ax + kx, by + ky, idesc, 1u);
-                    umma_bf16(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
-                    umma_bf16(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
+                    umma_bf16<CG>(d, ax, by, idesc, 1u);
+                    umma_bf16<CG>(d, ax + kx, by + ky, idesc, 1u);
+                    umma_bf16<CG>(d, ax + 2 * kx, by + 2 * ky, idesc, 1u);
+                    umma_bf16<CG>(d, ax + 3 * kx, by + 3 * ky, idesc, 1u);
                 }
-                umma_commit(empty(stage));
+                if constexpr (kPair)
+                    umma_commit_pair(empty(stage), (uint16_t)3);  // the slot of both CTAs
+                else
+                    umma_commit(empty(stage));
                 if (++stage == nst) {
                     stage = 0;
                     ph ^= 1u;
                 }
             }
             if (!ok) break;
-            umma_commit(accf(acc));
+            if constexpr (kPair)
+                umma_commit_pair(accf(acc), (uint16_t)3);  // both CTAs' epilogues
+            else
+                umma_commit(accf(acc));
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
         }
         // Every MMA this thread issued has completed once `done_bar` flips.
-        umma_commit(done_bar);
+        if constexpr (kPair)
+            umma_commit_pair(done_bar, (uint16_t)1);
+        else
+            umma_commit(done_bar);
         wait_bounded(done_bar, 0, abort_flag, p.err, kErrDrain, limit, false);
         }
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
         grid_dep_wait();
+        // The accumulator buffer goes back to the MMA issuer: the leader's
+        // barrier, from both CTAs of a pair.
+        auto release_acc = [&](int b) {
+            if (kPair && !leader)
+                mbar_arrive_remote(mapa_shared(acce(b), 0));
+            else
+                mbar_arrive(acce(b));
+        };
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint8_t* epi_g = gbase + (epi0 - base) + (warp - 2) * kEpiWarpBytes;
         const uint32_t epi_s = epi0 + (uint32_t)((warp - 2) * kEpiWarpBytes);
@@ -892,8 +1067,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t slab = 0;  // running slab index of this warp's bulk stores
         int acc = 0;
         uint32_t aph = 0;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Work w = decode(p, regs_s, u);
+        for (int u = u0; u < p.total_units; u += ustep) {
+            const Work w = decode(p, regs_s, u, rank);
             if (p.tma_d && p.beta != 0.0f && w.splits == 1 && !w.swap) prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
             int ok = 1;
             if (lane == 0)
@@ -935,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce(acc));
+                if (lane == 0) release_acc(acc);
             } else if (w.splits == 1) {
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
@@ -949,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce(acc));
+                if (lane == 0) release_acc(acc);
             } else {
                 // Split-K: park this split's partial (D-row-major per tile),
                 // free the TMEM buffer, wait until every split of the tile
@@ -1006,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acce(acc));  // TMEM buffer free for the next unit
+                if (lane == 0) release_acc(acc);  // TMEM buffer free for the next unit
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (threadIdx.x == 64) {
@@ -1059,9 +1234,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 
     grid_dep_wait();
     __syncthreads();
+    if constexpr (kPair) {
+        // After an abort, copies or commits of the peer may still be in
+        // flight towards this CTA: give them time to land (they need
+        // microseconds) before the pair leaves together.
+        if (threadIdx.x == 0 && *abort_flag) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
+        }
+        __syncthreads();
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc<CG>(tmem, kTmemCols);
     }
 }
 
@@ -1136,7 +1322,34 @@ struct DeviceState {
     uint64_t wait_limit_ns = 1000000000ull;  // 1 s
     // Tensor-map cache (only for handles, which serve one host thread).
     TmEntry* tm_cache = nullptr;
+    // Clusters of two CTAs of k_poly_gemm that can be resident at once (0:
+    // paired launches disabled).
+    int max_pairs = 0;
 };
+
+// Resident two-CTA clusters of the persistent kernel (0 if the query fails).
+int query_max_pairs(int num_sms) {
+    // MP_PAIR=0 leaves pair micro-kernels out of the handle's set.
+    if (const char* v = std::getenv("MP_PAIR"))
+        if (std::atoi(v) == 0) return 0;
+    cudaLaunchConfig_t oc = {};
+    oc.gridDim = dim3((unsigned)(2 * ((num_sms + 1) / 2)));
+    oc.blockDim = dim3(dev::kThreads);
+    oc.dynamicSmemBytes = dev::kSmemBytes;
+    cudaLaunchAttribute ca[1];
+    ca[0].id = cudaLaunchAttributeClusterDimension;
+    ca[0].val.clusterDim.x = 2;
+    ca[0].val.clusterDim.y = 1;
+    ca[0].val.clusterDim.z = 1;
+    oc.attrs = ca;
+    oc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<2>, &oc) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
 
 namespace {
 
@@ -1235,10 +1448,11 @@ bool tma_ok(const void* p, int64_t ld, int64_t batch, int64_t stride) {
     return true;
 }
 
-void log_plan(const mp_plan_info& plan, const GemmArgs& a, int grid) {
-    std::fprintf(stderr, "[mp] batch=%lld M=%lld N=%lld K=%lld pattern=%d regions=%d tasks=%lld grid=%d cost=%.2fus\n",
+void log_plan(const mp_plan_info& plan, const GemmArgs& a, int grid, int pair) {
+    std::fprintf(stderr,
+                 "[mp] batch=%lld M=%lld N=%lld K=%lld pattern=%d regions=%d tasks=%lld grid=%d paired=%d cost=%.2fus\n",
                  (long long)a.batch, (long long)a.M, (long long)a.N, (long long)a.K, plan.pattern,
-                 plan.num_regions, (long long)plan.total_tasks, grid, plan.cost_us);
+                 plan.num_regions, (long long)plan.total_tasks, grid, pair, plan.cost_us);
     for (int i = 0; i < plan.num_regions; i++) {
         const mp_region_info& r = plan.region[i];
         std::fprintf(stderr, "[mp]   R%d [%lld+%lld, %lld+%lld] kernel=%d (%dx%d%s) splits=%d f_num=%d waves=%lld pipe=%.2fus\n",
@@ -1290,9 +1504,12 @@ mp_status device_init(mp_handle h, int device) {
     if (cudaMalloc(&s->staging, (size_t)s->staging_bytes) != cudaSuccess) return MP_ERR_NO_MEMORY;
     if (cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)kMaxCounters) != cudaSuccess) return MP_ERR_CUDA;
     if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
-    if (cudaFuncSetAttribute(dev::k_poly_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dev::k_poly_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+            cudaSuccess)
         return MP_ERR_CUDA;
+    s->max_pairs = query_max_pairs(s->num_sms);
     if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
@@ -1324,9 +1541,12 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
         q != cudaDriverEntryPointSuccess || !fn)
         return MP_ERR_CUDA;
     s->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (cudaFuncSetAttribute(dev::k_poly_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dev::k_poly_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
+            cudaSuccess)
         return MP_ERR_CUDA;
+    s->max_pairs = query_max_pairs(s->num_sms);
     h->host_only = false;
     h->device = device;
     h->hw.num_pe = prop.multiProcessorCount;
@@ -1386,6 +1606,11 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     std::memset(&p, 0, sizeof(p));
     const int64_t batch = a.batch, M = a.M, N = a.N, K = a.K;
 
+    // ---- CTA pairs: the plan's regions are all pair tiles or none ----------
+    const int pair = plan.num_regions > 0 && plan.region[0].pair ? 1 : 0;
+    if (pair && s->max_pairs <= 0) return MP_ERR_UNSUPPORTED;
+    p.pair = pair;
+
     // ---- operands: TMA views, repacked when rows are not 16-byte aligned ----
     const void* A = a.A;
     const void* B = a.B;
@@ -1435,7 +1660,12 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
                 as_rows = std::min(as_rows, (int)r.um);
                 need_b4[1] = true;
             } else if (r.un >= 64 && r.un <= 256) {
-                need_b4[r.un / 64 - 1] = true;
+                const int nblk = (int)(r.un / 64);
+                if (r.pair) {  // each CTA of a pair holds half of the blocks
+                    need_b4[nblk / 2 - 1] = true;
+                } else {
+                    need_b4[nblk - 1] = true;
+                }
             }
         }
         p.as_rows = as_rows;
@@ -1510,15 +1740,30 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         const mp_region_info& r = plan.region[i];
         dev::Region& d = p.reg[i];
         const int bn = r.swap ? r.um : r.un;
-        if (r.uk != kUk || bn < 16 || bn > kMaxBn || bn % 16 != 0 || (!r.swap && (r.um != 128 || bn % 64 != 0)) ||
-            (r.swap && r.un != 128))
+        if (r.uk != kUk || bn < 16 || bn > kMaxBn || bn % 16 != 0 || (r.pair != 0) != (pair != 0) ||
+            (!r.swap && !r.pair && (r.um != 128 || bn % 64 != 0)) || (r.swap && (r.un != 128 || r.pair)) ||
+            (r.pair && (r.um != 256 || (bn != 128 && bn != 256) || r.splits != 1)))
             return MP_ERR_PLAN;
         d.m0 = (int)r.m0;
         d.n0 = (int)r.n0;
         d.m_end = (int)(r.m0 + r.m_ext);
         d.n_end = (int)(r.n0 + r.n_ext);
-        d.tiles_m = (int)cdiv(r.m_ext, r.um);
+        d.tiles_m = (int)cdiv(r.m_ext, r.um);  // pairs: rows of 256-row tile pairs
         d.tiles_n = (int)cdiv(r.n_ext, r.un);
+        {
+            // When one problem's operands do not stay in L2 across waves,
+            // order tiles so that a wave of `slots` tiles covers G rows x
+            // slots/G columns; A and B bytes per wave balance at
+            // G = sqrt(slots * un / um).
+            const int64_t slots = pair ? s->max_pairs : s->num_sms;
+            const double operand_bytes = 2.0 * (double)(M * K + K * N);
+            int grp = 1;
+            if ((int64_t)d.tiles_m * d.tiles_n > slots && operand_bytes > 0.6 * (double)h->hw.shared_mem_bytes) {
+                grp = (int)std::lround(std::sqrt((double)slots * (double)r.un / (double)r.um));
+                grp = std::max(1, std::min(grp, d.tiles_m));
+            }
+            d.group = grp;
+        }
         d.bn = bn;
         d.swap = r.swap;
         d.splits = r.splits;
@@ -1551,13 +1796,13 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // The single MMA-issuing thread pays a fixed cost per stage (barrier
     // wait, fence, commit) on top of each MMA; two K steps per stage halve
     // that cost per MMA wherever the ring still holds at least three stages.
-    p.sub_bytes = dev::kXBytes + bn_max * 128;
+    p.sub_bytes = dev::kXBytes + (pair ? bn_max / 2 : bn_max) * 128;  // a pair's CTA holds half of B
     p.kg = 3 * 2 * p.sub_bytes <= dev::kRingBytes ? 2 : 1;
     p.stage_bytes = p.kg * p.sub_bytes;
     p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
 
-    const int grid = (int)std::min<int64_t>(units, s->num_sms);
-    if (s->log) log_plan(plan, a, grid);
+    const int grid = pair ? 2 * (int)std::min<int64_t>(units, s->max_pairs) : (int)std::min<int64_t>(units, s->num_sms);
+    if (s->log) log_plan(plan, a, grid, pair);
     // One CTA per SM; launched as a programmatic dependent of the previous
     // kernel on the stream so that its set-up overlaps that kernel's tail.
     cudaLaunchConfig_t cfg = {};
@@ -1565,13 +1810,29 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     cfg.blockDim = dim3(dev::kThreads);
     cfg.dynamicSmemBytes = dev::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = pair ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, dev::k_poly_gemm, p) != cudaSuccess) return MP_ERR_CUDA;
+    cfg.numAttrs = pair ? 2 : 1;
+    const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<2>, p)
+                               : cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<1>, p);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
+}
+
+// A device that cannot hold two-CTA clusters of the kernel (or MP_PAIR=0)
+// keeps no pair micro-kernels in its set.
+void drop_unavailable_kernels(mp_handle h) {
+    if (!h || !h->dev || h->dev->max_pairs > 0) return;
+    int32_t n = 0;
+    for (int32_t k = 0; k < h->num_kernels; k++)
+        if (!h->kernels[k].pair) h->kernels[n++] = h->kernels[k];
+    h->num_kernels = n;
 }
 
 }  // namespace mp

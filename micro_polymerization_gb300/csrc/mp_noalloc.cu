@@ -72,6 +72,7 @@ mp_status setup(int device, PerDevice** out) {
                                                counters, status, staging, (int64_t)kStagingBytes);
         if (st != MP_OK) return st;
         mp::default_gb300_kernels(d.handle.hw, d.handle.kernels, &d.handle.num_kernels);
+        mp::drop_unavailable_kernels(&d.handle);
         d.counters = counters;
         d.ready = true;
     }

@@ -37,6 +37,9 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Latency of the split-K handshake (atomic arrive, acquire poll, barrier).
 constexpr double kSplitSyncUs = 1.0;
+// Extra fixed time of a CTA-pair task: cluster set-up and exit, the
+// leader's commits reaching the peer (measured on GB300: about 1.5 us).
+constexpr double kPairFixedUs = 1.5;
 
 struct RegionEval {
     int32_t kernel = -1;
@@ -87,7 +90,7 @@ RegionEval eval_region(const mp_handle_s* h, int32_t k, int64_t m_ext, int64_t n
     r.f_pipe = f_pipe_of(h, u, f_num, splits);
     r.cost = (double)r.f_wave * r.f_pipe;
     r.ws_floats = splits > 1 ? tiles * splits * (int64_t)u.um * u.un : 0;
-    r.ok = splits == 1 || (r.ws_floats <= h->workspace_floats && tiles <= kMaxCounters);
+    r.ok = splits == 1 || (!u.pair && r.ws_floats <= h->workspace_floats && tiles <= kMaxCounters);
     return r;
 }
 
@@ -97,7 +100,7 @@ int split_candidates(const mp_handle_s* h, const mp_kernel_desc& u, int64_t tile
                      int32_t* out) {
     int n = 0;
     out[n++] = 1;
-    if (kb <= 1 || tiles <= 0) return n;
+    if (kb <= 1 || tiles <= 0 || u.pair) return n;  // CTA pairs do not split K
     int64_t slots = slots_for(h, u);
     if (tiles >= slots) return n;
     static const int32_t kFactors[] = {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64};
@@ -166,7 +169,7 @@ void fill_info(const mp_handle_s* h, const Strategy& s, int64_t K, mp_plan_info*
         const mp_kernel_desc& u = h->kernels[e.kernel];
         mp_region_info& r = out->region[i];
         r.kernel = e.kernel;
-        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap;
+        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap; r.pair = u.pair;
         r.m0 = s.m0[i]; r.n0 = s.n0[i]; r.m_ext = s.m_ext[i]; r.n_ext = s.n_ext[i];
         r.splits = e.splits;
         r.f_num = e.f_num;
@@ -265,6 +268,7 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
                 for (int32_t b = 0; b < h->num_kernels; b++) {
                     const mp_kernel_desc& ub = h->kernels[b];
                     if (dir == 1 && ub.un % 8 != 0) continue;
+                    if (ub.pair != ua.pair) continue;  // one launch: all pairs or none
                     int64_t rm = dir == 0 ? rest : M, rn = dir == 0 ? N : rest;
                     int64_t tiles_b = cdiv(rm, ub.um) * cdiv(rn, ub.un) * batch;
                     int64_t kb = cdiv(K, ub.uk);
@@ -356,6 +360,7 @@ mp_status validate_plan(const mp_plan_info& p, int64_t M, int64_t N, int64_t K) 
         if (r.m0 + r.m_ext > M || r.n0 + r.n_ext > N) return MP_ERR_PLAN;
         if (r.n0 % 8 != 0) return MP_ERR_PLAN;  // TMA x coordinate rule on B
         if (r.splits < 1) return MP_ERR_PLAN;
+        if (r.pair != p.region[0].pair || (r.pair && r.splits != 1)) return MP_ERR_PLAN;
         area += r.m_ext * r.n_ext;
         for (int j = 0; j < i; j++) {
             const mp_region_info& q = p.region[j];
@@ -379,7 +384,7 @@ mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_
         if (r.kernel < 0 || r.kernel >= h->num_kernels) return MP_ERR_INVALID_ARG;
         RegionEval e = eval_region(h, r.kernel, r.m_ext, r.n_ext, K, batch, std::max(1, r.splits));
         const mp_kernel_desc& u = h->kernels[r.kernel];
-        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap;
+        r.um = u.um; r.un = u.un; r.uk = u.uk; r.swap = u.swap; r.pair = u.pair;
         r.splits = e.splits;
         r.f_num = e.f_num;
         r.f_parallel = e.f_parallel;
@@ -398,12 +403,17 @@ mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_
 // calibration table replaces it).  Normal kernels: a 128-row accumulator
 // (UMMA M = 128) against un = 64..256 columns of B.  Swapped kernels compute
 // D^T = B^T A^T: the UMMA M = 128 runs over N and the short M becomes the
-// UMMA N (16..128), so a skinny M wastes no tensor-core rows.
+// UMMA N (16..128), so a skinny M wastes no tensor-core rows.  Pair kernels
+// put a 256-row tile on two SMs (pair MMA): each SM loads 128 rows of A and
+// half of B's columns, so operand bytes per MMA fall by a third (256 wide) or
+// a quarter (128 wide); a task holds two SMs, and the cluster set-up and
+// exit cost a fixed extra.
 void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
-    struct G { int um, un, swap; };
+    struct G { int um, un, swap, pair; };
     static const G kSet[] = {
-        {128, 256, 0}, {128, 192, 0}, {128, 128, 0}, {128, 64, 0},
-        {16, 128, 1},  {32, 128, 1},  {64, 128, 1},  {128, 128, 1},
+        {128, 256, 0, 0}, {128, 192, 0, 0}, {128, 128, 0, 0}, {128, 64, 0, 0},
+        {16, 128, 1, 0},  {32, 128, 1, 0},  {64, 128, 1, 0},  {128, 128, 1, 0},
+        {256, 256, 0, 1}, {256, 128, 0, 1},
     };
     const double pe = std::max(1, hw.num_pe);
     const double mma_pe = hw.mma_tflops > 0 ? hw.mma_tflops / pe : 13.0;   // TFLOP/s per PE
@@ -415,16 +425,18 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
         d.um = g.um;
         d.un = g.un;
         d.uk = kUk;
-        d.warps = kModelWarpsPerTask;  // one CTA per SM: one task slot per PE
+        d.warps = kModelWarpsPerTask * (g.pair ? 2 : 1);  // one CTA per SM: one task slot per PE
         d.swap = g.swap;
+        d.pair = g.pair;
+        // Per SM: a 128-row accumulator; a pair's SM holds half of B.
         const double n_umma = g.swap ? g.um : g.un;
         const double flops = 2.0 * kUmmaM * std::max(32.0, n_umma) * kUk;
         const double mma_us = flops / (mma_pe * 1e6);
-        const double bytes = (kUmmaM + n_umma) * kUk * 2.0;
+        const double bytes = (kUmmaM + (g.pair ? n_umma / 2 : n_umma)) * kUk * 2.0;
         const double load_us = bytes / (l2_pe * 1e3);
         d.per_step_us = std::max(mma_us, load_us);
-        const double epi_bytes = 4.0 * g.um * g.un;
-        d.fixed_us = 0.6 + 0.5 * epi_bytes / (hbm_pe * 1e3);
+        const double epi_bytes = 4.0 * kUmmaM * (g.swap ? g.um : g.un);  // per SM
+        d.fixed_us = 0.6 + 0.5 * epi_bytes / (hbm_pe * 1e3) + (g.pair ? kPairFixedUs : 0.0);
     }
     *n = c;
 }

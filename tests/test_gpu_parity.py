@@ -93,6 +93,8 @@ def test_each_micro_kernel(splits):
     ks = _kernels()
     try:
         for k, desc in enumerate(ks):
+            if desc.pair and splits > 1:
+                continue  # CTA pairs do not split K
             for (M, N, K) in [(200, 300, 500), (37, 520, 130), (130, 129, 64)]:
                 mp.mp_force_plan(h, k, splits)
                 A, B, C = rand_problem(M, N, K, seed=k * 31 + M, beta=0.5)
@@ -103,12 +105,79 @@ def test_each_micro_kernel(splits):
         mp.mp_force_plan(h, -1, 0)
 
 
+@pytest.mark.parametrize("M,N,K", [(421, 1000, 320), (256, 512, 640), (1000, 768, 200), (128, 2304, 768),
+                                   (2048, 1024, 1024)])
+def test_pair_kernels_match_single_cta_kernels_and_oracle(M, N, K):
+    """A 256-row tile on a CTA pair (pair MMA, each CTA holding half of A's
+    rows and of B's columns) computes exactly what two 128-row tiles on one
+    CTA each compute: the same MMAs per output row, so the outputs agree bit
+    for bit.  Odd tile-row counts leave the second half of the last pair past
+    the end of D."""
+    h = handle()
+    ks = _kernels()
+    pairs = [(k, d) for k, d in enumerate(ks) if d.pair]
+    assert {(d.um, d.un) for _, d in pairs} == {(256, 256), (256, 128)}
+    try:
+        for k, d in pairs:
+            single = next(i for i, e in enumerate(ks) if not e.pair and not e.swap and e.un == d.un)
+            A, B, C = rand_problem(M, N, K, seed=k * 7 + M, beta=0.5)
+            mp.mp_force_plan(h, single, 1)
+            D1 = run_gemm(A, B, C, 1.25, 0.5)
+            mp.mp_force_plan(h, k, 1)
+            D2 = run_gemm(A, B, C, 1.25, 0.5)
+            assert torch.equal(D1, D2), f"pair kernel {k} ({d.um}x{d.un}) {(M, N, K)}"
+            assert_parity(D2, A, B, C, 1.25, 0.5, what=f"pair kernel {k} {(M, N, K)}")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
+def test_pair_kernel_launches_as_cluster(capfd):
+    """A plan of pair tiles launches as two-CTA clusters (the plan log says so)."""
+    import os
+    os.environ["MP_LOG"] = "1"
+    try:
+        h = mp.mp_init(0)
+    finally:
+        del os.environ["MP_LOG"]
+    try:
+        ks = _kernels()
+        k = next(i for i, d in enumerate(ks) if d.pair and d.un == 256)
+        mp.mp_force_plan(h, k, 1)
+        A, B, C = rand_problem(1024, 1024, 256, seed=3)
+        D = run_gemm(A, B, None, 1.0, 0.0, h=h)
+        err = capfd.readouterr().err
+        assert "paired=1" in err, err
+        assert_parity(D, A, B, None, 1.0, 0.0, what="pair 1024^2 x 256")
+    finally:
+        h.close()
+
+
+def test_handle_without_pairs_drops_pair_kernels():
+    """MP_PAIR=0 when the handle is made: no pair micro-kernels in its set,
+    and the other kernels keep their indices."""
+    import os
+    os.environ["MP_PAIR"] = "0"
+    try:
+        h = mp.mp_init(0)
+    finally:
+        del os.environ["MP_PAIR"]
+    try:
+        _, ks0 = mp.mp_get_hw(h)
+        ks = _kernels()
+        assert not any(d.pair for d in ks0)
+        assert [(d.um, d.un, d.swap) for d in ks0] == [(d.um, d.un, d.swap) for d in ks if not d.pair]
+        A, B, C = rand_problem(300, 1000, 500, seed=4)
+        assert_parity(run_gemm(A, B, None, 1.0, 0.0, h=h), A, B, None, 1.0, 0.0, what="no-pair handle")
+    finally:
+        h.close()
+
+
 def test_split_k_integer_exact_and_deterministic():
     h = handle()
     A, B, C = wl.integer_operands(105, 1024, 4000, seed=9)
     try:
-        for k in range(len(_kernels())):
-            mp.mp_force_plan(h, k, 7)
+        for k, desc in enumerate(_kernels()):
+            mp.mp_force_plan(h, k, 1 if desc.pair else 7)
             D1 = run_gemm(A, B, C, 1.0, 1.0)
             D2 = run_gemm(A, B, C, 1.0, 1.0)
             Dref, _ = oracle_full(A, B, C, 1.0, 1.0)
@@ -195,8 +264,8 @@ def test_output_guard_bands():
     A, B, _ = rand_problem(M, N, K, seed=12)
     buf = torch.full((pad + M * (N + 3) + pad,), -12345.0, device=dev)
     D = buf[pad:pad + M * (N + 3)].view(M, N + 3)[:, :N]
-    for k in range(len(_kernels())):
-        mp.mp_force_plan(handle(), k, 2)
+    for k, desc in enumerate(_kernels()):
+        mp.mp_force_plan(handle(), k, 1 if desc.pair else 2)
         mp.mp_gemm(handle(), A.to(dev), B.to(dev), None, D, 1.0, 0.0)
     mp.mp_force_plan(handle(), -1, 0)
     torch.cuda.synchronize()

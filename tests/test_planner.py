@@ -133,6 +133,14 @@ def test_forced_plan_and_errors():
     _, ks = mp.mp_get_hw(h)
     for k in range(len(ks)):
         mp.mp_force_plan(h, k, 3)
+        if ks[k].pair:
+            # CTA pairs never split K: a forced split has no valid plan.
+            with pytest.raises(mp.MPError):
+                mp.mp_plan(h, 300, 500, 700)
+            mp.mp_force_plan(h, k, 1)
+            p = mp.mp_plan(h, 300, 500, 700)
+            assert p.num_regions == 1 and p.region[0].kernel == k and p.region[0].pair == 1
+            continue
         p = mp.mp_plan(h, 300, 500, 700)
         assert p.num_regions == 1 and p.region[0].kernel == k and p.region[0].splits == 3
     mp.mp_force_plan(h, -1, 0)
@@ -155,4 +163,32 @@ def test_empty_shapes_plan_to_nothing():
     for M, N in [(0, 5), (5, 0), (0, 0)]:
         p = mp.mp_plan(h, M, N, 10)
         assert p.num_regions == 0 and p.total_tasks == 0
+    h.close()
+
+
+def test_pair_kernels_hold_two_sms_never_split_never_mix():
+    """Pair micro-kernels (a 256-row tile on a CTA pair) take two SMs' worth
+    of task slots, never split K, and never share a plan with one-CTA
+    kernels; a mixed plan is refused."""
+    h = gb300_handle()
+    hw, ks = mp.mp_get_hw(h)
+    pairs = [k for k, d in enumerate(ks) if d.pair]
+    singles = [k for k, d in enumerate(ks) if not d.pair]
+    assert pairs and all(ks[k].warps == 2 * ks[singles[0]].warps and ks[k].um == 256 for k in pairs)
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        M, N, K = int(rng.integers(1, 9000)), 8 * int(rng.integers(1, 1200)), int(rng.integers(1, 9000))
+        p = mp.mp_plan(h, M, N, K)
+        check_tiling(p, M, N)
+        assert len({r.pair for r in p.regions()}) == 1, (M, N, K)
+        for r in p.regions():
+            if r.pair:
+                assert r.splits == 1 and r.um == 256 and not r.swap
+    single = next(k for k in singles if not ks[k].swap and ks[k].un == 256)
+    bad = mp.MpPlanInfo()
+    bad.num_regions = 2
+    for i, (k, m0, me) in enumerate([(pairs[0], 0, 512), (single, 512, 512)]):
+        bad.region[i].kernel, bad.region[i].m0, bad.region[i].m_ext = k, m0, me
+        bad.region[i].n0, bad.region[i].n_ext, bad.region[i].splits = 0, 256, 1
+    assert mp.library().mp_evaluate_plan(h.ptr, 1, 1024, 256, 256, ctypes.byref(bad)) == mp.MP_ERR_PLAN
     h.close()
