@@ -1796,8 +1796,10 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // The single MMA-issuing thread pays a fixed cost per stage (barrier
     // wait, fence, commit) on top of each MMA; two K steps per stage halve
     // that cost per MMA wherever the ring still holds at least three stages.
+    // CTA pairs issue one MMA for two SMs, so there the deeper ring of
+    // single K steps hides more latency (measured: 6 x 32 KB beats 3 x 64 KB).
     p.sub_bytes = dev::kXBytes + (pair ? bn_max / 2 : bn_max) * 128;  // a pair's CTA holds half of B
-    p.kg = 3 * 2 * p.sub_bytes <= dev::kRingBytes ? 2 : 1;
+    p.kg = (!pair && 3 * 2 * p.sub_bytes <= dev::kRingBytes) ? 2 : 1;
     p.stage_bytes = p.kg * p.sub_bytes;
     p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
 
