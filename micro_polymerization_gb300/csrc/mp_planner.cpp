@@ -35,8 +35,14 @@ namespace {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Latency of the split-K handshake (atomic arrive, acquire poll, barrier).
-constexpr double kSplitSyncUs = 1.0;
+// Split-K: every split parks its fp32 partial, waits for the tile's other
+// splits (a counter round trip through L2) and sums 1/S of all partials.
+// Measured on GB300: about 6 us beyond the K loop for a 128 x 128 tile.
+constexpr double kSplitSyncUs = 4.0;
+constexpr double kSplitBytesFactor = 4.0;  // tile bytes moved, in L2 passes
+// Floor of one uk step of any micro-kernel: the single MMA-issuing thread's
+// per-instruction and per-stage cost (measured on GB300 with tiny tiles).
+constexpr double kStepFloorUs = 0.21;
 // Extra fixed time of a CTA-pair task: cluster set-up and exit, the
 // leader's commits reaching the peer (measured on GB300: about 1.5 us).
 constexpr double kPairFixedUs = 1.5;
@@ -66,7 +72,7 @@ inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f
     if (splits > 1 && h->hw.l2_gbs > 0 && h->hw.num_pe > 0) {
         double tile_bytes = 4.0 * u.um * u.un;
         double pe_gbs = h->hw.l2_gbs / h->hw.num_pe;
-        t += kSplitSyncUs + 2.0 * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
+        t += kSplitSyncUs + kSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
     }
     return t;
 }
@@ -434,9 +440,11 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
         const double mma_us = flops / (mma_pe * 1e6);
         const double bytes = (kUmmaM + (g.pair ? n_umma / 2 : n_umma)) * kUk * 2.0;
         const double load_us = bytes / (l2_pe * 1e3);
-        d.per_step_us = std::max(mma_us, load_us);
+        d.per_step_us = std::max(std::max(mma_us, load_us), kStepFloorUs);
+        // Epilogue: the tile's fp32 output at the SM's share of HBM; the
+        // swapped form stores straight from registers at about half the rate.
         const double epi_bytes = 4.0 * kUmmaM * (g.swap ? g.um : g.un);  // per SM
-        d.fixed_us = 0.6 + 0.5 * epi_bytes / (hbm_pe * 1e3) + (g.pair ? kPairFixedUs : 0.0);
+        d.fixed_us = 0.6 + (g.swap ? 2.0 : 1.0) * epi_bytes / (hbm_pe * 1e3) + (g.pair ? kPairFixedUs : 0.0);
     }
     *n = c;
 }
