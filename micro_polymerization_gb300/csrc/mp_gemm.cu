@@ -330,6 +330,9 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Every bulk store this thread issued has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Generic-proxy writes to shared memory become visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
@@ -608,6 +611,68 @@ __device__ __forceinline__ void transpose16(int lane, const float* v, float4* st
     __syncwarp();
 }
 
+// Normal tile whose D rows are not 16-byte aligned (no tensor map; any
+// alignment): the warp's 32 rows x 32 columns go through its shared-memory
+// slab (128-byte swizzle, conflict-free both ways) and come back one row at
+// a time with lane = column, so that every store instruction covers 128
+// contiguous bytes of one row of D.  Same arithmetic as the other paths.
+__device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int q, int lane, int c, const float* v,
+                                            uint8_t* slab) {
+    const float a = p.alpha, bt = p.beta;
+    const int n = w.n_t0 + c + lane;
+    const bool in_n = n < w.n_end;
+    const int mb = w.m_t0 + q * 32;
+    const int rows = min(32, w.m_end - mb);
+    float* dcol = p.D + (long long)w.b * p.strideD + n;
+    __syncwarp();  // the previous chunk's reads of the slab are done
+    uint8_t* row = slab + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+        *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    // Rows in two halves of 16; beta * C for a half is loaded first, all in
+    // flight at once (coalesced along each row; the values of the tile are
+    // in the slab by now).  Row pointers advance by the leading dimensions.
+    const uint8_t* src = slab + (lane & 3) * 4;
+    float* dp = dcol + (long long)mb * p.ldd;
+    const float* cp = p.C + (long long)w.b * p.strideC + (long long)mb * p.ldc + n;
+#pragma unroll 1
+    for (int h0 = 0; h0 < rows; h0 += 16) {
+        float cv[16];
+        if (bt != 0.0f) {
+            const float* cr = cp;
+#pragma unroll
+            for (int r = 0; r < 16; r++) {
+                cv[r] = (in_n && h0 + r < rows) ? *cr : 0.0f;
+                cr += p.ldc;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 16; r++) {
+            if (h0 + r >= rows) break;
+            const int rr = h0 + r;
+            const float x = *reinterpret_cast<const float*>(src + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4));
+            if (in_n) {
+                float o = a * x;
+                if (bt != 0.0f) o = fmaf(bt, cv[r], o);
+                *dp = o;
+            }
+            dp += p.ldd;
+        }
+        cp += 16 * p.ldc;
+    }
+}
+
+// L2 prefetch of the C rows a normal tile's epilogue will read (thread =
+// row of the tile, any alignment), issued before the accumulator is ready.
+__device__ __forceinline__ void prefetch_c_tile_row(const Params& p, const Work& w, int m) {
+    if (m >= w.m_end) return;
+    const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + w.n_t0;
+    const int cols = min(w.bn, w.n_end - w.n_t0);
+    for (int c = 0; c < cols + 31; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + min(c, cols - 1)));
+}
+
 __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
                                        float4* stage) {
     if (w.swap) {
@@ -712,6 +777,34 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
     const int L = w.swap ? 128 : w.bn;
     const int L4 = L / 4;
     const long long part_floats = 128ll * w.bn;
+    if (!p.vec_d) {
+        // D rows not 16-byte aligned: one column per thread, consecutive
+        // threads on consecutive columns (every store covers 128 contiguous
+        // bytes); the same split order per output.
+        const int tot = (r1 - r0) * L;
+        const float alpha = p.alpha, beta = p.beta;
+        for (int i = tid; i < tot; i += 128) {
+            const int rr = r0 + i / L, l = i - (i / L) * L;
+            const float* src = tile_ws + (long long)rr * L + l;
+            float acc = 0.0f;
+            int s = 0;
+            for (; s + 8 <= w.splits; s += 8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) x[e] = __ldcg(src + (s + e) * part_floats);
+#pragma unroll
+                for (int e = 0; e < 8; e++) acc += x[e];
+            }
+            for (; s < w.splits; s++) acc += __ldcg(src + s * part_floats);
+            const int m = w.m_t0 + rr, n = w.n_t0 + l;
+            if (m < w.m_end && n < w.n_end) {
+                float o = alpha * acc;
+                if (beta != 0.0f) o = fmaf(beta, p.C[(long long)w.b * p.strideC + (long long)m * p.ldc + n], o);
+                p.D[(long long)w.b * p.strideD + (long long)m * p.ldd + n] = o;
+            }
+        }
+        return;
+    }
     const int total = (r1 - r0) * L4;
     const long long step4 = part_floats / 4;
     // Each thread takes two outputs at a time and keeps 2 x 8 loads in
@@ -1069,7 +1162,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t aph = 0;
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (p.tma_d && p.beta != 0.0f && w.splits == 1 && !w.swap) prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
+            if (p.beta != 0.0f && w.splits == 1 && !w.swap) {
+                if (p.tma_d)
+                    prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
+                else
+                    prefetch_c_tile_row(p, w, w.m_t0 + q * 32 + lane);
+            }
             int ok = 1;
             if (lane == 0)
                 ok = wait_bounded(accf(acc), aph, abort_flag, p.err, kErrWaitAccFull, limit, true) ? 1 : 0;
@@ -1107,6 +1205,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                         emit32_tma(p, w, lane, m0, n0, v, cv, epi_g + off, epi_s + off);
                         ++slab;
                     }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_acc(acc);
+            } else if (w.splits == 1 && !w.swap && p.beta != 0.0f) {
+                // Unaligned D with beta * C (measured: faster than the
+                // transposed stores below once C has to be read).
+                // The slab area may still be read by an earlier tile's bulk stores.
+                if (lane == 0) bulk_wait_read_all();
+                for (int c = 0; c < w.bn; c += 32) {
+                    float v[32];
+                    if (has_k) {
+                        tmem_ld32(t + c, v);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] = 0.0f;
+                    }
+                    emit32_rows(p, w, q, lane, c, v, epi_g);
                 }
                 tc_fence_before();
                 __syncwarp();
