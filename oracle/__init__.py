@@ -10,9 +10,9 @@ leading dimensions; C is ``float32`` (ignored when beta == 0).  Every result is
 ``float64``.
 
 What each routine follows (page titles and sections):
-  * ``gemm_naive``  -- MikPoly summary, section 1.2: the plain i-j-k nest,
+  * ``gemm_naive``  -- MikPoly summary, preliminaries part 2 (loop tiling structure): the plain i-j-k nest,
     then the BOLT summary's epilogue ``alpha*A*W + beta*C``.
-  * ``gemm_tiled``  -- MikPoly summary, section 1.2: the TILE_SIZE 32 nest
+  * ``gemm_tiled``  -- MikPoly summary, preliminaries part 2 (loop tiling structure): the TILE_SIZE 32 nest
     (zeroed output, edges clamped).
   * ``gemm_rows``   -- the same definition in i-k-j order over OpenMP rows.
   * ``gemm_entries`` / ``magnitude`` / ``freivalds`` -- the same definition
@@ -130,12 +130,12 @@ def _gemm(name, A, B, C, alpha, beta, threads=None):
 
 
 def gemm_naive(A, B, C=None, alpha=1.0, beta=0.0) -> np.ndarray:
-    """Plain i-j-k nest (MikPoly summary, section 1.2) with the alpha/beta epilogue."""
+    """Plain i-j-k nest (MikPoly summary, preliminaries part 2) with the alpha/beta epilogue."""
     return _gemm("oracle_gemm_naive", A, B, C, alpha, beta)
 
 
 def gemm_tiled(A, B, C=None, alpha=1.0, beta=0.0) -> np.ndarray:
-    """Loop-tiled nest, TILE_SIZE 32 (MikPoly summary, section 1.2), edges clamped."""
+    """Loop-tiled nest, TILE_SIZE 32 (MikPoly summary, preliminaries part 2), edges clamped."""
     return _gemm("oracle_gemm_tiled", A, B, C, alpha, beta)
 
 

@@ -14,7 +14,7 @@
  *
  * Sources (page titles and sections):
  *   - "Optimizing Dynamic-Shape Neural Networks on Accelerators via On-the-Fly
- *     Micro-Kernel Polymerization" (MikPoly summary), section 1.2 "loop tiling":
+ *     Micro-Kernel Polymerization" (MikPoly summary), preliminaries part 2 "loop tiling structure":
  *     the plain i-j-k matrix-multiply nest (C[i][j] zeroed, then accumulated
  *     over k) and the loop-tiled nest with TILE_SIZE 32.
  *   - BOLT summary, "Persistent kernel (GEMM/Conv) fusion": the epilogue form
@@ -52,7 +52,7 @@ static double c_term(const float* C, int64_t ldc, int64_t i, int64_t j, double b
 }
 
 /*
- * The plain nest of the MikPoly summary, section 1.2: for each (i, j), zero
+ * The plain nest of the MikPoly summary, preliminaries part 2: for each (i, j), zero
  * the accumulator and add A[i][k]*B[k][j] for k = 0..K-1 in order; then the
  * epilogue of the BOLT summary.
  */
@@ -73,7 +73,7 @@ void oracle_gemm_naive(int64_t M, int64_t N, int64_t K,
 }
 
 /*
- * The loop-tiled nest of the MikPoly summary, section 1.2 (TILE_SIZE 32):
+ * The loop-tiled nest of the MikPoly summary, preliminaries part 2 (TILE_SIZE 32):
  * tiles of i, j, k outermost, then ii, jj, kk inside each tile, accumulating
  * straight into the output.  The output is zeroed first and every tile is
  * clamped to the matrix edge (reading noted above).  The sum for one (i, j)

@@ -168,7 +168,7 @@ def test_oracle_pins(form, pin):
 
 @pytest.mark.parametrize("M,N,K", [(64, 64, 64), (96, 32, 128), (37, 45, 70), (33, 1, 31), (1, 65, 97)])
 def test_naive_equals_tiled_bitwise(M, N, K):
-    """The two printed nests (MikPoly summary, section 1.2) agree exactly on
+    """The two printed nests (MikPoly summary, preliminaries part 2) agree exactly on
     integer data, for tile-multiple and ragged sizes."""
     rng = np.random.default_rng(M * 1000 + N * 10 + K)
     A, B = int_bits(rng, (M, K)), int_bits(rng, (K, N))
