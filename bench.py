@@ -300,16 +300,42 @@ def run_mp(args):
         d2h = sum(t[3].numel() * t[3].element_size() for t in host_in)
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
+        # Three streams, as a serving loop would use them: host-to-device
+        # copies, the GEMM calls (on the stream the calls were built for) and
+        # device-to-host copies.  GEMM j waits only for its own inputs, and its
+        # read-back only for GEMM j.  Across steps, a copy into an input waits
+        # until the previous step's GEMM j has read it, and GEMM j waits until
+        # the previous step's D_j has been read back.
+        s_comp = stream
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        n_ops = len(ops)
+        ev_in = [torch.cuda.Event() for _ in range(n_ops)]
+        ev_done = [torch.cuda.Event() for _ in range(n_ops)]
+        ev_back = [torch.cuda.Event() for _ in range(n_ops)]
+        started = [False]
+
         def e2e_step():
-            for (g, A, B, C, D), (hA, hB, hC, hD), (fn, a) in zip(ops, host_in, calls):
-                A.copy_(hA, non_blocking=True)
-                B.copy_(hB, non_blocking=True)
-                if C is not None:
-                    C.copy_(hC, non_blocking=True)
+            for j, ((g, A, B, C, D), (hA, hB, hC, hD), (fn, a)) in enumerate(zip(ops, host_in, calls)):
+                with torch.cuda.stream(s_in):
+                    if started[0]:
+                        s_in.wait_event(ev_done[j])
+                    A.copy_(hA, non_blocking=True)
+                    B.copy_(hB, non_blocking=True)
+                    if C is not None:
+                        C.copy_(hC, non_blocking=True)
+                    ev_in[j].record(s_in)
+                s_comp.wait_event(ev_in[j])
+                if started[0]:
+                    s_comp.wait_event(ev_back[j])
                 st = fn(*a)
                 if st != 0:
                     raise mp.MPError(st, "mp_gemm")
-                hD.copy_(D, non_blocking=True)
+                ev_done[j].record(s_comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[j])
+                    hD.copy_(D, non_blocking=True)
+                    ev_back[j].record(s_out)
+            started[0] = True
 
         e2e_step()
         torch.cuda.synchronize()
