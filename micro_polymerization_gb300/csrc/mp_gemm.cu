@@ -113,6 +113,11 @@ struct alignas(128) Params {
     int sub_bytes;       // one 64-deep K step: 16 KB X tile + the widest Y tile of the plan
     int kg;              // K steps per ring stage (1 or 2): one full/empty barrier pair per stage
     int stage_bytes;     // kg * sub_bytes
+    // S > 1: split-K on chip.  Clusters of S CTAs, one task each (unit =
+    // tile * S + split = blockIdx.x); each CTA leaves its partial in its
+    // shared memory and the cluster reduces it through distributed shared
+    // memory at the end of the kernel.
+    int csplit;
     // 1: clusters of two CTAs; a work unit is two vertically adjacent tiles
     // (rank r takes tile row 2 t + r) that share their B tile, each CTA
     // multicasting half of B's 64-column blocks into both shared memories.
@@ -423,6 +428,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
+}
+
+// 16 bytes of another CTA's shared memory (address from mapa).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
 }
 
 // Arrive on a barrier of another CTA of the cluster (address from mapa).
@@ -850,6 +865,41 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
 // once when there is none.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Split-K on chip: every split of a tile runs on one CTA of a cluster of S
+// and has left its fp32 partial in its own shared memory at `part_s`, as R
+// rows x L columns of the tile in D-row-major order with a row pitch of L + 4
+// floats.  After a cluster barrier, this CTA sums rows [R r / S, R (r+1) / S)
+// over the S partials in split order (the same order, hence the same bits, as
+// the global-memory reduction) and writes D.  All threads of the CTA take part.
+__device__ __forceinline__ void csplit_reduce(const Params& p, const Work& w, uint32_t part_s) {
+    const int S = w.splits, r = w.split;
+    const int R = w.swap ? w.bn : 128, L = w.swap ? 128 : w.bn, P = L + 4;
+    const int r0 = (int)((long long)R * r / S), r1 = (int)((long long)R * (r + 1) / S);
+    const int L4 = L / 4;
+    const int total = (r1 - r0) * L4;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int row = r0 + i / L4, g = i - (i / L4) * L4;
+        const uint32_t off = part_s + (uint32_t)((row * P + 4 * g) * 4);
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        int sp = 0;
+        for (; sp + 8 <= S; sp += 8) {
+            float4 x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] = ld_dsmem_v4(mapa_shared(off, (uint32_t)(sp + e)));
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                a.x += x[e].x; a.y += x[e].y; a.z += x[e].z; a.w += x[e].w;
+            }
+        }
+        for (; sp < S; sp++) {
+            const float4 x = ld_dsmem_v4(mapa_shared(off, (uint32_t)sp));
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+        }
+        const int m = w.m_t0 + row;
+        if (m < w.m_end) store4(p, w, m, w.n_t0 + 4 * g, a);
+    }
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -1247,7 +1297,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 // has parked, then sum this split's 1/S slice of the tile's
                 // rows over all partials, in split order, and write D.
                 float* part = p.ws + w.ws_tile + (long long)w.split * (128ll * w.bn);
-                if (w.swap) {
+                if (p.csplit) {
+                    // On chip: the partial goes to this CTA's shared memory
+                    // (the ring is idle: one task per CTA, all MMAs done); the
+                    // cluster sums it at the end of the kernel.
+                    float* ps = reinterpret_cast<float*>(gbase);
+                    const int P = (w.swap ? 128 : w.bn) + 4;
+                    if (!w.swap) {
+                        float* prow = ps + (q * 32 + lane) * P;
+                        for (int c = 0; c < w.bn; c += 32) {
+                            float v[32];
+                            if (has_k) {
+                                tmem_ld32(t + c, v);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; j++) v[j] = 0.0f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; j++)
+                                *reinterpret_cast<float4*>(prow + c + 4 * j) =
+                                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                    } else {
+                        float* pcol = ps + q * 32 + lane;
+                        for (int c = 0; c < w.bn; c += 16) {
+                            float v[16];
+                            if (has_k) {
+                                tmem_ld16(t + c, v);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 16; j++) v[j] = 0.0f;
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; j++) pcol[(c + j) * P] = v[j];
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) release_acc(acc);
+                } else if (w.swap) {
                     // lane = buffer column: every store covers 128 contiguous bytes.
                     for (int c = 0; c < w.bn; c += 16) {
                         float v[16];
@@ -1295,49 +1383,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) release_acc(acc);  // TMEM buffer free for the next unit
-                __threadfence();
-                named_bar_sync(1, 128);
-                if (threadIdx.x == 64) {
-                    unsigned int* cnt = p.cnt + w.cnt;
-                    atomicAdd(cnt, 1u);
-                    // Bounded wait for the other splits.  They are consecutive
-                    // work units on distinct CTAs, so none of them waits on
-                    // this CTA's later work.
-                    int arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits;
-                    if (!arrived) {
-                        const uint64_t t0 = globaltimer();
-                        while (!(arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits)) {
-                            if (*abort_flag) break;
-                            if (globaltimer() - t0 > limit) {
-                                *abort_flag = 1;
-                                atomicCAS(p.err, 0, kErrWaitSplits);
-                                break;
-                            }
-                            __nanosleep(64);
-                        }
-                    }
-                    *s_last = arrived;
-                }
-                named_bar_sync(1, 128);
-                const int arrived = *s_last;
-                named_bar_sync(1, 128);
-                if (arrived) {
+                if (!p.csplit) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) release_acc(acc);  // TMEM buffer free for the next unit
                     __threadfence();
-                    const int R = w.swap ? w.bn : 128;
-                    const int r0 = (int)((long long)R * w.split / w.splits);
-                    const int r1 = (int)((long long)R * (w.split + 1) / w.splits);
-                    reduce_rows(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
                     named_bar_sync(1, 128);
                     if (threadIdx.x == 64) {
-                        // The last split to leave resets the counter for the next launch.
-                        const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
-                        if (old == 2u * (unsigned)w.splits - 1u) p.cnt[w.cnt] = 0u;
+                        unsigned int* cnt = p.cnt + w.cnt;
+                        atomicAdd(cnt, 1u);
+                        // Bounded wait for the other splits.  They are consecutive
+                        // work units on distinct CTAs, so none of them waits on
+                        // this CTA's later work.
+                        int arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits;
+                        if (!arrived) {
+                            const uint64_t t0 = globaltimer();
+                            while (!(arrived = ld_acquire_u32(cnt) >= (unsigned)w.splits)) {
+                                if (*abort_flag) break;
+                                if (globaltimer() - t0 > limit) {
+                                    *abort_flag = 1;
+                                    atomicCAS(p.err, 0, kErrWaitSplits);
+                                    break;
+                                }
+                                __nanosleep(64);
+                            }
+                        }
+                        *s_last = arrived;
                     }
-                } else if (lane == 0) {
-                    *epi_abort = 1;  // stop at the next unit (the flag is read between its barriers)
+                    named_bar_sync(1, 128);
+                    const int arrived = *s_last;
+                    named_bar_sync(1, 128);
+                    if (arrived) {
+                        __threadfence();
+                        const int R = w.swap ? w.bn : 128;
+                        const int r0 = (int)((long long)R * w.split / w.splits);
+                        const int r1 = (int)((long long)R * (w.split + 1) / w.splits);
+                        reduce_rows(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
+                        named_bar_sync(1, 128);
+                        if (threadIdx.x == 64) {
+                            // The last split to leave resets the counter for the next launch.
+                            const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
+                            if (old == 2u * (unsigned)w.splits - 1u) p.cnt[w.cnt] = 0u;
+                        }
+                    } else if (lane == 0) {
+                        *epi_abort = 1;  // stop at the next unit (the flag is read between its barriers)
+                    }
                 }
             }
             acc ^= 1;
@@ -1350,6 +1440,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 
     grid_dep_wait();
     __syncthreads();
+    if constexpr (!kPair) {
+        if (p.csplit) {
+            // Every partial of this CTA's tile is now in its cluster's shared
+            // memory; sum this CTA's slice; leave only when no CTA of the
+            // cluster still reads this one's partial.
+            cluster_sync();
+            if ((int)blockIdx.x < p.total_units) csplit_reduce(p, decode(p, regs_s, (int)blockIdx.x, 0), ring0);
+            cluster_sync();
+        }
+    }
     if constexpr (kPair) {
         // After an abort, copies or commits of the peer may still be in
         // flight towards this CTA: give them time to land (they need
@@ -1442,6 +1542,41 @@ struct DeviceState {
     // paired launches disabled).
     int max_pairs = 0;
 };
+
+// Split-K on chip: for S = 2..16, the CTAs that clusters of S CTAs of the
+// one-CTA kernel can keep resident (queried once; sizes past 8 need the
+// non-portable cluster attribute).  MP_CSPLIT=0 disables it.
+void query_cluster_split(mp_handle h, int num_sms) {
+    h->cluster_split_max = 0;
+    for (int S = 0; S <= 16; S++) h->cluster_ctas[S] = 0;
+    if (const char* v = std::getenv("MP_CSPLIT"))
+        if (std::atoi(v) == 0) return;
+    const bool big = cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                     cudaSuccess;
+    if (!big) (void)cudaGetLastError();
+    for (int S = 2; S <= (big ? 16 : 8); S++) {
+        cudaLaunchConfig_t oc = {};
+        oc.gridDim = dim3((unsigned)(S * ((num_sms + S - 1) / S)));
+        oc.blockDim = dim3(dev::kThreads);
+        oc.dynamicSmemBytes = dev::kSmemBytes;
+        cudaLaunchAttribute ca[1];
+        ca[0].id = cudaLaunchAttributeClusterDimension;
+        ca[0].val.clusterDim.x = (unsigned)S;
+        ca[0].val.clusterDim.y = 1;
+        ca[0].val.clusterDim.z = 1;
+        oc.attrs = ca;
+        oc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<1>, &oc) != cudaSuccess) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        if (n > 0) {
+            h->cluster_ctas[S] = n * S;
+            h->cluster_split_max = S;
+        }
+    }
+}
 
 // Resident two-CTA clusters of the persistent kernel (0 if the query fails).
 int query_max_pairs(int num_sms) {
@@ -1566,7 +1701,7 @@ bool tma_ok(const void* p, int64_t ld, int64_t batch, int64_t stride) {
 
 void log_plan(const mp_plan_info& plan, const GemmArgs& a, int grid, int pair) {
     std::fprintf(stderr,
-                 "[mp] batch=%lld M=%lld N=%lld K=%lld pattern=%d regions=%d tasks=%lld grid=%d paired=%d cost=%.2fus\n",
+                 "[mp] batch=%lld M=%lld N=%lld K=%lld pattern=%d regions=%d tasks=%lld grid=%d cluster=%d cost=%.2fus\n",
                  (long long)a.batch, (long long)a.M, (long long)a.N, (long long)a.K, plan.pattern,
                  plan.num_regions, (long long)plan.total_tasks, grid, pair, plan.cost_us);
     for (int i = 0; i < plan.num_regions; i++) {
@@ -1626,6 +1761,7 @@ mp_status device_init(mp_handle h, int device) {
             cudaSuccess)
         return MP_ERR_CUDA;
     s->max_pairs = query_max_pairs(s->num_sms);
+    query_cluster_split(h, s->num_sms);
     if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
@@ -1663,6 +1799,7 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
             cudaSuccess)
         return MP_ERR_CUDA;
     s->max_pairs = query_max_pairs(s->num_sms);
+    query_cluster_split(h, s->num_sms);
     h->host_only = false;
     h->device = device;
     h->hw.num_pe = prop.multiProcessorCount;
@@ -1725,6 +1862,23 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // ---- CTA pairs: the plan's regions are all pair tiles or none ----------
     const int pair = plan.num_regions > 0 && plan.region[0].pair ? 1 : 0;
     if (pair && s->max_pairs <= 0) return MP_ERR_UNSUPPORTED;
+    // ---- split-K on chip: every region split S ways, one task per CTA in
+    // clusters of S, each partial fitting the idle operand ring ------------
+    int csplit = 0;
+    if (!pair && plan.num_regions > 0 && K > 0) {
+        const int S = plan.region[0].splits;
+        bool ok = S >= 2 && S <= h->cluster_split_max && S <= 8;  // past 8 measured no cheaper
+        int64_t tasks = 0;
+        for (int i = 0; i < plan.num_regions && ok; i++) {
+            const mp_region_info& r = plan.region[i];
+            const int64_t bn = r.swap ? r.um : r.un;
+            const int64_t R = r.swap ? bn : 128, L = r.swap ? 128 : bn;
+            ok = r.splits == S && R * (L + 4) * 4 <= dev::kRingBytes;
+            tasks += cdiv(r.m_ext, r.um) * cdiv(r.n_ext, r.un) * batch * S;
+        }
+        if (ok && tasks <= h->cluster_ctas[S]) csplit = S;
+    }
+    p.csplit = csplit;
     p.pair = pair;
 
     // ---- operands: TMA views, repacked when rows are not 16-byte aligned ----
@@ -1891,7 +2045,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         units += tiles * r.splits;
         d.ws_begin = ws_floats;
         d.cnt_begin = (int)counters;
-        if (r.splits > 1) {
+        if (r.splits > 1 && !csplit) {
             const int64_t rows = tiles * r.splits * 128;
             if (!r.swap && ws_floats + rows * bn <= h->workspace_floats &&
                 encode_3d_f32(s, &p.tmW[i], s->ws + ws_floats, (uint64_t)bn, (uint64_t)rows, 1,
@@ -1919,8 +2073,10 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     p.stage_bytes = p.kg * p.sub_bytes;
     p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
 
-    const int grid = pair ? 2 * (int)std::min<int64_t>(units, s->max_pairs) : (int)std::min<int64_t>(units, s->num_sms);
-    if (s->log) log_plan(plan, a, grid, pair);
+    const int grid = pair     ? 2 * (int)std::min<int64_t>(units, s->max_pairs)
+                     : csplit ? (int)units  // one task per CTA, a multiple of S
+                              : (int)std::min<int64_t>(units, s->num_sms);
+    if (s->log) log_plan(plan, a, grid, pair ? 2 : csplit);
     // One CTA per SM; launched as a programmatic dependent of the previous
     // kernel on the stream so that its set-up overlaps that kernel's tail.
     cudaLaunchConfig_t cfg = {};
@@ -1932,11 +2088,11 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = pair ? 2 : 1;
+    attr[1].val.clusterDim.x = pair ? 2 : (csplit ? (unsigned)csplit : 1u);
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pair ? 2 : 1;
+    cfg.numAttrs = (pair || csplit) ? 2 : 1;
     const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<2>, p)
                                : cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<1>, p);
     if (e != cudaSuccess) return MP_ERR_CUDA;

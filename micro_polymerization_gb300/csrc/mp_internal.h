@@ -57,6 +57,12 @@ struct mp_handle_s {
     std::vector<mp::PlanCacheEntry> cache;
     int64_t workspace_floats = mp::kDefaultWorkspaceFloats;
 
+    // Split-K on chip (clusters of S CTAs reduce through distributed shared
+    // memory): the largest S a cluster can hold (0: none), and per S the
+    // CTAs such clusters can keep resident at once.
+    int32_t cluster_split_max = 0;
+    int32_t cluster_ctas[17] = {};
+
     mp::DeviceState* dev = nullptr;
 };
 

@@ -40,6 +40,14 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Measured on GB300: about 6 us beyond the K loop for a 128 x 128 tile.
 constexpr double kSplitSyncUs = 4.0;
 constexpr double kSplitBytesFactor = 4.0;  // tile bytes moved, in L2 passes
+// On chip (clusters of S CTAs, one task each): the partial goes TMEM ->
+// shared memory, one cluster barrier, 1/S of the rows summed over S partials
+// through distributed shared memory, a second barrier before exit.  Measured
+// on GB300: 2-3 us cheaper than through L2 for S <= 8; past 8 (non-portable
+// cluster sizes) no cheaper, so only S <= 8 runs on chip.
+constexpr int kClusterSplitMax = 8;
+constexpr double kClusterSplitUs = 2.5;
+constexpr double kClusterSplitBytesFactor = 1.0;
 // Floor of one uk step of any micro-kernel: the single MMA-issuing thread's
 // per-instruction and per-stage cost (measured on GB300 with tiny tiles).
 constexpr double kStepFloorUs = 0.21;
@@ -64,15 +72,26 @@ inline int64_t slots_for(const mp_handle_s* h, const mp_kernel_desc& u) {
     return std::max<int64_t>(1, s);
 }
 
+// Split-K runs on chip when the handle's device can hold clusters of S CTAs
+// and all `tasks` fit one wave of them.
+inline bool split_on_chip(const mp_handle_s* h, const mp_kernel_desc& u, int64_t splits, int64_t tasks) {
+    return !u.pair && splits >= 2 && splits <= h->cluster_split_max && splits <= kClusterSplitMax &&
+           tasks <= h->cluster_ctas[splits];
+}
+
 // g_predict(f_num) plus the split-K reduction: every task of a split tile
 // writes an fp32 partial, waits for the tile's other splits (a counter round
 // trip through L2), then reads 1/S of every partial -- one partial's worth.
-inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f_num, int64_t splits) {
+inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f_num, int64_t splits,
+                        int64_t tasks) {
     double t = u.fixed_us + u.per_step_us * (double)f_num;
     if (splits > 1 && h->hw.l2_gbs > 0 && h->hw.num_pe > 0) {
         double tile_bytes = 4.0 * u.um * u.un;
         double pe_gbs = h->hw.l2_gbs / h->hw.num_pe;
-        t += kSplitSyncUs + kSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
+        if (split_on_chip(h, u, splits, tasks))
+            t += kClusterSplitUs + kClusterSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);
+        else
+            t += kSplitSyncUs + kSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
     }
     return t;
 }
@@ -93,7 +112,7 @@ RegionEval eval_region(const mp_handle_s* h, int32_t k, int64_t m_ext, int64_t n
     r.f_num = (int32_t)f_num;
     r.f_parallel = tiles * splits;
     r.f_wave = cdiv(r.f_parallel, slots_for(h, u));
-    r.f_pipe = f_pipe_of(h, u, f_num, splits);
+    r.f_pipe = f_pipe_of(h, u, f_num, splits, r.f_parallel);
     r.cost = (double)r.f_wave * r.f_pipe;
     r.ws_floats = splits > 1 ? tiles * splits * (int64_t)u.um * u.un : 0;
     r.ok = splits == 1 || (!u.pair && r.ws_floats <= h->workspace_floats && tiles <= kMaxCounters);
@@ -117,6 +136,13 @@ int split_candidates(const mp_handle_s* h, const mp_kernel_desc& u, int64_t tile
     }
     int64_t fill = std::min<int64_t>(kb, std::max<int64_t>(1, slots / tiles));
     if (fill > 1) out[n++] = (int32_t)fill;
+    // The largest on-chip split that one wave of clusters holds.
+    for (int32_t s = std::min<int32_t>(kClusterSplitMax, h->cluster_split_max); s >= 2; s--) {
+        if (s <= kb && tiles * s <= h->cluster_ctas[s]) {
+            out[n++] = s;
+            break;
+        }
+    }
     return n;
 }
 

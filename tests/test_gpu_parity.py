@@ -146,7 +146,7 @@ def test_pair_kernel_launches_as_cluster(capfd):
         A, B, C = rand_problem(1024, 1024, 256, seed=3)
         D = run_gemm(A, B, None, 1.0, 0.0, h=h)
         err = capfd.readouterr().err
-        assert "paired=1" in err, err
+        assert "cluster=2" in err, err
         assert_parity(D, A, B, None, 1.0, 0.0, what="pair 1024^2 x 256")
     finally:
         h.close()
@@ -185,6 +185,52 @@ def test_split_k_integer_exact_and_deterministic():
             assert torch.equal(D1, D2)
     finally:
         mp.mp_force_plan(h, -1, 0)
+
+
+def _handle_with(env):
+    """A handle made with extra environment settings (read at creation)."""
+    import os
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
+    try:
+        return mp.mp_init(0)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(105, 1024, 4000, 4), (300, 517, 2000, 3), (37, 520, 1300, 8),
+                                          (105, 1024, 12544, 16)])
+def test_split_k_on_chip_matches_global_bitwise(M, N, K, splits, capfd):
+    """Split-K reduced on chip (a cluster of S CTAs summing through
+    distributed shared memory) and through the global workspace add the same
+    partials in the same split order: bit-identical outputs, within the bound."""
+    hg = _handle_with({"MP_CSPLIT": "0"})
+    hc = _handle_with({"MP_LOG": "1"})
+    A, B, C = rand_problem(M, N, K, seed=M + splits, beta=0.5)
+    try:
+        for k, desc in enumerate(_kernels()):
+            if desc.pair:
+                continue
+            mp.mp_force_plan(hg, k, splits)
+            mp.mp_force_plan(hc, k, splits)
+            capfd.readouterr()
+            Dc = run_gemm(A, B, C, 1.5, 0.5, h=hc)
+            log = capfd.readouterr().err
+            Dg = run_gemm(A, B, C, 1.5, 0.5, h=hg)
+            p = mp.mp_plan(hc, M, N, K)
+            s_eff = p.region[0].splits
+            tasks = sum(r.f_parallel for r in p.regions())
+            if s_eff <= 8 and tasks <= 64:  # portable cluster sizes: surely one wave
+                assert f"cluster={s_eff}" in log, (k, log)
+            assert torch.equal(Dc, Dg), f"kernel {k} ({desc.um}x{desc.un} swap={desc.swap}) {(M, N, K)} S={s_eff}"
+            assert_parity(Dc, A, B, C, 1.5, 0.5, what=f"on-chip split kernel {k} {(M, N, K)} S={s_eff}")
+    finally:
+        hg.close()
+        hc.close()
 
 
 def test_repeat_runs_bitwise_equal():
