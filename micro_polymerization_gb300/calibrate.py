@@ -25,10 +25,14 @@ DEFAULT_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "calib",
 STEPS = (2, 8, 32, 96)
 
 
-def one_wave_shape(desc, num_pe: int):
-    """(M, N) whose tiles of this micro-kernel fill one wave of num_pe tasks."""
+def one_wave_shape(desc, hw):
+    """(M, N) whose tiles of this micro-kernel fill one wave of its task slots
+    (warps_per_wave / warps: one task per SM, or per SM pair for pair kernels)."""
+    slots = max(1, hw.warps_per_wave // max(1, desc.warps))
     tn = 8 if not desc.swap else 6
-    tm = max(1, num_pe // tn)
+    while tn > 1 and slots % tn:
+        tn -= 1
+    tm = max(1, slots // tn)
     return tm * desc.um, tn * desc.un
 
 
@@ -47,7 +51,7 @@ def measure(device: int = 0, reps: int = 30):
     try:
         for k, desc in enumerate(kernels):
             mp.mp_force_plan(h, k, 1)
-            M, N = one_wave_shape(desc, hw.num_pe)
+            M, N = one_wave_shape(desc, hw)
             pts = []
             for t in STEPS:
                 K = 64 * t

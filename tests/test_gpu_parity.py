@@ -416,6 +416,27 @@ def test_workload_samples_full_size(name, count):
                               g.alpha, g.beta, rng, what=f"{name} {(g.M, g.N, g.K)}")
 
 
+@pytest.mark.parametrize("M,N,K,alpha,beta", [(6144, 6144, 6144, 1.0, 0.0), (10332, 13649, 4045, 1.5, 0.5)])
+def test_large_pair_plans_in_grouped_order(M, N, K, alpha, beta):
+    """Large problems: CTA-pair micro-kernels, tiles handed out in groups of
+    tile rows (the operands do not fit L2), with aligned D and with unaligned
+    D plus beta * C."""
+    h = handle()
+    _, ks = mp.mp_get_hw(h)
+    p = mp.mp_plan(h, M, N, K)
+    if any(d.pair for d in ks):
+        assert all(r.pair for r in p.regions()), [(r.um, r.un, r.pair) for r in p.regions()]
+    dev = torch.device("cuda", 0)
+    g = wl.Gemm(M, N, K, alpha=alpha, beta=beta, seed=M % 97)
+    A, B, C = wl.make_operands(g, device=dev)
+    D = torch.empty(M, N, device=dev)
+    mp.mp_gemm(h, A, B, C, D, alpha, beta)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M)
+    assert_sampled_parity(D.cpu(), A.cpu(), B.cpu(), C.cpu() if C is not None else None, alpha, beta, rng,
+                          what=f"large {(M, N, K)}")
+
+
 def test_bounded_wait_reports_timeout_and_recovers():
     """A withheld pipeline stage makes the consumer's bounded wait expire; the
     kernel stops cleanly, mp_check reports it, and the next call is correct."""
