@@ -177,6 +177,53 @@ mp_status mp_evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int
                            mp_plan_info* inout);
 
 /*
+ * The candidate strategies of one shape, for exhaustive search and for the
+ * cost-model ablations of [MP section 5, "cost model effectiveness"] (an
+ * exhaustive-search variant picks the fastest candidate by running them):
+ *   - Pattern I: every micro-kernel with every split-K candidate;
+ *   - Pattern II: both cut directions, every micro-kernel for the first
+ *     region, cuts on its tile boundaries (every one up to 64 of them, else
+ *     64 spread evenly plus the wave-filling ones), every micro-kernel of the
+ *     same CTA grouping for the second region, unsplit or split to fill a
+ *     wave.
+ * Each is filled as by mp_evaluate_plan under the handle's model.  The
+ * candidates are sorted by cost_us; the first `capacity` go to `out` (may be
+ * NULL with capacity 0) and `*count` receives how many exist.
+ * Errors: MP_ERR_INVALID_ARG (bad sizes, count NULL, capacity < 0).
+ */
+mp_status mp_enumerate_plans(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp_plan_info* out,
+                             int32_t capacity, int32_t* count);
+
+/*
+ * mp_gemm with an explicit plan instead of the polymerizer's choice: one
+ * from mp_plan or mp_enumerate_plans, or regions filled by hand (kernel, m0,
+ * n0, m_ext, n_ext, splits; the rest is recomputed as by mp_evaluate_plan).
+ * Used for exhaustive search and ablations.  Same arguments, layout rules,
+ * ownership and asynchrony as mp_gemm.
+ * Errors: as mp_gemm, and MP_ERR_PLAN when the regions do not tile the
+ * output exactly once or mix CTA-pair and one-CTA micro-kernels.
+ */
+mp_status mp_gemm_with_plan(mp_handle h, const mp_plan_info* plan, int64_t M, int64_t N, int64_t K, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, const float* C, int64_t ldc, float* D,
+                            int64_t ldd, float alpha, float beta, mp_stream stream);
+
+/*
+ * Cost model the polymerizer searches with [MP section 5, "cost model
+ * effectiveness"]:
+ *   MP_PLAN_MIKPOLY (default): Cost(S,H) = sum over regions of f_wave * f_pipe,
+ *     floored at the HBM time of the algorithmic bytes;
+ *   MP_PLAN_WAVE: the fewest waves (sum of f_wave), which favours large
+ *     micro-kernels;
+ *   MP_PLAN_PIPE: the fastest pipeline tasks (sum of f_pipe), which favours
+ *     small micro-kernels.
+ * The plan cache is cleared.  Errors: MP_ERR_INVALID_ARG (unknown mode).
+ */
+#define MP_PLAN_MIKPOLY 0
+#define MP_PLAN_WAVE 1
+#define MP_PLAN_PIPE 2
+mp_status mp_set_plan_mode(mp_handle h, int32_t mode);
+
+/*
  * D = alpha * A * B + beta * C, asynchronously on `stream`.  Plans the shape
  * (as mp_plan) and issues one persistent kernel launch [MP section 4:
  * offsets and loop counts are run-time scalars of fixed-size micro-kernels;

@@ -19,11 +19,17 @@ __all__ = [
     "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched",
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
     "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
+    "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
+    "MP_PLAN_PIPE",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
 ]
 
 MP_MAX_REGIONS = 4
 MP_MAX_KERNELS = 16
+
+MP_PLAN_MIKPOLY = 0
+MP_PLAN_WAVE = 1
+MP_PLAN_PIPE = 2
 
 MP_OK = 0
 MP_ERR_INVALID_ARG = -1
@@ -113,6 +119,11 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_set_kernel_model": ([_vp, _i32, ctypes.c_double, ctypes.c_double], ctypes.c_int),
                 "mp_inject_wait_timeout": ([_vp, _i32, _i64], ctypes.c_int),
                 "mp_status_string": ([ctypes.c_int], ctypes.c_char_p),
+                "mp_enumerate_plans": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo), _i32,
+                                        ctypes.POINTER(_i32)], ctypes.c_int),
+                "mp_gemm_with_plan": ([_vp, ctypes.POINTER(MpPlanInfo), _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                       _vp, _i64, _vp, _i64, _f, _f, _vp], ctypes.c_int),
+                "mp_set_plan_mode": ([_vp, _i32], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -235,6 +246,50 @@ def mp_gemm(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream
                            c_ptr, ldc, D.data_ptr(), _ld(D, "D"), float(alpha), float(beta),
                            _stream_ptr(stream))
     _check(st, "mp_gemm")
+
+
+def _gemm_args(A, B, C, D, beta):
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or D.dtype != torch.float32:
+        raise TypeError("A and B must be bfloat16, D float32")
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-1]
+    if B.shape[-2] != K or D.shape[-2:] != (M, N):
+        raise ValueError("shape mismatch")
+    c_ptr, ldc = None, 0
+    if beta != 0.0:
+        if C is None or C.dtype != torch.float32 or C.shape[-2:] != (M, N):
+            raise ValueError("beta != 0 needs an fp32 C of D's shape")
+        c_ptr, ldc = C.data_ptr(), _ld(C, "C")
+    return M, N, K, c_ptr, ldc
+
+
+def mp_gemm_with_plan(h: Handle, plan: MpPlanInfo, A, B, C, D, alpha: float = 1.0, beta: float = 0.0,
+                      stream=None) -> None:
+    """mp_gemm with an explicit plan (from mp_plan, mp_enumerate_plans, or built by hand)."""
+    M, N, K, c_ptr, ldc = _gemm_args(A, B, C, D, beta)
+    st = library().mp_gemm_with_plan(h.ptr, ctypes.byref(plan), M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(),
+                                     _ld(B, "B"), c_ptr, ldc, D.data_ptr(), _ld(D, "D"), float(alpha), float(beta),
+                                     _stream_ptr(stream))
+    _check(st, "mp_gemm_with_plan")
+
+
+def mp_enumerate_plans(h: Handle, M: int, N: int, K: int, capacity=None, batch: int = 1):
+    """The candidate strategies of one shape, cheapest first under the handle's
+    cost model (all of them when capacity is None)."""
+    n = ctypes.c_int32(0)
+    lib = library()
+    if capacity is None:
+        _check(lib.mp_enumerate_plans(h.ptr, batch, M, N, K, None, 0, ctypes.byref(n)), "mp_enumerate_plans")
+        capacity = n.value
+    arr = (MpPlanInfo * max(1, capacity))()
+    _check(lib.mp_enumerate_plans(h.ptr, batch, M, N, K, arr, capacity, ctypes.byref(n)), "mp_enumerate_plans")
+    return [arr[i] for i in range(min(capacity, n.value))]
+
+
+def mp_set_plan_mode(h: Handle, mode: int) -> None:
+    """MP_PLAN_MIKPOLY (default), MP_PLAN_WAVE or MP_PLAN_PIPE cost model."""
+    _check(library().mp_set_plan_mode(h.ptr, int(mode)), "mp_set_plan_mode")
 
 
 def mp_gemm_batched(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:

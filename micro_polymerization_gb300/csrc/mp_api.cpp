@@ -7,6 +7,9 @@
 #include <cstring>
 #include <new>
 
+#include <algorithm>
+#include <climits>
+
 #include "mp_internal.h"
 
 namespace {
@@ -212,6 +215,47 @@ mp_status mp_gemm_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
     mp::GemmArgs a{batch, M, N, K, A, lda, strideA, B, ldb, strideB, C, ldc, strideC,
                    D, ldd, strideD, alpha, beta, stream};
     return run(h, a);
+}
+
+mp_status mp_enumerate_plans(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp_plan_info* out,
+                             int32_t capacity, int32_t* count) {
+    if (!h || !count || capacity < 0 || (capacity > 0 && !out)) return MP_ERR_INVALID_ARG;
+    if (batch < 1 || M < 1 || N < 1 || K < 0) return MP_ERR_INVALID_ARG;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || batch >= kMaxDim) return MP_ERR_INVALID_ARG;
+    std::vector<mp_plan_info> all;
+    mp_status st;
+    try {
+        st = mp::enumerate_plans(h, batch, M, N, K, &all);
+    } catch (...) {
+        return MP_ERR_NO_MEMORY;
+    }
+    if (st != MP_OK) return st;
+    *count = (int32_t)std::min<size_t>(all.size(), (size_t)INT32_MAX);
+    const size_t n = std::min<size_t>(all.size(), (size_t)capacity);
+    if (n) std::memcpy(out, all.data(), sizeof(mp_plan_info) * n);
+    return MP_OK;
+}
+
+mp_status mp_gemm_with_plan(mp_handle h, const mp_plan_info* plan, int64_t M, int64_t N, int64_t K, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, const float* C, int64_t ldc, float* D,
+                            int64_t ldd, float alpha, float beta, mp_stream stream) {
+    if (!h || !plan) return MP_ERR_INVALID_ARG;
+    mp::GemmArgs a{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, stream};
+    mp_status st = check_args(a);
+    if (st != MP_OK) return st;
+    if (M == 0 || N == 0) return MP_OK;
+    if (h->host_only) return MP_ERR_UNSUPPORTED;
+    mp_plan_info p = *plan;
+    st = mp::evaluate_plan(h, 1, M, N, K, &p);  // checks the tiling and refills every derived field
+    if (st != MP_OK) return st == MP_ERR_INVALID_ARG ? MP_ERR_PLAN : st;
+    return mp::device_run(h, p, a);
+}
+
+mp_status mp_set_plan_mode(mp_handle h, int32_t mode) {
+    if (!h || (mode != MP_PLAN_MIKPOLY && mode != MP_PLAN_WAVE && mode != MP_PLAN_PIPE)) return MP_ERR_INVALID_ARG;
+    h->plan_mode = mode;
+    mp::clear_plan_cache(h);
+    return MP_OK;
 }
 
 mp_status mp_check(mp_handle h, mp_stream stream) {

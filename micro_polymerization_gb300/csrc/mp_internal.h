@@ -49,9 +49,10 @@ struct mp_handle_s {
     mp_kernel_desc kernels[MP_MAX_KERNELS]{};
     int32_t num_kernels = 0;
 
-    // Test / ablation hook (mp_force_plan).
+    // Test / ablation hooks (mp_force_plan, mp_set_plan_mode).
     int32_t force_kernel = -1;
     int32_t force_splits = 0;
+    int32_t plan_mode = MP_PLAN_MIKPOLY;
 
     // Plan cache: shapes repeat in dynamic workloads; a hit skips the search.
     std::vector<mp::PlanCacheEntry> cache;
@@ -72,6 +73,9 @@ namespace mp {
 mp_status plan_shape(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
                      mp_plan_info* out);
 void clear_plan_cache(mp_handle h);
+// Every candidate strategy of the search space, sorted by cost (mp_enumerate_plans).
+mp_status enumerate_plans(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          std::vector<mp_plan_info>* out);
 mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
                         mp_plan_info* p);
 void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n);

@@ -173,7 +173,9 @@ bool better(const mp_handle_s* h, const Strategy& c, const Strategy& b) {
     if (c.cost < b.cost - tol) return true;
     if (c.cost > b.cost + tol) return false;
     if (c.nreg != b.nreg) return c.nreg < b.nreg;
-    if (std::fabs(c.sum - b.sum) > 0.005 * std::max(c.sum, b.sum)) return c.sum < b.sum;
+    // The ablation models break ties without the full model's work sum.
+    if (h->plan_mode == MP_PLAN_MIKPOLY && std::fabs(c.sum - b.sum) > 0.005 * std::max(c.sum, b.sum))
+        return c.sum < b.sum;
     double ta = tile_area(h, c), tb = tile_area(h, b);
     if (ta != tb) return ta > tb;
     int sc = 0, sb = 0;
@@ -186,6 +188,22 @@ double hbm_floor_us(const mp_handle_s* h, int64_t batch, int64_t M, int64_t N, i
     if (h->hw.hbm_gbs <= 0) return 0.0;
     double bytes = 2.0 * M * K + 2.0 * K * N + 4.0 * M * N + (beta_c ? 4.0 * M * N : 0.0);
     return bytes * (double)batch / (h->hw.hbm_gbs * 1e3);
+}
+
+// The strategy's cost under the handle's model (s.sum already holds the sum
+// of f_wave * f_pipe over its regions).
+double strategy_cost(const mp_handle_s* h, const Strategy& s, double floor_us) {
+    double c = 0.0;
+    switch (h->plan_mode) {
+        case MP_PLAN_WAVE:
+            for (int i = 0; i < s.nreg; i++) c += (double)s.ev[i].f_wave;
+            return c;
+        case MP_PLAN_PIPE:
+            for (int i = 0; i < s.nreg; i++) c += s.ev[i].f_pipe;
+            return c;
+        default:
+            return std::max(s.sum, floor_us);
+    }
 }
 
 void fill_info(const mp_handle_s* h, const Strategy& s, int64_t K, mp_plan_info* out, int evaluated,
@@ -218,10 +236,12 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
     const double floor_us = hbm_floor_us(h, batch, M, N, K, false);
     Strategy best;
     int evaluated = 0, pruned = 0;
+    // Pruning compares partial MikPoly costs, so it runs under that model only.
+    const bool prune = h->plan_mode == MP_PLAN_MIKPOLY;
     auto finish = [&](Strategy& s) {
         s.sum = 0.0;
         for (int i = 0; i < s.nreg; i++) s.sum += s.ev[i].cost;
-        s.cost = std::max(s.sum, floor_us);
+        s.cost = strategy_cost(h, s, floor_us);
         evaluated++;
         if (better(h, s, best)) best = s;
     };
@@ -295,7 +315,7 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
                 RegionEval ea = dir == 0 ? eval_region(h, a, cut, N, K, batch, 1)
                                          : eval_region(h, a, M, cut, K, batch, 1);
                 if (!ea.ok) continue;
-                if (std::max(ea.cost, floor_us) > best.cost * 1.005) { pruned++; continue; }
+                if (prune && std::max(ea.cost, floor_us) > best.cost * 1.005) { pruned++; continue; }
                 const int64_t rest = along - cut;
                 for (int32_t b = 0; b < h->num_kernels; b++) {
                     const mp_kernel_desc& ub = h->kernels[b];
@@ -314,7 +334,7 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
                     for (int is = 0; is < nsb; is++) {
                         RegionEval eb = eval_region(h, b, rm, rn, K, batch, sb[is]);
                         if (!eb.ok) { pruned++; continue; }
-                        if (std::max(ea.cost + eb.cost, floor_us) > best.cost * 1.005) {
+                        if (prune && std::max(ea.cost + eb.cost, floor_us) > best.cost * 1.005) {
                             pruned++;
                             continue;
                         }
@@ -352,6 +372,106 @@ inline size_t cache_slot(const PlanKey& k, size_t n) {
 
 void clear_plan_cache(mp_handle h) {
     for (auto& e : h->cache) e.key = PlanKey{-1, -1, -1, -1};
+}
+
+mp_status enumerate_plans(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,
+                          std::vector<mp_plan_info>* out) {
+    out->clear();
+    if (!h || batch < 1 || M < 1 || N < 1 || K < 0) return MP_ERR_INVALID_ARG;
+    const double floor_us = hbm_floor_us(h, batch, M, N, K, false);
+    std::vector<Strategy> all;
+    auto add = [&](Strategy& st) {
+        st.sum = 0.0;
+        for (int i = 0; i < st.nreg; i++) st.sum += st.ev[i].cost;
+        st.cost = strategy_cost(h, st, floor_us);
+        all.push_back(st);
+    };
+
+    // Pattern I: every micro-kernel with every split-K candidate.
+    for (int32_t k = 0; k < h->num_kernels; k++) {
+        const mp_kernel_desc& u = h->kernels[k];
+        const int64_t tiles = cdiv(M, u.um) * cdiv(N, u.un) * batch;
+        int32_t cands[16];
+        const int nc = split_candidates(h, u, tiles, cdiv(K, u.uk), cands);
+        for (int c = 0; c < nc; c++) {
+            RegionEval e = eval_region(h, k, M, N, K, batch, cands[c]);
+            if (!e.ok) continue;
+            Strategy st;
+            st.pattern = 1;
+            st.nreg = 1;
+            st.m0[0] = 0; st.n0[0] = 0; st.m_ext[0] = M; st.n_ext[0] = N;
+            st.ev[0] = e;
+            add(st);
+        }
+    }
+
+    // Pattern II: two regions cut along M or along N.
+    for (int dir = 0; dir < 2; dir++) {
+        const int64_t along = dir == 0 ? M : N;
+        const int64_t across = dir == 0 ? N : M;
+        for (int32_t a = 0; a < h->num_kernels; a++) {
+            const mp_kernel_desc& ua = h->kernels[a];
+            const int64_t step = dir == 0 ? ua.um : ua.un;
+            const int64_t total_blocks = cdiv(along, step);
+            if (total_blocks < 2) continue;
+            const int64_t blocks_across = cdiv(across, dir == 0 ? ua.un : ua.um) * batch;
+            const int64_t slots = slots_for(h, ua);
+            std::vector<int64_t> cuts;
+            if (total_blocks - 1 <= 64) {
+                for (int64_t c = 1; c < total_blocks; c++) cuts.push_back(c);
+            } else {
+                for (int i = 1; i <= 64; i++) cuts.push_back(std::max<int64_t>(1, (total_blocks - 1) * i / 65));
+                const int64_t waves = cdiv(total_blocks * blocks_across, slots);
+                for (int64_t w = 1; w < waves; w++) cuts.push_back((w * slots) / blocks_across);
+                if (along % step != 0) cuts.push_back(along / step);
+                std::sort(cuts.begin(), cuts.end());
+                cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+            }
+            for (int64_t cb : cuts) {
+                const int64_t cut = cb * step;
+                if (cut <= 0 || cut >= along) continue;
+                RegionEval ea = dir == 0 ? eval_region(h, a, cut, N, K, batch, 1) : eval_region(h, a, M, cut, K, batch, 1);
+                if (!ea.ok) continue;
+                const int64_t rest = along - cut;
+                for (int32_t b = 0; b < h->num_kernels; b++) {
+                    const mp_kernel_desc& ub = h->kernels[b];
+                    if (dir == 1 && ub.un % 8 != 0) continue;
+                    if (ub.pair != ua.pair) continue;
+                    const int64_t rm = dir == 0 ? rest : M, rn = dir == 0 ? N : rest;
+                    const int64_t tiles_b = cdiv(rm, ub.um) * cdiv(rn, ub.un) * batch;
+                    const int64_t kb = cdiv(K, ub.uk);
+                    int32_t sb[2] = {1, 1};
+                    int nsb = 1;
+                    const int64_t sl = slots_for(h, ub);
+                    if (!ub.pair && tiles_b < sl && kb > 1) {
+                        sb[1] = (int32_t)std::min<int64_t>(kb, std::max<int64_t>(1, sl / tiles_b));
+                        if (sb[1] > 1) nsb = 2;
+                    }
+                    for (int is = 0; is < nsb; is++) {
+                        RegionEval eb = eval_region(h, b, rm, rn, K, batch, sb[is]);
+                        if (!eb.ok) continue;
+                        Strategy st;
+                        st.pattern = 2;
+                        st.nreg = 2;
+                        if (dir == 0) {
+                            st.m0[0] = 0; st.n0[0] = 0; st.m_ext[0] = cut; st.n_ext[0] = N;
+                            st.m0[1] = cut; st.n0[1] = 0; st.m_ext[1] = rest; st.n_ext[1] = N;
+                        } else {
+                            st.m0[0] = 0; st.n0[0] = 0; st.m_ext[0] = M; st.n_ext[0] = cut;
+                            st.m0[1] = 0; st.n0[1] = cut; st.m_ext[1] = M; st.n_ext[1] = rest;
+                        }
+                        st.ev[0] = ea;
+                        st.ev[1] = eb;
+                        add(st);
+                    }
+                }
+            }
+        }
+    }
+    std::stable_sort(all.begin(), all.end(), [](const Strategy& x, const Strategy& y) { return x.cost < y.cost; });
+    out->resize(all.size());
+    for (size_t i = 0; i < all.size(); i++) fill_info(h, all[i], K, &(*out)[i], (int)all.size(), 0);
+    return MP_OK;
 }
 
 mp_status plan_shape(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp_plan_info* out) {

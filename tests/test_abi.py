@@ -78,6 +78,32 @@ def test_argument_checks_before_launch():
     h.close()
 
 
+def test_plan_search_entry_points_check_arguments():
+    """mp_enumerate_plans, mp_gemm_with_plan and mp_set_plan_mode reject bad
+    arguments with status codes; a planning-only handle plans but cannot run."""
+    lib = mp.library()
+    h = _host()
+    n = ctypes.c_int32(-1)
+    e = lambda *a: lib.mp_enumerate_plans(*a)
+    assert e(None, 1, 10, 10, 10, None, 0, ctypes.byref(n)) == mp.MP_ERR_INVALID_ARG
+    assert e(h.ptr, 1, 10, 10, 10, None, -1, ctypes.byref(n)) == mp.MP_ERR_INVALID_ARG
+    assert e(h.ptr, 1, 10, 10, 10, None, 5, ctypes.byref(n)) == mp.MP_ERR_INVALID_ARG  # capacity without array
+    assert e(h.ptr, 1, 0, 10, 10, None, 0, ctypes.byref(n)) == mp.MP_ERR_INVALID_ARG
+    assert e(h.ptr, 1, 10, 10, 10, None, 0, None) == mp.MP_ERR_INVALID_ARG
+    assert e(h.ptr, 1, 100, 100, 100, None, 0, ctypes.byref(n)) == mp.MP_OK and n.value > 0
+    assert lib.mp_set_plan_mode(None, 0) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_set_plan_mode(h.ptr, 3) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_set_plan_mode(h.ptr, mp.MP_PLAN_WAVE) == mp.MP_OK
+    assert lib.mp_set_plan_mode(h.ptr, mp.MP_PLAN_MIKPOLY) == mp.MP_OK
+    plan = mp.mp_plan(h, 64, 64, 64)
+    A, B, D = 0x10000, 0x20000000, 0x40000000  # never dereferenced
+    g = lambda p, *a: lib.mp_gemm_with_plan(h.ptr, p, *a)
+    assert g(ctypes.byref(plan), 64, 64, 64, A, 64, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_ERR_UNSUPPORTED
+    assert g(None, 64, 64, 64, A, 64, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    assert g(ctypes.byref(plan), 64, 64, 64, A, 63, B, 64, None, 0, D, 64, 1.0, 0.0, None) == mp.MP_ERR_INVALID_ARG
+    h.close()
+
+
 def test_null_handle_and_host_init_errors():
     lib = mp.library()
     assert lib.mp_plan(None, 1, 1, 1, None) == mp.MP_ERR_INVALID_ARG

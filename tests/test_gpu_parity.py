@@ -437,6 +437,42 @@ def test_large_pair_plans_in_grouped_order(M, N, K, alpha, beta):
                           what=f"large {(M, N, K)}")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 520, 700), (1000, 768, 1300), (129, 2304, 4096)])
+def test_explicit_plans_and_ablation_models_match_oracle(M, N, K):
+    """Any candidate of the search space (cheap or expensive, Pattern I or
+    II, split or not) run through mp_gemm_with_plan, and the plans of the
+    WAVE and PIPE cost models, compute the same D within the bound."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    A, B, C = rand_problem(M, N, K, seed=M + 3, beta=0.5)
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    cands = mp.mp_enumerate_plans(h, M, N, K)
+    two = [c for c in cands if c.pattern == 2]
+    mid = len(cands) // 2
+    picks = cands[:3] + two[:2] + two[len(two) // 2:len(two) // 2 + 1] + cands[mid:mid + 2] + cands[-2:]
+    for p in picks:
+        D = torch.full((M, N), float("nan"), device=dev)
+        mp.mp_gemm_with_plan(h, p, Ad, Bd, Cd, D, 1.5, 0.5)
+        torch.cuda.synchronize()
+        desc = [(r.um, r.un, r.swap, r.pair, r.splits, r.m0, r.n0, r.m_ext, r.n_ext) for r in p.regions()]
+        assert_parity(D.cpu(), A, B, C, 1.5, 0.5, what=f"plan {desc}")
+    try:
+        for mode in (mp.MP_PLAN_WAVE, mp.MP_PLAN_PIPE):
+            mp.mp_set_plan_mode(h, mode)
+            assert_parity(run_gemm(A, B, C, 1.5, 0.5), A, B, C, 1.5, 0.5, what=f"mode {mode}")
+    finally:
+        mp.mp_set_plan_mode(h, mp.MP_PLAN_MIKPOLY)
+    # Regions that overlap are refused before anything runs.
+    bad = mp.MpPlanInfo()
+    bad.num_regions = 2
+    for i, (m0, me) in enumerate([(0, M // 2 + 8), (M // 2, M - M // 2)]):
+        bad.region[i].kernel, bad.region[i].m0, bad.region[i].m_ext = 0, m0, me
+        bad.region[i].n0, bad.region[i].n_ext, bad.region[i].splits = 0, N, 1
+    with pytest.raises(mp.MPError) as e:
+        mp.mp_gemm_with_plan(h, bad, Ad, Bd, Cd, torch.empty(M, N, device=dev), 1.5, 0.5)
+    assert e.value.status == mp.MP_ERR_PLAN
+
+
 def test_bounded_wait_reports_timeout_and_recovers():
     """A withheld pipeline stage makes the consumer's bounded wait expire; the
     kernel stops cleanly, mp_check reports it, and the next call is correct."""

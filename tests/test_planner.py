@@ -192,3 +192,58 @@ def test_pair_kernels_hold_two_sms_never_split_never_mix():
         bad.region[i].n0, bad.region[i].n_ext, bad.region[i].splits = 0, 256, 1
     assert mp.library().mp_evaluate_plan(h.ptr, 1, 1024, 256, 256, ctypes.byref(bad)) == mp.MP_ERR_PLAN
     h.close()
+
+
+def test_enumeration_covers_the_search_and_tiles_exactly():
+    """mp_enumerate_plans: every candidate tiles the output once, never mixes
+    pair and one-CTA kernels, comes sorted by cost, and the cheapest costs no
+    more than the heuristic search's choice."""
+    h = gb300_handle()
+    rng = np.random.default_rng(11)
+    shapes = [(4096, 1024, 4096), (105, 1024, 12544), (1984, 2304, 768), (1, 3072, 1024)]
+    shapes += [(int(rng.integers(1, 6000)), 8 * int(rng.integers(1, 700)), int(rng.integers(1, 6000))) for _ in range(12)]
+    for (M, N, K) in shapes:
+        plans = mp.mp_enumerate_plans(h, M, N, K)
+        assert plans, (M, N, K)
+        costs = [p.cost_us for p in plans]
+        assert costs == sorted(costs)
+        for p in plans[:200] + plans[-50:]:
+            check_tiling(p, M, N)
+            assert len({r.pair for r in p.regions()}) == 1
+            for r in p.regions():
+                if r.pair:
+                    assert r.splits == 1
+        best = mp.mp_plan(h, M, N, K)
+        assert costs[0] <= best.cost_us * 1.005 + 1e-9, (M, N, K, costs[0], best.cost_us)
+        assert any(p.pattern == 1 for p in plans)
+    first3 = mp.mp_enumerate_plans(h, 4096, 1024, 4096, capacity=3)
+    assert len(first3) == 3
+    h.close()
+
+
+def test_wave_and_pipe_cost_models():
+    """The ablation models of the cost-model study: WAVE minimises the total
+    wave count (large micro-kernels), PIPE the total pipeline-task time (small
+    ones); the default model is restored by mode 0."""
+    h = gb300_handle()
+    for (M, N, K) in [(4096, 1024, 4096), (1984, 2304, 768), (300, 5000, 2000)]:
+        ref = mp.mp_plan(h, M, N, K)
+        cands = mp.mp_enumerate_plans(h, M, N, K)
+        mp.mp_set_plan_mode(h, mp.MP_PLAN_WAVE)
+        pw = mp.mp_plan(h, M, N, K)
+        assert pw.cost_us == sum(r.f_wave for r in pw.regions())
+        assert pw.cost_us <= min(sum(r.f_wave for r in c.regions()) for c in cands)
+        mp.mp_set_plan_mode(h, mp.MP_PLAN_PIPE)
+        pp = mp.mp_plan(h, M, N, K)
+        assert abs(pp.cost_us - sum(r.f_pipe_us for r in pp.regions())) < 1e-9
+        area = lambda p: min(r.um * r.un for r in p.regions())
+        assert area(pw) >= area(ref) >= area(pp) or area(pw) >= area(pp)
+        mp.mp_set_plan_mode(h, mp.MP_PLAN_MIKPOLY)
+        assert _key(mp.mp_plan(h, M, N, K)) == _key(ref)
+    with pytest.raises(mp.MPError):
+        mp.mp_set_plan_mode(h, 7)
+    h.close()
+
+
+def _key(p):
+    return [(r.kernel, r.m0, r.n0, r.m_ext, r.n_ext, r.splits) for r in p.regions()]
