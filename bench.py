@@ -41,6 +41,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_RECORD = {"kernel_sha1": "c34014ac9e57ce8ee9d83ef28087a75b110ea21f", "dram_bytes_per_alg_byte": 0.384}
 
 
+# --epilogue: (activation, bf16 D) of mp_gemm_ex.
+EPILOGUES = {"none": (0, False), "relu": (1, False), "gelu": (2, False), "bf16": (0, True),
+             "relu+bf16": (1, True), "gelu+bf16": (2, True)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -58,9 +63,9 @@ def kernel_sha1():
         return hashlib.sha1(f.read()).hexdigest()
 
 
-def roofline_us(g, peaks):
+def roofline_us(g, peaks, d_bytes=4):
     t_flop = g.flops / (peaks["bf16_tflops"] * 1e6)
-    t_mem = g.min_bytes() / (peaks["hbm_gbs"] * 1e3)
+    t_mem = g.min_bytes(d_bytes) / (peaks["hbm_gbs"] * 1e3)
     return max(t_flop, t_mem), ("tensor" if t_flop >= t_mem else "hbm")
 
 
@@ -188,11 +193,17 @@ def run_mp(args):
     sp = stream.cuda_stream
 
     gs = rank_workload(args.workload, rank)
+    act, out_bf16 = EPILOGUES[args.epilogue]
+    epi = act | (mp.MP_EPI_OUT_BF16 if out_bf16 else 0)
+    d_bytes = 2 if out_bf16 else 4
+    if epi and any(g.batch > 1 for g in gs):
+        raise SystemExit("--epilogue applies to workloads of single GEMMs")
     ops = []
     launches_per_step = 0
     for g in gs:
         A, B, C = wl.make_operands(g, device=dev)
-        D = torch.empty((g.batch, g.M, g.N) if g.batch > 1 else (g.M, g.N), device=dev)
+        D = torch.empty((g.batch, g.M, g.N) if g.batch > 1 else (g.M, g.N), device=dev,
+                        dtype=torch.bfloat16 if out_bf16 else torch.float32)
         ops.append((g, A, B, C, D))
         launches_per_step += 1 + int(needs_repack(A.data_ptr(), g.K)) + int(needs_repack(B.data_ptr(), g.N))
     torch.cuda.synchronize()
@@ -205,6 +216,9 @@ def run_mp(args):
             calls.append((lib.mp_gemm_batched, (h.ptr, g.batch, g.M, g.N, g.K, A.data_ptr(), g.K, g.M * g.K,
                                                 B.data_ptr(), g.N, g.K * g.N, cp, g.N, g.M * g.N,
                                                 D.data_ptr(), g.N, g.M * g.N, g.alpha, g.beta, sp)))
+        elif epi:
+            calls.append((lib.mp_gemm_ex, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
+                                           cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, epi, sp)))
         else:
             calls.append((lib.mp_gemm, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
                                         cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, sp)))
@@ -256,8 +270,8 @@ def run_mp(args):
     value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     # Per-shape roofline fractions (from the per-launch times).
-    troof = np.array([roofline_us(g, peaks)[0] for g in gs])
-    bounds = [roofline_us(g, peaks)[1] for g in gs]
+    troof = np.array([roofline_us(g, peaks, d_bytes)[0] for g in gs])
+    bounds = [roofline_us(g, peaks, d_bytes)[1] for g in gs]
     flops = np.array([g.flops for g in gs], dtype=np.float64)
     frac_shape = troof / per_launch
     flop_weighted = float(np.sum(flops * frac_shape) / np.sum(flops))
@@ -269,7 +283,7 @@ def run_mp(args):
     t_ten = sum(t for t, b in zip(troof, bounds) if b == "tensor")
     if t_hbm >= t_ten:
         sel = [i for i, b in enumerate(bounds) if b == "hbm"]
-        work = sum(gs[i].min_bytes() for i in sel)
+        work = sum(gs[i].min_bytes(d_bytes) for i in sel)
         achieved = work / (per_launch[sel].sum() * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
         unit, bound = "GB/s", "hbm"
@@ -280,7 +294,7 @@ def run_mp(args):
         peak = peaks["bf16_tflops"]
         unit, bound = "TFLOP/s", "tensor"
     traffic = None
-    if TRAFFIC_RECORD["kernel_sha1"] == kernel_sha1() and TRAFFIC_RECORD["dram_bytes_per_alg_byte"]:
+    if TRAFFIC_RECORD["kernel_sha1"] == kernel_sha1() and TRAFFIC_RECORD["dram_bytes_per_alg_byte"] and not epi:
         alg = sum(gs[i].min_bytes() for i in sel) / max(1, len(sel))
         traffic = TRAFFIC_RECORD["dram_bytes_per_alg_byte"] * alg
 
@@ -371,7 +385,8 @@ def run_mp(args):
                          "splits": r.splits, "tasks": r.f_parallel, "waves": r.f_wave}
                         for r in p.regions()]}) + "\n")
 
-    cpu = cpu_baseline(args, gs) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu = cpu_baseline(args, gs, act=act, out_bf16=out_bf16) \
+        if (rank == 0 and world == 1 and not args.no_cpu) else None
     if args.sweep and rank == 0:
         sweep(args, h, peaks, dev)
 
@@ -382,7 +397,7 @@ def run_mp(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": workload_desc(args.workload), "gemms_per_step": len(gs),
-                       "flops_per_step": int(flops_step), "l2": l2_note(gs),
+                       "flops_per_step": int(flops_step), "l2": l2_note(gs), "epilogue": args.epilogue,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
                                    "sum_troof_over_sum_t": round(time_ratio, 4),
@@ -475,7 +490,7 @@ def sweep(args, h, peaks, dev):
 # ---------------------------------------------------------------------------
 # the CPU oracle, timed on a bounded sample of the same workload
 # ---------------------------------------------------------------------------
-def cpu_baseline(args, gs, budget_s=None):
+def cpu_baseline(args, gs, budget_s=None, act=0, out_bf16=False):
     import torch
     import oracle
     from micro_polymerization_gb300 import workloads as wl
@@ -494,7 +509,11 @@ def cpu_baseline(args, gs, budget_s=None):
         Bb = wl.bf16_bits(B)
         Cn = C[:rows].numpy() if C is not None else None
         t0 = time.perf_counter()
-        _, used = oracle.gemm_rows(Ab, Bb, Cn, g.alpha, g.beta)
+        Dr, used = oracle.gemm_rows(Ab, Bb, Cn, g.alpha, g.beta)
+        if act:
+            Dr = oracle.epilogue(Dr, act)
+        if out_bf16:
+            Dr = oracle.bf16_round(Dr)
         t_total += time.perf_counter() - t0
         flops += 2.0 * rows * g.N * g.K
         done += 1
@@ -514,15 +533,16 @@ def run_reference(args):
     for _ in range(args.warmup):
         cpu_baseline(args, gs[:1], budget_s=0.01)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    act, out_bf16 = EPILOGUES[args.epilogue]
     vals = []
     for _ in range(args.steps):
-        vals.append(cpu_baseline(args, gs, budget_s=per_step))
+        vals.append(cpu_baseline(args, gs, budget_s=per_step, act=act, out_bf16=out_bf16))
     v = statistics.median(x["value"] for x in vals)
     line = {
         "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload)},
+        "config": {"workload": workload_desc(args.workload), "epilogue": args.epilogue},
         "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": vals[0]["cores"], "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -538,6 +558,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mp", "reference"], default="mp")
     ap.add_argument("--workload", default="dynamic_sequence")
+    ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="none",
+                    help="activation and D type of every GEMM (mp_gemm_ex); none = mp_gemm")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-count", type=int, default=128, help="GEMMs per workload in the sweep (sampled)")
     ap.add_argument("--dump", default=None, help="write per-GEMM time, roofline and plan (JSON lines)")

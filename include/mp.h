@@ -251,6 +251,28 @@ mp_status mp_gemm(mp_handle h, int64_t M, int64_t N, int64_t K,
                   float alpha, float beta, mp_stream stream);
 
 /*
+ * mp_gemm with an epilogue variant: an activation applied to
+ * alpha*A*B + beta*C, and the type of D.  These are the epilogue variants of
+ * templated GEMM libraries (BOLT summary, "Persistent kernel (GEMM/Conv)
+ * fusion": the alpha/beta epilogue form; activation and output type are the
+ * same epilogue's further stages).  The epilogue word is:
+ *   bits 0-7: MP_ACT_NONE, MP_ACT_RELU (max(x, 0)) or MP_ACT_GELU
+ *             (x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), computed in fp32);
+ *   MP_EPI_OUT_BF16: D is bf16 (row-major, ldd in elements, 2-byte aligned;
+ *             each value rounded to nearest even), else fp32.
+ * C stays fp32.  C and D must not overlap when D is bf16.  Otherwise the same
+ * arguments, rules and asynchrony as mp_gemm; mp_gemm is mp_gemm_ex with 0.
+ * Errors: as mp_gemm, and MP_ERR_INVALID_ARG for an unknown epilogue word.
+ */
+#define MP_ACT_NONE 0
+#define MP_ACT_RELU 1
+#define MP_ACT_GELU 2
+#define MP_EPI_OUT_BF16 0x100
+mp_status mp_gemm_ex(mp_handle h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                     int64_t ldb, const float* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta,
+                     int32_t epilogue, mp_stream stream);
+
+/*
  * `batch` same-shape problems in one launch [DISC, "GEMM merge" 2]: problem
  * b uses A + b*strideA, B + b*strideB, C + b*strideC, D + b*strideD (strides
  * in elements, >= 0).  Per-problem rules are those of mp_gemm; the D blocks

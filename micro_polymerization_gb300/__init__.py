@@ -20,12 +20,17 @@ __all__ = [
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
     "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
-    "MP_PLAN_PIPE",
+    "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
 ]
 
 MP_MAX_REGIONS = 4
 MP_MAX_KERNELS = 16
+
+MP_ACT_NONE = 0
+MP_ACT_RELU = 1
+MP_ACT_GELU = 2
+MP_EPI_OUT_BF16 = 0x100
 
 MP_PLAN_MIKPOLY = 0
 MP_PLAN_WAVE = 1
@@ -124,6 +129,8 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_gemm_with_plan": ([_vp, ctypes.POINTER(MpPlanInfo), _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                        _vp, _i64, _vp, _i64, _f, _f, _vp], ctypes.c_int),
                 "mp_set_plan_mode": ([_vp, _i32], ctypes.c_int),
+                "mp_gemm_ex": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                _f, _f, _i32, _vp], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -248,10 +255,10 @@ def mp_gemm(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, stream
     _check(st, "mp_gemm")
 
 
-def _gemm_args(A, B, C, D, beta):
+def _gemm_args(A, B, C, D, beta, d_types=("float32",)):
     import torch
-    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or D.dtype != torch.float32:
-        raise TypeError("A and B must be bfloat16, D float32")
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or str(D.dtype).split(".")[-1] not in d_types:
+        raise TypeError(f"A and B must be bfloat16, D one of {d_types}")
     M, K = A.shape[-2], A.shape[-1]
     N = B.shape[-1]
     if B.shape[-2] != K or D.shape[-2:] != (M, N):
@@ -272,6 +279,18 @@ def mp_gemm_with_plan(h: Handle, plan: MpPlanInfo, A, B, C, D, alpha: float = 1.
                                      _ld(B, "B"), c_ptr, ldc, D.data_ptr(), _ld(D, "D"), float(alpha), float(beta),
                                      _stream_ptr(stream))
     _check(st, "mp_gemm_with_plan")
+
+
+def mp_gemm_ex(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, act: int = MP_ACT_NONE,
+               stream=None) -> None:
+    """D = act(alpha*A@B + beta*C); D float32 or bfloat16 (the output bit of
+    the epilogue word follows D's dtype); C float32."""
+    import torch
+    M, N, K, c_ptr, ldc = _gemm_args(A, B, C, D, beta, d_types=("float32", "bfloat16"))
+    epi = int(act) | (MP_EPI_OUT_BF16 if D.dtype == torch.bfloat16 else 0)
+    st = library().mp_gemm_ex(h.ptr, M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"), c_ptr, ldc,
+                              D.data_ptr(), _ld(D, "D"), float(alpha), float(beta), epi, _stream_ptr(stream))
+    _check(st, "mp_gemm_ex")
 
 
 def mp_enumerate_plans(h: Handle, M: int, N: int, K: int, capacity=None, batch: int = 1):

@@ -79,10 +79,14 @@ mp_status check_args(const mp::GemmArgs& a) {
     const int64_t batch = a.batch, M = a.M, N = a.N, K = a.K;
     if (batch < 0 || M < 0 || N < 0 || K < 0) return MP_ERR_INVALID_ARG;
     if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || batch >= kMaxDim) return MP_ERR_INVALID_ARG;
+    const int act = a.epilogue & 0xff;
+    const bool d_bf16 = (a.epilogue & MP_EPI_OUT_BF16) != 0;
+    if ((a.epilogue & ~(0xff | MP_EPI_OUT_BF16)) != 0 || act > MP_ACT_GELU) return MP_ERR_INVALID_ARG;
     if (batch == 0 || M == 0 || N == 0) return MP_OK;
+    const int64_t d_elem = d_bf16 ? 2 : 4;
     if (!a.D) return MP_ERR_INVALID_ARG;
     if (a.ldd < (N > 1 ? N : 1)) return MP_ERR_INVALID_ARG;
-    if (((uintptr_t)a.D & 3) != 0) return MP_ERR_INVALID_ARG;
+    if (((uintptr_t)a.D & (uintptr_t)(d_elem - 1)) != 0) return MP_ERR_INVALID_ARG;
     if (a.strideA < 0 || a.strideB < 0 || a.strideC < 0 || a.strideD < 0) return MP_ERR_INVALID_ARG;
     if (K > 0) {
         if (!a.A || !a.B) return MP_ERR_INVALID_ARG;
@@ -96,13 +100,15 @@ mp_status check_args(const mp::GemmArgs& a) {
     }
     // Distinct problems of a batch must write disjoint D blocks.
     if (batch > 1 && a.strideD < (M - 1) * a.ldd + N) return MP_ERR_INVALID_ARG;
-    const Span d = span_of(a.D, M, N, a.ldd, 4, batch, a.strideD);
+    const Span d = span_of(a.D, M, N, a.ldd, d_elem, batch, a.strideD);
     if (K > 0) {
         if (overlap(d, span_of(a.A, M, K, a.lda, 2, batch, a.strideA))) return MP_ERR_INVALID_ARG;
         if (overlap(d, span_of(a.B, K, N, a.ldb, 2, batch, a.strideB))) return MP_ERR_INVALID_ARG;
     }
     if (read_c) {
-        const bool in_place = a.C == a.D && a.ldc == a.ldd && (batch == 1 || a.strideC == a.strideD);
+        // In place needs C and D of one type: fp32 D only.
+        const bool in_place =
+            !d_bf16 && a.C == a.D && a.ldc == a.ldd && (batch == 1 || a.strideC == a.strideD);
         if (!in_place && overlap(d, span_of(a.C, M, N, a.ldc, 4, batch, a.strideC)))
             return MP_ERR_INVALID_ARG;
     }
@@ -205,6 +211,14 @@ mp_status mp_gemm(mp_handle h, int64_t M, int64_t N, int64_t K, const void* A, i
                   const void* B, int64_t ldb, const float* C, int64_t ldc, float* D, int64_t ldd,
                   float alpha, float beta, mp_stream stream) {
     mp::GemmArgs a{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, D, ldd, 0, alpha, beta, stream};
+    return run(h, a);
+}
+
+mp_status mp_gemm_ex(mp_handle h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                     int64_t ldb, const float* C, int64_t ldc, void* D, int64_t ldd, float alpha, float beta,
+                     int32_t epilogue, mp_stream stream) {
+    mp::GemmArgs a{1, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, static_cast<float*>(D), ldd, 0, alpha, beta, stream,
+                   epilogue};
     return run(h, a);
 }
 

@@ -29,6 +29,7 @@
 // handle's status word, tells its other roles to stop, waits (bounded) for
 // its own copies and MMAs in flight, frees TMEM and returns.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -102,7 +103,9 @@ struct alignas(128) Params {
     int total_units;
     int num_regions;
     int inject_timeout;  // test hook: withhold the first stage of the first unit
-    int vec_c, vec_d;    // C / D rows allow 16-byte vector access
+    int vec_c, vec_d;    // C / D rows allow 16-byte (fp32 D) or 8-byte (bf16 D) vector access
+    int act;             // activation on alpha*acc + beta*C: 0 none, 1 ReLU, 2 GELU (erf form)
+    int out_bf16;        // 1: D is bf16 (round to nearest even), else fp32
     CUtensorMap tmD;     // D viewed as [batch][M][N] fp32, box {32 (N), 32 rows}, 128-byte swizzle
     // Split-K partials of region i viewed as [tiles*splits*128 rows][bn] fp32,
     // box {32, 32}, 128-byte swizzle (encoded for split regions of normal tiles).
@@ -529,13 +532,61 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn, int 
 // ---------------------------------------------------------------------------
 // Epilogue store of 16 accumulator columns of one TMEM lane
 // ---------------------------------------------------------------------------
+// Epilogue variants are compiled only into the EXT = true kernel, so that the
+// plain alpha/beta epilogue keeps its registers and instruction stream.
+//
+// The activation of the epilogue, applied to alpha*acc + beta*C.
+template <bool EXT>
+__device__ __forceinline__ float act_fn(int act, float x) {
+    if (!EXT || act == 0) return x;
+    if (act == 1) return fmaxf(x, 0.0f);
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));  // x Phi(x)
+}
+
+// D is addressed in bytes: an element is 4 bytes (fp32), or 2 (bf16) in the
+// EXT kernel, and row pointers advance by ldd elements of that size.
+template <bool EXT>
+__device__ __forceinline__ int d_esize(const Params& p) {
+    return (EXT && p.out_bf16) ? 2 : 4;
+}
+template <bool EXT>
+__device__ __forceinline__ uint8_t* d_ptr(const Params& p, long long off) {
+    return reinterpret_cast<uint8_t*>(p.D) + off * d_esize<EXT>(p);
+}
+
+// One output element at byte address `d` of D (fp32 or bf16).
+template <bool EXT>
+__device__ __forceinline__ void put_out(const Params& p, uint8_t* d, float x) {
+    if (EXT && p.out_bf16)
+        *reinterpret_cast<__nv_bfloat16*>(d) = __float2bfloat16_rn(x);
+    else
+        *reinterpret_cast<float*>(d) = x;
+}
+
+// Four consecutive elements (16-byte fp32 or 8-byte bf16 store; the caller
+// has checked the alignment).
+template <bool EXT>
+__device__ __forceinline__ void put_out4(const Params& p, uint8_t* d, float x0, float x1, float x2, float x3) {
+    if (EXT && p.out_bf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(x0, x1), hi = __floats2bfloat162_rn(x2, x3);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(d) = u;
+    } else {
+        *reinterpret_cast<float4*>(d) = make_float4(x0, x1, x2, x3);
+    }
+}
+
+template <bool EXT>
 __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, int c, const float* v) {
     const float alpha = p.alpha, beta = p.beta;
     if (!w.swap) {
         // lane = row of D, columns = columns of D
         const int m = w.m_t0 + tl;
         if (m >= w.m_end) return;
-        float* d = p.D + (long long)w.b * p.strideD + (long long)m * p.ldd;
+        uint8_t* d = d_ptr<EXT>(p, (long long)w.b * p.strideD + (long long)m * p.ldd);
+        const int es = d_esize<EXT>(p);
         const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc;
         const int n0 = w.n_t0 + c;
 #pragma unroll
@@ -544,14 +595,15 @@ __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, 
             if (n < w.n_end) {
                 float r = alpha * v[j];
                 if (beta != 0.0f) r = fmaf(beta, cr[n], r);
-                d[n] = r;
+                put_out<EXT>(p, d + (long long)n * es, act_fn<EXT>(p.act, r));
             }
         }
     } else {
         // lane = column of D, columns = rows of D
         const int n = w.n_t0 + tl;
         if (n >= w.n_end) return;
-        const long long bd = (long long)w.b * p.strideD + n;
+        uint8_t* bd = d_ptr<EXT>(p, (long long)w.b * p.strideD + n);
+        const long long ldd_b = p.ldd * d_esize<EXT>(p);
         const long long bc = (long long)w.b * p.strideC + n;
 #pragma unroll
         for (int j = 0; j < 16; j++) {
@@ -559,7 +611,7 @@ __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, 
             if (m < w.m_end) {
                 float r = alpha * v[j];
                 if (beta != 0.0f) r = fmaf(beta, p.C[bc + (long long)m * p.ldc], r);
-                p.D[bd + (long long)m * p.ldd] = r;
+                put_out<EXT>(p, bd + (long long)m * ldd_b, act_fn<EXT>(p.act, r));
             }
         }
     }
@@ -567,10 +619,11 @@ __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, 
 
 // Four consecutive columns n..n+3 of row m of D (vector access when allowed).
 // Same arithmetic as store16: alpha*acc, then fma with beta*C.
+template <bool EXT>
 __device__ __forceinline__ void store4(const Params& p, const Work& w, int m, int n, float4 x) {
     if (n >= w.n_end) return;
     const float alpha = p.alpha, beta = p.beta;
-    float* d = p.D + (long long)w.b * p.strideD + (long long)m * p.ldd + n;
+    uint8_t* d = d_ptr<EXT>(p, (long long)w.b * p.strideD + (long long)m * p.ldd + n);
     const float* cp = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + n;
     float o[4] = {alpha * x.x, alpha * x.y, alpha * x.z, alpha * x.w};
     if (p.vec_d && n + 3 < w.n_end) {
@@ -586,14 +639,14 @@ __device__ __forceinline__ void store4(const Params& p, const Work& w, int m, in
             o[2] = fmaf(beta, cv.z, o[2]);
             o[3] = fmaf(beta, cv.w, o[3]);
         }
-        *reinterpret_cast<float4*>(d) = make_float4(o[0], o[1], o[2], o[3]);
+        put_out4<EXT>(p, d, act_fn<EXT>(p.act, o[0]), act_fn<EXT>(p.act, o[1]), act_fn<EXT>(p.act, o[2]), act_fn<EXT>(p.act, o[3]));
     } else {
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             if (n + e < w.n_end) {
                 float r = o[e];
                 if (beta != 0.0f) r = fmaf(beta, cp[e], r);
-                d[e] = r;
+                put_out<EXT>(p, d + e * d_esize<EXT>(p), act_fn<EXT>(p.act, r));
             }
         }
     }
@@ -631,6 +684,7 @@ __device__ __forceinline__ void transpose16(int lane, const float* v, float4* st
 // slab (128-byte swizzle, conflict-free both ways) and come back one row at
 // a time with lane = column, so that every store instruction covers 128
 // contiguous bytes of one row of D.  Same arithmetic as the other paths.
+template <bool EXT>
 __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int q, int lane, int c, const float* v,
                                             uint8_t* slab) {
     const float a = p.alpha, bt = p.beta;
@@ -638,7 +692,6 @@ __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int 
     const bool in_n = n < w.n_end;
     const int mb = w.m_t0 + q * 32;
     const int rows = min(32, w.m_end - mb);
-    float* dcol = p.D + (long long)w.b * p.strideD + n;
     __syncwarp();  // the previous chunk's reads of the slab are done
     uint8_t* row = slab + lane * 128;
 #pragma unroll
@@ -650,7 +703,8 @@ __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int 
     // flight at once (coalesced along each row; the values of the tile are
     // in the slab by now).  Row pointers advance by the leading dimensions.
     const uint8_t* src = slab + (lane & 3) * 4;
-    float* dp = dcol + (long long)mb * p.ldd;
+    uint8_t* dp = d_ptr<EXT>(p, (long long)w.b * p.strideD + (long long)mb * p.ldd + n);
+    const long long ldd_b = p.ldd * d_esize<EXT>(p);
     const float* cp = p.C + (long long)w.b * p.strideC + (long long)mb * p.ldc + n;
 #pragma unroll 1
     for (int h0 = 0; h0 < rows; h0 += 16) {
@@ -671,9 +725,9 @@ __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int 
             if (in_n) {
                 float o = a * x;
                 if (bt != 0.0f) o = fmaf(bt, cv[r], o);
-                *dp = o;
+                put_out<EXT>(p, dp, act_fn<EXT>(p.act, o));
             }
-            dp += p.ldd;
+            dp += ldd_b;
         }
         cp += 16 * p.ldc;
     }
@@ -688,15 +742,16 @@ __device__ __forceinline__ void prefetch_c_tile_row(const Params& p, const Work&
     for (int c = 0; c < cols + 31; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + min(c, cols - 1)));
 }
 
+template <bool EXT>
 __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
                                        float4* stage) {
     if (w.swap) {
-        store16(p, w, q * 32 + lane, c, v);
+        store16<EXT>(p, w, q * 32 + lane, c, v);
         return;
     }
     transpose16(lane, v, stage, [&](int r, int g, float4 x) {
         const int m = w.m_t0 + q * 32 + r;
-        if (m < w.m_end) store4(p, w, m, w.n_t0 + c + 4 * g, x);
+        if (m < w.m_end) store4<EXT>(p, w, m, w.n_t0 + c + 4 * g, x);
     });
 }
 
@@ -709,13 +764,14 @@ __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, in
 // reading.
 // C for the same 32 x 32 block, one row per lane (zero outside the region);
 // issued before the TMEM load of the chunk so that both latencies overlap.
-__device__ __forceinline__ void load_c32(const Params& p, const Work& w, int lane, int m0, int n0, float* c) {
+template <int W>
+__device__ __forceinline__ void load_c(const Params& p, const Work& w, int lane, int m0, int n0, float* c) {
     const int m = m0 + lane;
     if (m < w.m_end) {
         const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + n0;
-        if (p.vec_c && n0 + 32 <= w.n_end) {
+        if (p.vec_c && n0 + W <= w.n_end) {
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
+            for (int j = 0; j < W / 4; j++) {
                 const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
                 c[4 * j] = x.x;
                 c[4 * j + 1] = x.y;
@@ -724,12 +780,16 @@ __device__ __forceinline__ void load_c32(const Params& p, const Work& w, int lan
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; j++) c[j] = n0 + j < w.n_end ? __ldg(cr + j) : 0.0f;
+            for (int j = 0; j < W; j++) c[j] = n0 + j < w.n_end ? __ldg(cr + j) : 0.0f;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; j++) c[j] = 0.0f;
+        for (int j = 0; j < W; j++) c[j] = 0.0f;
     }
+}
+
+__device__ __forceinline__ void load_c32(const Params& p, const Work& w, int lane, int m0, int n0, float* c) {
+    load_c<32>(p, w, lane, m0, n0, c);
 }
 
 // Ask L2 for this lane's row of C over the whole tile (one 128-byte line per
@@ -741,24 +801,33 @@ __device__ __forceinline__ void prefetch_c_row(const Params& p, const Work& w, i
         asm volatile("prefetch.global.L2 [%0];" ::"l"(cr + c));
 }
 
+template <bool EXT>
 __device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int lane, int m0, int n0,
                                            const float* v, const float* c, uint8_t* slab, uint32_t slab_s) {
     if (lane == 0) bulk_wait_read_1();
     __syncwarp();
     const float a = p.alpha, bt = p.beta;
+    const int act = EXT ? p.act : 0;
     uint8_t* row = slab + lane * 128;
-    if (bt == 0.0f) {
+    if (bt == 0.0f && act == 0) {
 #pragma unroll
         for (int j = 0; j < 8; j++)
             *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
                 make_float4(a * v[4 * j], a * v[4 * j + 1], a * v[4 * j + 2], a * v[4 * j + 3]);
     } else {
-        // Same arithmetic as the other epilogue paths: fma(beta, C, alpha*acc).
+        // Same arithmetic as the other epilogue paths: fma(beta, C, alpha*acc),
+        // then the activation.
 #pragma unroll
-        for (int j = 0; j < 8; j++)
-            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
-                make_float4(fmaf(bt, c[4 * j], a * v[4 * j]), fmaf(bt, c[4 * j + 1], a * v[4 * j + 1]),
-                            fmaf(bt, c[4 * j + 2], a * v[4 * j + 2]), fmaf(bt, c[4 * j + 3], a * v[4 * j + 3]));
+        for (int j = 0; j < 8; j++) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                o[e] = a * v[4 * j + e];
+                if (!EXT || bt != 0.0f) o[e] = fmaf(bt, c[4 * j + e], o[e]);  // without EXT, bt != 0 here
+                o[e] = act_fn<EXT>(act, o[e]);
+            }
+            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+        }
     }
     fence_async_smem();
     __syncwarp();
@@ -787,6 +856,7 @@ __device__ __forceinline__ void park16(const Work& w, int q, int lane, int c, co
 
 // Rows [r0, r1) of a split tile: sum the S partials in split order and write
 // D.  Consecutive threads take consecutive 16-byte groups of a row.
+template <bool EXT>
 __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, const float* tile_ws, int r0, int r1,
                                             int tid) {
     const int L = w.swap ? 128 : w.bn;
@@ -815,7 +885,8 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
             if (m < w.m_end && n < w.n_end) {
                 float o = alpha * acc;
                 if (beta != 0.0f) o = fmaf(beta, p.C[(long long)w.b * p.strideC + (long long)m * p.ldc + n], o);
-                p.D[(long long)w.b * p.strideD + (long long)m * p.ldd + n] = o;
+                put_out<EXT>(p, d_ptr<EXT>(p, (long long)w.b * p.strideD + (long long)m * p.ldd + n),
+                             act_fn<EXT>(p.act, o));
             }
         }
         return;
@@ -852,10 +923,10 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
             a1.x += x1.x; a1.y += x1.y; a1.z += x1.z; a1.w += x1.w;
         }
         const int m0 = w.m_t0 + r0 + i0 / L4;
-        if (m0 < w.m_end) store4(p, w, m0, w.n_t0 + 4 * (i0 % L4), a0);
+        if (m0 < w.m_end) store4<EXT>(p, w, m0, w.n_t0 + 4 * (i0 % L4), a0);
         if (two) {
             const int m1 = w.m_t0 + r0 + i1 / L4;
-            if (m1 < w.m_end) store4(p, w, m1, w.n_t0 + 4 * (i1 % L4), a1);
+            if (m1 < w.m_end) store4<EXT>(p, w, m1, w.n_t0 + 4 * (i1 % L4), a1);
         }
     }
 }
@@ -871,6 +942,7 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 // floats.  After a cluster barrier, this CTA sums rows [R r / S, R (r+1) / S)
 // over the S partials in split order (the same order, hence the same bits, as
 // the global-memory reduction) and writes D.  All threads of the CTA take part.
+template <bool EXT>
 __device__ __forceinline__ void csplit_reduce(const Params& p, const Work& w, uint32_t part_s) {
     const int S = w.splits, r = w.split;
     const int R = w.swap ? w.bn : 128, L = w.swap ? 128 : w.bn, P = L + 4;
@@ -896,7 +968,7 @@ __device__ __forceinline__ void csplit_reduce(const Params& p, const Work& w, ui
             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
         }
         const int m = w.m_t0 + row;
-        if (m < w.m_end) store4(p, w, m, w.n_t0 + 4 * g, a);
+        if (m < w.m_end) store4<EXT>(p, w, m, w.n_t0 + 4 * g, a);
     }
 }
 
@@ -911,7 +983,7 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
 // ---------------------------------------------------------------------------
 // CG = 1: one CTA per tile.  CG = 2: clusters of two CTAs on 256-row tile
 // pairs with the pair MMA (the even CTA issues for both; see umma_bf16).
-template <int CG>
+template <int CG, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
     constexpr bool kPair = CG == 2;
     extern __shared__ uint8_t smem_raw[];
@@ -1234,7 +1306,63 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
-            if (w.splits == 1 && p.tma_d && !w.swap) {
+            if (EXT && w.splits == 1 && p.tma_d && !w.swap && p.out_bf16) {
+                // bf16 D: 64-column chunks, so that a lane's row of the slab is
+                // 128 bytes (the 128-byte swizzle); two TMEM loads per chunk.
+                const bool with_c = p.beta != 0.0f;
+                const float a = p.alpha, bt = p.beta;
+                for (int c = 0; c < w.bn; c += 64) {
+                    const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
+                    const bool do_store = m0 < w.m_end && n0 < w.n_end;  // the same for the whole warp
+                    const uint32_t off = (slab & 1u) * 4096u;
+                    if (do_store) {
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
+                    }
+                    uint8_t* row = epi_g + off + lane * 128;
+#pragma unroll 1
+                    for (int qq = 0; qq < 4; qq++) {  // 16 columns = 32 bytes of bf16 at a time
+                        float cv[16];
+                        if (with_c) load_c<16>(p, w, lane, m0, n0 + 16 * qq, cv);
+                        float v[16];
+                        if (has_k) {
+                            tmem_ld16(t + c + 16 * qq, v);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; j++) v[j] = 0.0f;
+                        }
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int j = 0; j < 8; j++) {
+                            float x0 = a * v[2 * j], x1 = a * v[2 * j + 1];
+                            if (with_c) {
+                                x0 = fmaf(bt, cv[2 * j], x0);
+                                x1 = fmaf(bt, cv[2 * j + 1], x1);
+                            }
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(act_fn<EXT>(p.act, x0), act_fn<EXT>(p.act, x1));
+                            pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        if (do_store) {
+#pragma unroll
+                            for (int j = 0; j < 2; j++)
+                                *reinterpret_cast<uint4*>(row + (((2 * qq + j) ^ (lane & 7)) << 4)) =
+                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        }
+                    }
+                    if (do_store) {
+                        fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&p.tmD, epi_s + off, n0, m0, w.b);
+                            bulk_commit_group();
+                        }
+                        ++slab;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release_acc(acc);
+            } else if (w.splits == 1 && p.tma_d && !w.swap) {
                 const bool with_c = p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
@@ -1252,7 +1380,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     // alternation is kept by counting only real stores).
                     if (m0 < w.m_end && n0 < w.n_end) {
                         const uint32_t off = (slab & 1u) * 4096u;
-                        emit32_tma(p, w, lane, m0, n0, v, cv, epi_g + off, epi_s + off);
+                        emit32_tma<EXT>(p, w, lane, m0, n0, v, cv, epi_g + off, epi_s + off);
                         ++slab;
                     }
                 }
@@ -1272,7 +1400,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 #pragma unroll
                         for (int j = 0; j < 32; j++) v[j] = 0.0f;
                     }
-                    emit32_rows(p, w, q, lane, c, v, epi_g);
+                    emit32_rows<EXT>(p, w, q, lane, c, v, epi_g);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1286,7 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 #pragma unroll
                         for (int j = 0; j < 16; j++) v[j] = 0.0f;
                     }
-                    emit16(p, w, q, lane, c, v, stage);
+                    emit16<EXT>(p, w, q, lane, c, v, stage);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1418,7 +1546,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                         const int R = w.swap ? w.bn : 128;
                         const int r0 = (int)((long long)R * w.split / w.splits);
                         const int r1 = (int)((long long)R * (w.split + 1) / w.splits);
-                        reduce_rows(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
+                        reduce_rows<EXT>(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
                         named_bar_sync(1, 128);
                         if (threadIdx.x == 64) {
                             // The last split to leave resets the counter for the next launch.
@@ -1446,7 +1574,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             // memory; sum this CTA's slice; leave only when no CTA of the
             // cluster still reads this one's partial.
             cluster_sync();
-            if ((int)blockIdx.x < p.total_units) csplit_reduce(p, decode(p, regs_s, (int)blockIdx.x, 0), ring0);
+            if ((int)blockIdx.x < p.total_units) csplit_reduce<EXT>(p, decode(p, regs_s, (int)blockIdx.x, 0), ring0);
             cluster_sync();
         }
     }
@@ -1543,6 +1671,16 @@ struct DeviceState {
     int max_pairs = 0;
 };
 
+// The dynamic shared memory of every instantiation of the persistent kernel.
+bool set_kernel_smem() {
+    const int b = dev::kSmemBytes;
+    const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    return cudaFuncSetAttribute(dev::k_poly_gemm<1, false>, a, b) == cudaSuccess &&
+           cudaFuncSetAttribute(dev::k_poly_gemm<2, false>, a, b) == cudaSuccess &&
+           cudaFuncSetAttribute(dev::k_poly_gemm<1, true>, a, b) == cudaSuccess &&
+           cudaFuncSetAttribute(dev::k_poly_gemm<2, true>, a, b) == cudaSuccess;
+}
+
 // Split-K on chip: for S = 2..16, the CTAs that clusters of S CTAs of the
 // one-CTA kernel can keep resident (queried once; sizes past 8 need the
 // non-portable cluster attribute).  MP_CSPLIT=0 disables it.
@@ -1551,8 +1689,11 @@ void query_cluster_split(mp_handle h, int num_sms) {
     for (int S = 0; S <= 16; S++) h->cluster_ctas[S] = 0;
     if (const char* v = std::getenv("MP_CSPLIT"))
         if (std::atoi(v) == 0) return;
-    const bool big = cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                     cudaSuccess;
+    const bool big =
+        cudaFuncSetAttribute(dev::k_poly_gemm<1, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(dev::k_poly_gemm<1, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
     if (!big) (void)cudaGetLastError();
     for (int S = 2; S <= (big ? 16 : 8); S++) {
         cudaLaunchConfig_t oc = {};
@@ -1567,7 +1708,7 @@ void query_cluster_split(mp_handle h, int num_sms) {
         oc.attrs = ca;
         oc.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<1>, &oc) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<1, false>, &oc) != cudaSuccess) {
             (void)cudaGetLastError();
             continue;
         }
@@ -1595,7 +1736,7 @@ int query_max_pairs(int num_sms) {
     oc.attrs = ca;
     oc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<2>, &oc) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, dev::k_poly_gemm<2, false>, &oc) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -1755,11 +1896,7 @@ mp_status device_init(mp_handle h, int device) {
     if (cudaMalloc(&s->staging, (size_t)s->staging_bytes) != cudaSuccess) return MP_ERR_NO_MEMORY;
     if (cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)kMaxCounters) != cudaSuccess) return MP_ERR_CUDA;
     if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
-    if (cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(dev::k_poly_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-            cudaSuccess)
-        return MP_ERR_CUDA;
+    if (!set_kernel_smem()) return MP_ERR_CUDA;
     s->max_pairs = query_max_pairs(s->num_sms);
     query_cluster_split(h, s->num_sms);
     if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
@@ -1793,11 +1930,7 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
         q != cudaDriverEntryPointSuccess || !fn)
         return MP_ERR_CUDA;
     s->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (cudaFuncSetAttribute(dev::k_poly_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(dev::k_poly_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, dev::kSmemBytes) !=
-            cudaSuccess)
-        return MP_ERR_CUDA;
+    if (!set_kernel_smem()) return MP_ERR_CUDA;
     s->max_pairs = query_max_pairs(s->num_sms);
     query_cluster_split(h, s->num_sms);
     h->host_only = false;
@@ -1978,15 +2111,25 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // past M and N are clipped by the map; region cuts fall on tile
     // boundaries, so no tile reaches another region.  C (beta != 0) is read
     // by the epilogue threads and fused before the store.
+    // Epilogue variant: activation on alpha*acc + beta*C, and fp32 or bf16 D.
+    p.act = a.epilogue & 0xff;
+    p.out_bf16 = (a.epilogue & MP_EPI_OUT_BF16) ? 1 : 0;
+    const int64_t de = p.out_bf16 ? 2 : 4;  // bytes per element of D
     p.tma_d = 0;
-    if (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0 &&
-        (batch == 1 || (a.strideD * 4) % 16 == 0)) {
-        const uint64_t d_s2 = batch > 1 ? (uint64_t)a.strideD * 4 : (uint64_t)round_up(M * a.ldd * 4, 16);
-        if (encode_3d_f32(s, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch, (uint64_t)a.ldd * 4,
-                          d_s2, 32, 32))
+    if (((uintptr_t)a.D & 15u) == 0 && (a.ldd * de) % 16 == 0 && (batch == 1 || (a.strideD * de) % 16 == 0)) {
+        const uint64_t d_s2 = batch > 1 ? (uint64_t)(a.strideD * de) : (uint64_t)round_up(M * a.ldd * de, 16);
+        // fp32: slabs of 32 x 32; bf16: slabs of 64 columns x 32 rows (128-byte rows either way).
+        if (p.out_bf16 ? encode_3d(s, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch,
+                                   (uint64_t)(a.ldd * 2), d_s2, 64, 32)
+                       : encode_3d_f32(s, &p.tmD, a.D, (uint64_t)N, (uint64_t)M, (uint64_t)batch,
+                                       (uint64_t)a.ldd * 4, d_s2, 32, 32))
             p.tma_d = 1;
     }
-    p.vec_d = (((uintptr_t)a.D & 15u) == 0 && a.ldd % 4 == 0 && (batch == 1 || a.strideD % 4 == 0)) ? 1 : 0;
+    // Four consecutive elements per store: 16 bytes (fp32) or 8 bytes (bf16).
+    p.vec_d = (((uintptr_t)a.D & (uintptr_t)(4 * de - 1)) == 0 && a.ldd % 4 == 0 &&
+               (batch == 1 || a.strideD % 4 == 0))
+                  ? 1
+                  : 0;
     p.vec_c = (p.C && ((uintptr_t)a.C & 15u) == 0 && a.ldc % 4 == 0 && (batch == 1 || a.strideC % 4 == 0)) ? 1 : 0;
     p.D = a.D;
     p.ldc = a.ldc;
@@ -2093,8 +2236,13 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (pair || csplit) ? 2 : 1;
-    const cudaError_t e = pair ? cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<2>, p)
-                               : cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<1>, p);
+    // The plain alpha/beta epilogue runs in the kernel built without the
+    // variants; an activation or bf16 D selects the other instantiation.
+    const bool ext = p.act != 0 || p.out_bf16 != 0;
+    const cudaError_t e = pair ? (ext ? cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<2, true>, p)
+                                      : cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<2, false>, p))
+                               : (ext ? cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<1, true>, p)
+                                      : cudaLaunchKernelEx(&cfg, dev::k_poly_gemm<1, false>, p));
     if (e != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }

@@ -94,6 +94,7 @@ struct GemmArgs {
     float* D; int64_t ldd, strideD;
     float alpha, beta;
     void* stream;
+    int32_t epilogue = 0;  // mp_gemm_ex's epilogue word (activation, bf16 D)
 };
 mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a);
 mp_status device_check(mp_handle h, void* stream);

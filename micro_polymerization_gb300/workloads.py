@@ -37,9 +37,10 @@ class Gemm:
     def flops(self) -> int:
         return 2 * self.M * self.N * self.K * self.batch
 
-    def min_bytes(self) -> int:
-        """Each operand read once, D written once: the algorithmic traffic."""
-        per = 2 * self.M * self.K + 2 * self.K * self.N + 4 * self.M * self.N
+    def min_bytes(self, d_bytes: int = 4) -> int:
+        """Each operand read once, D written once: the algorithmic traffic
+        (d_bytes per element of D: 4 for fp32, 2 for bf16)."""
+        per = 2 * self.M * self.K + 2 * self.K * self.N + d_bytes * self.M * self.N
         if self.beta != 0.0:
             per += 4 * self.M * self.N
         return per * self.batch

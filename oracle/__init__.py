@@ -18,6 +18,13 @@ What each routine follows (page titles and sections):
   * ``gemm_entries`` / ``magnitude`` / ``freivalds`` -- the same definition
     evaluated at chosen entries, its element-wise magnitude, and a
     matrix-vector probe for outputs too large to recompute.
+  * ``epilogue`` -- the activation of the epilogue variants, applied in fp64
+    to alpha*A*B + beta*C: ReLU max(x, 0), GELU x*Phi(x) with Phi the standard
+    normal distribution function (BOLT summary, "Persistent kernel (GEMM/Conv)
+    fusion": activations as further epilogue stages).
+  * ``bf16_round`` -- fp64 values rounded to bf16 (nearest even), for the
+    bf16-output variant; ``within_bound_out`` the parity bound with the
+    activation's slope and one bf16 unit of the reference added.
 """
 from __future__ import annotations
 
@@ -210,6 +217,50 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 # The parity bound stated for bf16 inputs with fp32 accumulation and fp32 output:
 #   |D - D_ref| <= 2e-3 * (sum_k |A_ik||B_kj| + |beta*C_ij|)
 PARITY_RTOL = 2e-3
+
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+# Largest slope of the activations: ReLU 1; GELU x*Phi(x) has
+# d/dx = Phi(x) + x*phi(x), largest near x = 1.414 (about 1.1289).
+ACT_SLOPE = {ACT_NONE: 1.0, ACT_RELU: 1.0, ACT_GELU: 1.1290}
+
+
+def epilogue(X, act: int) -> np.ndarray:
+    """The activation of the epilogue variants, in fp64."""
+    import math
+    X = np.asarray(X, dtype=np.float64)
+    if act == ACT_NONE:
+        return X.copy()
+    if act == ACT_RELU:
+        return np.maximum(X, 0.0)
+    if act == ACT_GELU:
+        erf = np.vectorize(math.erf, otypes=[np.float64])
+        return X * 0.5 * (1.0 + erf(X / math.sqrt(2.0)))
+    raise ValueError(f"unknown activation {act}")
+
+
+def bf16_round(X) -> np.ndarray:
+    """fp64 -> nearest bf16 (ties to even), returned as fp64: the value rounded
+    once to fp32 by the same rule, then its low 16 bits rounded off."""
+    f = np.asarray(X, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    out = r.astype(np.uint32).view(np.float32).astype(np.float64)
+    return np.where(np.isnan(f), np.nan, out)
+
+
+def within_bound_out(D, Dref_act, mag, act: int, bf16: bool, rtol: float = PARITY_RTOL):
+    """Parity of an epilogue variant: |D - act(Dref)| <= rtol * slope(act) * mag
+    (the stated bound carried through the activation), plus one bf16 unit of
+    act(Dref) when D is bf16 (the output's own rounding)."""
+    D = np.asarray(D, dtype=np.float64)
+    bound = rtol * ACT_SLOPE[act] * np.asarray(mag, dtype=np.float64)
+    if bf16:
+        bound = bound + np.abs(Dref_act) * 2.0 ** -8
+    err = np.abs(D - Dref_act)
+    ok = bool(np.all(err <= bound))
+    worst = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    return ok, worst
 
 
 def within_bound(D, Dref, mag, rtol: float = PARITY_RTOL):

@@ -104,6 +104,28 @@ def test_plan_search_entry_points_check_arguments():
     h.close()
 
 
+def test_epilogue_word_and_bf16_output_checks():
+    """mp_gemm_ex validates the epilogue word, bf16 D's alignment, and
+    refuses C overlapping a bf16 D (different element types)."""
+    lib = mp.library()
+    h = _host()
+    A, B, C, D = 0x10000, 0x20000000, 0x30000000, 0x40000000  # never dereferenced
+    g = lambda epi, *a: lib.mp_gemm_ex(h.ptr, *a, epi, None)
+    args = (64, 64, 64, A, 64, B, 64, C, 64, D, 64, 1.0, 0.5)
+    assert g(0, *args) == mp.MP_ERR_UNSUPPORTED  # valid; planning-only handle
+    assert g(mp.MP_ACT_GELU | mp.MP_EPI_OUT_BF16, *args) == mp.MP_ERR_UNSUPPORTED
+    assert g(3, *args) == mp.MP_ERR_INVALID_ARG  # unknown activation
+    assert g(0x200, *args) == mp.MP_ERR_INVALID_ARG  # unknown bit
+    odd = (64, 64, 64, A, 64, B, 64, C, 64, D + 2, 64, 1.0, 0.5)
+    assert g(mp.MP_EPI_OUT_BF16, *odd) == mp.MP_ERR_UNSUPPORTED  # 2-byte aligned bf16 D is fine
+    assert g(0, *odd) == mp.MP_ERR_INVALID_ARG  # fp32 D needs 4-byte alignment
+    assert g(mp.MP_EPI_OUT_BF16, *(64, 64, 64, A, 64, B, 64, C, 64, D + 1, 64, 1.0, 0.5)) == mp.MP_ERR_INVALID_ARG
+    inplace = (64, 64, 64, A, 64, B, 64, D, 64, D, 64, 1.0, 0.5)
+    assert g(0, *inplace) == mp.MP_ERR_UNSUPPORTED  # fp32 in place is allowed
+    assert g(mp.MP_EPI_OUT_BF16, *inplace) == mp.MP_ERR_INVALID_ARG
+    h.close()
+
+
 def test_null_handle_and_host_init_errors():
     lib = mp.library()
     assert lib.mp_plan(None, 1, 1, 1, None) == mp.MP_ERR_INVALID_ARG

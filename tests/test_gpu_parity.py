@@ -473,6 +473,51 @@ def test_explicit_plans_and_ablation_models_match_oracle(M, N, K):
     assert e.value.status == mp.MP_ERR_PLAN
 
 
+@pytest.mark.parametrize("M,N,K,beta", [(300, 520, 700, 0.5), (300, 517, 450, 0.5), (130, 517, 200, 0.0)])
+def test_epilogue_variants_every_kernel(M, N, K, beta):
+    """mp_gemm_ex: ReLU / GELU on alpha*A*B + beta*C and fp32 / bf16 D, for
+    every micro-kernel with and without split-K, on aligned and odd-pitch D:
+    within the bound carried through the activation (plus one bf16 unit of
+    the reference for bf16 D)."""
+    import oracle
+    h = handle()
+    dev = torch.device("cuda", 0)
+    A, B, C = rand_problem(M, N, K, seed=M + N, beta=beta)
+    Dref, mag = oracle_full(A, B, C, 1.25, beta)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = C.to(dev) if C is not None else None
+    refs = {act: oracle.epilogue(Dref, act) for act in (mp.MP_ACT_NONE, mp.MP_ACT_RELU, mp.MP_ACT_GELU)}
+    try:
+        for k, desc in enumerate(_kernels()):
+            for splits in ((1,) if desc.pair else (1, 3)):
+                mp.mp_force_plan(h, k, splits)
+                for act, ref in refs.items():
+                    for dt in (torch.float32, torch.bfloat16):
+                        D = torch.full((M, N), float("nan"), device=dev, dtype=dt)
+                        mp.mp_gemm_ex(h, Ad, Bd, Cd, D, 1.25, beta, act=act)
+                        torch.cuda.synchronize()
+                        ok, worst = oracle.within_bound_out(D.float().cpu().numpy(), ref, mag, act,
+                                                            dt == torch.bfloat16)
+                        assert ok, (f"kernel {k} ({desc.um}x{desc.un} swap={desc.swap} pair={desc.pair}) "
+                                    f"splits={splits} act={act} {dt} worst={worst:.3g}")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
+def test_epilogue_word_zero_is_mp_gemm():
+    """mp_gemm is mp_gemm_ex with epilogue 0: the same bits."""
+    dev = torch.device("cuda", 0)
+    for (M, N, K, beta) in [(1000, 768, 1300, 0.5), (105, 1024, 12544, 1.0), (4096, 4096, 512, 0.0)]:
+        A, B, C = rand_problem(M, N, K, seed=K, beta=beta)
+        Cd = C.to(dev) if C is not None else None
+        D1 = torch.empty(M, N, device=dev)
+        D2 = torch.empty(M, N, device=dev)
+        mp.mp_gemm(handle(), A.to(dev), B.to(dev), Cd, D1, 1.0, beta)
+        mp.mp_gemm_ex(handle(), A.to(dev), B.to(dev), Cd, D2, 1.0, beta, act=mp.MP_ACT_NONE)
+        torch.cuda.synchronize()
+        assert torch.equal(D1, D2)
+
+
 def test_bounded_wait_reports_timeout_and_recovers():
     """A withheld pipeline stage makes the consumer's bounded wait expire; the
     kernel stops cleanly, mp_check reports it, and the next call is correct."""

@@ -333,3 +333,40 @@ def test_generator_is_seeded_and_in_range():
     x = np.random.default_rng(0).uniform(-1, 1, 1000).astype(np.float32)
     import torch
     assert np.array_equal(wl.bf16_bits(torch.from_numpy(x).to(torch.bfloat16)), f32_to_bf16_bits(x))
+
+
+# ----------------------------------------------------------------------------
+# Epilogue variants: activations and bf16 output
+# ----------------------------------------------------------------------------
+
+def test_activation_pins():
+    """ReLU's closed form; GELU = x*Phi(x) against standard-normal table values
+    (Phi(1) = 0.8413447460685429, Phi(-1) = 0.15865525393145707,
+    Phi(2) = 0.9772498680518208), the identity gelu(x) - gelu(-x) = x, and its
+    tails."""
+    x = np.array([-3.0, -1.0, -0.0, 0.0, 0.5, 1.0, 2.0, 40.0])
+    assert np.array_equal(oracle.epilogue(x, oracle.ACT_RELU), np.maximum(x, 0.0))
+    assert np.array_equal(oracle.epilogue(x, oracle.ACT_NONE), x)
+    g = oracle.epilogue(np.array([1.0, -1.0, 2.0]), oracle.ACT_GELU)
+    assert np.allclose(g, [0.8413447460685429, -0.15865525393145707, 2 * 0.9772498680518208], rtol=0, atol=1e-15)
+    y = np.linspace(-6, 6, 241)
+    assert np.allclose(oracle.epilogue(y, oracle.ACT_GELU) - oracle.epilogue(-y, oracle.ACT_GELU), y, atol=1e-14)
+    assert abs(oracle.epilogue(np.array([40.0]), oracle.ACT_GELU)[0] - 40.0) < 1e-12
+    assert abs(oracle.epilogue(np.array([-40.0]), oracle.ACT_GELU)[0]) < 1e-12
+    # the slope bound used by the parity check
+    h = 1e-6
+    slope = (oracle.epilogue(y + h, oracle.ACT_GELU) - oracle.epilogue(y - h, oracle.ACT_GELU)) / (2 * h)
+    assert slope.max() <= oracle.ACT_SLOPE[oracle.ACT_GELU] and slope.max() > 1.12
+
+
+def test_bf16_rounding_pins():
+    """Nearest-even rounding to bf16: exact values stay, halfway cases go to
+    the even neighbour, and the result matches torch's own conversion."""
+    import torch
+    vals = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -9, -2.5, 3.0e38, 1e-40])
+    r = oracle.bf16_round(vals)
+    assert r[0] == 1.0 and r[1] == 1.0 and r[2] == 1.0 + 4 * 2 ** -8 and r[3] == 1.0 and r[4] == -2.5
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(10000) * 10.0 ** rng.integers(-6, 6, 10000)
+    t = torch.tensor(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.bf16_round(x.astype(np.float32).astype(np.float64)), t)
