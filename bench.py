@@ -58,9 +58,11 @@ def load_peaks():
 
 
 def kernel_sha1():
-    p = os.path.join(ROOT, "micro_polymerization_gb300", "csrc", "mp_gemm.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+    h = hashlib.sha1()
+    for name in ("mp_kernel.cuh", "mp_gemm.cu"):  # the kernel and its launch
+        with open(os.path.join(ROOT, "micro_polymerization_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def roofline_us(g, peaks, d_bytes=4):

@@ -1,6 +1,6 @@
 """Build the C-ABI shared library libmp.so in-tree with nvcc for sm_103a.
 
-The three translation units are compiled in parallel and linked into
+The translation units are compiled in parallel and linked into
 ``micro_polymerization_gb300/_lib/libmp.so``; nothing is installed elsewhere.
 """
 from __future__ import annotations
@@ -16,8 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmp.so")
-SOURCES = ["mp_api.cpp", "mp_planner.cpp", "mp_gemm.cu", "mp_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "mp_internal.h"), os.path.join(ROOT, "include", "mp.h")]
+SOURCES = ["mp_api.cpp", "mp_planner.cpp", "mp_gemm.cu", "mp_gemm_act_f32.cu", "mp_gemm_bf16.cu", "mp_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "mp_internal.h"), os.path.join(CSRC, "mp_kernel.cuh"), os.path.join(ROOT, "include", "mp.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -504,6 +504,31 @@ def test_epilogue_variants_every_kernel(M, N, K, beta):
         mp.mp_force_plan(h, -1, 0)
 
 
+def test_activation_values_exact_inputs():
+    """alpha = 0, beta = 1: D = act(C) with C exact, so the activation alone is
+    measured, far below the GEMM bound: ReLU exactly; GELU within 1e-6 |x|
+    (Hastings' erf approximation, 1.5e-7, plus fp32 rounding)."""
+    import oracle
+    dev = torch.device("cuda", 0)
+    M, N, K = 256, 512, 64
+    A, B, _ = rand_problem(M, N, K, seed=5, beta=0.0)
+    x = np.linspace(-12.0, 12.0, M * N, dtype=np.float32).reshape(M, N)
+    x[0, :8] = [0.0, -0.0, 1e-30, -1e-30, 3.0e4, -3.0e4, 0.5, -0.5]
+    C = torch.from_numpy(x)
+    h = handle()
+    for act in (mp.MP_ACT_RELU, mp.MP_ACT_GELU):
+        D = torch.empty(M, N, device=dev)
+        mp.mp_gemm_ex(h, A.to(dev), B.to(dev), C.to(dev), D, 0.0, 1.0, act=act)
+        torch.cuda.synchronize()
+        got = D.cpu().numpy().astype(np.float64)
+        ref = oracle.epilogue(x.astype(np.float64), act)
+        if act == mp.MP_ACT_RELU:
+            assert np.array_equal(got, ref)
+        else:
+            err = np.abs(got - ref)
+            assert np.all(err <= 1e-6 * np.abs(x)), float((err / np.maximum(np.abs(x), 1e-30)).max())
+
+
 def test_epilogue_word_zero_is_mp_gemm():
     """mp_gemm is mp_gemm_ex with epilogue 0: the same bits."""
     dev = torch.device("cuda", 0)
