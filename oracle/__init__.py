@@ -25,6 +25,13 @@ What each routine follows (page titles and sections):
   * ``bf16_round`` -- fp64 values rounded to bf16 (nearest even), for the
     bf16-output variant; ``within_bound_out`` the parity bound with the
     activation's slope and one bf16 unit of the reference added.
+  * ``b2b`` -- back-to-back GEMMs (BOLT summary, "Persistent kernel
+    (GEMM/Conv) fusion"): D0 = alpha0*A0*W0 + beta0*C0, then
+    D1 = alpha1*D0*W1 + beta1*C1, in fp64 with no rounding of D0; an optional
+    activation on D0 (the epilogue variants above) sits between the two.
+    ``b2b_bound`` carries the stated per-GEMM bound through the second GEMM
+    and adds one bf16 rounding of D0 (the operand type of the second GEMM
+    when D0 stays on chip).
 """
 from __future__ import annotations
 
@@ -272,3 +279,48 @@ def within_bound(D, Dref, mag, rtol: float = PARITY_RTOL):
         ratio = np.where(lim > 0, err / np.where(lim > 0, lim, 1.0), np.where(err > 0, np.inf, 0.0))
     ok = bool(np.all(np.isfinite(D)) and np.all(err <= lim))
     return ok, float(ratio.max()) if ratio.size else 0.0
+
+
+def b2b(A0, W0, C0, W1, C1, alpha0, beta0, alpha1, beta1, act0: int = ACT_NONE):
+    """D1 = alpha1 * act0(alpha0 A0 W0 + beta0 C0) W1 + beta1 C1 in fp64.
+
+    A0 [M, K0], W0 [K0, N0] and W1 [N0, N1] are bf16 bit patterns; C0 [M, N0]
+    and C1 [M, N1] float32 (ignored when their beta is 0).  Returns (D1, D0),
+    D0 after the activation."""
+    D0 = epilogue(gemm(A0, W0, C0, alpha0, beta0), act0)
+    W1f = bf16_bits_to_f64(W1)
+    if D0.shape[1] != W1f.shape[0]:
+        raise ValueError("W1 rows must equal the columns of D0")
+    D1 = alpha1 * (D0 @ W1f)
+    if beta1 != 0.0:
+        D1 = D1 + beta1 * np.asarray(C1, dtype=np.float64)
+    return D1, D0
+
+
+def b2b_bound(A0, W0, C0, W1, C1, alpha0, beta0, alpha1, beta1, act0, D0, rtol: float = PARITY_RTOL):
+    """Element-wise bound on |D1 - D1_ref| for the fused back-to-back GEMM.
+
+    The first GEMM is within e0 = rtol * (|alpha0| sum|A0||W0| + |beta0 C0|);
+    the activation (slope at most L) carries it as L*e0; D0 is then rounded to
+    bf16 (at most 2^-8 of its value); the second GEMM adds its own stated bound
+    rtol * (|alpha1| |D0| |W1| + |beta1 C1|).  So
+      bound = rtol*mag1 + |alpha1| * ((L e0 (1 + 2^-8) + 2^-8 |D0|) |W1|)."""
+    u = 2.0 ** -8
+    e0 = rtol * (abs(alpha0) * magnitude(A0, W0) +
+                 (abs(beta0) * np.abs(np.asarray(C0, dtype=np.float64)) if beta0 != 0.0 else 0.0))
+    absW1 = np.abs(bf16_bits_to_f64(W1))
+    absD0 = np.abs(np.asarray(D0, dtype=np.float64))
+    mag1 = abs(alpha1) * (absD0 @ absW1)
+    if beta1 != 0.0:
+        mag1 = mag1 + abs(beta1) * np.abs(np.asarray(C1, dtype=np.float64))
+    carried = abs(alpha1) * ((ACT_SLOPE[act0] * e0 * (1.0 + u) + u * absD0) @ absW1)
+    return rtol * mag1 + carried
+
+
+def within_b2b(D1, D1ref, bound):
+    """(every |D1 - D1ref| <= bound and D1 finite, worst err/bound)."""
+    D1 = np.asarray(D1, dtype=np.float64)
+    err = np.abs(D1 - D1ref)
+    ok = bool(np.all(np.isfinite(D1)) and np.all(err <= bound))
+    worst = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    return ok, worst

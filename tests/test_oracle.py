@@ -370,3 +370,123 @@ def test_bf16_rounding_pins():
     x = rng.standard_normal(10000) * 10.0 ** rng.integers(-6, 6, 10000)
     t = torch.tensor(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.array_equal(oracle.bf16_round(x.astype(np.float32).astype(np.float64)), t)
+
+
+# ---------------------------------------------------------------------------
+# Back-to-back GEMMs (BOLT summary, persistent kernel (GEMM/Conv) fusion)
+# ---------------------------------------------------------------------------
+def oracle_bits(rng, shape):
+    """uniform[-1, 1) values cut to bf16 bit patterns (any bf16 values serve)."""
+    v = rng.uniform(-1, 1, size=shape).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _int_bf16(rng, shape, lo=-3, hi=4):
+    """Small integers: exact in bf16, and every sum below stays exact in fp64."""
+    v = rng.integers(lo, hi, size=shape).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16), v.astype(np.float64)
+
+
+def test_b2b_brute_force_small():
+    """Pure-Python loops over the two formulas on tiny integer inputs: exact
+    for no activation and ReLU, within 1e-12 for GELU."""
+    import math
+    rng = np.random.default_rng(7)
+    M, K0, N0, N1 = 3, 5, 4, 2
+    A0, a0 = _int_bf16(rng, (M, K0))
+    W0, w0 = _int_bf16(rng, (K0, N0))
+    W1, w1 = _int_bf16(rng, (N0, N1))
+    C0 = rng.integers(-5, 6, size=(M, N0)).astype(np.float32)
+    C1 = rng.integers(-5, 6, size=(M, N1)).astype(np.float32)
+    al0, be0, al1, be1 = 2.0, -1.0, 0.5, 3.0
+
+    def act(x, a):
+        if a == oracle.ACT_RELU:
+            return max(x, 0.0)
+        if a == oracle.ACT_GELU:
+            return x * 0.5 * (1.0 + math.erf(x / math.sqrt(2.0)))
+        return x
+
+    for a in (oracle.ACT_NONE, oracle.ACT_RELU, oracle.ACT_GELU):
+        ref = np.zeros((M, N1))
+        for r in range(M):
+            d0 = []
+            for k in range(N0):
+                s = 0.0
+                for i in range(K0):
+                    s += a0[r, i] * w0[i, k]
+                d0.append(act(al0 * s + be0 * float(C0[r, k]), a))
+            for j in range(N1):
+                t = 0.0
+                for k in range(N0):
+                    t += d0[k] * w1[k, j]
+                ref[r, j] = al1 * t + be1 * float(C1[r, j])
+        D1, _ = oracle.b2b(A0, W0, C0, W1, C1, al0, be0, al1, be1, a)
+        if a == oracle.ACT_GELU:
+            assert np.allclose(D1, ref, rtol=0, atol=1e-12)
+        else:
+            assert np.array_equal(D1, ref)
+
+
+def test_b2b_associativity():
+    """No activation and beta0 = 0: D1 = alpha1 alpha0 A0 (W0 W1) + beta1 C1,
+    the product taken in the other order, exact on integer inputs; a transposed
+    or swapped operand fails it."""
+    rng = np.random.default_rng(11)
+    M, K0, N0, N1 = 9, 7, 6, 5
+    A0, a0 = _int_bf16(rng, (M, K0))
+    W0, w0 = _int_bf16(rng, (K0, N0))
+    W1, w1 = _int_bf16(rng, (N0, N1))
+    C1 = rng.integers(-5, 6, size=(M, N1)).astype(np.float32)
+    D1, _ = oracle.b2b(A0, W0, None, W1, C1, 3.0, 0.0, -2.0, 0.5)
+    assert np.array_equal(D1, -6.0 * (a0 @ (w0 @ w1)) + 0.5 * C1)
+
+
+def test_b2b_identity_second_gemm_is_epilogue_gemm():
+    """W1 = I, alpha1 = 1, beta1 = 0: D1 is the first GEMM with its activation."""
+    rng = np.random.default_rng(3)
+    M, K0, N0 = 17, 40, 24
+    A0 = oracle_bits(rng, (M, K0))
+    W0 = oracle_bits(rng, (K0, N0))
+    C0 = rng.uniform(-1, 1, size=(M, N0)).astype(np.float32)
+    eye = (np.eye(N0, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for a in (oracle.ACT_NONE, oracle.ACT_RELU, oracle.ACT_GELU):
+        D1, D0 = oracle.b2b(A0, W0, C0, eye, None, 1.5, 0.25, 1.0, 0.0, a)
+        assert np.array_equal(D1, oracle.epilogue(oracle.gemm(A0, W0, C0, 1.5, 0.25), a))
+        assert np.array_equal(D1, D0)
+
+
+def _fp32_b2b(A0, W0, C0, W1, C1, al0, be0, al1, be1, a, drop=None):
+    """The fused kernel's precision path in numpy: fp32 products, D0 rounded to
+    bf16 on chip.  `drop` plants one mistake."""
+    f = lambda b: oracle.bf16_bits_to_f64(b).astype(np.float32)
+    d0 = np.float32(al0) * (f(A0) @ f(W0))
+    if be0 != 0.0 and drop != "beta0":
+        d0 = d0 + np.float32(be0) * C0
+    if drop != "act":
+        d0 = oracle.epilogue(d0.astype(np.float64), a).astype(np.float32)
+    d0 = oracle.bf16_round(d0).astype(np.float32)
+    w1 = f(W1).T if drop == "transpose" else f(W1)
+    d1 = np.float32(al1) * (d0 @ w1)
+    if be1 != 0.0 and drop != "beta1":
+        d1 = d1 + np.float32(be1) * C1
+    return d1.astype(np.float64)
+
+
+def test_b2b_bound_admits_fused_precision_and_rejects_mistakes():
+    rng = np.random.default_rng(5)
+    M, K0, N0, N1 = 64, 96, 80, 80
+    A0 = oracle_bits(rng, (M, K0))
+    W0 = oracle_bits(rng, (K0, N0))
+    W1 = oracle_bits(rng, (N0, N1))
+    C0 = rng.uniform(-1, 1, size=(M, N0)).astype(np.float32)
+    C1 = rng.uniform(-1, 1, size=(M, N1)).astype(np.float32)
+    args = (A0, W0, C0, W1, C1, 1.25, 0.75, 0.5, 1.5)
+    for a in (oracle.ACT_NONE, oracle.ACT_RELU, oracle.ACT_GELU):
+        ref, d0 = oracle.b2b(*args, a)
+        bound = oracle.b2b_bound(*args, a, d0)
+        ok, worst = oracle.within_b2b(_fp32_b2b(*args, a), ref, bound)
+        assert ok, worst
+        for mistake in ("beta0", "beta1", "transpose") + (("act",) if a != oracle.ACT_NONE else ()):
+            ok, worst = oracle.within_b2b(_fp32_b2b(*args, a, drop=mistake), ref, bound)
+            assert not ok, (a, mistake, worst)
