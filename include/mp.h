@@ -351,6 +351,55 @@ mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double pe
 /* Static text for a status code. */
 const char* mp_status_string(mp_status s);
 
+/*
+ * Back-to-back GEMMs in one launch (BOLT summary, "Persistent kernel
+ * (GEMM/Conv) fusion"):
+ *     D0 = act0(alpha0 * A0 W0 + beta0 * C0)
+ *     D1 = alpha1 * D0 W1 + beta1 * C1
+ * A0 [M x K0], W0 [K0 x N0] and W1 [N0 x N1] are bf16, row-major; C0
+ * [M x N0], C1 and D1 [M x N1] are fp32, row-major; leading dimensions in
+ * elements.  D0 is never written to memory: each 128-row block of it stays
+ * in the producing CTA's shared memory, rounded to bf16 (the type of the
+ * second GEMM's operand), and feeds that CTA's second GEMM (the summary's
+ * threadblock residence).  That needs N0 <= 256.  act0 is MP_ACT_NONE,
+ * MP_ACT_RELU or MP_ACT_GELU (the epilogue variants' activations).  C0 is not
+ * read when beta0 == 0, nor C1 when beta1 == 0; C1 may be D1 (same pointer
+ * and ld).  Asynchronous on `stream`, like mp_gemm.
+ * M == 0 or N1 == 0 is a no-op; K0 == 0 gives D0 = act0(beta0 * C0); N0 == 0
+ * gives D1 = beta1 * C1.
+ * Errors: MP_ERR_INVALID_ARG (negative size, NULL operand that is read, ld
+ * too small, misaligned element, D1 overlapping an input other than an
+ * identical C1, unknown act0); MP_ERR_UNSUPPORTED (N0 > 256, host-only
+ * handle, or an A0, W0 or W1 whose base or row pitch is not 16-byte aligned
+ * and that does not fit the staging area, where such operands are copied
+ * with padded rows, as in mp_gemm); MP_ERR_CUDA (launch failure).
+ */
+mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, const void* A0, int64_t lda0,
+                      const void* W0, int64_t ldw0, const float* C0, int64_t ldc0, const void* W1, int64_t ldw1,
+                      const float* C1, int64_t ldc1, float* D1, int64_t ldd1, float alpha0, float beta0,
+                      float alpha1, float beta1, int32_t act0, mp_stream stream);
+
+/*
+ * How mp_gemm_b2b splits a problem (host only; any handle).  A work unit is
+ * 128 rows of M and `cpg` consecutive chunks of `bn1` columns of D1; the
+ * units of one row block each recompute that block of D0.  `cpg` minimises
+ * the cost model: waves of units x (first GEMM + cpg chunks).
+ */
+typedef struct {
+    int32_t n0p;          /* N0 rounded up to 64 */
+    int32_t bn1;          /* D1 columns per chunk */
+    int32_t chunks;       /* ceil(N1 / bn1) */
+    int32_t mblocks;      /* ceil(M / 128) */
+    int32_t cpg;          /* chunks per work unit */
+    int32_t units;        /* mblocks * ceil(chunks / cpg) */
+    int32_t grid;         /* CTAs launched: min(units, #SMs) */
+    int32_t num_stages;   /* shared-memory ring depth */
+    int32_t stage_bytes;  /* bytes per ring stage */
+    int32_t smem_bytes;   /* dynamic shared memory per CTA */
+    double cost_us;       /* model estimate */
+} mp_b2b_plan;
+mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
+
 #ifdef __cplusplus
 }
 #endif

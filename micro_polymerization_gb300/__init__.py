@@ -22,6 +22,7 @@ __all__ = [
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
+    "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan",
 ]
 
 MP_MAX_REGIONS = 4
@@ -78,6 +79,13 @@ class MpPlanInfo(ctypes.Structure):
         return [self.region[i] for i in range(self.num_regions)]
 
 
+class MpB2BPlan(ctypes.Structure):
+    _fields_ = [("n0p", ctypes.c_int32), ("bn1", ctypes.c_int32), ("chunks", ctypes.c_int32),
+                ("mblocks", ctypes.c_int32), ("cpg", ctypes.c_int32), ("units", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("num_stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("cost_us", ctypes.c_double)]
+
+
 class MPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -131,6 +139,9 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_set_plan_mode": ([_vp, _i32], ctypes.c_int),
                 "mp_gemm_ex": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                 _f, _f, _i32, _vp], ctypes.c_int),
+                "mp_gemm_b2b": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
+                                 _vp, _i64, _vp, _i64, _f, _f, _f, _f, _i32, _vp], ctypes.c_int),
+                "mp_plan_b2b": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpB2BPlan)], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -291,6 +302,44 @@ def mp_gemm_ex(h: Handle, A, B, C, D, alpha: float = 1.0, beta: float = 0.0, act
     st = library().mp_gemm_ex(h.ptr, M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"), c_ptr, ldc,
                               D.data_ptr(), _ld(D, "D"), float(alpha), float(beta), epi, _stream_ptr(stream))
     _check(st, "mp_gemm_ex")
+
+
+def mp_gemm_b2b(h: Handle, A0, W0, C0, W1, C1, D1, alpha0: float = 1.0, beta0: float = 0.0, alpha1: float = 1.0,
+                beta1: float = 0.0, act0: int = MP_ACT_NONE, stream=None) -> None:
+    """D1 = alpha1 * act0(alpha0*A0@W0 + beta0*C0) @ W1 + beta1*C1 in one launch,
+    the intermediate kept on chip (A0, W0, W1 bf16; C0, C1, D1 float32)."""
+    import torch
+    for name, t in (("A0", A0), ("W0", W0), ("W1", W1)):
+        if t.dtype != torch.bfloat16 or t.dim() != 2:
+            raise TypeError(f"{name} must be a 2-D bfloat16 tensor")
+    if D1.dtype != torch.float32 or D1.dim() != 2:
+        raise TypeError("D1 must be a 2-D float32 tensor")
+    M, K0 = A0.shape
+    N0 = W0.shape[1]
+    N1 = W1.shape[1]
+    if W0.shape[0] != K0 or W1.shape[0] != N0 or tuple(D1.shape) != (M, N1):
+        raise ValueError("shape mismatch")
+    c0, ldc0, c1, ldc1 = None, 0, None, 0
+    if beta0 != 0.0:
+        if C0 is None or C0.dtype != torch.float32 or tuple(C0.shape) != (M, N0):
+            raise ValueError("beta0 != 0 needs an fp32 C0 of shape (M, N0)")
+        c0, ldc0 = C0.data_ptr(), _ld(C0, "C0")
+    if beta1 != 0.0:
+        if C1 is None or C1.dtype != torch.float32 or tuple(C1.shape) != (M, N1):
+            raise ValueError("beta1 != 0 needs an fp32 C1 of shape (M, N1)")
+        c1, ldc1 = C1.data_ptr(), _ld(C1, "C1")
+    st = library().mp_gemm_b2b(h.ptr, M, N0, N1, K0, A0.data_ptr(), _ld(A0, "A0"), W0.data_ptr(), _ld(W0, "W0"),
+                               c0, ldc0, W1.data_ptr(), _ld(W1, "W1"), c1, ldc1, D1.data_ptr(), _ld(D1, "D1"),
+                               float(alpha0), float(beta0), float(alpha1), float(beta1), int(act0),
+                               _stream_ptr(stream))
+    _check(st, "mp_gemm_b2b")
+
+
+def mp_plan_b2b(h: Handle, M: int, N0: int, N1: int, K0: int) -> MpB2BPlan:
+    """How mp_gemm_b2b splits an (M, N0, N1, K0) problem (host only)."""
+    out = MpB2BPlan()
+    _check(library().mp_plan_b2b(h.ptr, M, N0, N1, K0, ctypes.byref(out)), "mp_plan_b2b")
+    return out
 
 
 def mp_enumerate_plans(h: Handle, M: int, N: int, K: int, capacity=None, batch: int = 1):

@@ -115,6 +115,35 @@ mp_status check_args(const mp::GemmArgs& a) {
     return MP_OK;
 }
 
+// Argument rules of mp_gemm_b2b (include/mp.h).
+mp_status check_b2b(const mp::B2BArgs& a) {
+    const int64_t M = a.M, N0 = a.N0, N1 = a.N1, K0 = a.K0;
+    if (M < 0 || N0 < 0 || N1 < 0 || K0 < 0) return MP_ERR_INVALID_ARG;
+    if (M >= kMaxDim || N0 >= kMaxDim || N1 >= kMaxDim || K0 >= kMaxDim) return MP_ERR_INVALID_ARG;
+    if (a.act0 < MP_ACT_NONE || a.act0 > MP_ACT_GELU) return MP_ERR_INVALID_ARG;
+    if (M == 0 || N1 == 0) return MP_OK;
+    auto one = [](int64_t n) { return n > 1 ? n : (int64_t)1; };
+    if (!a.D1 || a.ldd1 < one(N1) || ((uintptr_t)a.D1 & 3) != 0) return MP_ERR_INVALID_ARG;
+    const bool first = N0 > 0 && K0 > 0, read_c0 = N0 > 0 && a.beta0 != 0.0f, second = N0 > 0;
+    const bool read_c1 = a.beta1 != 0.0f;
+    if (first) {
+        if (!a.A0 || !a.W0 || a.lda0 < K0 || a.ldw0 < one(N0)) return MP_ERR_INVALID_ARG;
+        if (((uintptr_t)a.A0 & 1) != 0 || ((uintptr_t)a.W0 & 1) != 0) return MP_ERR_INVALID_ARG;
+    }
+    if (read_c0 && (!a.C0 || a.ldc0 < one(N0) || ((uintptr_t)a.C0 & 3) != 0)) return MP_ERR_INVALID_ARG;
+    if (second && (!a.W1 || a.ldw1 < one(N1) || ((uintptr_t)a.W1 & 1) != 0)) return MP_ERR_INVALID_ARG;
+    if (read_c1 && (!a.C1 || a.ldc1 < one(N1) || ((uintptr_t)a.C1 & 3) != 0)) return MP_ERR_INVALID_ARG;
+    const Span d = span_of(a.D1, M, N1, a.ldd1, 4, 1, 0);
+    if (first && (overlap(d, span_of(a.A0, M, K0, a.lda0, 2, 1, 0)) || overlap(d, span_of(a.W0, K0, N0, a.ldw0, 2, 1, 0))))
+        return MP_ERR_INVALID_ARG;
+    if (read_c0 && overlap(d, span_of(a.C0, M, N0, a.ldc0, 4, 1, 0))) return MP_ERR_INVALID_ARG;
+    if (second && overlap(d, span_of(a.W1, N0, N1, a.ldw1, 2, 1, 0))) return MP_ERR_INVALID_ARG;
+    if (read_c1 && !(a.C1 == a.D1 && a.ldc1 == a.ldd1) && overlap(d, span_of(a.C1, M, N1, a.ldc1, 4, 1, 0)))
+        return MP_ERR_INVALID_ARG;
+    if (N0 > 256) return MP_ERR_UNSUPPORTED;
+    return MP_OK;
+}
+
 mp_status run(mp_handle h, const mp::GemmArgs& a) {
     if (!h) return MP_ERR_INVALID_ARG;
     mp_status st = check_args(a);
@@ -270,6 +299,28 @@ mp_status mp_set_plan_mode(mp_handle h, int32_t mode) {
     h->plan_mode = mode;
     mp::clear_plan_cache(h);
     return MP_OK;
+}
+
+mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, const void* A0, int64_t lda0,
+                      const void* W0, int64_t ldw0, const float* C0, int64_t ldc0, const void* W1, int64_t ldw1,
+                      const float* C1, int64_t ldc1, float* D1, int64_t ldd1, float alpha0, float beta0,
+                      float alpha1, float beta1, int32_t act0, mp_stream stream) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    const mp::B2BArgs a{M, N0, N1, K0, A0, lda0, W0, ldw0, C0, ldc0, W1, ldw1, C1, ldc1, D1, ldd1,
+                        alpha0, beta0, alpha1, beta1, act0, stream};
+    mp_status st = check_b2b(a);
+    if (st != MP_OK) return st;
+    if (M == 0 || N1 == 0) return MP_OK;
+    if (h->host_only) return MP_ERR_UNSUPPORTED;
+    mp_b2b_plan plan;
+    st = mp::plan_b2b(h->hw, M, N0, N1, K0, &plan);
+    if (st != MP_OK) return st;
+    return mp::device_run_b2b(h, plan, a);
+}
+
+mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
+    if (!h || !out) return MP_ERR_INVALID_ARG;
+    return mp::plan_b2b(h->hw, M, N0, N1, K0, out);
 }
 
 mp_status mp_check(mp_handle h, mp_stream stream) {

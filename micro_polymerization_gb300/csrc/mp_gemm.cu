@@ -14,6 +14,7 @@
 
 #include "mp_internal.h"
 #include "mp_kernel.cuh"
+#include "mp_b2b.cuh"
 
 namespace mp {
 namespace dev {
@@ -96,7 +97,7 @@ struct DeviceState {
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
 bool set_kernel_smem() {
-    return set_poly_gemm_smem<0>() && set_poly_gemm_smem_act_f32() && set_poly_gemm_smem_bf16();
+    return set_poly_gemm_smem<0>() && set_poly_gemm_smem_act_f32() && set_poly_gemm_smem_bf16() && b2b::set_smem();
 }
 
 // Split-K on chip: for S = 2..16, the CTAs that clusters of S CTAs of the
@@ -670,6 +671,94 @@ void drop_unavailable_kernels(mp_handle h) {
     for (int32_t k = 0; k < h->num_kernels; k++)
         if (!h->kernels[k].pair) h->kernels[n++] = h->kernels[k];
     h->num_kernels = n;
+}
+
+// ---------------------------------------------------------------------------
+// Back-to-back GEMMs: tensor maps and the launch of k_b2b_gemm
+// ---------------------------------------------------------------------------
+// A bf16 matrix whose base or row pitch TMA cannot address is copied into
+// the staging area with rows padded to a multiple of 8 elements.
+mp_status stage_if_unaligned(DeviceState* s, cudaStream_t stream, const void*& P, int64_t& ld, int64_t rows,
+                             int64_t cols, int64_t& used) {
+    if (tma_ok(P, ld, 1, 0)) return MP_OK;
+    const int64_t ld2 = round_up(cols, 8);
+    const int64_t bytes = round_up(2 * rows * ld2, 256);
+    if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
+    const int blocks = (int)std::min<int64_t>(cdiv(rows * (ld2 / 8), 256), 4096);
+    dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(P), ld, 0, dst, ld2, 0,
+                                                   (int)rows, (int)cols, 1);
+    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+    P = dst;
+    ld = ld2;
+    used += bytes;
+    return MP_OK;
+}
+
+mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    DeviceGuard g(s->device);
+    b2b::Params p;
+    std::memset(&p, 0, sizeof(p));
+    const int64_t M = a.M, N0 = a.N0, N1 = a.N1, K0 = a.N0 > 0 ? a.K0 : 0;
+    cudaStream_t stream = (cudaStream_t)a.stream;
+    const void *A0 = a.A0, *W0 = a.W0, *W1 = a.W1;
+    int64_t lda0 = a.lda0, ldw0 = a.ldw0, ldw1 = a.ldw1, used = 0;
+    mp_status st = MP_OK;
+    if (K0 > 0) {
+        if ((st = stage_if_unaligned(s, stream, A0, lda0, M, K0, used)) != MP_OK) return st;
+        if ((st = stage_if_unaligned(s, stream, W0, ldw0, K0, N0, used)) != MP_OK) return st;
+        if (!encode_3d(s, &p.tmA0, A0, K0, M, 1, lda0 * 2, round_up(M * lda0 * 2, 16), 64, 128) ||
+            !encode_3d(s, &p.tmW0, W0, N0, K0, 1, ldw0 * 2, round_up(K0 * ldw0 * 2, 16), 64, 64))
+            return MP_ERR_CUDA;
+    }
+    if (N0 > 0) {
+        if ((st = stage_if_unaligned(s, stream, W1, ldw1, N0, N1, used)) != MP_OK) return st;
+        if (!encode_3d(s, &p.tmW1, W1, N1, N0, 1, ldw1 * 2, round_up(N0 * ldw1 * 2, 16), 64, 64))
+            return MP_ERR_CUDA;
+    }
+    p.tma_d = (((uintptr_t)a.D1 & 15u) == 0 && (a.ldd1 * 4) % 16 == 0) ? 1 : 0;
+    if (p.tma_d && !encode_3d_f32(s, &p.tmD1, a.D1, N1, M, 1, a.ldd1 * 4, round_up(M * a.ldd1 * 4, 16), 32, 32))
+        return MP_ERR_CUDA;
+    p.C0 = a.C0;
+    p.C1 = a.C1;
+    p.D1 = a.D1;
+    p.ldc0 = a.ldc0;
+    p.ldc1 = a.ldc1;
+    p.ldd1 = a.ldd1;
+    p.M = (int)M;
+    p.N0 = (int)N0;
+    p.N1 = (int)N1;
+    p.K0 = (int)K0;
+    p.n0p = pl.n0p;
+    p.bn1 = pl.bn1;
+    p.chunks = pl.chunks;
+    p.mblocks = pl.mblocks;
+    p.cpg = pl.cpg;
+    p.units = pl.units;
+    p.num_stages = pl.num_stages;
+    p.stage_bytes = pl.stage_bytes;
+    p.alpha0 = a.alpha0;
+    p.beta0 = a.beta0;
+    p.alpha1 = a.alpha1;
+    p.beta1 = a.beta1;
+    p.act0 = a.act0;
+    p.vec_c0 = (a.C0 && ((uintptr_t)a.C0 & 15u) == 0 && a.ldc0 % 4 == 0) ? 1 : 0;
+    p.vec_c1 = (a.C1 && ((uintptr_t)a.C1 & 15u) == 0 && a.ldc1 % 4 == 0) ? 1 : 0;
+    p.err = s->err;
+    p.wait_limit_ns = s->wait_limit_ns;
+    if (s->log)
+        std::fprintf(stderr, "[mp] b2b M=%lld N0=%lld N1=%lld K0=%lld bn1=%d cpg=%d units=%d grid=%d stages=%d\n",
+                     (long long)M, (long long)N0, (long long)N1, (long long)K0, pl.bn1, pl.cpg, pl.units, pl.grid,
+                     pl.num_stages);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(b2b::kThreads);
+    cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+    cfg.stream = stream;
+    if (b2b::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
+    return MP_OK;
 }
 
 }  // namespace mp

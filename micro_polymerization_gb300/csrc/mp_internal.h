@@ -105,4 +105,21 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
 // Argument rules of mp_gemm (mp_api.cpp).
 mp_status validate_args(const GemmArgs& a);
 
+// Back-to-back GEMMs (mp_gemm_b2b): planner (mp_planner.cpp) and launch
+// (mp_gemm.cu).
+struct B2BArgs {
+    int64_t M, N0, N1, K0;
+    const void* A0; int64_t lda0;
+    const void* W0; int64_t ldw0;
+    const float* C0; int64_t ldc0;
+    const void* W1; int64_t ldw1;
+    const float* C1; int64_t ldc1;
+    float* D1; int64_t ldd1;
+    float alpha0, beta0, alpha1, beta1;
+    int32_t act0;
+    void* stream;
+};
+mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
+mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& plan, const B2BArgs& a);
+
 }  // namespace mp

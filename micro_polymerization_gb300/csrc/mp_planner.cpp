@@ -29,6 +29,7 @@
 #include <cstring>
 
 #include "mp_internal.h"
+#include "mp_b2b.cuh"
 
 namespace mp {
 namespace {
@@ -593,6 +594,61 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
         d.fixed_us = 0.6 + (g.swap ? 2.0 : 1.0) * epi_bytes / (hbm_pe * 1e3) + (g.pair ? kPairFixedUs : 0.0);
     }
     *n = c;
+}
+
+// ---------------------------------------------------------------------------
+// Back-to-back GEMMs (BOLT summary, persistent kernel (GEMM/Conv) fusion)
+// ---------------------------------------------------------------------------
+// Work unit: 128 rows x `cpg` chunks of D1.  Each unit runs the first GEMM
+// for its rows (nk0 K steps of a 128 x n0p tile), then cpg chunks of the
+// second (nk1 = n0p / 64 K steps of a 128 x bn1 tile, each followed by its
+// fp32 epilogue; a chunk's epilogue overlaps the next chunk's MMAs).  Fewer
+// chunks per unit give more units to spread over the SMs, at the price of
+// recomputing the block of D0 once per unit.
+mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
+    if (!out || M < 0 || N0 < 0 || N1 < 0 || K0 < 0) return MP_ERR_INVALID_ARG;
+    if (N0 > 256) return MP_ERR_UNSUPPORTED;
+    if (M >= ((int64_t)1 << 31) || N1 >= ((int64_t)1 << 31) || K0 >= ((int64_t)1 << 31)) return MP_ERR_INVALID_ARG;
+    mp_b2b_plan p;
+    std::memset(&p, 0, sizeof p);
+    const int64_t k0 = N0 > 0 ? K0 : 0;  // no first GEMM without columns of D0
+    p.n0p = (int32_t)(((N0 + 63) / 64) * 64);
+    p.bn1 = (int32_t)std::min<int64_t>(256, std::max<int64_t>(64, ((N1 + 63) / 64) * 64));
+    p.chunks = (int32_t)((N1 + p.bn1 - 1) / p.bn1);
+    p.mblocks = (int32_t)((M + 127) / 128);
+    const int nk0 = (int)((k0 + 63) / 64), nk1 = p.n0p / 64;
+    p.stage_bytes = std::max(nk0 > 0 ? 16384 + p.n0p * 128 : 0, p.bn1 * 128);
+    const int room = b2b::kSmemLimit - p.n0p * 256 - 4 * b2b::kEpiSlabBytes - 2048;
+    p.num_stages = std::min(b2b::kMaxStages, room / p.stage_bytes);
+    if (p.num_stages < 2) return MP_ERR_PLAN;
+    p.smem_bytes = b2b::smem_bytes(p.num_stages, p.stage_bytes, p.n0p);
+
+    const int sms = std::max(1, hw.num_pe);
+    const double mma_pe = hw.mma_tflops > 0 ? hw.mma_tflops / sms : 13.0;  // TFLOP/s per SM
+    auto step_us = [&](int n) { return std::max(kStepFloorUs, 2.0 * 128 * n * 64 / (mma_pe * 1e6)); };
+    const double t0 = nk0 * (p.n0p > 0 ? step_us(p.n0p) : 0.0) + 0.5;  // + the D0 hand-over
+    const double mma1 = nk1 * step_us(p.bn1);
+    double best = 1e300;
+    for (int cpg = 1; cpg <= std::max(1, p.chunks); cpg++) {
+        const int64_t groups = (p.chunks + cpg - 1) / cpg;
+        if (cpg > 1 && (p.chunks + cpg - 2) / (cpg - 1) == groups) continue;  // same grouping as cpg - 1
+        const int64_t units = (int64_t)p.mblocks * std::max<int64_t>(1, groups);
+        const int64_t active = std::min<int64_t>(units, sms);
+        // A chunk's fp32 output at the active SMs' share of HBM bandwidth.
+        const double hbm_pe = (hw.hbm_gbs > 0 ? hw.hbm_gbs : 6700.0) / (double)active;
+        const double epi = 4.0 * 128 * p.bn1 / (hbm_pe * 1e3);
+        const double waves = (double)((units + sms - 1) / sms);
+        const double cost = waves * (t0 + cpg * std::max(mma1, epi) + epi) + 2.0;
+        if (cost < best * (1.0 - 1e-9)) {
+            best = cost;
+            p.cpg = cpg;
+            p.units = (int32_t)units;
+        }
+    }
+    p.grid = (int32_t)std::min<int64_t>(p.units, sms);
+    p.cost_us = best;
+    *out = p;
+    return MP_OK;
 }
 
 }  // namespace mp

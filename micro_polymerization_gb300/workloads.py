@@ -79,6 +79,50 @@ def integer_operands(M: int, N: int, K: int, seed: int, lo: int = -4, hi: int = 
     return A, B, C
 
 
+@dataclasses.dataclass(frozen=True)
+class B2B:
+    """Back-to-back GEMMs: D1[M,N1] = alpha1 * act0(alpha0 * A0[M,K0] W0[K0,N0]
+    + beta0 * C0[M,N0]) W1[N0,N1] + beta1 * C1[M,N1]."""
+    M: int
+    N0: int
+    N1: int
+    K0: int
+    alpha0: float = 1.0
+    beta0: float = 0.0
+    alpha1: float = 1.0
+    beta1: float = 0.0
+    act0: int = 0
+    seed: int = 0
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N0 * self.K0 + 2 * self.M * self.N1 * self.N0
+
+    def min_bytes(self) -> int:
+        """A0, W0, W1 (and C0, C1 when read) once, D1 written once; D0 never
+        leaves the chip."""
+        b = 2 * self.M * self.K0 + 2 * self.K0 * self.N0 + 2 * self.N0 * self.N1 + 4 * self.M * self.N1
+        if self.beta0 != 0.0:
+            b += 4 * self.M * self.N0
+        if self.beta1 != 0.0:
+            b += 4 * self.M * self.N1
+        return b
+
+
+def make_b2b_operands(b: B2B, device="cpu"):
+    """(A0, W0, W1) bf16 and (C0, C1) fp32 or None, uniform [-1, 1), seeded by b.seed."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(b.seed))
+    A0 = _uniform((b.M, b.K0), gen, dev).to(torch.bfloat16)
+    W0 = _uniform((b.K0, b.N0), gen, dev).to(torch.bfloat16)
+    W1 = _uniform((b.N0, b.N1), gen, dev).to(torch.bfloat16)
+    gen.manual_seed(int(b.seed) + 1)
+    C0 = _uniform((b.M, b.N0), gen, dev) if b.beta0 != 0.0 else None
+    C1 = _uniform((b.M, b.N1), gen, dev) if b.beta1 != 0.0 else None
+    return A0, W0, C0, W1, C1
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a CPU tensor as numpy uint16 (no conversion)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -156,6 +200,32 @@ def stress(count: int = 1000) -> List[Gemm]:
            for i, (m, n, k) in enumerate(dims)]
     out.append(Gemm(4096, 4096, 4096, alpha=1.5, beta=0.5, seed=1000 + 500 + 7 * count))
     return out
+
+
+def b2b_adapter(count: int = 64) -> List[B2B]:
+    """Bottleneck pairs at dynamic sequence length: M = 8 * seq (seq uniform
+    in [1, 512], as in the dynamic-sequence workload), 768 -> 256 (ReLU) ->
+    768.  N0 = 256 is the widest D0 one CTA keeps on chip."""
+    rng = np.random.default_rng(1000 + 600)
+    return [B2B(8 * int(rng.integers(1, 513)), 256, 768, 768, act0=1, seed=1000 + 600 + 7 * i)
+            for i in range(count)]
+
+
+def b2b_1x1(count: int = 64) -> List[B2B]:
+    """Two consecutive 1x1 convolutions as GEMMs at dynamic resolution (the
+    BOLT summary's deepening with 1x1 convolutions): M = batch * H * W with
+    batch in [1, 32] and H = W in {7, 14, 28, 56}, channels 256 -> 64 (ReLU)
+    -> 256."""
+    rng = np.random.default_rng(1000 + 700)
+    out = []
+    for i in range(count):
+        batch = int(rng.integers(1, 33))
+        hw = int(rng.choice([7, 14, 28, 56]))
+        out.append(B2B(batch * hw * hw, 64, 256, 256, act0=1, seed=1000 + 700 + 7 * i))
+    return out
+
+
+B2B_WORKLOADS = {"b2b_adapter": b2b_adapter, "b2b_1x1": b2b_1x1}
 
 
 WORKLOADS = {

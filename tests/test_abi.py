@@ -142,3 +142,66 @@ def test_mp_init_without_gpu_fails_cleanly():
     out = ctypes.c_void_p()
     st = mp.library().mp_init(ctypes.byref(out), 0, None)
     assert st in (mp.MP_ERR_UNSUPPORTED, mp.MP_ERR_CUDA) and not out.value
+
+
+def test_b2b_argument_checks():
+    """mp_gemm_b2b validates sizes, pointers, leading dimensions, overlaps and
+    act0 before planning; valid calls on a planning-only handle report
+    MP_ERR_UNSUPPORTED."""
+    lib = mp.library()
+    h = _host()
+    A0, W0, C0, W1, C1, D1 = 0x10000, 0x20000000, 0x30000000, 0x40000000, 0x50000000, 0x60000000
+    M, N0, N1, K0 = 100, 64, 96, 80
+
+    def g(**kw):
+        v = dict(M=M, N0=N0, N1=N1, K0=K0, A0=A0, lda0=K0, W0=W0, ldw0=N0, C0=C0, ldc0=N0, W1=W1, ldw1=N1,
+                 C1=C1, ldc1=N1, D1=D1, ldd1=N1, a0=1.0, b0=0.5, a1=1.0, b1=0.5, act=0)
+        v.update(kw)
+        return lib.mp_gemm_b2b(h.ptr, v["M"], v["N0"], v["N1"], v["K0"], v["A0"], v["lda0"], v["W0"], v["ldw0"],
+                               v["C0"], v["ldc0"], v["W1"], v["ldw1"], v["C1"], v["ldc1"], v["D1"], v["ldd1"],
+                               v["a0"], v["b0"], v["a1"], v["b1"], v["act"], None)
+
+    assert g() == mp.MP_ERR_UNSUPPORTED  # valid; no device
+    assert g(act=2) == mp.MP_ERR_UNSUPPORTED
+    assert g(M=0) == mp.MP_OK and g(N1=0) == mp.MP_OK  # no-ops
+    for bad in (dict(M=-1), dict(K0=-1), dict(act=3), dict(act=-1), dict(D1=None), dict(ldd1=N1 - 1),
+                dict(lda0=K0 - 1), dict(ldw0=N0 - 1), dict(ldw1=N1 - 1), dict(ldc0=N0 - 1), dict(ldc1=N1 - 1),
+                dict(A0=None), dict(W1=None), dict(C0=None), dict(C1=None), dict(D1=D1 + 2), dict(A0=A0 + 1),
+                dict(D1=C0), dict(D1=W1), dict(D1=A0), dict(C1=D1 + 4)):
+        assert g(**bad) == mp.MP_ERR_INVALID_ARG, bad
+    # C0 / C1 are not read when their beta is 0; W0, A0 not needed when K0 = 0.
+    assert g(b0=0.0, C0=None, ldc0=0) == mp.MP_ERR_UNSUPPORTED
+    assert g(b1=0.0, C1=None, ldc1=0) == mp.MP_ERR_UNSUPPORTED
+    assert g(K0=0, A0=None, W0=None) == mp.MP_ERR_UNSUPPORTED
+    # In place: C1 is D1 (same pointer and ld).
+    assert g(C1=D1) == mp.MP_ERR_UNSUPPORTED
+    # N0 past one accumulator: not supported.
+    assert g(N0=257, ldw0=257, ldc0=257) == mp.MP_ERR_UNSUPPORTED
+    h.close()
+
+
+def test_b2b_plan_rules():
+    h = _host()
+    for M, N0, N1, K0 in [(1, 1, 1, 1), (1000, 256, 768, 768), (128 * 400, 64, 256, 256), (256, 128, 4096, 64),
+                          (300, 96, 520, 0), (77, 0, 300, 50), (5000, 200, 100, 3000)]:
+        p = mp.mp_plan_b2b(h, M, N0, N1, K0)
+        assert p.n0p == -(-N0 // 64) * 64 and p.n0p <= 256
+        assert p.bn1 % 64 == 0 and 64 <= p.bn1 <= 256 and p.chunks * p.bn1 >= N1 > (p.chunks - 1) * p.bn1
+        assert p.mblocks == -(-M // 128)
+        groups = -(-p.chunks // p.cpg)
+        assert 1 <= p.cpg <= p.chunks and p.units == p.mblocks * groups
+        assert p.grid == min(p.units, 148)
+        assert 2 <= p.num_stages <= 8 and p.smem_bytes <= 232448
+        ring_need = max((16384 + p.n0p * 128) if (K0 > 0 and N0 > 0) else 0, p.bn1 * 128)
+        assert p.stage_bytes == ring_need and p.stage_bytes % 8192 == 0
+        assert p.cost_us > 0
+    # Many row blocks: every unit takes all chunks (no recomputation of D0).
+    assert mp.mp_plan_b2b(h, 128 * 1000, 64, 1024, 256).cpg == 4
+    # One row block, many chunks, a cheap first GEMM: chunks spread over SMs.
+    p = mp.mp_plan_b2b(h, 128, 128, 8192, 64)
+    assert p.cpg < p.chunks and p.units > 1
+    with pytest.raises(mp.MPError):
+        mp.mp_plan_b2b(h, 10, 257, 10, 10)
+    with pytest.raises(mp.MPError):
+        mp.mp_plan_b2b(h, -1, 64, 10, 10)
+    h.close()
