@@ -433,6 +433,8 @@ def l2_note(gs):
 
 
 def workload_desc(name):
+    if name.startswith("b2bshape:"):
+        return f"one fused back-to-back GEMM (M,N0,N1,K0[,act0]) = ({name[len('b2bshape:'):]})"
     if name.startswith("shape:"):
         return f"single GEMM (M,N,K[,beta]) = ({name[len('shape:'):]}), alpha=1"
     return {
@@ -443,6 +445,10 @@ def workload_desc(name):
         "merged_qkv": "A x concat(Wq,Wk,Wv), K=1024, N=3072, M uniform [1,4096], 64 draws",
         "merged_batched": "batched 12 x (seq,seq,64), seq uniform [16,512], 64 draws",
         "stress": "1000 log-uniform shapes in [1,16384]^3 plus 4096^3, alpha=1.5, beta=0.5",
+        "b2b_adapter": "fused back-to-back GEMMs, 64 problems, M = 8*seq (seq uniform [1,512]), "
+                       "768 -> 256 (ReLU) -> 768, bf16 A0,W0,W1, beta0=beta1=0",
+        "b2b_1x1": "fused back-to-back GEMMs as two 1x1 convolutions, 64 problems, M = batch*H*W "
+                   "(batch [1,32], H=W in {7,14,28,56}), 256 -> 64 (ReLU) -> 256",
     }[name]
 
 
@@ -526,19 +532,237 @@ def cpu_baseline(args, gs, budget_s=None, act=0, out_bf16=False):
                       f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)"}
 
 
+def is_b2b(name: str) -> bool:
+    from micro_polymerization_gb300 import workloads as wl
+    return name in wl.B2B_WORKLOADS or name.startswith("b2bshape:")
+
+
+def b2b_workload(name: str):
+    """A named fused-pair workload, or ``b2bshape:M,N0,N1,K0[,act0]`` for one
+    problem (alpha = 1, beta = 0), for profiling one shape."""
+    from micro_polymerization_gb300 import workloads as wl
+    if name.startswith("b2bshape:"):
+        v = [int(x) for x in name[len("b2bshape:"):].split(",")]
+        return [wl.B2B(v[0], v[1], v[2], v[3], act0=v[4] if len(v) > 4 else 0, seed=78)]
+    return wl.B2B_WORKLOADS[name]()
+
+
+def cpu_baseline_b2b(args, bs, budget_s=None):
+    """The oracle's fused-pair evaluation on the first min(M, 256) rows of each
+    problem (first GEMM in C over OpenMP rows, second a numpy fp64 product)."""
+    import oracle
+    from micro_polymerization_gb300 import workloads as wl
+    budget_s = budget_s or args.cpu_seconds
+    flops = t_total = 0.0
+    done = 0
+    for b in bs:
+        A0, W0, C0, W1, C1 = wl.make_b2b_operands(b)
+        rows = min(b.M, 256)
+        a0, w0, w1 = wl.bf16_bits(A0[:rows]), wl.bf16_bits(W0), wl.bf16_bits(W1)
+        c0 = C0[:rows].numpy() if C0 is not None else None
+        c1 = C1[:rows].numpy() if C1 is not None else None
+        t0 = time.perf_counter()
+        oracle.b2b(a0, w0, c0, w1, c1, b.alpha0, b.beta0, b.alpha1, b.beta1, b.act0)
+        t_total += time.perf_counter() - t0
+        flops += 2.0 * rows * (b.N0 * b.K0 + b.N1 * b.N0)
+        done += 1
+        if t_total >= budget_s:
+            break
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(oracle.max_threads()),
+            "kind": "oracle",
+            "sample": f"first min(M, 256) rows of each of the first {done} problems of the workload "
+                      f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64)"}
+
+
+def run_b2b(args):
+    """Fused back-to-back GEMMs (mp_gemm_b2b), one call per problem, back to
+    back on one stream; the unfused pair (mp_gemm_ex writing a bf16 D0 with
+    the activation, then mp_gemm) is timed beside it on the same operands."""
+    import torch
+    import micro_polymerization_gb300 as mp
+    from micro_polymerization_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    h = mp.mp_init(local)
+    lib = mp.library()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    bs = b2b_workload(args.workload)
+    if rank > 0:
+        import dataclasses
+        bs = [dataclasses.replace(b, seed=b.seed + 1_000_003 * rank) for b in bs]
+    ops = []
+    for b in bs:
+        t = [x.to(dev) if x is not None else None for x in wl.make_b2b_operands(b)]
+        D1 = torch.empty(b.M, b.N1, device=dev)
+        D0 = torch.empty(b.M, b.N0, device=dev, dtype=torch.bfloat16)
+        ops.append((b, *t, D1, D0))
+    torch.cuda.synchronize()
+    ptr = lambda x: x.data_ptr() if x is not None else None
+    fused, unfused = [], []
+    for b, A0, W0, C0, W1, C1, D1, D0 in ops:
+        fused.append((lib.mp_gemm_b2b, (h.ptr, b.M, b.N0, b.N1, b.K0, A0.data_ptr(), b.K0, W0.data_ptr(), b.N0,
+                                        ptr(C0), b.N0, W1.data_ptr(), b.N1, ptr(C1), b.N1, D1.data_ptr(), b.N1,
+                                        b.alpha0, b.beta0, b.alpha1, b.beta1, b.act0, sp)))
+        unfused.append((lib.mp_gemm_ex, (h.ptr, b.M, b.N0, b.K0, A0.data_ptr(), b.K0, W0.data_ptr(), b.N0, ptr(C0),
+                                         b.N0, D0.data_ptr(), b.N0, b.alpha0, b.beta0,
+                                         b.act0 | mp.MP_EPI_OUT_BF16, sp)))
+        unfused.append((lib.mp_gemm, (h.ptr, b.M, b.N1, b.N0, D0.data_ptr(), b.N0, W1.data_ptr(), b.N1, ptr(C1),
+                                      b.N1, D1.data_ptr(), b.N1, b.alpha1, b.beta1, sp)))
+
+    def step(calls, evs=None):
+        for i, (fn, a) in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            st = fn(*a)
+            if st != 0:
+                raise mp.MPError(st, fn.__name__)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    def timed(calls, steps):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(calls)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+
+    for _ in range(args.warmup):
+        step(fused)
+        step(unfused)
+    torch.cuda.synchronize()
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    n = len(fused)
+    per_launch = np.zeros(n)
+    reps = max(1, min(args.steps, 20))
+    for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        step(fused, evs)
+        torch.cuda.synchronize()
+        per_launch += np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+    per_launch /= reps
+    with ClockSampler(local) as clocks:
+        ms_step = timed(fused, args.steps)
+    ms_unfused = timed(unfused, args.steps)
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set in the timed region")
+    flops_step = sum(b.flops for b in bs)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    t_flop = np.array([b.flops / (peaks["bf16_tflops"] * 1e6) for b in bs])
+    t_mem = np.array([b.min_bytes() / (peaks["hbm_gbs"] * 1e3) for b in bs])
+    troof = np.maximum(t_flop, t_mem)
+    if t_flop.sum() >= t_mem.sum():
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+        achieved = flops_step / (per_launch.sum() * 1e-6) / 1e12
+    else:
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
+        achieved = sum(b.min_bytes() for b in bs) / (per_launch.sum() * 1e-6) / 1e9
+    flops = np.array([b.flops for b in bs], dtype=np.float64)
+    flop_weighted = float(np.sum(flops * troof / per_launch) / np.sum(flops))
+
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for b, A0, W0, C0, W1, C1, D1, D0 in ops:
+            hx = []
+            for x in (A0, W0, C0, W1, C1, D1):
+                if x is None:
+                    hx.append(None)
+                    continue
+                y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                y.copy_(x)
+                hx.append(y)
+            host.append(hx)
+        h2d = sum(x.numel() * x.element_size() for hx in host for x in hx[:5] if x is not None)
+        d2h = sum(hx[5].numel() * hx[5].element_size() for hx in host)
+
+        def e2e_step():
+            for (b, A0, W0, C0, W1, C1, D1, D0), hx, (fn, a) in zip(ops, host, fused):
+                for dst, src in zip((A0, W0, C0, W1, C1), hx[:5]):
+                    if dst is not None:
+                        dst.copy_(src, non_blocking=True)
+                st = fn(*a)
+                if st != 0:
+                    raise mp.MPError(st, "mp_gemm_b2b")
+                hx[5].copy_(D1, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": round(flops_step * world * e2e_steps / t_e2e / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    cpu = cpu_baseline_b2b(args, bs) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank == 0:
+        b0 = bs[0]
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(args.workload), "problems_per_step": len(bs),
+                       "shape": {"N0": b0.N0, "N1": b0.N1, "K0": b0.K0, "act0": b0.act0},
+                       "flops_per_step": int(flops_step),
+                       "l2": "inputs larger than L2" if sum(b.min_bytes() for b in bs) > L2_BYTES else
+                             "inputs smaller than L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "unfused": {"ms_per_step": round(ms_unfused, 4),
+                        "value": round(flops_step * world / (ms_unfused * 1e-3) / 1e12, 3),
+                        "calls": "mp_gemm_ex (bf16 D0, activation) + mp_gemm",
+                        "fused_speedup": round(ms_unfused / ms_step, 3)},
+            "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
+                                   "sum_troof_over_sum_t": round(float(troof.sum() / per_launch.sum()), 4),
+                                   "peaks": peak_src},
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": None, "launches": n,
+                         "kernel": "k_b2b_gemm", "peak_source": peak_src},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n * args.steps,
+            "clocks": clocks.summary(), "impl": "mp",
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    gs = rank_workload(args.workload, 0)
+    from micro_polymerization_gb300 import workloads as wl
     import oracle  # noqa: F401
-    for _ in range(args.warmup):
-        cpu_baseline(args, gs[:1], budget_s=0.01)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    act, out_bf16 = EPILOGUES[args.epilogue]
-    vals = []
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(args, gs, budget_s=per_step, act=act, out_bf16=out_bf16))
+    if is_b2b(args.workload):
+        bs = b2b_workload(args.workload)
+        for _ in range(args.warmup):
+            cpu_baseline_b2b(args, bs[:1], budget_s=0.01)
+        vals = [cpu_baseline_b2b(args, bs, budget_s=per_step) for _ in range(args.steps)]
+    else:
+        gs = rank_workload(args.workload, 0)
+        for _ in range(args.warmup):
+            cpu_baseline(args, gs[:1], budget_s=0.01)
+        act, out_bf16 = EPILOGUES[args.epilogue]
+        vals = [cpu_baseline(args, gs, budget_s=per_step, act=act, out_bf16=out_bf16) for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     line = {
         "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -575,6 +799,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif is_b2b(args.workload):
+        run_b2b(args)
     else:
         run_mp(args)
 

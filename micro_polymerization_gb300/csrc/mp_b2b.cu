@@ -34,120 +34,173 @@ using namespace mp::dev;
 
 constexpr int kErrWaitD0 = 7;  // the MMA issuer gave up waiting for D0 in shared memory
 
-// Columns [c, c + 32) of this lane's row of the D0 block: alpha0*acc +
-// beta0*C0, the activation, bf16, into the K-major swizzled operand.
+// 64 consecutive accumulator columns of this thread's TMEM lane, one load
+// and one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]),
+                   "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]),
+                   "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]),
+                   "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]),
+                   "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+                 :
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Columns [c, c + 64) of this lane's row of the D0 block (one swizzle atom):
+// alpha0*acc + beta0*C0, the activation, bf16, into the K-major operand.
 template <int ACT>
-__device__ __forceinline__ void d0_piece(const Params& p, uint32_t t, bool has_k, int row, int r, int c,
-                                         uint8_t* d0g) {
-    float v[32];
+__device__ __forceinline__ void d0_atom(const Params& p, uint32_t t, bool has_k, int row, int r, int c,
+                                        uint8_t* d0g) {
+    float v[64];
     if (has_k) {
-        tmem_ld32(t + (uint32_t)c, v);
+        tmem_ld64(t + (uint32_t)c, v);
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; j++) v[j] = 0.0f;
+        for (int j = 0; j < 64; j++) v[j] = 0.0f;
     }
     const float a = p.alpha0, b = p.beta0;
     const bool row_ok = row < p.M;
-    float cv[32];
-    if (b != 0.0f) {
-        const float* cr = p.C0 + (long long)row * p.ldc0 + c;
-        if (row_ok && p.vec_c0 && c + 32 <= p.N0) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
-                cv[4 * j] = x.x;
-                cv[4 * j + 1] = x.y;
-                cv[4 * j + 2] = x.z;
-                cv[4 * j + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; j++) cv[j] = (row_ok && c + j < p.N0) ? __ldg(cr + j) : 0.0f;
-        }
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int j = 0; j < 16; j++) {
-        float x0 = a * v[2 * j], x1 = a * v[2 * j + 1];
-        if (b != 0.0f) {
-            x0 = fmaf(b, cv[2 * j], x0);
-            x1 = fmaf(b, cv[2 * j + 1], x1);
-        }
-        const __nv_bfloat162 h = __floats2bfloat162_rn(act_fn<ACT>(x0), act_fn<ACT>(x1));
-        pk[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
     uint8_t* line = d0g + (c >> 6) * 16384 + r * 128;
-    const int ch0 = (c & 63) >> 3;  // 0 or 4: the first 16-byte chunk of these 32 columns
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-        *reinterpret_cast<uint4*>(line + (((ch0 + i) ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    for (int h = 0; h < 2; h++) {  // 32 columns = four 16-byte chunks of bf16 at a time
+        float cv[32];
+        if (b != 0.0f) {
+            const int cc = c + 32 * h;
+            const float* cr = p.C0 + (long long)row * p.ldc0 + cc;
+            if (row_ok && p.vec_c0 && cc + 32 <= p.N0) {
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
+                    cv[4 * j] = x.x;
+                    cv[4 * j + 1] = x.y;
+                    cv[4 * j + 2] = x.z;
+                    cv[4 * j + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; j++) cv[j] = (row_ok && cc + j < p.N0) ? __ldg(cr + j) : 0.0f;
+            }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            float x0 = a * v[32 * h + 2 * j], x1 = a * v[32 * h + 2 * j + 1];
+            if (b != 0.0f) {
+                x0 = fmaf(b, cv[2 * j], x0);
+                x1 = fmaf(b, cv[2 * j + 1], x1);
+            }
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(act_fn<ACT>(x0), act_fn<ACT>(x1));
+            pk[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            *reinterpret_cast<uint4*>(line + (((4 * h + i) ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
 }
 
 template <int ACT>
 __device__ __forceinline__ void d0_block(const Params& p, uint32_t t, bool has_k, int row, int r, uint8_t* d0g) {
-    for (int c = 0; c < p.n0p; c += 32) d0_piece<ACT>(p, t, has_k, row, r, c, d0g);
+    for (int c = 0; c < p.n0p; c += 64) d0_atom<ACT>(p, t, has_k, row, r, c, d0g);
 }
 
-// One chunk of D1 for this warp's 32 rows: alpha1*acc + beta1*C1, 32 columns
-// at a time, through the warp's slab and a bulk tensor store (rows and
-// columns past the edge are clipped by the store), or with plain stores when
-// D1's rows are not 16-byte aligned.
+// One chunk of D1 for this warp's 32 rows: alpha1*acc + beta1*C1, 64 columns
+// of TMEM at a time, stored as 32 x 16 boxes through the warp's two
+// slabs in turn (bulk tensor stores clip rows and columns past the edge; a
+// slab is rewritten once its previous store has read it, while the other
+// slab's store may still be in flight), or with plain stores when D1's rows
+// are not 16-byte aligned.  `slab_seq` counts this warp's stores.
 __device__ __forceinline__ void d1_chunk(const Params& p, uint32_t t, bool has_k, int m_w, int lane, int n_base,
-                                         uint8_t* slab, uint32_t slab_s) {
+                                         uint8_t* slab, uint32_t slab_s, uint32_t& slab_seq) {
     if (m_w >= p.M) return;  // the whole warp is past the last row
     const int row = m_w + lane;
     const bool row_ok = row < p.M;
     const float a = p.alpha1, b = p.beta1;
-    for (int c = 0; c < p.bn1; c += 32) {
-        const int n0 = n_base + c;
-        if (n0 >= p.N1) break;
-        float v[32];
+    for (int c = 0; c < p.bn1; c += 64) {  // one TMEM round trip per 64 columns
+        if (n_base + c >= p.N1) break;
+        float v[64];
         if (has_k) {
-            tmem_ld32(t + (uint32_t)c, v);
+            tmem_ld64(t + (uint32_t)c, v);
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; j++) v[j] = 0.0f;
+            for (int j = 0; j < 64; j++) v[j] = 0.0f;
         }
-        float o[32];
 #pragma unroll
-        for (int j = 0; j < 32; j++) o[j] = a * v[j];
-        if (b != 0.0f) {
-            const float* cr = p.C1 + (long long)row * p.ldc1 + n0;
-            if (row_ok && p.vec_c1 && n0 + 32 <= p.N1) {
+        for (int h = 0; h < 2; h++) {
+            const int n0 = n_base + c + 32 * h;
+            if (n0 >= p.N1) break;
+            float o[32];
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
-                    o[4 * j] = fmaf(b, x.x, o[4 * j]);
-                    o[4 * j + 1] = fmaf(b, x.y, o[4 * j + 1]);
-                    o[4 * j + 2] = fmaf(b, x.z, o[4 * j + 2]);
-                    o[4 * j + 3] = fmaf(b, x.w, o[4 * j + 3]);
+            for (int j = 0; j < 32; j++) o[j] = a * v[32 * h + j];
+            if (b != 0.0f) {
+                const float* cr = p.C1 + (long long)row * p.ldc1 + n0;
+                if (row_ok && p.vec_c1 && n0 + 32 <= p.N1) {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const float4 x = __ldg(reinterpret_cast<const float4*>(cr) + j);
+                        o[4 * j] = fmaf(b, x.x, o[4 * j]);
+                        o[4 * j + 1] = fmaf(b, x.y, o[4 * j + 1]);
+                        o[4 * j + 2] = fmaf(b, x.z, o[4 * j + 2]);
+                        o[4 * j + 3] = fmaf(b, x.w, o[4 * j + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j++)
+                        if (row_ok && n0 + j < p.N1) o[j] = fmaf(b, __ldg(cr + j), o[j]);
                 }
-            } else {
+            }
+            if (p.tma_d) {
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    const int nh = n0 + 16 * hh;
+                    if (nh >= p.N1) break;
+                    const uint32_t buf = (slab_seq & 1u) * 2048u;
+                    if (lane == 0) bulk_wait_read_1();  // this slab's previous store has read it
+                    __syncwarp();
+                    // 64-byte rows, 64-byte swizzle: chunk j of row `lane` at j ^ ((lane >> 1) & 3).
+                    uint8_t* line = slab + buf + lane * 64;
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        *reinterpret_cast<float4*>(line + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            make_float4(o[16 * hh + 4 * j], o[16 * hh + 4 * j + 1], o[16 * hh + 4 * j + 2],
+                                        o[16 * hh + 4 * j + 3]);
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&p.tmD1, slab_s + buf, nh, m_w, 0);
+                        bulk_commit_group();
+                    }
+                    ++slab_seq;
+                }
+            } else if (row_ok) {
+                float* dr = p.D1 + (long long)row * p.ldd1 + n0;
 #pragma unroll
                 for (int j = 0; j < 32; j++)
-                    if (row_ok && n0 + j < p.N1) o[j] = fmaf(b, __ldg(cr + j), o[j]);
+                    if (n0 + j < p.N1) dr[j] = o[j];
             }
-        }
-        if (p.tma_d) {
-            if (lane == 0) bulk_wait_read_all();  // the slab's previous store has read it
-            __syncwarp();
-            uint8_t* line = slab + lane * 128;
-#pragma unroll
-            for (int j = 0; j < 8; j++)
-                *reinterpret_cast<float4*>(line + ((j ^ (lane & 7)) << 4)) =
-                    make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(&p.tmD1, slab_s, n0, m_w, 0);
-                bulk_commit_group();
-            }
-        } else if (row_ok) {
-            float* dr = p.D1 + (long long)row * p.ldd1 + n0;
-#pragma unroll
-            for (int j = 0; j < 32; j++)
-                if (n0 + j < p.N1) dr[j] = o[j];
         }
     }
 }
@@ -177,6 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int nk0 = (p.K0 + 63) >> 6;  // first GEMM: K steps of 64
     const int nk1 = p.n0p >> 6;        // second GEMM: K = n0p
+    // Units are numbered row block by row block, so the units that share a
+    // block of A0 (and recompute its D0) run side by side and read it from L2.
+    const int groups = (p.chunks + p.cpg - 1) / p.cpg;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; s++) {
@@ -215,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         // counts them).
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const int mb = u % p.mblocks, grp = u / p.mblocks;
+            const int mb = u / groups, grp = u % groups;
             const int m0 = mb * 128;
             const int c0 = grp * p.cpg, c1 = min(p.chunks, c0 + p.cpg);
             const int steps = nk0 + (c1 - c0) * nk1;
@@ -265,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
             const uint32_t id1 = idesc_bf16(p.bn1, false, true);
             bool ok = true;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, uc++) {
-                const int grp = u / p.mblocks;
+                const int grp = u % groups;
                 const int c0 = grp * p.cpg, c1 = min(p.chunks, c0 + p.cpg);
                 // First GEMM: D0 accumulator.
                 ok = wait_fast(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit);
@@ -335,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const bool has_k0 = nk0 > 0, has_k1 = nk1 > 0;
         int acc = 0;
-        uint32_t aph = 0;
+        uint32_t aph = 0, slab_seq = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            const int mb = u % p.mblocks, grp = u / p.mblocks;
+            const int mb = u / groups, grp = u % groups;
             const int m0 = mb * 128;
             const int c0 = grp * p.cpg, c1 = min(p.chunks, c0 + p.cpg);
             int w = 1;
@@ -370,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
                 }
                 tc_fence_after();
                 const uint32_t t1 = tmem + (uint32_t)(acc * 256) + lane_off;
-                d1_chunk(p, t1, has_k1, m0 + 32 * q, lane, c * p.bn1, slab, slab_s);
+                d1_chunk(p, t1, has_k1, m0 + 32 * q, lane, c * p.bn1, slab, slab_s, slab_seq);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce(acc));

@@ -8,7 +8,7 @@
 // needs every column of D0 in the block: N0 <= 256 (one TMEM accumulator).
 //
 // Work unit: 128 rows of M x a group of `cpg` consecutive chunks of bn1
-// columns of D1.  A unit computes its 128 x N0 block of D0 once (first GEMM
+// columns of D1 (unit u: row block u / groups, group u % groups).  A unit computes its 128 x N0 block of D0 once (first GEMM
 // into TMEM, epilogue warps convert it into the second GEMM's K-major
 // 128-byte-swizzled operand in shared memory), then each chunk of D1 (second
 // GEMM into TMEM, epilogue to global memory).  Several groups of one row
@@ -26,14 +26,14 @@ namespace b2b {
 
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kMaxStages = 8;
-constexpr int kEpiSlabBytes = 32 * 32 * 4;  // one 32 x 32 fp32 box per epilogue warp
+constexpr int kEpiSlabBytes = 2 * 32 * 16 * 4;  // two 32 x 16 fp32 boxes per epilogue warp
 constexpr int kSmemLimit = 232448;          // dynamic shared memory per CTA (227 KB)
 
 struct alignas(128) Params {
     CUtensorMap tmA0;  // A0 [M][K0] bf16, box {64, 128}
     CUtensorMap tmW0;  // W0 [K0][N0] bf16, box {64, 64}
     CUtensorMap tmW1;  // W1 [N0][N1] bf16, box {64, 64}
-    CUtensorMap tmD1;  // D1 [M][N1] fp32, box {32, 32} (bulk stores, when tma_d)
+    CUtensorMap tmD1;  // D1 [M][N1] fp32, box {16, 32}, 64-byte swizzle (bulk stores, when tma_d)
     const float* C0;
     const float* C1;
     float* D1;

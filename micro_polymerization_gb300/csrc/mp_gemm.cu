@@ -176,13 +176,15 @@ struct DeviceGuard {
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
-// Tiled map, interleave none, 128-byte swizzle, zero fill, element strides 1.
+// Tiled map, interleave none, 128-byte swizzle (or `swz`), zero fill,
+// element strides 1.
 bool encode_tiled(DeviceState* s, CUtensorMap* m, CUtensorMapDataType dt, uint32_t rank, const void* ptr,
-                  const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+                  const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     TmKey key;
     std::memset(&key, 0, sizeof key);
     key.ptr = (uint64_t)(uintptr_t)ptr;
-    key.dtype = (uint32_t)dt;
+    key.dtype = (uint32_t)dt | ((uint32_t)swz << 8);
     key.rank = rank;
     for (uint32_t i = 0; i < rank; i++) {
         key.dims[i] = dims[i];
@@ -213,7 +215,7 @@ bool encode_tiled(DeviceState* s, CUtensorMap* m, CUtensorMapDataType dt, uint32
         if (i + 1 < rank) st[i] = strides[i];
     }
     CUresult r = s->encode(m, dt, rank, const_cast<void*>(ptr), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     if (e) {
@@ -239,6 +241,15 @@ bool encode_3d_f32(DeviceState* s, CUtensorMap* m, void* ptr, uint64_t d0, uint6
     const uint64_t strides[2] = {stride1_bytes, stride2_bytes};
     const uint32_t box[3] = {box0, box1, 1};
     return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box);
+}
+
+// fp32 output view with the 64-byte swizzle (boxes of 16 fp32 columns).
+bool encode_3d_f32_sw64(DeviceState* s, CUtensorMap* m, void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                        uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const uint32_t box[3] = {box0, box1, 1};
+    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool encode_4d(DeviceState* s, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
@@ -719,7 +730,8 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
             return MP_ERR_CUDA;
     }
     p.tma_d = (((uintptr_t)a.D1 & 15u) == 0 && (a.ldd1 * 4) % 16 == 0) ? 1 : 0;
-    if (p.tma_d && !encode_3d_f32(s, &p.tmD1, a.D1, N1, M, 1, a.ldd1 * 4, round_up(M * a.ldd1 * 4, 16), 32, 32))
+    if (p.tma_d &&
+        !encode_3d_f32_sw64(s, &p.tmD1, a.D1, N1, M, 1, a.ldd1 * 4, round_up(M * a.ldd1 * 4, 16), 16, 32))
         return MP_ERR_CUDA;
     p.C0 = a.C0;
     p.C1 = a.C1;

@@ -602,52 +602,82 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
 // Work unit: 128 rows x `cpg` chunks of D1.  Each unit runs the first GEMM
 // for its rows (nk0 K steps of a 128 x n0p tile), then cpg chunks of the
 // second (nk1 = n0p / 64 K steps of a 128 x bn1 tile, each followed by its
-// fp32 epilogue; a chunk's epilogue overlaps the next chunk's MMAs).  Fewer
+// fp32 epilogue; a chunk's epilogue overlaps the next chunk's MMAs, and a
+// unit's last epilogue the next unit's first GEMM).  Fewer
 // chunks per unit give more units to spread over the SMs, at the price of
 // recomputing the block of D0 once per unit.
 mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     if (!out || M < 0 || N0 < 0 || N1 < 0 || K0 < 0) return MP_ERR_INVALID_ARG;
     if (N0 > 256) return MP_ERR_UNSUPPORTED;
     if (M >= ((int64_t)1 << 31) || N1 >= ((int64_t)1 << 31) || K0 >= ((int64_t)1 << 31)) return MP_ERR_INVALID_ARG;
-    mp_b2b_plan p;
-    std::memset(&p, 0, sizeof p);
     const int64_t k0 = N0 > 0 ? K0 : 0;  // no first GEMM without columns of D0
-    p.n0p = (int32_t)(((N0 + 63) / 64) * 64);
-    p.bn1 = (int32_t)std::min<int64_t>(256, std::max<int64_t>(64, ((N1 + 63) / 64) * 64));
-    p.chunks = (int32_t)((N1 + p.bn1 - 1) / p.bn1);
-    p.mblocks = (int32_t)((M + 127) / 128);
-    const int nk0 = (int)((k0 + 63) / 64), nk1 = p.n0p / 64;
-    p.stage_bytes = std::max(nk0 > 0 ? 16384 + p.n0p * 128 : 0, p.bn1 * 128);
-    const int room = b2b::kSmemLimit - p.n0p * 256 - 4 * b2b::kEpiSlabBytes - 2048;
-    p.num_stages = std::min(b2b::kMaxStages, room / p.stage_bytes);
-    if (p.num_stages < 2) return MP_ERR_PLAN;
-    p.smem_bytes = b2b::smem_bytes(p.num_stages, p.stage_bytes, p.n0p);
-
+    const int n0p = (int)(((N0 + 63) / 64) * 64);
+    const int nk0 = (int)((k0 + 63) / 64), nk1 = n0p / 64;
+    const int mblocks = (int)((M + 127) / 128);
     const int sms = std::max(1, hw.num_pe);
-    const double mma_pe = hw.mma_tflops > 0 ? hw.mma_tflops / sms : 13.0;  // TFLOP/s per SM
-    auto step_us = [&](int n) { return std::max(kStepFloorUs, 2.0 * 128 * n * 64 / (mma_pe * 1e6)); };
-    const double t0 = nk0 * (p.n0p > 0 ? step_us(p.n0p) : 0.0) + 0.5;  // + the D0 hand-over
-    const double mma1 = nk1 * step_us(p.bn1);
-    double best = 1e300;
-    for (int cpg = 1; cpg <= std::max(1, p.chunks); cpg++) {
-        const int64_t groups = (p.chunks + cpg - 1) / cpg;
-        if (cpg > 1 && (p.chunks + cpg - 2) / (cpg - 1) == groups) continue;  // same grouping as cpg - 1
-        const int64_t units = (int64_t)p.mblocks * std::max<int64_t>(1, groups);
-        const int64_t active = std::min<int64_t>(units, sms);
-        // A chunk's fp32 output at the active SMs' share of HBM bandwidth.
-        const double hbm_pe = (hw.hbm_gbs > 0 ? hw.hbm_gbs : 6700.0) / (double)active;
-        const double epi = 4.0 * 128 * p.bn1 / (hbm_pe * 1e3);
-        const double waves = (double)((units + sms - 1) / sms);
-        const double cost = waves * (t0 + cpg * std::max(mma1, epi) + epi) + 2.0;
-        if (cost < best * (1.0 - 1e-9)) {
-            best = cost;
-            p.cpg = cpg;
-            p.units = (int32_t)units;
+    const double hbm = hw.hbm_gbs > 0 ? hw.hbm_gbs : 6700.0;
+    // Phase times of one unit, measured on GB300 with timestamped copies of
+    // the kernel: a 64-deep K step of a 128 x n tile costs about 0.40 us at
+    // n = 256 (operand ingest and the MMA issuer), never below the issuer's
+    // floor; the hand-over of D0 about 0.3 us + 0.9 us per 256 columns; a
+    // chunk's epilogue about 1.6 us per 256 columns when its stores are not
+    // HBM-bound; the first operands of a CTA arrive after about 1 us.
+    auto step_us = [&](int n) { return std::max(kStepFloorUs, 0.40 * n / 256.0); };
+    const double handover = 0.3 + 0.9 * n0p / 256.0;
+    const double t0 = nk0 * (n0p > 0 ? step_us(n0p) : 0.0) + handover;
+    mp_b2b_plan best;
+    std::memset(&best, 0, sizeof best);
+    best.cost_us = 1e300;
+    const int widest = (int)std::min<int64_t>(256, std::max<int64_t>(64, ((N1 + 63) / 64) * 64));
+    // Chunk width: the widest tile that covers N1 (up to 256), or 128 (twice
+    // the units per row block, each chunk's MMAs and stores half as long).
+    const int widths[2] = {widest, widest > 128 ? 128 : 0};
+    for (int bn1 : widths) {
+        if (bn1 == 0) continue;
+        const int chunks = (int)((N1 + bn1 - 1) / bn1);
+        const int stage_bytes = std::max(nk0 > 0 ? 16384 + n0p * 128 : 0, bn1 * 128);
+        const int room = b2b::kSmemLimit - n0p * 256 - 4 * b2b::kEpiSlabBytes - 2048;
+        const int stages = std::min(b2b::kMaxStages, room / stage_bytes);
+        if (stages < 2) continue;
+        const double mma1 = nk1 * step_us(bn1);
+        for (int cpg = 1; cpg <= std::max(1, chunks); cpg++) {
+            const int64_t groups = (chunks + cpg - 1) / cpg;
+            if (cpg > 1 && (chunks + cpg - 2) / (cpg - 1) == groups) continue;  // same grouping as cpg - 1
+            const int64_t units = (int64_t)mblocks * std::max<int64_t>(1, groups);
+            const int64_t active = std::min<int64_t>(units, sms);
+            // A chunk's fp32 output at the active SMs' share of HBM bandwidth,
+            // or the epilogue warps' own rate, whichever is slower.
+            const double hbm_pe = hbm * 1e3 / (double)active;  // bytes per us per active SM
+            const double epi = std::max(1.6 * bn1 / 256.0, 4.0 * 128 * bn1 / hbm_pe);
+            // The block of A0 comes from HBM once per row block (the units of a
+            // row block run side by side), so each unit carries 1/groups of it.
+            const double a0_us = 2.0 * 128 * (double)k0 / (double)std::max<int64_t>(1, groups) / hbm_pe;
+            // A CTA's units form a pipeline: the MMA side (first GEMM, hand-over,
+            // the chunks' MMAs) of one unit overlaps the epilogue warps' side
+            // (hand-over, the chunks' stores, and the unit's share of HBM
+            // traffic) of the one before, so each unit costs the slower side,
+            // plus one fill/drain.
+            const double mma_side = t0 + cpg * mma1;
+            const double epi_side = handover + std::max(cpg * epi, a0_us + cpg * 4.0 * 128 * bn1 / hbm_pe);
+            const double waves = (double)((units + sms - 1) / sms);
+            const double cost = 1.0 + waves * std::max(mma_side, epi_side) + std::min(mma_side, epi_side) + 2.0;
+            if (cost < best.cost_us * (1.0 - 1e-9)) {
+                best.cost_us = cost;
+                best.n0p = n0p;
+                best.bn1 = bn1;
+                best.chunks = chunks;
+                best.mblocks = mblocks;
+                best.cpg = cpg;
+                best.units = (int32_t)units;
+                best.num_stages = stages;
+                best.stage_bytes = stage_bytes;
+            }
         }
     }
-    p.grid = (int32_t)std::min<int64_t>(p.units, sms);
-    p.cost_us = best;
-    *out = p;
+    if (best.bn1 == 0) return MP_ERR_PLAN;
+    best.grid = (int32_t)std::min<int64_t>(best.units, sms);
+    best.smem_bytes = b2b::smem_bytes(best.num_stages, best.stage_bytes, best.n0p);
+    *out = best;
     return MP_OK;
 }
 

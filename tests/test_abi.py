@@ -195,8 +195,9 @@ def test_b2b_plan_rules():
         ring_need = max((16384 + p.n0p * 128) if (K0 > 0 and N0 > 0) else 0, p.bn1 * 128)
         assert p.stage_bytes == ring_need and p.stage_bytes % 8192 == 0
         assert p.cost_us > 0
-    # Many row blocks: every unit takes all chunks (no recomputation of D0).
-    assert mp.mp_plan_b2b(h, 128 * 1000, 64, 1024, 256).cpg == 4
+    # A costly first GEMM with many row blocks: no recomputation of D0.
+    p = mp.mp_plan_b2b(h, 128 * 1000, 256, 1024, 4096)
+    assert p.cpg == p.chunks and p.units == 1000
     # One row block, many chunks, a cheap first GEMM: chunks spread over SMs.
     p = mp.mp_plan_b2b(h, 128, 128, 8192, 64)
     assert p.cpg < p.chunks and p.units > 1
