@@ -32,6 +32,13 @@ What each routine follows (page titles and sections):
     ``b2b_bound`` carries the stated per-GEMM bound through the second GEMM
     and adds one bf16 rounding of D0 (the operand type of the second GEMM
     when D0 stays on chip).
+  * ``conv2d_nhwc`` -- a stride-1 2-D convolution (MikPoly summary, section 5:
+    convolutions run as GEMM), written as its definition: for every filter
+    tap (r, s), the zero-padded input shifted by (r, s) times that tap's
+    C x K slice, summed over taps; then alpha and beta*Cin as for a GEMM.
+    ``conv2d_magnitude`` is the same sum over absolute values (the
+    tolerance scale, as ``magnitude`` for a GEMM); ``im2col_nhwc`` builds the
+    explicit [N*P*Q, R*S*C] matrix that a GEMM-based convolution multiplies.
 """
 from __future__ import annotations
 
@@ -324,3 +331,64 @@ def within_b2b(D1, D1ref, bound):
     ok = bool(np.all(np.isfinite(D1)) and np.all(err <= bound))
     worst = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
     return ok, worst
+
+
+def _conv_out(H, W, R, S, pad_h, pad_w):
+    return H + 2 * pad_h - R + 1, W + 2 * pad_w - S + 1
+
+
+def _conv_taps(Xf, Wf, pad_h, pad_w):
+    """sum over taps (r, s) of the shifted, zero-padded input times Wf[r, s]."""
+    N, H, W, C = Xf.shape
+    R, S, C2, K = Wf.shape
+    if C2 != C:
+        raise ValueError("filter channels must match the input's")
+    P, Q = _conv_out(H, W, R, S, pad_h, pad_w)
+    Xp = np.zeros((N, H + 2 * pad_h, W + 2 * pad_w, C), dtype=np.float64)
+    Xp[:, pad_h:pad_h + H, pad_w:pad_w + W, :] = Xf
+    D = np.zeros((N, P, Q, K), dtype=np.float64)
+    for r in range(R):
+        for s in range(S):
+            D += Xp[:, r:r + P, s:s + Q, :] @ Wf[r, s]
+    return D
+
+
+def conv2d_nhwc(X, Wt, Cin=None, alpha=1.0, beta=0.0, pad_h=1, pad_w=1):
+    """D[n,p,q,k] = alpha * sum_{r,s,c} X[n, p+r-pad_h, q+s-pad_w, c] * Wt[r,s,c,k]
+    + beta * Cin[n,p,q,k]  (stride 1, zero padding), in fp64.
+
+    X [N,H,W,C] and Wt [R,S,C,K] are bf16 bit patterns; Cin [N,P,Q,K] float32
+    (ignored when beta == 0)."""
+    D = alpha * _conv_taps(bf16_bits_to_f64(X), bf16_bits_to_f64(Wt), pad_h, pad_w)
+    if beta != 0.0:
+        D = D + beta * np.asarray(Cin, dtype=np.float64)
+    return D
+
+
+def conv2d_magnitude(X, Wt, Cin=None, beta=0.0, pad_h=1, pad_w=1):
+    """sum_{r,s,c} |X||Wt| + |beta*Cin| at every output (the tolerance scale)."""
+    G = _conv_taps(np.abs(bf16_bits_to_f64(X)), np.abs(bf16_bits_to_f64(Wt)), pad_h, pad_w)
+    if beta != 0.0:
+        G = G + abs(beta) * np.abs(np.asarray(Cin, dtype=np.float64))
+    return G
+
+
+def im2col_nhwc(X, R, S, pad_h=1, pad_w=1):
+    """The [N*P*Q, R*S*C] matrix of a GEMM-based convolution: row (n, p, q),
+    column (r, s, c) holds X[n, p+r-pad_h, q+s-pad_w, c] (0 outside the input).
+    Returns bf16 bit patterns (a copy of X's bits, zeros as 0x0000)."""
+    X = np.asarray(X, dtype=np.uint16)
+    N, H, W, C = X.shape
+    P, Q = _conv_out(H, W, R, S, pad_h, pad_w)
+    out = np.zeros((N, P, Q, R, S, C), dtype=np.uint16)
+    for r in range(R):
+        for s in range(S):
+            for p in range(P):
+                h = p + r - pad_h
+                if not 0 <= h < H:
+                    continue
+                for q in range(Q):
+                    w = q + s - pad_w
+                    if 0 <= w < W:
+                        out[:, p, q, r, s, :] = X[:, h, w, :]
+    return out.reshape(N * P * Q, R * S * C)

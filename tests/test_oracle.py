@@ -490,3 +490,83 @@ def test_b2b_bound_admits_fused_precision_and_rejects_mistakes():
         for mistake in ("beta0", "beta1", "transpose") + (("act",) if a != oracle.ACT_NONE else ()):
             ok, worst = oracle.within_b2b(_fp32_b2b(*args, a, drop=mistake), ref, bound)
             assert not ok, (a, mistake, worst)
+
+
+# ---------------------------------------------------------------------------
+# Convolution (MikPoly summary, section 5: convolutions run as GEMM)
+# ---------------------------------------------------------------------------
+def _int_bits(rng, shape, lo=-3, hi=4):
+    v = rng.integers(lo, hi, size=shape).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16), v.astype(np.float64)
+
+
+def test_conv_brute_force_small():
+    """Seven nested Python loops over the definition, integer inputs: exact."""
+    rng = np.random.default_rng(21)
+    for (N, H, W, C, K, R, S, ph, pw) in [(2, 4, 3, 3, 2, 3, 3, 1, 1), (1, 5, 5, 2, 3, 3, 3, 0, 0),
+                                         (1, 3, 6, 2, 2, 1, 3, 0, 2), (2, 2, 2, 1, 1, 3, 3, 2, 1)]:
+        X, x = _int_bits(rng, (N, H, W, C))
+        Wt, w = _int_bits(rng, (R, S, C, K))
+        Cin_shape = (N, H + 2 * ph - R + 1, W + 2 * pw - S + 1, K)
+        Cin = rng.integers(-5, 6, size=Cin_shape).astype(np.float32)
+        P, Q = Cin_shape[1], Cin_shape[2]
+        ref = np.zeros(Cin_shape)
+        for n in range(N):
+            for p in range(P):
+                for q in range(Q):
+                    for k in range(K):
+                        acc = 0.0
+                        for r in range(R):
+                            for s in range(S):
+                                h, ww = p + r - ph, q + s - pw
+                                if 0 <= h < H and 0 <= ww < W:
+                                    for c in range(C):
+                                        acc += x[n, h, ww, c] * w[r, s, c, k]
+                        ref[n, p, q, k] = 2.0 * acc - 0.5 * Cin[n, p, q, k]
+        D = oracle.conv2d_nhwc(X, Wt, Cin, 2.0, -0.5, ph, pw)
+        assert np.array_equal(D, ref), (N, H, W, C, K, R, S, ph, pw)
+
+
+def test_conv_is_gemm_on_im2col():
+    """A GEMM-based convolution: the C GEMM oracle on the explicit im2col
+    matrix and the filter as [R*S*C, K] gives the same values."""
+    rng = np.random.default_rng(22)
+    N, H, W, C, K = 2, 7, 9, 16, 24
+    X = oracle_bits(rng, (N, H, W, C))
+    Wt = oracle_bits(rng, (3, 3, C, K))
+    Cin = rng.uniform(-1, 1, size=(N, H, W, K)).astype(np.float32)
+    D = oracle.conv2d_nhwc(X, Wt, Cin, 1.5, 0.25)
+    A = oracle.im2col_nhwc(X, 3, 3)
+    G = oracle.gemm(A, Wt.reshape(9 * C, K), Cin.reshape(N * H * W, K), 1.5, 0.25)
+    assert np.allclose(D.reshape(N * H * W, K), G, rtol=1e-12, atol=1e-12)
+    mag = oracle.conv2d_magnitude(X, Wt, Cin, 0.25).reshape(N * H * W, K)
+    assert np.allclose(mag, oracle.magnitude(A, Wt.reshape(9 * C, K), Cin.reshape(N * H * W, K), 0.25), rtol=1e-12)
+
+
+def test_conv_1x1_is_gemm_and_delta_filter_is_identity():
+    rng = np.random.default_rng(23)
+    N, H, W, C, K = 3, 5, 4, 8, 6
+    X = oracle_bits(rng, (N, H, W, C))
+    Wt = oracle_bits(rng, (1, 1, C, K))
+    D = oracle.conv2d_nhwc(X, Wt, pad_h=0, pad_w=0)
+    assert np.array_equal(D.reshape(N * H * W, K), oracle.gemm(X.reshape(N * H * W, C), Wt.reshape(C, K)))
+    # Centre tap = identity (C = K): a 3x3 "same" convolution returns its input.
+    delta = np.zeros((3, 3, C, C), dtype=np.float32)
+    delta[1, 1] = np.eye(C)
+    db = (delta.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(oracle.conv2d_nhwc(X, db), oracle.bf16_bits_to_f64(X))
+
+
+def test_conv_ones_closed_form():
+    """All-ones input and filter, padding 1: each output counts its valid taps,
+    C * rows(p) * cols(q), with rows(p) = 3 minus the taps off the top or
+    bottom edge (likewise for columns)."""
+    N, H, W, C, K = 1, 6, 5, 4, 2
+    one = np.uint16(0x3F80)
+    X = np.full((N, H, W, C), one, dtype=np.uint16)
+    Wt = np.full((3, 3, C, K), one, dtype=np.uint16)
+    D = oracle.conv2d_nhwc(X, Wt)
+    valid = lambda i, n: 3 - (i == 0) - (i == n - 1)
+    for p in range(H):
+        for q in range(W):
+            assert np.all(D[0, p, q] == C * valid(p, H) * valid(q, W))
