@@ -400,6 +400,51 @@ typedef struct {
 } mp_b2b_plan;
 mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
 
+/*
+ * 2-D convolution, stride 1, zero padding, NHWC, as an implicit GEMM (the
+ * MikPoly summary, section 5, runs convolutions as GEMMs; here the im2col
+ * matrix [N*P*Q, R*S*C] is never built, its tiles are loaded from X):
+ *     D[n,p,q,k] = alpha * sum_{r,s,c} X[n, p+r-pad_h, q+s-pad_w, c] * F[r,s,c,k]
+ *                + beta * Cin[n,p,q,k]
+ * with P = H + 2*pad_h - R + 1, Q = W + 2*pad_w - S + 1.  X [N][H][W][C] and
+ * F [R][S][C][K] are bf16, dense; Cin and D [N][P][Q][K] are fp32 with
+ * `ldc` / `ldd` elements from one output pixel to the next (>= K).  Cin is
+ * not read when beta == 0 and may be D (same pointer and ld).  Asynchronous
+ * on `stream`, like mp_gemm.  An empty output (N, K, P or Q <= 0) is a no-op;
+ * C == 0 gives D = beta * Cin.
+ * Errors: MP_ERR_INVALID_ARG (negative size or padding, R or S < 1, NULL
+ * operand that is read, ld < K, misaligned element, D overlapping X, F or a
+ * Cin other than D itself); MP_ERR_UNSUPPORTED (host-only handle, or an X or
+ * F whose pixel / row pitch is not 16-byte aligned and that does not fit the
+ * staging area, where such operands are copied with padded rows);
+ * MP_ERR_CUDA (launch failure).
+ */
+mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                    int64_t pad_h, int64_t pad_w, const void* X, const void* F, const float* Cin, int64_t ldc,
+                    float* D, int64_t ldd, float alpha, float beta, mp_stream stream);
+
+/*
+ * How mp_conv2d tiles a problem (host only; any handle).  An output tile is
+ * wb x hb x nb pixels (along Q, P and images; powers of two, product 128) by
+ * bn output channels; the tile shape and bn minimise the cost model (waves of
+ * tiles x the K loop over R*S*ceil(C/64) steps, against the tile's stores).
+ */
+typedef struct {
+    int32_t wb, hb, nb;       /* output pixels per tile along Q, P and images */
+    int32_t bn;               /* output channels per tile */
+    int32_t tiles_q, tiles_p, tiles_n, tiles_k;
+    int32_t ksteps;           /* R * S * ceil(C / 64) */
+    int32_t units;            /* tiles */
+    int32_t grid;             /* CTAs launched: min(units, #SMs) */
+    int32_t num_stages;
+    int32_t stage_bytes;
+    int32_t smem_bytes;
+    double useful;            /* output pixels / pixels the tiles cover */
+    double cost_us;           /* model estimate */
+} mp_conv_plan;
+mp_status mp_plan_conv(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                       int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = [
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
-    "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan",
+    "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan", "mp_conv2d", "mp_plan_conv", "MpConvPlan",
 ]
 
 MP_MAX_REGIONS = 4
@@ -86,6 +86,14 @@ class MpB2BPlan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("cost_us", ctypes.c_double)]
 
 
+class MpConvPlan(ctypes.Structure):
+    _fields_ = [("wb", ctypes.c_int32), ("hb", ctypes.c_int32), ("nb", ctypes.c_int32), ("bn", ctypes.c_int32),
+                ("tiles_q", ctypes.c_int32), ("tiles_p", ctypes.c_int32), ("tiles_n", ctypes.c_int32),
+                ("tiles_k", ctypes.c_int32), ("ksteps", ctypes.c_int32), ("units", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("num_stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("useful", ctypes.c_double), ("cost_us", ctypes.c_double)]
+
+
 class MPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -142,6 +150,10 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_gemm_b2b": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                  _vp, _i64, _vp, _i64, _f, _f, _f, _f, _i32, _vp], ctypes.c_int),
                 "mp_plan_b2b": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpB2BPlan)], ctypes.c_int),
+                "mp_conv2d": ([_vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _i64,
+                               _vp, _i64, _f, _f, _vp], ctypes.c_int),
+                "mp_plan_conv": ([_vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                                  ctypes.POINTER(MpConvPlan)], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -339,6 +351,53 @@ def mp_plan_b2b(h: Handle, M: int, N0: int, N1: int, K0: int) -> MpB2BPlan:
     """How mp_gemm_b2b splits an (M, N0, N1, K0) problem (host only)."""
     out = MpB2BPlan()
     _check(library().mp_plan_b2b(h.ptr, M, N0, N1, K0, ctypes.byref(out)), "mp_plan_b2b")
+    return out
+
+
+def _pixel_pitch(t, name, K):
+    """Elements from one output pixel to the next of a [N, P, Q, K] tensor
+    whose pixels are evenly spaced (NHWC, channels possibly padded)."""
+    if t.dim() != 4 or (t.size(3) > 1 and t.stride(3) != 1):
+        raise ValueError(f"{name} must be [N, P, Q, K] with unit channel stride")
+    N, P, Q, _ = t.shape
+    ld = t.stride(2) if Q > 1 else (t.stride(1) if P > 1 else (t.stride(0) if N > 1 else K))
+    if (Q > 1 and t.stride(1) != Q * ld and P > 1) or (P * Q > 1 and N > 1 and t.stride(0) != P * Q * ld):
+        raise ValueError(f"{name} pixels must be evenly spaced")
+    return max(ld, K)
+
+
+def mp_conv2d(h: Handle, X, F, Cin, D, alpha: float = 1.0, beta: float = 0.0, pad_h: int = 1, pad_w: int = 1,
+              stream=None) -> None:
+    """D = alpha * conv2d(X, F) + beta * Cin, stride 1, zero padding, NHWC, as an
+    implicit GEMM.  X [N,H,W,C] and F [R,S,C,K] contiguous bfloat16; Cin and D
+    [N,P,Q,K] float32."""
+    import torch
+    if X.dtype != torch.bfloat16 or F.dtype != torch.bfloat16 or X.dim() != 4 or F.dim() != 4:
+        raise TypeError("X [N,H,W,C] and F [R,S,C,K] must be bfloat16")
+    if not (X.is_contiguous() and F.is_contiguous()):
+        raise ValueError("X and F must be contiguous")
+    if D.dtype != torch.float32:
+        raise TypeError("D must be float32")
+    N, H, W, C = X.shape
+    R, S, C2, K = F.shape
+    P, Q = H + 2 * pad_h - R + 1, W + 2 * pad_w - S + 1
+    if C2 != C or tuple(D.shape) != (N, P, Q, K):
+        raise ValueError("shape mismatch")
+    c_ptr, ldc = None, 0
+    if beta != 0.0:
+        if Cin is None or Cin.dtype != torch.float32 or tuple(Cin.shape) != (N, P, Q, K):
+            raise ValueError("beta != 0 needs an fp32 Cin of D's shape")
+        c_ptr, ldc = Cin.data_ptr(), _pixel_pitch(Cin, "Cin", K)
+    st = library().mp_conv2d(h.ptr, N, H, W, C, K, R, S, pad_h, pad_w, X.data_ptr(), F.data_ptr(), c_ptr, ldc,
+                             D.data_ptr(), _pixel_pitch(D, "D", K), float(alpha), float(beta), _stream_ptr(stream))
+    _check(st, "mp_conv2d")
+
+
+def mp_plan_conv(h: Handle, N: int, H: int, W: int, C: int, K: int, R: int = 3, S: int = 3, pad_h: int = 1,
+                 pad_w: int = 1) -> MpConvPlan:
+    """How mp_conv2d tiles a problem (host only)."""
+    out = MpConvPlan()
+    _check(library().mp_plan_conv(h.ptr, N, H, W, C, K, R, S, pad_h, pad_w, ctypes.byref(out)), "mp_plan_conv")
     return out
 
 

@@ -144,6 +144,29 @@ mp_status check_b2b(const mp::B2BArgs& a) {
     return MP_OK;
 }
 
+// Argument rules of mp_conv2d (include/mp.h).
+mp_status check_conv(const mp::ConvArgs& a) {
+    if (a.N < 0 || a.H < 0 || a.W < 0 || a.C < 0 || a.K < 0 || a.R < 1 || a.S < 1 || a.pad_h < 0 || a.pad_w < 0)
+        return MP_ERR_INVALID_ARG;
+    for (int64_t v : {a.N, a.H, a.W, a.C, a.K, a.R, a.S, a.pad_h, a.pad_w})
+        if (v >= kMaxDim) return MP_ERR_INVALID_ARG;
+    const int64_t P = a.H + 2 * a.pad_h - a.R + 1, Q = a.W + 2 * a.pad_w - a.S + 1;
+    if (a.N == 0 || a.K == 0 || P <= 0 || Q <= 0) return MP_OK;
+    if (a.N * a.H * a.W >= kMaxDim || a.N * P * Q >= kMaxDim || a.R * a.S * (a.C + 63) >= kMaxDim)
+        return MP_ERR_INVALID_ARG;
+    if (!a.D || a.ldd < a.K || ((uintptr_t)a.D & 3) != 0) return MP_ERR_INVALID_ARG;
+    const bool reads_x = a.C > 0, read_c = a.beta != 0.0f;
+    if (reads_x && (!a.X || !a.F || ((uintptr_t)a.X & 1) != 0 || ((uintptr_t)a.F & 1) != 0)) return MP_ERR_INVALID_ARG;
+    if (read_c && (!a.Cin || a.ldc < a.K || ((uintptr_t)a.Cin & 3) != 0)) return MP_ERR_INVALID_ARG;
+    const Span d = span_of(a.D, a.N * P * Q, a.K, a.ldd, 4, 1, 0);
+    if (reads_x && (overlap(d, span_of(a.X, a.N * a.H * a.W, a.C, a.C, 2, 1, 0)) ||
+                    overlap(d, span_of(a.F, a.R * a.S * a.C, a.K, a.K, 2, 1, 0))))
+        return MP_ERR_INVALID_ARG;
+    if (read_c && !(a.Cin == a.D && a.ldc == a.ldd) && overlap(d, span_of(a.Cin, a.N * P * Q, a.K, a.ldc, 4, 1, 0)))
+        return MP_ERR_INVALID_ARG;
+    return MP_OK;
+}
+
 mp_status run(mp_handle h, const mp::GemmArgs& a) {
     if (!h) return MP_ERR_INVALID_ARG;
     mp_status st = check_args(a);
@@ -321,6 +344,28 @@ mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0
 mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     if (!h || !out) return MP_ERR_INVALID_ARG;
     return mp::plan_b2b(h->hw, M, N0, N1, K0, out);
+}
+
+mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                    int64_t pad_h, int64_t pad_w, const void* X, const void* F, const float* Cin, int64_t ldc,
+                    float* D, int64_t ldd, float alpha, float beta, mp_stream stream) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    const mp::ConvArgs a{N, H, W, C, K, R, S, pad_h, pad_w, X, F, Cin, ldc, D, ldd, alpha, beta, stream};
+    mp_status st = check_conv(a);
+    if (st != MP_OK) return st;
+    const int64_t P = H + 2 * pad_h - R + 1, Q = W + 2 * pad_w - S + 1;
+    if (N == 0 || K == 0 || P <= 0 || Q <= 0) return MP_OK;
+    if (h->host_only) return MP_ERR_UNSUPPORTED;
+    mp_conv_plan plan;
+    st = mp::plan_conv(h->hw, N, H, W, C, K, R, S, pad_h, pad_w, &plan);
+    if (st != MP_OK) return st;
+    return mp::device_run_conv(h, plan, a);
+}
+
+mp_status mp_plan_conv(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                       int64_t pad_h, int64_t pad_w, mp_conv_plan* out) {
+    if (!h || !out) return MP_ERR_INVALID_ARG;
+    return mp::plan_conv(h->hw, N, H, W, C, K, R, S, pad_h, pad_w, out);
 }
 
 mp_status mp_check(mp_handle h, mp_stream stream) {

@@ -1,0 +1,66 @@
+// Implicit-GEMM 2-D convolution (stride 1, zero padding), NHWC:
+//   D[n,p,q,k] = alpha * sum_{r,s,c} X[n, p+r-pad_h, q+s-pad_w, c] * F[r,s,c,k]
+//              + beta * Cin[n,p,q,k]
+// The MikPoly summary (section 5) runs convolutions as GEMMs over the im2col
+// matrix [N*P*Q, R*S*C].  Here that matrix is never built: the TMA producer
+// loads each 128 x 64 A tile straight from X.
+//
+// An output tile is a box of wb x hb x nb output pixels (powers of two,
+// wb*hb*nb = 128: a rectangle of one image, or the same rectangle of several
+// small images) by bn output channels.  For filter tap (r, s) and channels
+// [c0, c0+64), the A tile is the 4-D box {64 channels, wb, hb, nb} of X at
+// (c0, q0+s-pad_w, p0+r-pad_h, n0): in shared memory 128 rows of 64 bf16
+// with the 128-byte swizzle, row = pixel (w fastest, then h, then n), the
+// layout a GEMM A tile has.  TMA fills coordinates outside X (the padding,
+// and the box's overhang past the image) with zeros.  The B tile is rows
+// tap*C + c0 .. +63 of F as a [R*S*C] x K matrix; when C is not a multiple
+// of 64, rows past the tap's C meet zero A channels, so they add nothing.
+// The epilogue stores each warp's 32 pixels as a 4-D box of D, clipped at
+// the edges.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mp {
+namespace conv {
+
+constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr int kMaxStages = 8;
+constexpr int kEpiSlabBytes = 2 * 32 * 32 * 4;  // two 32-pixel x 32-channel fp32 slabs per epilogue warp
+constexpr int kSmemLimit = 232448;             // dynamic shared memory per CTA (227 KB)
+
+struct alignas(128) Params {
+    CUtensorMap tmX;  // X as {C, W, H, N} bf16, box {64, wb, hb, nb}
+    CUtensorMap tmF;  // F as {K, R*S*C, 1} bf16, box {64, 64, 1}
+    CUtensorMap tmD;  // D as {K, Q, P, N} fp32, box {32, bw, bh, bnn} (bulk stores, when tma_d)
+    const float* Cin;
+    float* D;
+    long long ldc, ldd;  // elements from one output pixel to the next in Cin and D
+    int N, H, W, C, K, R, S, pad_h, pad_w, P, Q;
+    int wb, hb, nb;     // output pixels per tile along Q, P and images
+    int bw, bh, bnn;    // one warp's 32 pixels: the first 32 rows of the tile's order
+    int tiles_q, tiles_p, tiles_n, tiles_k;
+    int bn;             // output channels per tile (64, 128 or 256)
+    int cblocks;        // ceil(C / 64)
+    int ksteps;         // R * S * cblocks
+    int units;          // tiles_n * tiles_p * tiles_q * tiles_k
+    int num_stages, stage_bytes;
+    float alpha, beta;
+    int tma_d;          // D 16-byte aligned with ldd % 4 == 0: bulk tensor stores
+    int vec_c;          // Cin rows allow 16-byte loads
+    int* err;           // the handle's status word
+    unsigned long long wait_limit_ns;
+};
+
+inline int smem_bytes(int num_stages, int stage_bytes) {
+    return num_stages * stage_bytes + 4 * kEpiSlabBytes + 1024 + 1024;
+}
+
+cudaError_t launch(const cudaLaunchConfig_t& cfg, const Params& p);
+bool set_smem();
+
+}  // namespace conv
+}  // namespace mp

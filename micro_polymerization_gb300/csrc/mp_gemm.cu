@@ -15,6 +15,7 @@
 #include "mp_internal.h"
 #include "mp_kernel.cuh"
 #include "mp_b2b.cuh"
+#include "mp_conv.cuh"
 
 namespace mp {
 namespace dev {
@@ -97,7 +98,8 @@ struct DeviceState {
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
 bool set_kernel_smem() {
-    return set_poly_gemm_smem<0>() && set_poly_gemm_smem_act_f32() && set_poly_gemm_smem_bf16() && b2b::set_smem();
+    return set_poly_gemm_smem<0>() && set_poly_gemm_smem_act_f32() && set_poly_gemm_smem_bf16() && b2b::set_smem() &&
+           conv::set_smem();
 }
 
 // Split-K on chip: for S = 2..16, the CTAs that clusters of S CTAs of the
@@ -770,6 +772,90 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
     if (b2b::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
+    return MP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Implicit-GEMM convolution: tensor maps and the launch of k_conv_igemm
+// ---------------------------------------------------------------------------
+mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    DeviceGuard g(s->device);
+    conv::Params p;
+    std::memset(&p, 0, sizeof(p));
+    cudaStream_t stream = (cudaStream_t)a.stream;
+    const int64_t N = a.N, H = a.H, W = a.W, C = a.C, K = a.K, R = a.R, S = a.S;
+    const int64_t P = H + 2 * a.pad_h - R + 1, Q = W + 2 * a.pad_w - S + 1;
+    if (C > 0) {
+        // X as [N*H*W] rows of C channels and F as [R*S*C] rows of K: copied
+        // with padded rows when TMA cannot address them.
+        const void* X = a.X;
+        const void* F = a.F;
+        int64_t ldx = C, ldf = K, used = 0;
+        mp_status st = stage_if_unaligned(s, stream, X, ldx, N * H * W, C, used);
+        if (st != MP_OK) return st;
+        if ((st = stage_if_unaligned(s, stream, F, ldf, R * S * C, K, used)) != MP_OK) return st;
+        const uint64_t xd[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
+        const uint64_t xs[3] = {(uint64_t)ldx * 2, (uint64_t)(W * ldx * 2), (uint64_t)(H * W * ldx * 2)};
+        const uint32_t xb[4] = {64, (uint32_t)pl.wb, (uint32_t)pl.hb, (uint32_t)pl.nb};
+        if (!encode_tiled(s, &p.tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, X, xd, xs, xb) ||
+            !encode_3d(s, &p.tmF, F, K, R * S * C, 1, ldf * 2, round_up(R * S * C * ldf * 2, 16), 64, 64))
+            return MP_ERR_CUDA;
+    }
+    p.tma_d = (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0) ? 1 : 0;
+    p.bw = pl.wb >= 32 ? 32 : pl.wb;
+    p.bh = pl.wb >= 32 ? 1 : (pl.wb * pl.hb >= 32 ? 32 / pl.wb : pl.hb);
+    p.bnn = 32 / (p.bw * p.bh);
+    if (p.tma_d) {
+        const uint64_t dd[4] = {(uint64_t)K, (uint64_t)Q, (uint64_t)P, (uint64_t)N};
+        const uint64_t ds[3] = {(uint64_t)a.ldd * 4, (uint64_t)(Q * a.ldd * 4), (uint64_t)(P * Q * a.ldd * 4)};
+        const uint32_t db[4] = {32, (uint32_t)p.bw, (uint32_t)p.bh, (uint32_t)p.bnn};
+        if (!encode_tiled(s, &p.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.D, dd, ds, db)) return MP_ERR_CUDA;
+    }
+    p.Cin = a.Cin;
+    p.D = a.D;
+    p.ldc = a.ldc;
+    p.ldd = a.ldd;
+    p.N = (int)N;
+    p.H = (int)H;
+    p.W = (int)W;
+    p.C = (int)C;
+    p.K = (int)K;
+    p.R = (int)R;
+    p.S = (int)S;
+    p.pad_h = (int)a.pad_h;
+    p.pad_w = (int)a.pad_w;
+    p.P = (int)P;
+    p.Q = (int)Q;
+    p.wb = pl.wb;
+    p.hb = pl.hb;
+    p.nb = pl.nb;
+    p.tiles_q = pl.tiles_q;
+    p.tiles_p = pl.tiles_p;
+    p.tiles_n = pl.tiles_n;
+    p.tiles_k = pl.tiles_k;
+    p.bn = pl.bn;
+    p.cblocks = (int)cdiv(C, 64);
+    p.ksteps = pl.ksteps;
+    p.units = pl.units;
+    p.num_stages = pl.num_stages;
+    p.stage_bytes = pl.stage_bytes;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.vec_c = (a.Cin && ((uintptr_t)a.Cin & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
+    p.err = s->err;
+    p.wait_limit_ns = s->wait_limit_ns;
+    if (s->log)
+        std::fprintf(stderr, "[mp] conv N=%lld H=%lld W=%lld C=%lld K=%lld RxS=%lldx%lld tile %dx%dx%d bn=%d units=%d\n",
+                     (long long)N, (long long)H, (long long)W, (long long)C, (long long)K, (long long)R, (long long)S,
+                     pl.wb, pl.hb, pl.nb, pl.bn, pl.units);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid);
+    cfg.blockDim = dim3(conv::kThreads);
+    cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+    cfg.stream = stream;
+    if (conv::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 

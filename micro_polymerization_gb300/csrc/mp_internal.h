@@ -122,4 +122,19 @@ struct B2BArgs {
 mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
 mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& plan, const B2BArgs& a);
 
+// Implicit-GEMM convolution (mp_conv2d): planner (mp_planner.cpp) and launch
+// (mp_gemm.cu).
+struct ConvArgs {
+    int64_t N, H, W, C, K, R, S, pad_h, pad_w;
+    const void* X;
+    const void* F;
+    const float* Cin; int64_t ldc;
+    float* D; int64_t ldd;
+    float alpha, beta;
+    void* stream;
+};
+mp_status plan_conv(const mp_hw& hw, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                    int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
+mp_status device_run_conv(mp_handle h, const mp_conv_plan& plan, const ConvArgs& a);
+
 }  // namespace mp

@@ -123,6 +123,80 @@ def make_b2b_operands(b: B2B, device="cpu"):
     return A0, W0, C0, W1, C1
 
 
+@dataclasses.dataclass(frozen=True)
+class Conv:
+    """Stride-1 2-D convolution, NHWC: D[N,P,Q,K] = alpha * conv(X[N,H,W,C],
+    F[R,S,C,K]) + beta * Cin, P = H + 2 pad_h - R + 1, Q likewise."""
+    N: int
+    H: int
+    W: int
+    C: int
+    K: int
+    R: int = 3
+    S: int = 3
+    pad_h: int = 1
+    pad_w: int = 1
+    alpha: float = 1.0
+    beta: float = 0.0
+    seed: int = 0
+
+    @property
+    def P(self) -> int:
+        return self.H + 2 * self.pad_h - self.R + 1
+
+    @property
+    def Q(self) -> int:
+        return self.W + 2 * self.pad_w - self.S + 1
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.N * self.P * self.Q * self.K * self.R * self.S * self.C
+
+    def as_gemm(self) -> "Gemm":
+        """The GEMM a GEMM-based convolution runs: [N*P*Q, R*S*C] x [R*S*C, K]."""
+        return Gemm(self.N * self.P * self.Q, self.K, self.R * self.S * self.C, self.alpha, self.beta, seed=self.seed)
+
+    def min_bytes(self) -> int:
+        """X and F read once, D written once (and Cin read when beta != 0)."""
+        b = 2 * self.N * self.H * self.W * self.C + 2 * self.R * self.S * self.C * self.K
+        b += 4 * self.N * self.P * self.Q * self.K * (2 if self.beta != 0.0 else 1)
+        return b
+
+
+def make_conv_operands(c: Conv, device="cpu"):
+    """(X bf16 [N,H,W,C], F bf16 [R,S,C,K], Cin fp32 [N,P,Q,K] or None), uniform [-1, 1)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(int(c.seed))
+    X = _uniform((c.N, c.H, c.W, c.C), gen, dev).to(torch.bfloat16)
+    F = _uniform((c.R, c.S, c.C, c.K), gen, dev).to(torch.bfloat16)
+    Cin = None
+    if c.beta != 0.0:
+        gen.manual_seed(int(c.seed) + 1)
+        Cin = _uniform((c.N, c.P, c.Q, c.K), gen, dev)
+    return X, F, Cin
+
+
+def conv_resolution(count: int = 64) -> List[Conv]:
+    """The dynamic-resolution workload's layers as convolutions: the same draws
+    (batch uniform on [1, 32], side uniform on [160, 320], stage s in 0..3),
+    each a 3x3 stride-1 'same' convolution on an H x H input, H = ceil(side /
+    (4 * 2^s)), C = K = 64 * 2^s.  Its GEMM is the dynamic-resolution GEMM."""
+    rng = np.random.default_rng(1002)
+    out = []
+    for i in range(count):
+        batch = int(rng.integers(1, 33))
+        side = int(rng.integers(160, 321))
+        s = int(rng.integers(0, 4))
+        ch = 64 * 2 ** s
+        h = math.ceil(side / (4 * 2 ** s))
+        out.append(Conv(batch, h, h, ch, ch, seed=1000 + 800 + 7 * i))
+    return out
+
+
+CONV_WORKLOADS = {"conv_resolution": conv_resolution}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a CPU tensor as numpy uint16 (no conversion)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

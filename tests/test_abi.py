@@ -206,3 +206,53 @@ def test_b2b_plan_rules():
     with pytest.raises(mp.MPError):
         mp.mp_plan_b2b(h, -1, 64, 10, 10)
     h.close()
+
+
+def test_conv_argument_checks():
+    lib = mp.library()
+    h = _host()
+    X, F, Cin, D = 0x10000, 0x20000000, 0x30000000, 0x40000000
+    base = dict(N=2, H=8, W=9, C=16, K=24, R=3, S=3, ph=1, pw=1, X=X, F=F, Cin=Cin, ldc=24, D=D, ldd=24,
+                a=1.0, b=0.5)
+
+    def g(**kw):
+        v = dict(base)
+        v.update(kw)
+        return lib.mp_conv2d(h.ptr, v["N"], v["H"], v["W"], v["C"], v["K"], v["R"], v["S"], v["ph"], v["pw"],
+                             v["X"], v["F"], v["Cin"], v["ldc"], v["D"], v["ldd"], v["a"], v["b"], None)
+
+    assert g() == mp.MP_ERR_UNSUPPORTED  # valid; no device
+    for empty in (dict(N=0), dict(K=0), dict(H=1, ph=0), dict(W=2, pw=0)):
+        assert g(**empty) == mp.MP_OK, empty
+    for bad in (dict(N=-1), dict(C=-1), dict(R=0), dict(S=0), dict(ph=-1), dict(D=None), dict(ldd=23),
+                dict(X=None), dict(F=None), dict(Cin=None), dict(ldc=23), dict(D=D + 2), dict(X=X + 1),
+                dict(D=X), dict(D=F), dict(Cin=D + 4)):
+        assert g(**bad) == mp.MP_ERR_INVALID_ARG, bad
+    assert g(b=0.0, Cin=None, ldc=0) == mp.MP_ERR_UNSUPPORTED  # Cin not read
+    assert g(C=0, X=None, F=None) == mp.MP_ERR_UNSUPPORTED    # no operand read
+    assert g(Cin=D) == mp.MP_ERR_UNSUPPORTED                  # in place
+    h.close()
+
+
+def test_conv_plan_rules():
+    h = _host()
+    for (N, H, W, C, K, R, S, ph, pw) in [(1, 1, 1, 1, 1, 1, 1, 0, 0), (32, 80, 80, 64, 64, 3, 3, 1, 1),
+                                           (5, 5, 5, 512, 512, 3, 3, 1, 1), (2, 7, 9, 16, 24, 3, 3, 1, 1),
+                                           (3, 30, 17, 12, 20, 5, 5, 2, 2), (1, 224, 224, 3, 64, 1, 1, 0, 0)]:
+        p = mp.mp_plan_conv(h, N, H, W, C, K, R, S, ph, pw)
+        P, Q = H + 2 * ph - R + 1, W + 2 * pw - S + 1
+        assert p.wb * p.hb * p.nb == 128 and all(x & (x - 1) == 0 for x in (p.wb, p.hb, p.nb))
+        assert p.tiles_q == -(-Q // p.wb) and p.tiles_p == -(-P // p.hb) and p.tiles_n == -(-N // p.nb)
+        assert p.bn in (64, 128, 256) and p.tiles_k == -(-K // p.bn)
+        assert p.units == p.tiles_q * p.tiles_p * p.tiles_n * p.tiles_k and p.grid == min(p.units, 148)
+        assert p.ksteps == R * S * -(-C // 64)
+        assert 0 < p.useful <= 1 and p.useful == pytest.approx(N * P * Q / (p.tiles_q * p.wb * p.tiles_p * p.hb
+                                                                             * p.tiles_n * p.nb))
+        assert 2 <= p.num_stages <= 8 and p.smem_bytes <= 232448 and p.stage_bytes == 16384 + 128 * p.bn
+    # Small images: tiles take several images rather than padding one image.
+    assert mp.mp_plan_conv(h, 32, 7, 7, 512, 512).nb > 1
+    p = mp.mp_plan_conv(h, 2, 0, 5, 8, 8)  # empty output
+    assert p.units == 0 and p.grid == 0
+    with pytest.raises(mp.MPError):
+        mp.mp_plan_conv(h, 1, 5, 5, 8, 8, 0, 3)
+    h.close()
