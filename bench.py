@@ -445,6 +445,8 @@ def workload_desc(name):
         "merged_qkv": "A x concat(Wq,Wk,Wv), K=1024, N=3072, M uniform [1,4096], 64 draws",
         "merged_batched": "batched 12 x (seq,seq,64), seq uniform [16,512], 64 draws",
         "stress": "1000 log-uniform shapes in [1,16384]^3 plus 4096^3, alpha=1.5, beta=0.5",
+        "conv_resolution": "implicit-GEMM convolutions, the 64 dynamic-resolution layers as 3x3 stride-1 "
+                           "NHWC convolutions",
         "b2b_adapter": "fused back-to-back GEMMs, 64 problems, M = 8*seq (seq uniform [1,512]), "
                        "768 -> 256 (ReLU) -> 768, bf16 A0,W0,W1, beta0=beta1=0",
         "b2b_1x1": "fused back-to-back GEMMs as two 1x1 convolutions, 64 problems, M = batch*H*W "
@@ -530,6 +532,21 @@ def cpu_baseline(args, gs, budget_s=None, act=0, out_bf16=False):
     return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(used), "kind": "oracle",
             "sample": f"first min(M, 256) rows of each of the first {done} GEMMs of the workload "
                       f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)"}
+
+
+def is_conv(name: str) -> bool:
+    from micro_polymerization_gb300 import workloads as wl
+    return name in wl.CONV_WORKLOADS or name.startswith("convshape:")
+
+
+def conv_workload(name: str):
+    """A named convolution workload, or ``convshape:N,H,W,C,K`` for one 3x3
+    'same' layer (alpha = 1, beta = 0), for profiling one shape."""
+    from micro_polymerization_gb300 import workloads as wl
+    if name.startswith("convshape:"):
+        v = [int(x) for x in name[len("convshape:"):].split(",")]
+        return [wl.Conv(v[0], v[1], v[2], v[3], v[4], seed=79)]
+    return wl.CONV_WORKLOADS[name]()
 
 
 def is_b2b(name: str) -> bool:
@@ -745,6 +762,219 @@ def run_b2b(args):
         dist.destroy_process_group()
 
 
+def cpu_baseline_conv(args, cs, budget_s=None):
+    """The oracle's convolution on the first image of each layer."""
+    import oracle
+    from micro_polymerization_gb300 import workloads as wl
+    budget_s = budget_s or args.cpu_seconds
+    flops = t_total = 0.0
+    done = 0
+    for c in cs:
+        X, F, Cin = wl.make_conv_operands(c)
+        xb, fb = wl.bf16_bits(X[:1]), wl.bf16_bits(F)
+        cn = Cin[:1].numpy() if Cin is not None else None
+        t0 = time.perf_counter()
+        oracle.conv2d_nhwc(xb, fb, cn, c.alpha, c.beta, c.pad_h, c.pad_w)
+        t_total += time.perf_counter() - t0
+        flops += c.flops / c.N
+        done += 1
+        if t_total >= budget_s:
+            break
+    import os as _os
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(_os.cpu_count() or 1),
+            "kind": "oracle",
+            "sample": f"first image of each of the first {done} layers ({flops / 1e9:.1f} GFLOP in "
+                      f"{t_total:.1f} s, fp64, numpy products per filter tap)"}
+
+
+def run_conv(args):
+    """Implicit-GEMM convolutions (mp_conv2d), one call per layer, back to back
+    on one stream; mp_gemm on each layer's prebuilt im2col matrix (the GEMM a
+    GEMM-based convolution runs) is timed beside it."""
+    import torch
+    import torch.nn.functional as tnf
+    import micro_polymerization_gb300 as mp
+    from micro_polymerization_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
+    h = mp.mp_init(local, calib if (os.path.exists(calib) and not args.no_calib) else None)
+    lib = mp.library()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    cs = conv_workload(args.workload)
+    if rank > 0:
+        import dataclasses
+        cs = [dataclasses.replace(c, seed=c.seed + 1_000_003 * rank) for c in cs]
+    ops, conv_calls, gemm_calls = [], [], []
+    for c in cs:
+        X, F, Cin = [t.to(dev) if t is not None else None for t in wl.make_conv_operands(c)]
+        D = torch.empty(c.N, c.P, c.Q, c.K, device=dev)
+        # The GEMM path's operands: im2col in (c, r, s) column order (unfold's),
+        # the filter permuted to match.
+        A = tnf.unfold(X.permute(0, 3, 1, 2).float(), (c.R, c.S), padding=(c.pad_h, c.pad_w))
+        A = A.transpose(1, 2).reshape(c.N * c.P * c.Q, c.C * c.R * c.S).to(torch.bfloat16).contiguous()
+        B = F.permute(2, 0, 1, 3).reshape(c.C * c.R * c.S, c.K).contiguous()
+        Dg = torch.empty(c.N * c.P * c.Q, c.K, device=dev)
+        ops.append((c, X, F, Cin, D, A, B, Dg))
+        conv_calls.append((lib.mp_conv2d, (h.ptr, c.N, c.H, c.W, c.C, c.K, c.R, c.S, c.pad_h, c.pad_w,
+                                           X.data_ptr(), F.data_ptr(), Cin.data_ptr() if Cin is not None else None,
+                                           c.K, D.data_ptr(), c.K, c.alpha, c.beta, sp)))
+        gemm_calls.append((lib.mp_gemm, (h.ptr, A.shape[0], c.K, A.shape[1], A.data_ptr(), A.shape[1],
+                                         B.data_ptr(), c.K, None, c.K, Dg.data_ptr(), c.K, c.alpha, 0.0, sp)))
+    torch.cuda.synchronize()
+
+    def step(calls, evs=None):
+        for i, (fn, a) in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            st = fn(*a)
+            if st != 0:
+                raise mp.MPError(st, fn.__name__)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    def timed(calls, steps):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(calls)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+
+    for _ in range(args.warmup):
+        step(conv_calls)
+        step(gemm_calls)
+    torch.cuda.synchronize()
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    n = len(conv_calls)
+    per_launch = np.zeros(n)
+    reps = max(1, min(args.steps, 20))
+    for _ in range(reps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        step(conv_calls, evs)
+        torch.cuda.synchronize()
+        per_launch += np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+    per_launch /= reps
+    with ClockSampler(local) as clocks:
+        ms_step = timed(conv_calls, args.steps)
+    ms_gemm = timed(gemm_calls, args.steps)
+    if args.dump and rank == 0:
+        per_gemm = np.zeros(n)
+        for _ in range(reps):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            step(gemm_calls, evs)
+            torch.cuda.synchronize()
+            per_gemm += np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+        per_gemm /= reps
+        with open(args.dump, "w") as f:
+            for c, t, tg in zip(cs, per_launch, per_gemm):
+                pl = mp.mp_plan_conv(h, c.N, c.H, c.W, c.C, c.K, c.R, c.S, c.pad_h, c.pad_w)
+                f.write(json.dumps({"N": c.N, "H": c.H, "C": c.C, "K": c.K, "t_us": round(float(t), 2),
+                                    "gemm_us": round(float(tg), 2), "wb": pl.wb, "hb": pl.hb, "nb": pl.nb,
+                                    "bn": pl.bn, "units": pl.units, "ksteps": pl.ksteps,
+                                    "useful": round(pl.useful, 3), "model_us": round(pl.cost_us, 2)}) + "\n")
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set in the timed region")
+    flops_step = sum(c.flops for c in cs)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    t_flop = np.array([c.flops / (peaks["bf16_tflops"] * 1e6) for c in cs])
+    t_mem = np.array([c.min_bytes() / (peaks["hbm_gbs"] * 1e3) for c in cs])
+    troof = np.maximum(t_flop, t_mem)
+    if t_flop.sum() >= t_mem.sum():
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_tflops"]
+        achieved = flops_step / (per_launch.sum() * 1e-6) / 1e12
+    else:
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm_gbs"]
+        achieved = sum(c.min_bytes() for c in cs) / (per_launch.sum() * 1e-6) / 1e9
+    flops = np.array([c.flops for c in cs], dtype=np.float64)
+    flop_weighted = float(np.sum(flops * troof / per_launch) / np.sum(flops))
+
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for (c, X, F, Cin, D, A, B, Dg) in ops:
+            hx = []
+            for x in (X, F, Cin, D):
+                if x is None:
+                    hx.append(None)
+                    continue
+                y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                y.copy_(x)
+                hx.append(y)
+            host.append(hx)
+        h2d = sum(x.numel() * x.element_size() for hx in host for x in hx[:3] if x is not None)
+        d2h = sum(hx[3].numel() * hx[3].element_size() for hx in host)
+
+        def e2e_step():
+            for (c, X, F, Cin, D, A, B, Dg), hx, (fn, a) in zip(ops, host, conv_calls):
+                for dst, src in zip((X, F, Cin), hx[:3]):
+                    if dst is not None:
+                        dst.copy_(src, non_blocking=True)
+                st = fn(*a)
+                if st != 0:
+                    raise mp.MPError(st, "mp_conv2d")
+                hx[3].copy_(D, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": round(flops_step * world * e2e_steps / t_e2e / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    cpu = cpu_baseline_conv(args, cs) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank == 0:
+        im2col_bytes = sum(2 * c.N * c.P * c.Q * c.R * c.S * c.C for c in cs)
+        x_bytes = sum(2 * c.N * c.H * c.W * c.C for c in cs)
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "implicit-GEMM convolutions of the dynamic-resolution workload: 64 3x3 "
+                                   "stride-1 'same' layers, NHWC, batch [1,32], C = K = 64*2^s",
+                       "layers_per_step": len(cs), "flops_per_step": int(flops_step),
+                       "l2": "inputs larger than L2" if sum(c.min_bytes() for c in cs) > L2_BYTES else
+                             "inputs smaller than L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "gemm_on_im2col": {"ms_per_step": round(ms_gemm, 4),
+                               "value": round(flops_step * world / (ms_gemm * 1e-3) / 1e12, 3),
+                               "calls": "mp_gemm on each layer's prebuilt im2col matrix (building it not timed)",
+                               "im2col_bytes_per_step": int(im2col_bytes), "x_bytes_per_step": int(x_bytes),
+                               "implicit_speedup": round(ms_gemm / ms_step, 3)},
+            "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
+                                   "sum_troof_over_sum_t": round(float(troof.sum() / per_launch.sum()), 4),
+                                   "peaks": peak_src},
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": None, "launches": n,
+                         "kernel": "k_conv_igemm", "peak_source": peak_src},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n * args.steps,
+            "clocks": clocks.summary(), "impl": "mp",
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -752,7 +982,12 @@ def run_reference(args):
     from micro_polymerization_gb300 import workloads as wl
     import oracle  # noqa: F401
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
-    if is_b2b(args.workload):
+    if is_conv(args.workload):
+        cs = conv_workload(args.workload)
+        for _ in range(args.warmup):
+            cpu_baseline_conv(args, cs[:1], budget_s=0.01)
+        vals = [cpu_baseline_conv(args, cs, budget_s=per_step) for _ in range(args.steps)]
+    elif is_b2b(args.workload):
         bs = b2b_workload(args.workload)
         for _ in range(args.warmup):
             cpu_baseline_b2b(args, bs[:1], budget_s=0.01)
@@ -801,6 +1036,8 @@ def main(argv=None):
         run_reference(args)
     elif is_b2b(args.workload):
         run_b2b(args)
+    elif is_conv(args.workload):
+        run_conv(args)
     else:
         run_mp(args)
 

@@ -89,7 +89,8 @@ class MpB2BPlan(ctypes.Structure):
 class MpConvPlan(ctypes.Structure):
     _fields_ = [("wb", ctypes.c_int32), ("hb", ctypes.c_int32), ("nb", ctypes.c_int32), ("bn", ctypes.c_int32),
                 ("tiles_q", ctypes.c_int32), ("tiles_p", ctypes.c_int32), ("tiles_n", ctypes.c_int32),
-                ("tiles_k", ctypes.c_int32), ("ksteps", ctypes.c_int32), ("units", ctypes.c_int32),
+                ("tiles_k", ctypes.c_int32), ("ksteps", ctypes.c_int32), ("tiles", ctypes.c_int32),
+                ("splits", ctypes.c_int32), ("units", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("useful", ctypes.c_double), ("cost_us", ctypes.c_double)]
 

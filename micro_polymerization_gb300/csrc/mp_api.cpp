@@ -357,7 +357,7 @@ mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int
     if (N == 0 || K == 0 || P <= 0 || Q <= 0) return MP_OK;
     if (h->host_only) return MP_ERR_UNSUPPORTED;
     mp_conv_plan plan;
-    st = mp::plan_conv(h->hw, N, H, W, C, K, R, S, pad_h, pad_w, &plan);
+    st = mp::plan_conv(h->hw, h->workspace_floats, N, H, W, C, K, R, S, pad_h, pad_w, &plan);
     if (st != MP_OK) return st;
     return mp::device_run_conv(h, plan, a);
 }
@@ -365,7 +365,7 @@ mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int
 mp_status mp_plan_conv(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
                        int64_t pad_h, int64_t pad_w, mp_conv_plan* out) {
     if (!h || !out) return MP_ERR_INVALID_ARG;
-    return mp::plan_conv(h->hw, N, H, W, C, K, R, S, pad_h, pad_w, out);
+    return mp::plan_conv(h->hw, h->workspace_floats, N, H, W, C, K, R, S, pad_h, pad_w, out);
 }
 
 mp_status mp_check(mp_handle h, mp_stream stream) {

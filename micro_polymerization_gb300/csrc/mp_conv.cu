@@ -33,16 +33,22 @@ struct Tile {
     int n0, p0, q0, k0;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Params& p, int u) {
+__device__ __forceinline__ Tile decode_tile(const Params& p, int t) {
     // Units run channel tile fastest, so the units that read one box of X
     // (and its halo) run side by side.
-    const int kt = u % p.tiles_k;
-    int m = u / p.tiles_k;
+    const int kt = t % p.tiles_k;
+    int m = t / p.tiles_k;
     const int tq = m % p.tiles_q;
     m /= p.tiles_q;
     const int tp = m % p.tiles_p;
     const int tn = m / p.tiles_p;
     return Tile{tn * p.nb, tp * p.hb, tq * p.wb, kt * p.bn};
+}
+
+// K steps [kb0, kb1) of split `sp`: the tile's ksteps cut into equal slices.
+__device__ __forceinline__ void split_range(const Params& p, int sp, int& kb0, int& kb1) {
+    kb0 = (int)((long long)p.ksteps * sp / p.splits);
+    kb1 = (int)((long long)p.ksteps * (sp + 1) / p.splits);
 }
 
 // Pixel of tile row `row` (w fastest, then h, then image).
@@ -121,6 +127,25 @@ __device__ __forceinline__ void conv_epilogue(const Params& p, const Tile& t, ui
     }
 }
 
+// Split-K: this warp's 32 rows of the raw fp32 accumulator into the
+// workspace slot of (tile, split), row-major [128][bn], 16-byte stores.
+__device__ __forceinline__ void conv_partial(const Params& p, int tile, int sp, uint32_t tacc, bool has_k, int q,
+                                             int lane) {
+    float* row = p.ws + (((long long)tile * p.splits + sp) * 128 + 32 * q + lane) * p.bn;
+    for (int c = 0; c < p.bn; c += 32) {
+        float v[32];
+        if (has_k) {
+            tmem_ld32(tacc + (uint32_t)c, v);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; j++) v[j] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            *reinterpret_cast<float4*>(row + c + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -173,8 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         // ------------------------------ TMA producer --------------------------
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const Tile t = decode_tile(p, u);
-            for (int kb = 0; kb < p.ksteps; kb++, g++) {
+            const Tile t = decode_tile(p, u / p.splits);
+            int kb0, kb1;
+            split_range(p, u % p.splits, kb0, kb1);
+            for (int kb = kb0; kb < kb1; kb++, g++) {
                 const int stage = (int)(g % (uint32_t)nst);
                 const uint32_t ph = (g / (uint32_t)nst) & 1u;
                 int ok = 1;
@@ -209,11 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
             const uint32_t idesc = idesc_bf16(p.bn, false, true);
             bool ok = true;
             for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+                int kb0, kb1;
+                split_range(p, u % p.splits, kb0, kb1);
                 ok = wait_fast(acce(acc), aph ^ 1u, abort_flag, p.err, kErrWaitAccEmpty, limit);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * 256);
-                for (int kb = 0; kb < p.ksteps; kb++) {
+                for (int kb = kb0; kb < kb1; kb++) {
                     ok = wait_fast(full(stage), ph, abort_flag, p.err, kErrWaitFull, limit);
                     if (!ok) break;
                     tc_fence_after();
@@ -221,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
                     const uint64_t da = desc_kmajor(st, 0), db = desc_mnmajor(st + 16384u, 0);
 #pragma unroll
                     for (int j = 0; j < 4; j++)
-                        umma_bf16<1>(d, da + 2u * j, db + 128u * j, idesc, (kb | j) ? 1u : 0u);
+                        umma_bf16<1>(d, da + 2u * j, db + 128u * j, idesc, (kb > kb0 || j) ? 1u : 0u);
                     umma_commit(empty(stage));
                     if (++stage == nst) {
                         stage = 0;
@@ -246,13 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         int acc = 0;
         uint32_t aph = 0, slab_seq = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const Tile t = decode_tile(p, u);
+            const int tile = u / p.splits, sp = u % p.splits;
+            int kb0, kb1;
+            split_range(p, sp, kb0, kb1);
             int w = 1;
             if (lane == 0) w = wait_fast(accf(acc), aph, abort_flag, p.err, kErrWaitAccFull, limit) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, w, 0)) break;
             tc_fence_after();
-            conv_epilogue(p, t, tmem + (uint32_t)(acc * 256) + lane_off, p.ksteps > 0, q, lane, slab, slab_s,
-                          slab_seq);
+            const uint32_t tacc = tmem + (uint32_t)(acc * 256) + lane_off;
+            if (p.splits > 1)
+                conv_partial(p, tile, sp, tacc, kb1 > kb0, q, lane);
+            else
+                conv_epilogue(p, decode_tile(p, tile), tacc, kb1 > kb0, q, lane, slab, slab_s, slab_seq);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce(acc));
@@ -267,6 +301,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         tc_fence_after();
         tmem_dealloc<1>(tmem, 512);
     }
+}
+
+// Split-K reduction: thread i handles 4 channels of one tile row; the splits
+// are summed in order, then the epilogue arithmetic of the one-pass path.
+__global__ void __launch_bounds__(256) k_conv_reduce(const __grid_constant__ Params p) {
+    const int groups = p.bn >> 2;
+    const long long total = (long long)p.tiles * 128 * groups;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int g4 = (int)(i % groups);
+        const long long tr = i / groups;
+        const int row = (int)(tr % 128);
+        const int tile = (int)(tr / 128);
+        const Tile t = decode_tile(p, tile);
+        int n, ph, qw;
+        tile_pixel(p, t, row, n, ph, qw);
+        const int k = t.k0 + 4 * g4;
+        if (n >= p.N || ph >= p.P || qw >= p.Q || k >= p.K) continue;
+        const float* src = p.ws + ((long long)tile * p.splits * 128 + row) * p.bn + 4 * g4;
+        float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+        for (int s = 1; s < p.splits; s++) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (long long)s * 128 * p.bn));
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+        }
+        const long long pix = ((long long)n * p.P + ph) * p.Q + qw;
+        float o[4] = {p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            if (k + e >= p.K) break;
+            if (p.beta != 0.0f) o[e] = fmaf(p.beta, __ldg(p.Cin + pix * p.ldc + k + e), o[e]);
+            p.D[pix * p.ldd + k + e] = o[e];
+        }
+    }
+}
+
+cudaError_t launch_reduce(cudaStream_t stream, const Params& p) {
+    const long long total = (long long)p.tiles * 128 * (p.bn >> 2);
+    const int blocks = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
+    k_conv_reduce<<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch(const cudaLaunchConfig_t& cfg, const Params& p) {

@@ -16,7 +16,10 @@
 // tap*C + c0 .. +63 of F as a [R*S*C] x K matrix; when C is not a multiple
 // of 64, rows past the tap's C meet zero A channels, so they add nothing.
 // The epilogue stores each warp's 32 pixels as a 4-D box of D, clipped at
-// the edges.
+// the edges.  Layers with few tiles and long K loops split K: a tile's
+// splits run side by side, each writes its raw fp32 partial to a workspace,
+// and a second kernel sums the partials in split order (so the result does
+// not depend on timing) before alpha, beta*Cin and the store.
 #pragma once
 
 #include <cuda.h>
@@ -38,6 +41,7 @@ struct alignas(128) Params {
     CUtensorMap tmD;  // D as {K, Q, P, N} fp32, box {32, bw, bh, bnn} (bulk stores, when tma_d)
     const float* Cin;
     float* D;
+    float* ws;           // split-K partials: [tile][split][128 rows][bn] fp32
     long long ldc, ldd;  // elements from one output pixel to the next in Cin and D
     int N, H, W, C, K, R, S, pad_h, pad_w, P, Q;
     int wb, hb, nb;     // output pixels per tile along Q, P and images
@@ -46,7 +50,9 @@ struct alignas(128) Params {
     int bn;             // output channels per tile (64, 128 or 256)
     int cblocks;        // ceil(C / 64)
     int ksteps;         // R * S * cblocks
-    int units;          // tiles_n * tiles_p * tiles_q * tiles_k
+    int tiles;          // tiles_n * tiles_p * tiles_q * tiles_k
+    int splits;         // K slices per tile (split-K); > 1: partials go to `ws`
+    int units;          // tiles * splits
     int num_stages, stage_bytes;
     float alpha, beta;
     int tma_d;          // D 16-byte aligned with ldd % 4 == 0: bulk tensor stores
@@ -60,6 +66,9 @@ inline int smem_bytes(int num_stages, int stage_bytes) {
 }
 
 cudaError_t launch(const cudaLaunchConfig_t& cfg, const Params& p);
+// Split-K: sum each tile's partials in split order, then alpha, beta*Cin and
+// the store of the tile's pixels (one thread per 4 channels of a tile row).
+cudaError_t launch_reduce(cudaStream_t stream, const Params& p);
 bool set_smem();
 
 }  // namespace conv

@@ -838,7 +838,11 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
     p.bn = pl.bn;
     p.cblocks = (int)cdiv(C, 64);
     p.ksteps = pl.ksteps;
+    p.tiles = pl.tiles;
+    p.splits = pl.splits;
     p.units = pl.units;
+    p.ws = s->ws;
+    if (pl.splits > 1 && (int64_t)pl.tiles * pl.splits * 128 * pl.bn > h->workspace_floats) return MP_ERR_PLAN;
     p.num_stages = pl.num_stages;
     p.stage_bytes = pl.stage_bytes;
     p.alpha = a.alpha;
@@ -847,15 +851,16 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
     p.err = s->err;
     p.wait_limit_ns = s->wait_limit_ns;
     if (s->log)
-        std::fprintf(stderr, "[mp] conv N=%lld H=%lld W=%lld C=%lld K=%lld RxS=%lldx%lld tile %dx%dx%d bn=%d units=%d\n",
+        std::fprintf(stderr, "[mp] conv N=%lld H=%lld W=%lld C=%lld K=%lld RxS=%lldx%lld tile %dx%dx%d bn=%d splits=%d units=%d\n",
                      (long long)N, (long long)H, (long long)W, (long long)C, (long long)K, (long long)R, (long long)S,
-                     pl.wb, pl.hb, pl.nb, pl.bn, pl.units);
+                     pl.wb, pl.hb, pl.nb, pl.bn, pl.splits, pl.units);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid);
     cfg.blockDim = dim3(conv::kThreads);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
     if (conv::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
+    if (pl.splits > 1 && conv::launch_reduce(stream, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 

@@ -133,8 +133,8 @@ struct ConvArgs {
     float alpha, beta;
     void* stream;
 };
-mp_status plan_conv(const mp_hw& hw, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
-                    int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
+mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K,
+                    int64_t R, int64_t S, int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
 mp_status device_run_conv(mp_handle h, const mp_conv_plan& plan, const ConvArgs& a);
 
 }  // namespace mp

@@ -692,8 +692,8 @@ mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K
 // tried: the cost is the waves of tiles times the slower of a tile's K loop
 // and its stores (a CTA's tiles pipeline through two accumulators), plus
 // one fill.  The constants are those measured for the GEMM kernels.
-mp_status plan_conv(const mp_hw& hw, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
-                    int64_t pad_h, int64_t pad_w, mp_conv_plan* out) {
+mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K,
+                    int64_t R, int64_t S, int64_t pad_h, int64_t pad_w, mp_conv_plan* out) {
     if (!out || N < 0 || H < 0 || W < 0 || C < 0 || K < 0 || R < 1 || S < 1 || pad_h < 0 || pad_w < 0)
         return MP_ERR_INVALID_ARG;
     const int64_t lim = (int64_t)1 << 31;
@@ -707,6 +707,7 @@ mp_status plan_conv(const mp_hw& hw, int64_t N, int64_t H, int64_t W, int64_t C,
         best.wb = 128;
         best.hb = best.nb = 1;
         best.bn = 64;
+        best.splits = 1;
         *out = best;
         return MP_OK;
     }
@@ -715,43 +716,58 @@ mp_status plan_conv(const mp_hw& hw, int64_t N, int64_t H, int64_t W, int64_t C,
     const int64_t ksteps = R * S * ((C + 63) / 64);
     best.cost_us = 1e300;
     const int64_t kcover = ((K + 63) / 64) * 64;
+    // A K step of this kernel (a 4-D box of X and the filter's boxes), measured
+    // on GB300: about 0.6 us up to bn = 128 (operand requests, not MMAs,
+    // bound it), more for the widest tile.
+    auto step_us = [](int bn) { return bn <= 128 ? 0.6 : 0.8; };
     for (int bn : {64, 128, 256}) {
         if (bn > 64 && bn / 2 >= kcover) continue;  // wider than the channels need
         const int64_t tiles_k = (K + bn - 1) / bn;
-        const double step = std::max(kStepFloorUs, 0.40 * bn / 256.0);
         const int stage_bytes = 16384 + bn * 128;
         const int stages = std::min(conv::kMaxStages, (conv::kSmemLimit - 4 * conv::kEpiSlabBytes - 2048) / stage_bytes);
         for (int wb = 1; wb <= 128; wb *= 2) {
             for (int hb = 1; wb * hb <= 128; hb *= 2) {
                 const int nb = 128 / (wb * hb);
                 const int64_t tq = (Q + wb - 1) / wb, tp = (P + hb - 1) / hb, tn = (N + nb - 1) / nb;
-                const int64_t units = tq * tp * tn * tiles_k;
-                const int64_t active = std::min<int64_t>(units, sms);
-                const double hbm_pe = hbm * 1e3 / (double)active;  // bytes per us per active SM
-                const double epi = std::max(1.6 * bn / 256.0, 4.0 * 128 * bn / hbm_pe);
-                const double mma = (double)ksteps * step;
-                const double waves = (double)((units + sms - 1) / sms);
-                const double cost = 1.0 + waves * std::max(mma, epi) + std::min(mma, epi) + 2.0;
+                const int64_t tiles = tq * tp * tn * tiles_k;
                 const double useful = (double)(N * P * Q) / (double)(tq * wb * tp * hb * tn * nb);
-                if (cost < best.cost_us * (1.0 - 1e-9) ||
-                    (cost < best.cost_us * (1.0 + 1e-9) && useful > best.useful)) {
-                    best.cost_us = cost;
-                    best.wb = wb;
-                    best.hb = hb;
-                    best.nb = nb;
-                    best.bn = bn;
-                    best.tiles_q = (int32_t)tq;
-                    best.tiles_p = (int32_t)tp;
-                    best.tiles_n = (int32_t)tn;
-                    best.tiles_k = (int32_t)tiles_k;
-                    best.units = (int32_t)std::min<int64_t>(units, lim - 1);
-                    best.useful = useful;
-                    best.num_stages = stages;
-                    best.stage_bytes = stage_bytes;
+                for (int splits : {1, 2, 3, 4, 6, 8, 12, 16}) {
+                    if (splits > 1 && (splits > ksteps || tiles * splits * 128 * bn > ws_floats)) continue;
+                    const int64_t units = tiles * splits;
+                    if (units >= lim) continue;
+                    const int64_t active = std::min<int64_t>(units, sms);
+                    const double hbm_pe = hbm * 1e3 / (double)active;  // bytes per us per active SM
+                    const double epi = std::max(1.6 * bn / 256.0, 4.0 * 128 * bn / hbm_pe);
+                    const double mma = (double)((ksteps + splits - 1) / splits) * step_us(bn);
+                    const double waves = (double)((units + sms - 1) / sms);
+                    // The reduction: a second launch reading every partial once.
+                    const double reduce = splits > 1 ? 3.0 + (double)(tiles * splits * 128 * bn * 4 + N * P * Q * K * 4) /
+                                                               (hbm * 1e3)
+                                                     : 0.0;
+                    const double cost = 1.0 + waves * std::max(mma, epi) + std::min(mma, epi) + 2.0 + reduce;
+                    if (cost < best.cost_us * (1.0 - 1e-9) ||
+                        (cost < best.cost_us * (1.0 + 1e-9) && useful > best.useful)) {
+                        best.cost_us = cost;
+                        best.wb = wb;
+                        best.hb = hb;
+                        best.nb = nb;
+                        best.bn = bn;
+                        best.tiles_q = (int32_t)tq;
+                        best.tiles_p = (int32_t)tp;
+                        best.tiles_n = (int32_t)tn;
+                        best.tiles_k = (int32_t)tiles_k;
+                        best.tiles = (int32_t)tiles;
+                        best.splits = splits;
+                        best.units = (int32_t)units;
+                        best.useful = useful;
+                        best.num_stages = stages;
+                        best.stage_bytes = stage_bytes;
+                    }
                 }
             }
         }
     }
+    if (best.units == 0) return MP_ERR_PLAN;
     best.ksteps = (int32_t)ksteps;
     best.grid = (int32_t)std::min<int64_t>(best.units, sms);
     best.smem_bytes = conv::smem_bytes(best.num_stages, best.stage_bytes);

@@ -244,13 +244,17 @@ def test_conv_plan_rules():
         assert p.wb * p.hb * p.nb == 128 and all(x & (x - 1) == 0 for x in (p.wb, p.hb, p.nb))
         assert p.tiles_q == -(-Q // p.wb) and p.tiles_p == -(-P // p.hb) and p.tiles_n == -(-N // p.nb)
         assert p.bn in (64, 128, 256) and p.tiles_k == -(-K // p.bn)
-        assert p.units == p.tiles_q * p.tiles_p * p.tiles_n * p.tiles_k and p.grid == min(p.units, 148)
+        assert p.tiles == p.tiles_q * p.tiles_p * p.tiles_n * p.tiles_k
+        assert 1 <= p.splits <= max(1, p.ksteps) and p.units == p.tiles * p.splits and p.grid == min(p.units, 148)
+        assert p.splits == 1 or p.tiles * p.splits * 128 * p.bn <= 16 << 20  # the workspace
         assert p.ksteps == R * S * -(-C // 64)
         assert 0 < p.useful <= 1 and p.useful == pytest.approx(N * P * Q / (p.tiles_q * p.wb * p.tiles_p * p.hb
                                                                              * p.tiles_n * p.nb))
         assert 2 <= p.num_stages <= 8 and p.smem_bytes <= 232448 and p.stage_bytes == 16384 + 128 * p.bn
     # Small images: tiles take several images rather than padding one image.
     assert mp.mp_plan_conv(h, 32, 7, 7, 512, 512).nb > 1
+    # Few tiles and a long K loop: split K.
+    assert mp.mp_plan_conv(h, 1, 7, 7, 512, 512).splits > 1
     p = mp.mp_plan_conv(h, 2, 0, 5, 8, 8)  # empty output
     assert p.units == 0 and p.grid == 0
     with pytest.raises(mp.MPError):

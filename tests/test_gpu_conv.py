@@ -75,6 +75,20 @@ def test_conv_integer_exact():
         assert np.array_equal(D.numpy().astype(np.float64), ref), (N, H, W, C, K)
 
 
+def test_conv_split_k_parity_and_determinism():
+    """Few tiles and a long K loop: the plan splits K; partials are summed in
+    split order, so two runs give the same bits."""
+    for shape in [(1, 7, 7, 512, 512), (2, 5, 6, 256, 320), (1, 9, 9, 300, 72)]:
+        N, H, W, C, K = shape
+        c = wl.Conv(N, H, W, C, K, alpha=1.5, beta=0.5, seed=N + C)
+        plan = mp.mp_plan_conv(handle(), N, H, W, C, K)
+        assert plan.splits > 1, (shape, plan.splits)
+        check(c)
+        D1, _, _, _ = run_conv(c)
+        D2, _, _, _ = run_conv(c)
+        assert torch.equal(D1, D2)
+
+
 def test_conv_c_zero_and_in_place():
     c = wl.Conv(2, 6, 6, 0, 64, alpha=1.0, beta=0.5, seed=3)
     X = torch.zeros(2, 6, 6, 0, dtype=torch.bfloat16)
