@@ -1,9 +1,10 @@
 // The fused back-to-back GEMM kernel (see mp_b2b.cuh for the operation and
 // the work decomposition).
 //
-// Roles (192 threads): warp 0 issues the TMA copies, lane 0 of warp 1 issues
-// every tcgen05.mma and commit, warps 2..5 run the epilogues (warp w reads
-// TMEM lanes 32*(w%4)..+31, i.e. those rows of the tile).  One ring of
+// Roles (224 threads): warps 0 and 6 issue the TMA copies of alternate ring
+// stages, lane 0 of warp 1 issues every tcgen05.mma and commit, warps 2..5
+// run the epilogues (warp w reads TMEM lanes 32*(w%4)..+31, i.e. those rows
+// of the tile).  One ring of
 // shared-memory stages carries, per work unit, the first GEMM's K steps (an
 // A0 box of 128 x 64 and the 64 x n0p W0 boxes) and then, per chunk of D1,
 // the second GEMM's K steps (64 x bn1 W1 boxes).  Two TMEM accumulators of
@@ -262,13 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------ TMA producer --------------------------
+    if (warp == 0 || warp == 6) {
+        // ------------------------------ TMA producers (two warps) -------------
+        // Stage g of the CTA's sequence belongs to warp 0 when g is even, to
+        // warp 6 when it is odd.
         // Lane 0 probes the slot; the copies of one stage go out from
         // different lanes (A0 from lane 0 and W0 boxes from lanes 1..; or the
         // W1 boxes from lanes 0..), then lane 0 arms the stage with its bytes
         // (full boxes: TMA fills out-of-range elements with zeros and still
         // counts them).
+        const uint32_t pid = warp == 0 ? 0u : 1u;
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int mb = u / groups, grp = u % groups;
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
             const int c0 = grp * p.cpg, c1 = min(p.chunks, c0 + p.cpg);
             const int steps = nk0 + (c1 - c0) * nk1;
             for (int i = 0; i < steps; i++, g++) {
+                if ((g & 1u) != pid) continue;
                 const int stage = (int)(g % (uint32_t)nst);
                 const uint32_t ph = (g / (uint32_t)nst) & 1u;
                 int ok = 1;

@@ -1,9 +1,12 @@
 // The implicit-GEMM convolution kernel (see mp_conv.cuh for the operation
 // and the tiling).
 //
-// Roles (192 threads), as in the GEMM kernels: warp 0 issues the TMA copies,
-// lane 0 of warp 1 every tcgen05.mma and commit, warps 2..5 the epilogue
-// (warp w reads TMEM lanes 32*(w%4)..+31: those 32 pixels of the tile).  A
+// Roles (224 threads), as in the GEMM kernel: warps 0 and 6 issue the TMA
+// copies of alternate stages (issuing a stage -- probe the slot, the copies,
+// the expect-tx -- is several hundred cycles of dependent latency, longer
+// than the MMAs of a narrow stage), lane 0 of warp 1 every tcgen05.mma and
+// commit, warps 2..5 the epilogue (warp w reads TMEM lanes 32*(w%4)..+31:
+// those 32 pixels of the tile).  A
 // work unit is one output tile; its K loop runs over filter taps and blocks
 // of 64 input channels, one ring stage per step (the A box from X, the
 // tile's 64-column boxes of the filter).  Two 256-column TMEM accumulators
@@ -194,14 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------ TMA producer --------------------------
+    if (warp == 0 || warp == 6) {
+        // ------------------------------ TMA producers (two warps) -------------
+        // Stage g of the CTA's sequence uses ring slot g % nst and belongs to
+        // warp 0 when g is even, to warp 6 when it is odd.
+        const uint32_t pid = warp == 0 ? 0u : 1u;
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const Tile t = decode_tile(p, u / p.splits);
             int kb0, kb1;
             split_range(p, u % p.splits, kb0, kb1);
             for (int kb = kb0; kb < kb1; kb++, g++) {
+                if ((g & 1u) != pid) continue;
                 const int stage = (int)(g % (uint32_t)nst);
                 const uint32_t ph = (g / (uint32_t)nst) & 1u;
                 int ok = 1;

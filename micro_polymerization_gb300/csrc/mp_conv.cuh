@@ -30,7 +30,7 @@
 namespace mp {
 namespace conv {
 
-constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr int kThreads = 224;                  // warps 0, 6 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kMaxStages = 8;
 constexpr int kEpiSlabBytes = 2 * 32 * 32 * 4;  // two 32-pixel x 32-channel fp32 slabs per epilogue warp
 constexpr int kSmemLimit = 232448;             // dynamic shared memory per CTA (227 KB)
