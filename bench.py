@@ -158,6 +158,8 @@ def rank_workload(name: str, rank: int):
         M, N, K = (int(v) for v in vals[:3])
         beta = vals[3] if len(vals) > 3 else 0.0
         gs = [wl.Gemm(M, N, K, alpha=1.0, beta=beta, seed=77)]
+    elif name in wl.GROUPED_WORKLOADS:
+        gs = wl.GROUPED_WORKLOADS[name]()
     else:
         gs = wl.workload(name)
     if rank == 0:
@@ -445,6 +447,8 @@ def workload_desc(name):
         "merged_qkv": "A x concat(Wq,Wk,Wv), K=1024, N=3072, M uniform [1,4096], 64 draws",
         "merged_batched": "batched 12 x (seq,seq,64), seq uniform [16,512], 64 draws",
         "stress": "1000 log-uniform shapes in [1,16384]^3 plus 4096^3, alpha=1.5, beta=0.5",
+        "grouped_experts": "grouped GEMM: 48 expert problems of one layer, M uniform [1,512], (N,K) = (2048,1024), "
+                           "one mp_gemm_grouped call",
         "conv_resolution": "implicit-GEMM convolutions, the 64 dynamic-resolution layers as 3x3 stride-1 "
                            "NHWC convolutions",
         "b2b_adapter": "fused back-to-back GEMMs, 64 problems, M = 8*seq (seq uniform [1,512]), "
@@ -532,6 +536,11 @@ def cpu_baseline(args, gs, budget_s=None, act=0, out_bf16=False):
     return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(used), "kind": "oracle",
             "sample": f"first min(M, 256) rows of each of the first {done} GEMMs of the workload "
                       f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)"}
+
+
+def grouped_names():
+    from micro_polymerization_gb300 import workloads as wl
+    return set(wl.GROUPED_WORKLOADS)
 
 
 def is_conv(name: str) -> bool:
@@ -975,6 +984,150 @@ def run_conv(args):
         dist.destroy_process_group()
 
 
+def run_grouped(args):
+    """A group of problems of different shapes as one mp_gemm_grouped call per
+    step; the same problems as separate mp_gemm calls are timed beside it."""
+    import ctypes
+    import torch
+    import micro_polymerization_gb300 as mp
+    from micro_polymerization_gb300 import workloads as wl
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
+    h = mp.mp_init(local, calib if (os.path.exists(calib) and not args.no_calib) else None)
+    lib = mp.library()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    gs = rank_workload(args.workload, rank)
+    ops = []
+    for g in gs:
+        A, B, C = wl.make_operands(g, device=dev)
+        ops.append((g, A, B, C, torch.empty(g.M, g.N, device=dev)))
+    torch.cuda.synchronize()
+    arr = (mp.MpGemmProblem * len(ops))()
+    singles = []
+    for i, (g, A, B, C, D) in enumerate(ops):
+        cp = C.data_ptr() if C is not None else None
+        arr[i] = mp.MpGemmProblem(g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N, cp, g.N, D.data_ptr(), g.N,
+                                  g.alpha, g.beta)
+        singles.append((h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N, cp, g.N, D.data_ptr(), g.N,
+                        g.alpha, g.beta, sp))
+    count = len(ops)
+
+    def grouped_step():
+        st = lib.mp_gemm_grouped(h.ptr, count, arr, sp)
+        if st != 0:
+            raise mp.MPError(st, "mp_gemm_grouped")
+
+    def singles_step():
+        for a in singles:
+            st = lib.mp_gemm(*a)
+            if st != 0:
+                raise mp.MPError(st, "mp_gemm")
+
+    def timed(fn, steps):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / steps
+
+    for _ in range(args.warmup):
+        grouped_step()
+        singles_step()
+    torch.cuda.synchronize()
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set during warm-up")
+    with ClockSampler(local) as clocks:
+        ms_step = timed(grouped_step, args.steps)
+    ms_single = timed(singles_step, args.steps)
+    if mp.mp_check(h) != 0:
+        raise RuntimeError("device status word set in the timed region")
+    flops_step = sum(g.flops for g in gs)
+    bytes_step = sum(g.min_bytes() for g in gs)
+    value = flops_step * world / (ms_step * 1e-3) / 1e12
+    t_flop = flops_step / (peaks["bf16_tflops"] * 1e6)
+    t_mem = bytes_step / (peaks["hbm_gbs"] * 1e3)
+    launches = -(-count // 48)
+    if t_flop >= t_mem:
+        bound, unit, peak, achieved = "tensor", "TFLOP/s", peaks["bf16_tflops"], flops_step / (ms_step * 1e-3) / 1e12
+    else:
+        bound, unit, peak, achieved = "hbm", "GB/s", peaks["hbm_gbs"], bytes_step / (ms_step * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        host = []
+        for (g, A, B, C, D) in ops:
+            hx = []
+            for x in (A, B, C, D):
+                if x is None:
+                    hx.append(None)
+                    continue
+                y = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+                y.copy_(x)
+                hx.append(y)
+            host.append(hx)
+        h2d = sum(x.numel() * x.element_size() for hx in host for x in hx[:3] if x is not None)
+        d2h = sum(hx[3].numel() * hx[3].element_size() for hx in host)
+
+        def e2e_step():
+            for (g, A, B, C, D), hx in zip(ops, host):
+                for dst, src in zip((A, B, C), hx[:3]):
+                    if dst is not None:
+                        dst.copy_(src, non_blocking=True)
+            grouped_step()
+            for (g, A, B, C, D), hx in zip(ops, host):
+                hx[3].copy_(D, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": round(flops_step * world * e2e_steps / t_e2e / 1e12, 3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+    cpu = cpu_baseline(args, gs) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank == 0:
+        plan = mp.mp_plan_grouped(h, [(g.M, g.N, g.K) for g in gs])
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(args.workload), "problems_per_step": count,
+                       "flops_per_step": int(flops_step), "bn": plan.bn, "launches_per_step": launches,
+                       "l2": "inputs larger than L2" if bytes_step > L2_BYTES else "inputs smaller than L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "separate_calls": {"ms_per_step": round(ms_single, 4),
+                               "value": round(flops_step * world / (ms_single * 1e-3) / 1e12, 3),
+                               "calls": f"{count} mp_gemm calls", "grouped_speedup": round(ms_single / ms_step, 3)},
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": None, "launches": launches,
+                         "kernel": "k_gemm_grouped", "peak_source": peak_src},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+            "clocks": clocks.summary(), "impl": "mp",
+        }
+        print(json.dumps(line), flush=True)
+    h.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -1038,6 +1191,8 @@ def main(argv=None):
         run_b2b(args)
     elif is_conv(args.workload):
         run_conv(args)
+    elif args.workload in grouped_names():
+        run_grouped(args)
     else:
         run_mp(args)
 

@@ -450,6 +450,51 @@ typedef struct {
 mp_status mp_plan_conv(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
                        int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
 
+/*
+ * Grouped GEMM: `count` independent problems of any shapes in as few launches
+ * as possible (48 problems per launch), D_i = alpha_i * A_i B_i + beta_i * C_i.
+ * The BladeDISC v0.2.0 notes merge same-shape GEMMs into a batched GEMM to
+ * fill the machine and launch fewer kernels; a group drops the same-shape
+ * condition.  Each problem follows mp_gemm's rules (types, layouts, leading
+ * dimensions, C not read when beta_i == 0, C_i == D_i allowed); no D_i may
+ * overlap another problem's A, B, C or D.  `problems` is a host array, read
+ * before the call returns; the work is asynchronous on `stream`.  Problems
+ * with M, N == 0 are skipped; K == 0 gives D = beta * C.  count <= 4096.
+ * Errors: MP_ERR_INVALID_ARG (a problem breaking mp_gemm's rules, overlapping
+ * outputs, count < 0 or > 4096, NULL problems with count > 0);
+ * MP_ERR_UNSUPPORTED (host-only handle, or unaligned operands beyond the
+ * staging area); MP_ERR_CUDA.
+ */
+typedef struct {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    const float* C;
+    int64_t ldc;
+    float* D;
+    int64_t ldd;
+    float alpha, beta;
+} mp_gemm_problem;
+mp_status mp_gemm_grouped(mp_handle h, int32_t count, const mp_gemm_problem* problems, mp_stream stream);
+
+/*
+ * How mp_gemm_grouped runs a group (host only; any handle): one tile width
+ * bn for all problems, chosen by the cost model (the group's tiles spread
+ * over the SMs, against the longest tile).
+ */
+typedef struct {
+    int32_t bn;           /* output columns per tile: 64, 128 or 256 */
+    int32_t units;        /* tiles of all non-empty problems */
+    int32_t launches;     /* ceil(non-empty problems / 48) */
+    int32_t num_stages;
+    int32_t stage_bytes;
+    int32_t smem_bytes;
+    double cost_us;       /* model estimate */
+} mp_grouped_plan;
+mp_status mp_plan_grouped(mp_handle h, int32_t count, const mp_gemm_problem* problems, mp_grouped_plan* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,6 +23,7 @@ __all__ = [
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
     "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan", "mp_conv2d", "mp_plan_conv", "MpConvPlan",
+    "mp_gemm_grouped", "mp_plan_grouped", "MpGemmProblem", "MpGroupedPlan",
 ]
 
 MP_MAX_REGIONS = 4
@@ -95,6 +96,19 @@ class MpConvPlan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int32), ("useful", ctypes.c_double), ("cost_us", ctypes.c_double)]
 
 
+class MpGemmProblem(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
+
+class MpGroupedPlan(ctypes.Structure):
+    _fields_ = [("bn", ctypes.c_int32), ("units", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("num_stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("cost_us", ctypes.c_double)]
+
+
 class MPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -151,6 +165,9 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_gemm_b2b": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                  _vp, _i64, _vp, _i64, _f, _f, _f, _f, _i32, _vp], ctypes.c_int),
                 "mp_plan_b2b": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpB2BPlan)], ctypes.c_int),
+                "mp_gemm_grouped": ([_vp, _i32, ctypes.POINTER(MpGemmProblem), _vp], ctypes.c_int),
+                "mp_plan_grouped": ([_vp, _i32, ctypes.POINTER(MpGemmProblem), ctypes.POINTER(MpGroupedPlan)],
+                                    ctypes.c_int),
                 "mp_conv2d": ([_vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _i64,
                                _vp, _i64, _f, _f, _vp], ctypes.c_int),
                 "mp_plan_conv": ([_vp, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
@@ -352,6 +369,39 @@ def mp_plan_b2b(h: Handle, M: int, N0: int, N1: int, K0: int) -> MpB2BPlan:
     """How mp_gemm_b2b splits an (M, N0, N1, K0) problem (host only)."""
     out = MpB2BPlan()
     _check(library().mp_plan_b2b(h.ptr, M, N0, N1, K0, ctypes.byref(out)), "mp_plan_b2b")
+    return out
+
+
+def _problems(items):
+    """(A, B, C, D, alpha, beta) tuples of torch tensors -> MpGemmProblem array."""
+    arr = (MpGemmProblem * max(1, len(items)))()
+    for i, (A, B, C, D, alpha, beta) in enumerate(items):
+        M, N, K, c_ptr, ldc = _gemm_args(A, B, C, D, beta)
+        arr[i] = MpGemmProblem(M, N, K, A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"), c_ptr, ldc,
+                               D.data_ptr(), _ld(D, "D"), float(alpha), float(beta))
+    return arr
+
+
+def mp_gemm_grouped(h: Handle, items, stream=None) -> None:
+    """Every D_i = alpha_i*A_i@B_i + beta_i*C_i of a group of problems of any
+    shapes, in as few launches as possible.  `items`: (A, B, C, D, alpha, beta)."""
+    arr = _problems(items)
+    _check(library().mp_gemm_grouped(h.ptr, len(items), arr, _stream_ptr(stream)), "mp_gemm_grouped")
+
+
+def mp_plan_grouped(h: Handle, shapes) -> MpGroupedPlan:
+    """The plan of a group given as (M, N, K) shapes (host only; no operands
+    are read: the pointers are placeholders laid out without overlap)."""
+    arr = (MpGemmProblem * max(1, len(shapes)))()
+    base = 1 << 20
+    for i, (M, N, K) in enumerate(shapes):
+        a = base
+        b = a + 2 * M * K + 256
+        d = b + 2 * K * N + 256
+        base = d + 4 * M * N + 256
+        arr[i] = MpGemmProblem(M, N, K, a, max(K, 1), b, max(N, 1), None, 0, d, max(N, 1), 1.0, 0.0)
+    out = MpGroupedPlan()
+    _check(library().mp_plan_grouped(h.ptr, len(shapes), arr, ctypes.byref(out)), "mp_plan_grouped")
     return out
 
 

@@ -17,9 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmp.so")
 SOURCES = ["mp_api.cpp", "mp_planner.cpp", "mp_gemm.cu", "mp_gemm_act_f32.cu", "mp_gemm_bf16.cu", "mp_b2b.cu",
-           "mp_conv.cu", "mp_noalloc.cu"]
+           "mp_conv.cu", "mp_grouped.cu", "mp_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "mp_internal.h"), os.path.join(CSRC, "mp_kernel.cuh"), os.path.join(CSRC, "mp_b2b.cuh"),
-           os.path.join(CSRC, "mp_conv.cuh"),
+           os.path.join(CSRC, "mp_conv.cuh"), os.path.join(CSRC, "mp_grouped.cuh"),
            os.path.join(ROOT, "include", "mp.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

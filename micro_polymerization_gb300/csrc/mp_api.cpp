@@ -10,6 +10,8 @@
 #include <algorithm>
 #include <climits>
 
+#include <vector>
+
 #include "mp_internal.h"
 
 namespace {
@@ -366,6 +368,66 @@ mp_status mp_plan_conv(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, 
                        int64_t pad_h, int64_t pad_w, mp_conv_plan* out) {
     if (!h || !out) return MP_ERR_INVALID_ARG;
     return mp::plan_conv(h->hw, h->workspace_floats, N, H, W, C, K, R, S, pad_h, pad_w, out);
+}
+
+}  // extern "C"
+
+namespace {
+
+mp::GemmArgs problem_args(const mp_gemm_problem& q) {
+    return mp::GemmArgs{1, q.M, q.N, q.K, q.A, q.lda, 0, q.B, q.ldb, 0, q.C, q.ldc, 0, q.D, q.ldd, 0,
+                        q.alpha, q.beta, nullptr};
+}
+
+// Each problem by mp_gemm's rules; no output overlaps another problem's
+// operands or output.  Fills `live` with the non-empty problems.
+mp_status check_group(int32_t count, const mp_gemm_problem* probs, std::vector<mp_gemm_problem>& live) {
+    if (count < 0 || count > 4096 || (count > 0 && !probs)) return MP_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < count; i++) {
+        const mp_status st = check_args(problem_args(probs[i]));
+        if (st != MP_OK) return st;
+        if (probs[i].M > 0 && probs[i].N > 0) live.push_back(probs[i]);
+    }
+    const size_t n = live.size();
+    for (size_t i = 0; i < n; i++) {
+        const mp_gemm_problem& a = live[i];
+        const Span d = span_of(a.D, a.M, a.N, a.ldd, 4, 1, 0);
+        for (size_t j = 0; j < n; j++) {
+            if (j == i) continue;
+            const mp_gemm_problem& b = live[j];
+            if (overlap(d, span_of(b.D, b.M, b.N, b.ldd, 4, 1, 0))) return MP_ERR_INVALID_ARG;
+            if (b.K > 0 && (overlap(d, span_of(b.A, b.M, b.K, b.lda, 2, 1, 0)) ||
+                            overlap(d, span_of(b.B, b.K, b.N, b.ldb, 2, 1, 0))))
+                return MP_ERR_INVALID_ARG;
+            if (b.beta != 0.0f && overlap(d, span_of(b.C, b.M, b.N, b.ldc, 4, 1, 0))) return MP_ERR_INVALID_ARG;
+        }
+    }
+    return MP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mp_status mp_gemm_grouped(mp_handle h, int32_t count, const mp_gemm_problem* problems, mp_stream stream) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    std::vector<mp_gemm_problem> live;
+    mp_status st = check_group(count, problems, live);
+    if (st != MP_OK) return st;
+    if (live.empty()) return MP_OK;
+    if (h->host_only) return MP_ERR_UNSUPPORTED;
+    mp_grouped_plan plan;
+    st = mp::plan_grouped(h->hw, (int32_t)live.size(), live.data(), &plan);
+    if (st != MP_OK) return st;
+    return mp::device_run_grouped(h, plan, (int32_t)live.size(), live.data(), stream);
+}
+
+mp_status mp_plan_grouped(mp_handle h, int32_t count, const mp_gemm_problem* problems, mp_grouped_plan* out) {
+    if (!h || !out) return MP_ERR_INVALID_ARG;
+    std::vector<mp_gemm_problem> live;
+    mp_status st = check_group(count, problems, live);
+    if (st != MP_OK) return st;
+    return mp::plan_grouped(h->hw, (int32_t)live.size(), live.data(), out);
 }
 
 mp_status mp_check(mp_handle h, mp_stream stream) {

@@ -16,6 +16,7 @@
 #include "mp_kernel.cuh"
 #include "mp_b2b.cuh"
 #include "mp_conv.cuh"
+#include "mp_grouped.cuh"
 
 namespace mp {
 namespace dev {
@@ -99,7 +100,7 @@ struct DeviceState {
 // The dynamic shared memory of every instantiation of the persistent kernel.
 bool set_kernel_smem() {
     return set_poly_gemm_smem<0>() && set_poly_gemm_smem_act_f32() && set_poly_gemm_smem_bf16() && b2b::set_smem() &&
-           conv::set_smem();
+           conv::set_smem() && grp::set_smem();
 }
 
 // Split-K on chip: for S = 2..16, the CTAs that clusters of S CTAs of the
@@ -862,6 +863,81 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
     if (conv::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
     if (pl.splits > 1 && conv::launch_reduce(stream, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM: per-problem tensor maps in the kernel parameters, one launch
+// per 48 problems
+// ---------------------------------------------------------------------------
+mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& pl, int32_t count, const mp_gemm_problem* probs,
+                             void* stream_ptr) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    DeviceGuard g(s->device);
+    cudaStream_t stream = (cudaStream_t)stream_ptr;
+    static_assert(sizeof(grp::Params) <= 32764, "the problem table must fit the kernel parameters");
+    grp::Params* p = new (std::nothrow) grp::Params;
+    if (!p) return MP_ERR_NO_MEMORY;
+    int64_t used = 0;  // staging bytes taken by repacked operands (the whole group's)
+    mp_status st = MP_OK;
+    for (int32_t first = 0; first < count && st == MP_OK; first += grp::kMaxGroup) {
+        std::memset(p, 0, sizeof(*p));
+        const int32_t n = std::min<int32_t>(grp::kMaxGroup, count - first);
+        int units = 0;
+        for (int32_t j = 0; j < n && st == MP_OK; j++) {
+            const mp_gemm_problem& a = probs[first + j];
+            grp::Problem& q = p->prob[j];
+            const void* A = a.A;
+            const void* B = a.B;
+            int64_t lda = a.lda, ldb = a.ldb;
+            if (a.K > 0) {
+                if ((st = stage_if_unaligned(s, stream, A, lda, a.M, a.K, used)) != MP_OK) break;
+                if ((st = stage_if_unaligned(s, stream, B, ldb, a.K, a.N, used)) != MP_OK) break;
+                if (!encode_3d(s, &q.tmA, A, a.K, a.M, 1, lda * 2, round_up(a.M * lda * 2, 16), 64, 128) ||
+                    !encode_3d(s, &q.tmB, B, a.N, a.K, 1, ldb * 2, round_up(a.K * ldb * 2, 16), 64, 64)) {
+                    st = MP_ERR_CUDA;
+                    break;
+                }
+            }
+            q.tma_d = (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0) ? 1 : 0;
+            if (q.tma_d &&
+                !encode_3d_f32(s, &q.tmD, a.D, a.N, a.M, 1, a.ldd * 4, round_up(a.M * a.ldd * 4, 16), 32, 32)) {
+                st = MP_ERR_CUDA;
+                break;
+            }
+            q.C = a.C;
+            q.D = a.D;
+            q.ldc = a.ldc;
+            q.ldd = a.ldd;
+            q.M = (int)a.M;
+            q.N = (int)a.N;
+            q.K = (int)a.K;
+            q.tiles_n = (int)cdiv(a.N, pl.bn);
+            q.tile0 = units;
+            q.alpha = a.alpha;
+            q.beta = a.beta;
+            q.vec_c = (a.C && ((uintptr_t)a.C & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
+            units += (int)(cdiv(a.M, 128) * q.tiles_n);
+        }
+        if (st != MP_OK) break;
+        p->count = n;
+        p->units = units;
+        p->bn = pl.bn;
+        p->num_stages = pl.num_stages;
+        p->stage_bytes = pl.stage_bytes;
+        p->err = s->err;
+        p->wait_limit_ns = s->wait_limit_ns;
+        if (s->log)
+            std::fprintf(stderr, "[mp] grouped problems=%d bn=%d units=%d\n", n, pl.bn, units);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)std::min<int64_t>(units, s->num_sms));
+        cfg.blockDim = dim3(grp::kThreads);
+        cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+        cfg.stream = stream;
+        if (grp::launch(cfg, *p) != cudaSuccess) st = MP_ERR_CUDA;
+    }
+    delete p;
+    return st;
 }
 
 }  // namespace mp

@@ -137,4 +137,10 @@ mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, in
                     int64_t R, int64_t S, int64_t pad_h, int64_t pad_w, mp_conv_plan* out);
 mp_status device_run_conv(mp_handle h, const mp_conv_plan& plan, const ConvArgs& a);
 
+// Grouped GEMM (mp_gemm_grouped): planner (mp_planner.cpp) and launches
+// (mp_gemm.cu).  `probs` holds only non-empty problems.
+mp_status plan_grouped(const mp_hw& hw, int32_t count, const mp_gemm_problem* probs, mp_grouped_plan* out);
+mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& plan, int32_t count, const mp_gemm_problem* probs,
+                             void* stream);
+
 }  // namespace mp

@@ -31,6 +31,7 @@
 #include "mp_internal.h"
 #include "mp_b2b.cuh"
 #include "mp_conv.cuh"
+#include "mp_grouped.cuh"
 
 namespace mp {
 namespace {
@@ -771,6 +772,55 @@ mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, in
     best.ksteps = (int32_t)ksteps;
     best.grid = (int32_t)std::min<int64_t>(best.units, sms);
     best.smem_bytes = conv::smem_bytes(best.num_stages, best.stage_bytes);
+    *out = best;
+    return MP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM (BladeDISC v0.2.0 notes, GEMM merging, any shapes)
+// ---------------------------------------------------------------------------
+// One micro-kernel (128 x bn) for the whole group.  Cost: the group's tile
+// work spread over the SMs (or the longest tile, if that is longer), plus
+// one fill and launch per 48 problems.  Step times as for the other kernels.
+mp_status plan_grouped(const mp_hw& hw, int32_t count, const mp_gemm_problem* probs, mp_grouped_plan* out) {
+    if (!out || count < 0 || (count > 0 && !probs)) return MP_ERR_INVALID_ARG;
+    mp_grouped_plan best;
+    std::memset(&best, 0, sizeof best);
+    best.cost_us = 1e300;
+    const int sms = std::max(1, hw.num_pe);
+    const double hbm = hw.hbm_gbs > 0 ? hw.hbm_gbs : 6700.0;
+    int64_t maxn = 64;
+    for (int32_t i = 0; i < count; i++) maxn = std::max<int64_t>(maxn, probs[i].N);
+    for (int bn : {64, 128, 256}) {
+        if (bn > 64 && bn / 2 >= ((maxn + 63) / 64) * 64) continue;
+        const double step = std::max(kStepFloorUs, 0.40 * bn / 256.0);
+        const double epi = 1.6 * bn / 256.0;
+        int64_t units = 0;
+        double work = 0.0, longest = 0.0;
+        for (int32_t i = 0; i < count; i++) {
+            const mp_gemm_problem& q = probs[i];
+            const int64_t tiles = ((q.M + 127) / 128) * ((q.N + bn - 1) / bn);
+            const double t = (double)((q.K + 63) / 64) * step + epi;
+            units += tiles;
+            work += (double)tiles * t;
+            longest = std::max(longest, t);
+        }
+        const int64_t active = std::max<int64_t>(1, std::min<int64_t>(units, sms));
+        double bytes = 0.0;  // D of every problem, at HBM speed: the floor of a store-bound group
+        for (int32_t i = 0; i < count; i++) bytes += 4.0 * (double)probs[i].M * (double)probs[i].N;
+        const int launches = (count + grp::kMaxGroup - 1) / grp::kMaxGroup;
+        const double cost = std::max(std::max(work / (double)active, longest), bytes / (hbm * 1e3)) + 3.0 * launches;
+        if (cost < best.cost_us * (1.0 - 1e-9)) {
+            best.cost_us = cost;
+            best.bn = bn;
+            best.units = (int32_t)std::min<int64_t>(units, ((int64_t)1 << 31) - 1);
+            best.launches = launches;
+            best.stage_bytes = 16384 + bn * 128;
+            best.num_stages =
+                std::min(grp::kMaxStages, (grp::kSmemLimit - 4 * grp::kEpiSlabBytes - 2048) / best.stage_bytes);
+        }
+    }
+    best.smem_bytes = grp::smem_bytes(best.num_stages, best.stage_bytes);
     *out = best;
     return MP_OK;
 }

@@ -197,6 +197,18 @@ def conv_resolution(count: int = 64) -> List[Conv]:
 CONV_WORKLOADS = {"conv_resolution": conv_resolution}
 
 
+def grouped_experts(count: int = 48) -> List[Gemm]:
+    """Non-uniform merged problems: 48 expert GEMMs of one layer, tokens per
+    expert uniform on [1, 512], (N, K) = (2048, 1024).  BladeDISC's merge of
+    same-shape GEMMs into a batched GEMM does not apply (every M differs); a
+    grouped GEMM runs them in one launch."""
+    rng = np.random.default_rng(1000 + 900)
+    return [Gemm(int(rng.integers(1, 513)), 2048, 1024, seed=1000 + 900 + 7 * i) for i in range(count)]
+
+
+GROUPED_WORKLOADS = {"grouped_experts": grouped_experts}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a CPU tensor as numpy uint16 (no conversion)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -39,6 +39,9 @@ What each routine follows (page titles and sections):
     ``conv2d_magnitude`` is the same sum over absolute values (the
     tolerance scale, as ``magnitude`` for a GEMM); ``im2col_nhwc`` builds the
     explicit [N*P*Q, R*S*C] matrix that a GEMM-based convolution multiplies.
+  * ``gemm_group`` -- a group of independent GEMMs of different shapes
+    (BladeDISC v0.2.0 notes, GEMM merging, widened from same-shape problems
+    to any shapes): the definition applied to each problem.
 """
 from __future__ import annotations
 
@@ -392,3 +395,9 @@ def im2col_nhwc(X, R, S, pad_h=1, pad_w=1):
                     if 0 <= w < W:
                         out[:, p, q, r, s, :] = X[:, h, w, :]
     return out.reshape(N * P * Q, R * S * C)
+
+
+def gemm_group(problems):
+    """[(D_i, magnitude_i)] for problems given as (A_bits, B_bits, C, alpha,
+    beta) tuples: each problem's own definition, nothing shared."""
+    return [(gemm(A, B, C, alpha, beta), magnitude(A, B, C, beta)) for (A, B, C, alpha, beta) in problems]

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import micro_polymerization_gb300 as mp
@@ -259,4 +260,36 @@ def test_conv_plan_rules():
     assert p.units == 0 and p.grid == 0
     with pytest.raises(mp.MPError):
         mp.mp_plan_conv(h, 1, 5, 5, 8, 8, 0, 3)
+    h.close()
+
+
+def test_grouped_argument_checks_and_plan():
+    lib = mp.library()
+    h = _host()
+    P = mp.MpGemmProblem
+
+    def call(probs):
+        arr = (P * max(1, len(probs)))(*probs)
+        return lib.mp_gemm_grouped(h.ptr, len(probs), arr, None)
+
+    a0 = P(100, 96, 80, 0x10000, 80, 0x100000, 96, None, 0, 0x200000, 96, 1.0, 0.0)
+    a1 = P(33, 17, 5, 0x300000, 5, 0x310000, 17, 0x320000, 17, 0x330000, 17, 1.0, 0.5)
+    assert call([a0, a1]) == mp.MP_ERR_UNSUPPORTED  # valid; no device
+    assert call([]) == mp.MP_OK
+    assert call([P(0, 5, 5, 0, 5, 0, 5, None, 0, 0, 5, 1.0, 0.0)]) == mp.MP_OK  # only empty problems
+    # One problem breaking mp_gemm's rules.
+    assert call([a0, P(10, 10, 10, 0x10000, 9, 0x20000, 10, None, 0, 0x500000, 10, 1.0, 0.0)]) == mp.MP_ERR_INVALID_ARG
+    # Output of one problem overlapping another's output or operands.
+    clash_d = P(10, 10, 10, 0x600000, 10, 0x610000, 10, None, 0, 0x200000 + 4 * 96, 10, 1.0, 0.0)
+    assert call([a0, clash_d]) == mp.MP_ERR_INVALID_ARG
+    clash_a = P(10, 10, 10, 0x600000, 10, 0x610000, 10, None, 0, 0x10000 + 64, 10, 1.0, 0.0)
+    assert call([a0, clash_a]) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_gemm_grouped(h.ptr, -1, None, None) == mp.MP_ERR_INVALID_ARG
+    assert lib.mp_gemm_grouped(h.ptr, 2, None, None) == mp.MP_ERR_INVALID_ARG
+    # Plan: one tile width, the group's tiles, one launch per 48 problems.
+    shapes = [(int(m), 2048, 1024) for m in np.random.default_rng(0).integers(1, 513, 100)]
+    p = mp.mp_plan_grouped(h, shapes)
+    assert p.bn in (64, 128, 256) and p.launches == 3
+    assert p.units == sum(-(-m // 128) * -(-n // p.bn) for m, n, _ in shapes)
+    assert p.smem_bytes <= 232448 and p.stage_bytes == 16384 + 128 * p.bn and p.cost_us > 0
     h.close()

@@ -570,3 +570,25 @@ def test_conv_ones_closed_form():
     for p in range(H):
         for q in range(W):
             assert np.all(D[0, p, q] == C * valid(p, H) * valid(q, W))
+
+
+def test_gemm_group_is_each_problem_and_matches_batched_case():
+    """A group of same-shape problems is the batched GEMM (the merge of the
+    BladeDISC notes): stacked, the group's results equal one fp64 product per
+    problem computed with numpy on the widened values."""
+    rng = np.random.default_rng(31)
+    probs = []
+    for i in range(5):
+        A = oracle_bits(rng, (7, 11))
+        B = oracle_bits(rng, (11, 6))
+        C = rng.uniform(-1, 1, size=(7, 6)).astype(np.float32)
+        probs.append((A, B, C, 1.0 + i, 0.5))
+    out = oracle.gemm_group(probs)
+    for (A, B, C, al, be), (D, mag) in zip(probs, out):
+        ref = al * (oracle.bf16_bits_to_f64(A) @ oracle.bf16_bits_to_f64(B)) + be * C.astype(np.float64)
+        assert np.allclose(D, ref, rtol=1e-13, atol=1e-13)
+        assert np.all(mag >= np.abs(D - be * C) / al - 1e-12)
+    # Different shapes in one group: each keeps its own shape.
+    shapes = [(3, 5, 2), (1, 64, 9), (17, 3, 33)]
+    probs = [(oracle_bits(rng, (m, k)), oracle_bits(rng, (k, n)), None, 1.0, 0.0) for m, n, k in shapes]
+    assert [d.shape for d, _ in oracle.gemm_group(probs)] == [(m, n) for m, n, _ in shapes]
