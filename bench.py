@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the persistent kernel from one ncu capture (bytes per
 # algorithmic byte, i.e. dram read+write / (2MK+2KN+4MN)), valid only for the
 # kernel source it was taken on; see profiles/.
-TRAFFIC_RECORD = {"kernel_sha1": "e44c9c79e3f07463e81aa32fd04b4de70d00f546", "dram_bytes_per_alg_byte": 0.384}
+TRAFFIC_RECORD = {"kernel_sha1": "abbd3ffab242de4856a0ef4f576d18e465f09369", "dram_bytes_per_alg_byte": 0.384}
 
 
 # --epilogue: (activation, bf16 D) of mp_gemm_ex.
