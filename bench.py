@@ -670,6 +670,9 @@ def run_b2b(args):
     torch.cuda.synchronize()
     if mp.mp_check(h) != 0:
         raise RuntimeError("device status word set during warm-up")
+    # The fused kernel itself (forced), per launch, for its roofline.
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
+    step(fused)
     n = len(fused)
     per_launch = np.zeros(n)
     reps = max(1, min(args.steps, 20))
@@ -679,6 +682,10 @@ def run_b2b(args):
         torch.cuda.synchronize()
         per_launch += np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
     per_launch /= reps
+    ms_kernel = timed(fused, args.steps)
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_AUTO)
+    modes = [mp.mp_plan_b2b(h, b.M, b.N0, b.N1, b.K0).mode for b in bs]
+    step(fused)
     with ClockSampler(local) as clocks:
         ms_step = timed(fused, args.steps)
     ms_unfused = timed(unfused, args.steps)
@@ -755,6 +762,10 @@ def run_b2b(args):
                         "value": round(flops_step * world / (ms_unfused * 1e-3) / 1e12, 3),
                         "calls": "mp_gemm_ex (bf16 D0, activation) + mp_gemm",
                         "fused_speedup": round(ms_unfused / ms_step, 3)},
+            "forms": {"fused_kernel": modes.count(mp.MP_B2B_FUSED),
+                      "two_launch": modes.count(mp.MP_B2B_TWO_LAUNCH),
+                      "fused_kernel_only_ms_per_step": round(ms_kernel, 4),
+                      "note": "value times mp_gemm_b2b with its automatic choice of form per problem"},
             "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
                                    "sum_troof_over_sum_t": round(float(troof.sum() / per_launch.sum()), 4),
                                    "peaks": peak_src},

@@ -361,7 +361,9 @@ const char* mp_status_string(mp_status s);
  * elements.  D0 is never written to memory: each 128-row block of it stays
  * in the producing CTA's shared memory, rounded to bf16 (the type of the
  * second GEMM's operand), and feeds that CTA's second GEMM (the summary's
- * threadblock residence).  That needs N0 <= 256.  act0 is MP_ACT_NONE,
+ * threadblock residence).  That needs N0 <= 256.  For shapes where two
+ * launches are faster (few row blocks), D0 goes through a bf16 scratch
+ * buffer instead (mp_set_b2b_mode).  act0 is MP_ACT_NONE,
  * MP_ACT_RELU or MP_ACT_GELU (the epilogue variants' activations).  C0 is not
  * read when beta0 == 0, nor C1 when beta1 == 0; C1 may be D1 (same pointer
  * and ld).  Asynchronous on `stream`, like mp_gemm.
@@ -396,9 +398,26 @@ typedef struct {
     int32_t num_stages;   /* shared-memory ring depth */
     int32_t stage_bytes;  /* bytes per ring stage */
     int32_t smem_bytes;   /* dynamic shared memory per CTA */
-    double cost_us;       /* model estimate */
+    double cost_us;       /* model estimate of the fused kernel */
+    int32_t mode;         /* what mp_gemm_b2b runs: MP_B2B_FUSED or MP_B2B_TWO_LAUNCH */
+    double two_launch_cost_us;  /* model estimate of the two-launch form */
 } mp_b2b_plan;
 mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
+
+/*
+ * Which form mp_gemm_b2b runs.  MP_B2B_FUSED: the fused kernel (D0 stays on
+ * chip).  MP_B2B_TWO_LAUNCH: mp_gemm_ex writes D0 = act0(alpha0*A0*W0 +
+ * beta0*C0) in bf16 (the same rounding as on chip) to a scratch buffer of the
+ * handle, grown on first need, then mp_gemm runs the second GEMM.  With few
+ * row blocks the fused kernel runs each block's first GEMM serially on one
+ * SM and the two launches are faster.  MP_B2B_AUTO (the default) picks
+ * per shape, comparing the two forms' cost models (mp_plan_b2b reports the
+ * choice).  Errors: MP_ERR_INVALID_ARG (unknown mode).
+ */
+#define MP_B2B_AUTO 0
+#define MP_B2B_FUSED 1
+#define MP_B2B_TWO_LAUNCH 2
+mp_status mp_set_b2b_mode(mp_handle h, int32_t mode);
 
 /*
  * 2-D convolution, stride 1, zero padding, NHWC, as an implicit GEMM (the

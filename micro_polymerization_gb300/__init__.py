@@ -22,7 +22,8 @@ __all__ = [
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
-    "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan", "mp_conv2d", "mp_plan_conv", "MpConvPlan",
+    "mp_gemm_b2b", "mp_plan_b2b", "MpB2BPlan", "mp_set_b2b_mode", "MP_B2B_AUTO", "MP_B2B_FUSED",
+    "MP_B2B_TWO_LAUNCH", "mp_conv2d", "mp_plan_conv", "MpConvPlan",
     "mp_gemm_grouped", "mp_plan_grouped", "MpGemmProblem", "MpGroupedPlan",
 ]
 
@@ -84,7 +85,8 @@ class MpB2BPlan(ctypes.Structure):
     _fields_ = [("n0p", ctypes.c_int32), ("bn1", ctypes.c_int32), ("chunks", ctypes.c_int32),
                 ("mblocks", ctypes.c_int32), ("cpg", ctypes.c_int32), ("units", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("num_stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("cost_us", ctypes.c_double)]
+                ("smem_bytes", ctypes.c_int32), ("cost_us", ctypes.c_double), ("mode", ctypes.c_int32),
+                ("two_launch_cost_us", ctypes.c_double)]
 
 
 class MpConvPlan(ctypes.Structure):
@@ -165,6 +167,7 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_gemm_b2b": ([_vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                  _vp, _i64, _vp, _i64, _f, _f, _f, _f, _i32, _vp], ctypes.c_int),
                 "mp_plan_b2b": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpB2BPlan)], ctypes.c_int),
+                "mp_set_b2b_mode": ([_vp, _i32], ctypes.c_int),
                 "mp_gemm_grouped": ([_vp, _i32, ctypes.POINTER(MpGemmProblem), _vp], ctypes.c_int),
                 "mp_plan_grouped": ([_vp, _i32, ctypes.POINTER(MpGemmProblem), ctypes.POINTER(MpGroupedPlan)],
                                     ctypes.c_int),
@@ -363,6 +366,14 @@ def mp_gemm_b2b(h: Handle, A0, W0, C0, W1, C1, D1, alpha0: float = 1.0, beta0: f
                                float(alpha0), float(beta0), float(alpha1), float(beta1), int(act0),
                                _stream_ptr(stream))
     _check(st, "mp_gemm_b2b")
+
+
+MP_B2B_AUTO, MP_B2B_FUSED, MP_B2B_TWO_LAUNCH = 0, 1, 2
+
+
+def mp_set_b2b_mode(h: Handle, mode: int) -> None:
+    """MP_B2B_AUTO (default), MP_B2B_FUSED or MP_B2B_TWO_LAUNCH for mp_gemm_b2b."""
+    _check(library().mp_set_b2b_mode(h.ptr, int(mode)), "mp_set_b2b_mode")
 
 
 def mp_plan_b2b(h: Handle, M: int, N0: int, N1: int, K0: int) -> MpB2BPlan:

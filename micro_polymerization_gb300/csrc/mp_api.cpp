@@ -169,6 +169,30 @@ mp_status check_conv(const mp::ConvArgs& a) {
     return MP_OK;
 }
 
+// The fused plan and the form mp_gemm_b2b runs.  The two-launch form costs
+// the GEMM planner's estimates of both GEMMs plus 6.8 us, the fused kernel
+// its own estimate plus 3.3 us: fixed costs the two models leave out (the
+// launches, fill and drain), fitted to measured pairs on GB300.
+mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
+    mp_status st = mp::plan_b2b(h->hw, M, N0, N1, K0, out);
+    if (st != MP_OK) return st;
+    mp_plan_info p0, p1;
+    const int64_t k0 = N0 > 0 ? K0 : 0;
+    double two = 6.8;
+    if (N0 > 0) {
+        if ((st = mp::plan_shape(h, 1, M, N0, k0, &p0)) != MP_OK) return st;
+        two += p0.cost_us;
+    }
+    if ((st = mp::plan_shape(h, 1, M, N1, N0, &p1)) != MP_OK) return st;
+    two += p1.cost_us;
+    out->two_launch_cost_us = two;
+    if (h->b2b_mode != MP_B2B_AUTO)
+        out->mode = h->b2b_mode;
+    else
+        out->mode = (out->cost_us + 3.3 <= two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
+    return MP_OK;
+}
+
 mp_status run(mp_handle h, const mp::GemmArgs& a) {
     if (!h) return MP_ERR_INVALID_ARG;
     mp_status st = check_args(a);
@@ -338,14 +362,20 @@ mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0
     if (M == 0 || N1 == 0) return MP_OK;
     if (h->host_only) return MP_ERR_UNSUPPORTED;
     mp_b2b_plan plan;
-    st = mp::plan_b2b(h->hw, M, N0, N1, K0, &plan);
+    st = plan_b2b_mode(h, M, N0, N1, K0, &plan);
     if (st != MP_OK) return st;
-    return mp::device_run_b2b(h, plan, a);
+    return plan.mode == MP_B2B_TWO_LAUNCH ? mp::device_run_b2b_two(h, a) : mp::device_run_b2b(h, plan, a);
 }
 
 mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     if (!h || !out) return MP_ERR_INVALID_ARG;
-    return mp::plan_b2b(h->hw, M, N0, N1, K0, out);
+    return plan_b2b_mode(h, M, N0, N1, K0, out);
+}
+
+mp_status mp_set_b2b_mode(mp_handle h, int32_t mode) {
+    if (!h || mode < MP_B2B_AUTO || mode > MP_B2B_TWO_LAUNCH) return MP_ERR_INVALID_ARG;
+    h->b2b_mode = mode;
+    return MP_OK;
 }
 
 mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,

@@ -95,6 +95,9 @@ struct DeviceState {
     // Clusters of two CTAs of k_poly_gemm that can be resident at once (0:
     // paired launches disabled).
     int max_pairs = 0;
+    // bf16 D0 of the two-launch form of mp_gemm_b2b (grown on first need).
+    void* b2b_scratch = nullptr;
+    size_t b2b_scratch_bytes = 0;
 };
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
@@ -387,6 +390,7 @@ void device_destroy(mp_handle h) {
         cudaFree(s->cnt);
         cudaFree(s->err);
         cudaFree(s->staging);
+        cudaFree(s->b2b_scratch);
     }
     delete[] s->tm_cache;
     delete s;
@@ -774,6 +778,41 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     cfg.stream = stream;
     if (b2b::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
+}
+
+// The two-launch form of a back-to-back pair: the first GEMM with the
+// activation and a bf16 D (the rounding D0 gets on chip) into the handle's
+// scratch buffer, then the second GEMM reading it.  Both launches go to the
+// same stream, so the second reads D0 after the first has written it.
+mp_status device_run_b2b_two(mp_handle h, const B2BArgs& a) {
+    DeviceState* s = h->dev;
+    if (!s) return MP_ERR_UNSUPPORTED;
+    DeviceGuard g(s->device);
+    const int64_t ld0 = round_up(std::max<int64_t>(a.N0, 1), 8);
+    const size_t bytes = (size_t)(a.M * ld0 * 2);
+    if (bytes > s->b2b_scratch_bytes) {
+        // cudaFree waits for the device, so no launch still reads the old buffer.
+        cudaFree(s->b2b_scratch);
+        s->b2b_scratch = nullptr;
+        s->b2b_scratch_bytes = 0;
+        if (cudaMalloc(&s->b2b_scratch, bytes) != cudaSuccess) return MP_ERR_NO_MEMORY;
+        s->b2b_scratch_bytes = bytes;
+    }
+    mp_status st = MP_OK;
+    if (a.N0 > 0) {
+        GemmArgs g0{1, a.M, a.N0, a.K0, a.A0, a.lda0, 0, a.W0, a.ldw0, 0, a.C0, a.ldc0, 0,
+                    static_cast<float*>(s->b2b_scratch), ld0, 0, a.alpha0, a.beta0, a.stream,
+                    a.act0 | MP_EPI_OUT_BF16};
+        mp_plan_info p0;
+        if ((st = validate_args(g0)) != MP_OK || (st = plan_shape(h, 1, a.M, a.N0, a.K0, &p0)) != MP_OK ||
+            (st = device_run(h, p0, g0)) != MP_OK)
+            return st;
+    }
+    GemmArgs g1{1, a.M, a.N1, a.N0, s->b2b_scratch, ld0, 0, a.W1, a.ldw1, 0, a.C1, a.ldc1, 0, a.D1, a.ldd1, 0,
+                a.alpha1, a.beta1, a.stream, 0};
+    mp_plan_info p1;
+    if ((st = validate_args(g1)) != MP_OK || (st = plan_shape(h, 1, a.M, a.N1, a.N0, &p1)) != MP_OK) return st;
+    return device_run(h, p1, g1);
 }
 
 // ---------------------------------------------------------------------------

@@ -53,6 +53,7 @@ struct mp_handle_s {
     int32_t force_kernel = -1;
     int32_t force_splits = 0;
     int32_t plan_mode = MP_PLAN_MIKPOLY;
+    int32_t b2b_mode = MP_B2B_AUTO;
 
     // Plan cache: shapes repeat in dynamic workloads; a hit skips the search.
     std::vector<mp::PlanCacheEntry> cache;
@@ -121,6 +122,8 @@ struct B2BArgs {
 };
 mp_status plan_b2b(const mp_hw& hw, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out);
 mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& plan, const B2BArgs& a);
+// The same pair as two launches through a bf16 scratch buffer for D0.
+mp_status device_run_b2b_two(mp_handle h, const B2BArgs& a);
 
 // Implicit-GEMM convolution (mp_conv2d): planner (mp_planner.cpp) and launch
 // (mp_gemm.cu).

@@ -181,6 +181,23 @@ def test_b2b_argument_checks():
     h.close()
 
 
+def test_b2b_form_choice():
+    """Few row blocks: two launches; many: the fused kernel; a forced mode wins."""
+    h = _host()
+    assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
+    assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_FUSED
+    for M in (1, 512, 4096, 100352):
+        p = mp.mp_plan_b2b(h, M, 64, 256, 256)
+        assert p.two_launch_cost_us > 0 and p.cost_us > 0
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
+    assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_FUSED
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_TWO_LAUNCH)
+    assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_TWO_LAUNCH
+    with pytest.raises(mp.MPError):
+        mp.mp_set_b2b_mode(h, 3)
+    h.close()
+
+
 def test_b2b_plan_rules():
     h = _host()
     for M, N0, N1, K0 in [(1, 1, 1, 1), (1000, 256, 768, 768), (128 * 400, 64, 256, 256), (256, 128, 4096, 64),

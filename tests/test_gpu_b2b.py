@@ -19,6 +19,15 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
+@pytest.fixture(autouse=True)
+def fused_form():
+    """These tests check the fused kernel itself: force it (the automatic
+    choice would take the two-launch form for small M), then restore."""
+    mp.mp_set_b2b_mode(handle(), mp.MP_B2B_FUSED)
+    yield
+    mp.mp_set_b2b_mode(handle(), mp.MP_B2B_AUTO)
+
+
 def _bits(t):
     return wl.bf16_bits(t.cpu())
 
@@ -129,3 +138,40 @@ def test_b2b_identity_w1_matches_fused_epilogue_gemm():
     # rounding step in case the two launches accumulate K in another order.
     assert torch.all((got - want).abs() <= want.abs() * 2.0 ** -7)
     assert (got == want).double().mean() > 0.99
+
+
+def test_b2b_adapter_workload_sampled():
+    """Full-size problems of the b2b_adapter workload (the largest M, and a
+    mid-size one) on sampled rows, with the bench's parameters."""
+    bs = sorted(wl.b2b_adapter(), key=lambda b: b.M)
+    rng = np.random.default_rng(1)
+    for b in (bs[-1], bs[len(bs) // 2]):
+        rows = np.unique(np.concatenate([[0, b.M - 1], rng.integers(0, b.M, 48)]))
+        got, ref, bound = run_b2b(b, rows=rows)
+        ok, worst = oracle.within_b2b(got, ref, bound)
+        assert ok, (b, worst)
+
+
+@pytest.mark.parametrize("shape", [(300, 96, 520, 200, 2), (129, 256, 768, 768, 1), (200, 17, 33, 5, 0),
+                                   (150, 64, 200, 0, 1), (4096, 256, 768, 768, 1)])
+def test_b2b_two_launch_form(shape):
+    """The two-launch form (bf16 D0 in the handle's scratch buffer) meets the
+    same bound."""
+    M, N0, N1, K0, act = shape
+    mp.mp_set_b2b_mode(handle(), mp.MP_B2B_TWO_LAUNCH)
+    check(wl.B2B(M, N0, N1, K0, alpha0=1.25, beta0=0.5, alpha1=0.75, beta1=-0.5, act0=act, seed=M + K0))
+
+
+def test_b2b_auto_choice_runs_the_planned_form():
+    """AUTO takes the form mp_plan_b2b reports: two launches for few row
+    blocks, the fused kernel for many; both within the bound."""
+    mp.mp_set_b2b_mode(handle(), mp.MP_B2B_AUTO)
+    small = wl.B2B(2048, 256, 768, 768, act0=1, seed=21)
+    large = wl.B2B(128 * 400, 64, 256, 256, act0=1, seed=22)
+    assert mp.mp_plan_b2b(handle(), small.M, small.N0, small.N1, small.K0).mode == mp.MP_B2B_TWO_LAUNCH
+    assert mp.mp_plan_b2b(handle(), large.M, large.N0, large.N1, large.K0).mode == mp.MP_B2B_FUSED
+    check(small)
+    rows = np.arange(0, large.M, 331)
+    got, ref, bound = run_b2b(large, rows=rows)
+    ok, worst = oracle.within_b2b(got, ref, bound)
+    assert ok, worst

@@ -85,3 +85,26 @@ def test_grouped_integer_exact():
     for it, (A, B, C) in zip(items, host):
         ref = oracle.gemm(_bits(A), _bits(B), C.numpy(), 1.0, 1.0)
         assert np.array_equal(it[3].cpu().numpy().astype(np.float64), ref)
+
+
+def test_grouped_experts_workload_sampled():
+    """The full grouped_experts workload (48 problems, one call as the bench
+    times it), every problem checked on sampled rows against the oracle."""
+    gs = wl.grouped_experts()
+    rng = np.random.default_rng(3)
+    items, host = [], []
+    for g in gs:
+        A, B, _ = wl.make_operands(g)
+        D = torch.full((g.M, g.N), float("nan"), device=DEV)
+        items.append((A.to(DEV), B.to(DEV), None, D, g.alpha, g.beta))
+        host.append((A, B))
+    mp.mp_gemm_grouped(handle(), items)
+    torch.cuda.synchronize()
+    assert mp.mp_check(handle()) == 0
+    for g, it, (A, B) in zip(gs, items, host):
+        rows = np.unique(np.concatenate([[0, g.M - 1], rng.integers(0, g.M, 6)]))
+        Ab = _bits(A)[rows]
+        ref = oracle.gemm(Ab, _bits(B))
+        mag = oracle.magnitude(Ab, _bits(B))
+        ok, worst = oracle.within_bound(it[3].cpu().numpy()[rows], ref, mag)
+        assert ok, (g, worst)
