@@ -271,6 +271,40 @@ def run_mp(args):
     flops_step = sum(g.flops for g in gs)
     value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
 
+    # The same problems as one grouped submission (only when they are all
+    # single GEMMs with the plain epilogue): informational, not the headline,
+    # which times the separate calls above.
+    as_group = None
+    if not epi and all(g.batch == 1 for g in gs) and not args.no_group:
+        arr = (mp.MpGemmProblem * len(ops))()
+        for i, (g, A, B, C, D) in enumerate(ops):
+            arr[i] = mp.MpGemmProblem(g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
+                                      C.data_ptr() if C is not None else None, g.N, D.data_ptr(), g.N,
+                                      g.alpha, g.beta)
+
+        def group_step():
+            st = lib.mp_gemm_grouped(h.ptr, len(ops), arr, sp)
+            if st != 0:
+                raise mp.MPError(st, "mp_gemm_grouped")
+
+        for _ in range(3):
+            group_step()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            group_step()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        ms_group = g0.elapsed_time(g1) / args.steps
+        as_group = {"ms_per_step": round(ms_group, 4),
+                    "value": round(sum(g.flops for g in gs) / (ms_group * 1e-3) / 1e12, 3),
+                    "launches_per_step": -(-len(ops) // 48),
+                    "note": "the same independent problems as one mp_gemm_grouped call per step; "
+                            "not the headline, which times one mp_gemm call per problem"}
+        if mp.mp_check(h) != 0:
+            raise RuntimeError("device status word set by the grouped submission")
+
     # Per-shape roofline fractions (from the per-launch times).
     troof = np.array([roofline_us(g, peaks, d_bytes)[0] for g in gs])
     bounds = [roofline_us(g, peaks, d_bytes)[1] for g in gs]
@@ -408,6 +442,7 @@ def run_mp(args):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "launches": len(sel), "kernel": "k_poly_gemm", "peak_source": peak_src},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "as_one_group": as_group,
             "plan_us": round(plan_us, 3) if plan_us is not None else None,
             "cost_model": "calibrated" if calib else "analytic",
             "clocks": clocks.summary(), "impl": "mp",
@@ -1188,6 +1223,7 @@ def main(argv=None):
     ap.add_argument("--dump", default=None, help="write per-GEMM time, roofline and plan (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-group", action="store_true", help="skip the informational grouped submission")
     ap.add_argument("--no-calib", action="store_true", help="plan with the analytic cost model")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
