@@ -331,7 +331,8 @@ mp_status mp_force_plan(mp_handle h, int32_t kernel, int32_t splits);
 
 /*
  * Test hook for failure detection: with enable != 0 the next launch on this
- * handle withholds one shared-memory stage of its first work unit, so the
+ * handle (of any kernel: GEMM, fused pair, convolution, grouped GEMM)
+ * withholds one shared-memory stage of its first work unit, so the
  * consumer's bounded wait runs out after limit_ns nanoseconds (0 keeps the
  * handle's limit, 1 s by default; a positive value also becomes the limit of
  * later launches).  The kernel then stops cleanly and mp_check reports

@@ -274,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         // counts them).
         const uint32_t pid = warp == 0 ? 0u : 1u;
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
+        // Test hook (failure detection): warp 0 leaves its first stage empty,
+        // so the MMA issuer's bounded wait on it runs out.
+        bool withhold = pid == 0 && p.inject_timeout != 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int mb = u / groups, grp = u % groups;
             const int m0 = mb * 128;
@@ -286,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
                 int ok = 1;
                 if (lane == 0) ok = wait_fast(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_out;
+                if (withhold) {  // neither copies nor an arrive: the stage never completes
+                    withhold = false;
+                    continue;
+                }
                 const uint32_t st = ring0 + (uint32_t)stage * sb;
                 uint32_t bytes;
                 if (i < nk0) {

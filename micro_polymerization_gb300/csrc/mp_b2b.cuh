@@ -52,6 +52,7 @@ struct alignas(128) Params {
     int vec_c0, vec_c1;  // C rows allow 16-byte loads
     int* err;            // the handle's status word
     unsigned long long wait_limit_ns;
+    int inject_timeout;  // test hook: producer warp 0 withholds its first stage
 };
 
 // Dynamic shared memory of a launch: operand ring, D0 operand (128 rows of

@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         // warp 0 when g is even, to warp 6 when it is odd.
         const uint32_t pid = warp == 0 ? 0u : 1u;
         uint32_t g = 0, armed_mask = 0, armed_ph = 0;
+        // Test hook (failure detection): warp 0 leaves its first stage empty,
+        // so the MMA issuer's bounded wait on it runs out.
+        bool withhold = pid == 0 && p.inject_timeout != 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const Tile t = decode_tile(p, u / p.splits);
             int kb0, kb1;
@@ -214,6 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
                 int ok = 1;
                 if (lane == 0) ok = wait_fast(empty(stage), ph ^ 1u, abort_flag, p.err, kErrWaitEmpty, limit) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_out;
+                if (withhold) {  // neither copies nor an arrive: the stage never completes
+                    withhold = false;
+                    continue;
+                }
                 const int tap = kb / p.cblocks, cb = kb - tap * p.cblocks;
                 const int r = tap / p.S, s = tap - r * p.S;
                 const uint32_t st = ring0 + (uint32_t)stage * sb;

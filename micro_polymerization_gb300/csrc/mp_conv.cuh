@@ -59,6 +59,7 @@ struct alignas(128) Params {
     int vec_c;          // Cin rows allow 16-byte loads
     int* err;           // the handle's status word
     unsigned long long wait_limit_ns;
+    int inject_timeout;  // test hook: producer warp 0 withholds its first stage
 };
 
 inline int smem_bytes(int num_stages, int stage_bytes) {

@@ -767,6 +767,8 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     p.vec_c1 = (a.C1 && ((uintptr_t)a.C1 & 15u) == 0 && a.ldc1 % 4 == 0) ? 1 : 0;
     p.err = s->err;
     p.wait_limit_ns = s->wait_limit_ns;
+    p.inject_timeout = s->inject_timeout;
+    s->inject_timeout = 0;
     if (s->log)
         std::fprintf(stderr, "[mp] b2b M=%lld N0=%lld N1=%lld K0=%lld bn1=%d cpg=%d units=%d grid=%d stages=%d\n",
                      (long long)M, (long long)N0, (long long)N1, (long long)K0, pl.bn1, pl.cpg, pl.units, pl.grid,
@@ -890,6 +892,8 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
     p.vec_c = (a.Cin && ((uintptr_t)a.Cin & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
     p.err = s->err;
     p.wait_limit_ns = s->wait_limit_ns;
+    p.inject_timeout = s->inject_timeout;
+    s->inject_timeout = 0;
     if (s->log)
         std::fprintf(stderr, "[mp] conv N=%lld H=%lld W=%lld C=%lld K=%lld RxS=%lldx%lld tile %dx%dx%d bn=%d splits=%d units=%d\n",
                      (long long)N, (long long)H, (long long)W, (long long)C, (long long)K, (long long)R, (long long)S,
@@ -966,6 +970,8 @@ mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& pl, int32_t cou
         p->stage_bytes = pl.stage_bytes;
         p->err = s->err;
         p->wait_limit_ns = s->wait_limit_ns;
+        p->inject_timeout = s->inject_timeout;
+        s->inject_timeout = 0;
         if (s->log)
             std::fprintf(stderr, "[mp] grouped problems=%d bn=%d units=%d\n", n, pl.bn, units);
         cudaLaunchConfig_t cfg = {};

@@ -48,6 +48,7 @@ struct alignas(128) Params {
     int num_stages, stage_bytes;
     int* err;
     unsigned long long wait_limit_ns;
+    int inject_timeout;  // test hook: producer warp 0 withholds its first stage
 };
 
 inline int smem_bytes(int num_stages, int stage_bytes) {

@@ -557,3 +557,55 @@ def test_bounded_wait_reports_timeout_and_recovers():
     assert mp.mp_check(h) == mp.MP_OK
     D2 = run_gemm(A, B, C, 1.0, 0.5)
     assert_parity(D2, A, B, C, 1.0, 0.5, what="after timeout")
+
+
+def test_bounded_waits_of_the_other_kernels_report_and_recover():
+    """The same withheld stage in the fused pair, the convolution and the
+    grouped GEMM: each kernel's bounded wait runs out, it stops cleanly,
+    mp_check reports the timeout, and the next call is correct."""
+    import oracle
+    h = handle()
+    dev = torch.device("cuda", 0)
+    b = wl.B2B(256, 128, 256, 192, act0=1, seed=3)
+    A0, W0, C0, W1, C1 = wl.make_b2b_operands(b)
+    c = wl.Conv(2, 9, 9, 64, 64, seed=4)
+    X, F, _ = wl.make_conv_operands(c)
+    g = wl.Gemm(200, 300, 256, seed=5)
+    A, B, _ = wl.make_operands(g)
+
+    def fused():
+        D1 = torch.empty(b.M, b.N1, device=dev)
+        mp.mp_gemm_b2b(h, A0.to(dev), W0.to(dev), None, W1.to(dev), None, D1, 1.0, 0.0, 1.0, 0.0, b.act0)
+        return D1
+
+    def conv():
+        D = torch.empty(c.N, c.P, c.Q, c.K, device=dev)
+        mp.mp_conv2d(h, X.to(dev), F.to(dev), None, D)
+        return D
+
+    def grouped():
+        D = torch.empty(g.M, g.N, device=dev)
+        mp.mp_gemm_grouped(h, [(A.to(dev), B.to(dev), None, D, 1.0, 0.0)])
+        return D
+
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
+    try:
+        for run in (fused, conv, grouped):
+            mp.mp_inject_wait_timeout(h, True, 50_000_000)  # 50 ms
+            run()
+            assert mp.mp_check(h) == mp.MP_ERR_DEVICE_TIMEOUT, run.__name__
+            mp.mp_inject_wait_timeout(h, False, 1_000_000_000)
+            assert mp.mp_check(h) == mp.MP_OK
+        bits = wl.bf16_bits
+        D1 = fused().cpu().numpy()
+        args = (bits(A0), bits(W0), None, bits(W1), None, 1.0, 0.0, 1.0, 0.0)
+        ref, d0 = oracle.b2b(*args, b.act0)
+        assert oracle.within_b2b(D1, ref, oracle.b2b_bound(*args, b.act0, d0))[0]
+        D = conv().cpu().numpy().reshape(-1, c.K)
+        assert oracle.within_bound(D, oracle.conv2d_nhwc(bits(X), bits(F)).reshape(-1, c.K),
+                                   oracle.conv2d_magnitude(bits(X), bits(F)).reshape(-1, c.K))[0]
+        D = grouped().cpu().numpy()
+        assert oracle.within_bound(D, oracle.gemm(bits(A), bits(B)), oracle.magnitude(bits(A), bits(B)))[0]
+    finally:
+        mp.mp_set_b2b_mode(h, mp.MP_B2B_AUTO)
+        mp.mp_inject_wait_timeout(h, False, 1_000_000_000)
