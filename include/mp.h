@@ -445,13 +445,14 @@ mp_status mp_conv2d(mp_handle h, int64_t N, int64_t H, int64_t W, int64_t C, int
 
 /*
  * How mp_conv2d tiles a problem (host only; any handle).  An output tile is
- * wb x hb x nb pixels (along Q, P and images; powers of two, product 128) by
- * bn output channels, its K loop (R*S*ceil(C/64) steps) cut into `splits`
+ * wb x hb x nb pixels (along Q, P and images; at most 128: powers of two with
+ * product 128, or sides that divide a small output exactly) by bn output
+ * channels, its K loop (R*S*ceil(C/64) steps) cut into `splits`
  * slices; tile shape, bn and splits minimise the cost model (waves of units
  * x the slice's K loop, against the tile's stores, plus the reduction).
  */
 typedef struct {
-    int32_t wb, hb, nb;       /* output pixels per tile along Q, P and images */
+    int32_t wb, hb, nb;       /* output pixels per tile along Q, P and images (product <= 128) */
     int32_t bn;               /* output channels per tile */
     int32_t tiles_q, tiles_p, tiles_n, tiles_k;
     int32_t ksteps;           /* R * S * ceil(C / 64) */

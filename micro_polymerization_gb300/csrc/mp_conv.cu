@@ -72,7 +72,7 @@ __device__ __forceinline__ void conv_epilogue(const Params& p, const Tile& t, ui
     if (n_w >= p.N || p_w >= p.P || q_w >= p.Q) return;  // the whole box is outside D
     int n_l, p_l, q_l;
     tile_pixel(p, t, 32 * q + lane, n_l, p_l, q_l);
-    const bool px_ok = n_l < p.N && p_l < p.P && q_l < p.Q;
+    const bool px_ok = 32 * q + lane < p.box_rows && n_l < p.N && p_l < p.P && q_l < p.Q;
     const long long pix = ((long long)n_l * p.P + p_l) * p.Q + q_l;
     const float a = p.alpha, b = p.beta;
     for (int c = 0; c < p.bn; c += 32) {
@@ -123,9 +123,15 @@ __device__ __forceinline__ void conv_epilogue(const Params& p, const Tile& t, ui
             ++slab_seq;
         } else if (px_ok) {
             float* dr = p.D + pix * p.ldd + k0;
+            if (p.vec_d && k0 + 32 <= p.K) {
 #pragma unroll
-            for (int j = 0; j < 32; j++)
-                if (k0 + j < p.K) dr[j] = o[j];
+                for (int j = 0; j < 8; j++)
+                    reinterpret_cast<float4*>(dr)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; j++)
+                    if (k0 + j < p.K) dr[j] = o[j];
+            }
         }
     }
 }
@@ -196,8 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Programmatic dependent launch, as in the GEMM kernel: the set-up above
+    // may overlap the previous kernel on the stream; every role that touches
+    // global memory first waits until that kernel has finished (its writes
+    // visible), and every thread waits once more before exit.  The next
+    // kernel (the split-K reduction) may start its own set-up early.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || warp == 6) {
+        grid_dep_wait();
         // ------------------------------ TMA producers (two warps) -------------
         // Stage g of the CTA's sequence uses ring slot g % nst and belongs to
         // warp 0 when g is even, to warp 6 when it is odd.
@@ -230,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
                     tma_load_3d(st + 16384u + (uint32_t)(lane - 1) * 8192u, &p.tmF, full(stage), t.k0 + 64 * (lane - 1),
                                 tap * p.C + cb * 64, 0);
                 __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(full(stage), 16384u + (uint32_t)p.bn * 128u);
+                if (lane == 0) mbar_arrive_expect_tx(full(stage), (uint32_t)(p.box_rows + p.bn) * 128u);
                 armed_mask |= 1u << stage;
                 armed_ph = (armed_ph & ~(1u << stage)) | (ph << stage);
             }
@@ -282,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         __syncwarp();
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        grid_dep_wait();
         const int q = warp & 3;
         uint8_t* slab = gbase + (epi0 - base) + q * kEpiSlabBytes;
         const uint32_t slab_s = epi0 + (uint32_t)(q * kEpiSlabBytes);
@@ -310,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
+    grid_dep_wait();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -320,6 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
 // Split-K reduction: thread i handles 4 channels of one tile row; the splits
 // are summed in order, then the epilogue arithmetic of the one-pass path.
 __global__ void __launch_bounds__(256) k_conv_reduce(const __grid_constant__ Params p) {
+    // Launched as a programmatic dependent of the convolution kernel: wait
+    // until it has finished and its partials are visible.
+    grid_dep_wait();
     const int groups = p.bn >> 2;
     const long long total = (long long)p.tiles * 128 * groups;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(256) k_conv_reduce(const __grid_constant__ Par
         int n, ph, qw;
         tile_pixel(p, t, row, n, ph, qw);
         const int k = t.k0 + 4 * g4;
-        if (n >= p.N || ph >= p.P || qw >= p.Q || k >= p.K) continue;
+        if (row >= p.box_rows || n >= p.N || ph >= p.P || qw >= p.Q || k >= p.K) continue;
         const float* src = p.ws + ((long long)tile * p.splits * 128 + row) * p.bn + 4 * g4;
         float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
         for (int s = 1; s < p.splits; s++) {
@@ -355,9 +373,16 @@ __global__ void __launch_bounds__(256) k_conv_reduce(const __grid_constant__ Par
 
 cudaError_t launch_reduce(cudaStream_t stream, const Params& p) {
     const long long total = (long long)p.tiles * 128 * (p.bn >> 2);
-    const int blocks = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
-    k_conv_reduce<<<blocks, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<long long>((total + 255) / 256, 152LL * 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_conv_reduce, p);
 }
 
 cudaError_t launch(const cudaLaunchConfig_t& cfg, const Params& p) {

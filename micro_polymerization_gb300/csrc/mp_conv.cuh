@@ -5,9 +5,13 @@
 // matrix [N*P*Q, R*S*C].  Here that matrix is never built: the TMA producer
 // loads each 128 x 64 A tile straight from X.
 //
-// An output tile is a box of wb x hb x nb output pixels (powers of two,
-// wb*hb*nb = 128: a rectangle of one image, or the same rectangle of several
-// small images) by bn output channels.  For filter tap (r, s) and channels
+// An output tile is a box of wb x hb x nb output pixels (a rectangle of one
+// image, or the same rectangle of several small images), at most 128 of them
+// (the UMMA's rows), by bn output channels.  Power-of-two sides with product
+// 128 let each epilogue warp store its 32 pixels as one box; sides that
+// divide a small image exactly (5 x 5 x 5, 3 x 9 x 4, ...) waste fewer MMA
+// rows, and their pixels are stored one by one.  Rows past wb*hb*nb hold
+// whatever the stage held before; their accumulator rows are never read.  For filter tap (r, s) and channels
 // [c0, c0+64), the A tile is the 4-D box {64 channels, wb, hb, nb} of X at
 // (c0, q0+s-pad_w, p0+r-pad_h, n0): in shared memory 128 rows of 64 bf16
 // with the 128-byte swizzle, row = pixel (w fastest, then h, then n), the
@@ -45,6 +49,7 @@ struct alignas(128) Params {
     long long ldc, ldd;  // elements from one output pixel to the next in Cin and D
     int N, H, W, C, K, R, S, pad_h, pad_w, P, Q;
     int wb, hb, nb;     // output pixels per tile along Q, P and images
+    int box_rows;       // wb * hb * nb <= 128: the A box's rows; the tile's later rows are unused
     int bw, bh, bnn;    // one warp's 32 pixels: the first 32 rows of the tile's order
     int tiles_q, tiles_p, tiles_n, tiles_k;
     int bn;             // output channels per tile (64, 128 or 256)
@@ -55,7 +60,8 @@ struct alignas(128) Params {
     int units;          // tiles * splits
     int num_stages, stage_bytes;
     float alpha, beta;
-    int tma_d;          // D 16-byte aligned with ldd % 4 == 0: bulk tensor stores
+    int tma_d;          // bulk tensor stores (D 16-byte aligned, ldd % 4 == 0, power-of-two box sides)
+    int vec_d;          // D rows allow 16-byte stores
     int vec_c;          // Cin rows allow 16-byte loads
     int* err;           // the handle's status word
     unsigned long long wait_limit_ns;

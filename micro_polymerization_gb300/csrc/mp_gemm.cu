@@ -845,7 +845,12 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
             !encode_3d(s, &p.tmF, F, K, R * S * C, 1, ldf * 2, round_up(R * S * C * ldf * 2, 16), 64, 64))
             return MP_ERR_CUDA;
     }
-    p.tma_d = (((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0) ? 1 : 0;
+    const bool d_aligned = ((uintptr_t)a.D & 15u) == 0 && (a.ldd * 4) % 16 == 0;
+    auto pow2 = [](int v) { return v > 0 && (v & (v - 1)) == 0; };
+    const bool pow2_box = pow2(pl.wb) && pow2(pl.hb) && pow2(pl.nb) && pl.wb * pl.hb * pl.nb == 128;
+    p.tma_d = d_aligned && pow2_box ? 1 : 0;
+    p.vec_d = d_aligned ? 1 : 0;
+    p.box_rows = pl.wb * pl.hb * pl.nb;
     p.bw = pl.wb >= 32 ? 32 : pl.wb;
     p.bh = pl.wb >= 32 ? 1 : (pl.wb * pl.hb >= 32 ? 32 / pl.wb : pl.hb);
     p.bnn = 32 / (p.bw * p.bh);
@@ -903,6 +908,11 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
     cfg.blockDim = dim3(conv::kThreads);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (conv::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
     if (pl.splits > 1 && conv::launch_reduce(stream, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;

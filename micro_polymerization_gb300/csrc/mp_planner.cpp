@@ -24,6 +24,8 @@
 // split-K reduction traffic, and the total is floored by the algorithmic
 // bytes over HBM bandwidth ("HBM bytes versus MMA cycles").
 #include <algorithm>
+#include <array>
+#include <vector>
 #include <chrono>
 #include <cmath>
 #include <cstring>
@@ -726,9 +728,25 @@ mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, in
         const int64_t tiles_k = (K + bn - 1) / bn;
         const int stage_bytes = 16384 + bn * 128;
         const int stages = std::min(conv::kMaxStages, (conv::kSmemLimit - 4 * conv::kEpiSlabBytes - 2048) / stage_bytes);
-        for (int wb = 1; wb <= 128; wb *= 2) {
-            for (int hb = 1; wb * hb <= 128; hb *= 2) {
-                const int nb = 128 / (wb * hb);
+        // Box shapes: powers of two with product 128, and sides that divide
+        // the output exactly (Q / k, P / k) with as many images as fit.
+        std::vector<std::array<int, 3>> boxes;
+        for (int wb = 1; wb <= 128; wb *= 2)
+            for (int hb = 1; wb * hb <= 128; hb *= 2) boxes.push_back({wb, hb, 128 / (wb * hb)});
+        for (int kq = 1; kq <= 4; kq++) {
+            const int wb = (int)((Q + kq - 1) / kq);
+            if (wb > 128) continue;
+            for (int kp = 1; kp <= 8; kp++) {
+                const int hb = (int)((P + kp - 1) / kp);
+                if (wb * hb > 128) continue;
+                const int nb = (int)std::min<int64_t>(N, 128 / (wb * hb));
+                boxes.push_back({wb, hb, nb});
+            }
+        }
+        for (const auto& box : boxes) {
+            {
+                const int wb = box[0], hb = box[1], nb = box[2];
+                const bool pow2 = wb * hb * nb == 128 && !(wb & (wb - 1)) && !(hb & (hb - 1)) && !(nb & (nb - 1));
                 const int64_t tq = (Q + wb - 1) / wb, tp = (P + hb - 1) / hb, tn = (N + nb - 1) / nb;
                 const int64_t tiles = tq * tp * tn * tiles_k;
                 const double useful = (double)(N * P * Q) / (double)(tq * wb * tp * hb * tn * nb);
@@ -738,7 +756,9 @@ mp_status plan_conv(const mp_hw& hw, int64_t ws_floats, int64_t N, int64_t H, in
                     if (units >= lim) continue;
                     const int64_t active = std::min<int64_t>(units, sms);
                     const double hbm_pe = hbm * 1e3 / (double)active;  // bytes per us per active SM
-                    const double epi = std::max(1.6 * bn / 256.0, 4.0 * 128 * bn / hbm_pe);
+                    // Pixel-by-pixel stores (boxes that are not powers of two)
+                    // take about twice as long as the warps' box stores.
+                    const double epi = std::max(1.6 * bn / 256.0 * (pow2 ? 1.0 : 2.0), 4.0 * 128 * bn / hbm_pe);
                     const double mma = (double)((ksteps + splits - 1) / splits) * step_us(bn);
                     const double waves = (double)((units + sms - 1) / sms);
                     // The reduction: a second launch reading every partial once.

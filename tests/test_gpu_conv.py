@@ -62,6 +62,20 @@ def test_conv_parity(shape):
     check(wl.Conv(N, H, W, C, K, R, S, ph, pw, alpha=1.25, beta=0.5, seed=sum(shape)))
 
 
+@pytest.mark.parametrize("shape", [(20, 5, 5, 512, 512), (9, 9, 9, 256, 256), (7, 7, 7, 128, 96), (3, 6, 10, 64, 64)])
+def test_conv_exact_fit_boxes(shape):
+    """Small images: boxes whose sides divide the image (not powers of two,
+    fewer than 128 rows, pixel-by-pixel stores) within the bound."""
+    N, H, W, C, K = shape
+    c = wl.Conv(N, H, W, C, K, alpha=1.25, beta=0.5, seed=H * W + C)
+    check(c)
+
+
+def test_conv_some_plan_uses_an_exact_fit_box():
+    boxes = [mp.mp_plan_conv(handle(), *s) for s in [(20, 5, 5, 512, 512), (9, 9, 9, 256, 256), (7, 7, 7, 128, 96)]]
+    assert any(p.wb * p.hb * p.nb < 128 for p in boxes), [(p.wb, p.hb, p.nb) for p in boxes]
+
+
 def test_conv_integer_exact():
     """Integer data: every partial sum is exact in fp32, so bitwise equal."""
     for (N, H, W, C, K) in [(2, 9, 7, 24, 40), (3, 5, 5, 128, 64), (1, 33, 17, 64, 192)]:
