@@ -170,15 +170,16 @@ mp_status check_conv(const mp::ConvArgs& a) {
 }
 
 // The fused plan and the form mp_gemm_b2b runs.  The two-launch form costs
-// the GEMM planner's estimates of both GEMMs plus 6.8 us, the fused kernel
-// its own estimate plus 3.3 us: fixed costs the two models leave out (the
-// launches, fill and drain), fitted to measured pairs on GB300.
+// the GEMM planner's estimates of both GEMMs plus 7.7 us, the fused kernel
+// its own estimate plus 2.0 us: fixed costs the two models leave out (the
+// launches, fill and drain), fitted on GB300 to the measured workloads of
+// fused pairs (64 problems each) in both forms.
 mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     mp_status st = mp::plan_b2b(h->hw, M, N0, N1, K0, out);
     if (st != MP_OK) return st;
     mp_plan_info p0, p1;
     const int64_t k0 = N0 > 0 ? K0 : 0;
-    double two = 6.8;
+    double two = 7.7;
     if (N0 > 0) {
         if ((st = mp::plan_shape(h, 1, M, N0, k0, &p0)) != MP_OK) return st;
         two += p0.cost_us;
@@ -189,7 +190,7 @@ mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t 
     if (h->b2b_mode != MP_B2B_AUTO)
         out->mode = h->b2b_mode;
     else
-        out->mode = (out->cost_us + 3.3 <= two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
+        out->mode = (out->cost_us + 2.0 <= two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
     return MP_OK;
 }
 

@@ -262,8 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Programmatic dependent launch, as in the GEMM kernel: the set-up above
+    // may overlap the previous kernel on the stream; every role that touches
+    // global memory first waits until that kernel has finished (its writes
+    // visible), and every thread waits once more before exit.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 || warp == 6) {
+        grid_dep_wait();
         // ------------------------------ TMA producers (two warps) -------------
         // Stage g of the CTA's sequence belongs to warp 0 when g is even, to
         // warp 6 when it is odd.
@@ -396,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         __syncwarp();
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        grid_dep_wait();
         const int q = warp & 3;  // TMEM lane quarter = rows 32q..32q+31 of the tile
         uint8_t* slab = gbase + (epi0 - base) + q * kEpiSlabBytes;
         const uint32_t slab_s = epi0 + (uint32_t)(q * kEpiSlabBytes);
@@ -449,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         if (lane == 0) bulk_wait_all();  // the stores have finished before the CTA exits
         __syncwarp();
     }
+    grid_dep_wait();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();

@@ -778,6 +778,11 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     cfg.blockDim = dim3(b2b::kThreads);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (b2b::launch(cfg, p) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
@@ -989,6 +994,11 @@ mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& pl, int32_t cou
         cfg.blockDim = dim3(grp::kThreads);
         cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
         cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         if (grp::launch(cfg, *p) != cudaSuccess) st = MP_ERR_CUDA;
     }
     delete p;

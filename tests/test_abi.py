@@ -184,13 +184,13 @@ def test_b2b_argument_checks():
 def test_b2b_form_choice():
     """Few row blocks: two launches; many: the fused kernel; a forced mode wins."""
     h = _host()
-    assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
+    assert mp.mp_plan_b2b(h, 256, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_FUSED
     for M in (1, 512, 4096, 100352):
         p = mp.mp_plan_b2b(h, M, 64, 256, 256)
         assert p.two_launch_cost_us > 0 and p.cost_us > 0
     mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
-    assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_FUSED
+    assert mp.mp_plan_b2b(h, 256, 256, 768, 768).mode == mp.MP_B2B_FUSED
     mp.mp_set_b2b_mode(h, mp.MP_B2B_TWO_LAUNCH)
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_TWO_LAUNCH
     with pytest.raises(mp.MPError):

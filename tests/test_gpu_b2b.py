@@ -166,7 +166,7 @@ def test_b2b_auto_choice_runs_the_planned_form():
     """AUTO takes the form mp_plan_b2b reports: two launches for few row
     blocks, the fused kernel for many; both within the bound."""
     mp.mp_set_b2b_mode(handle(), mp.MP_B2B_AUTO)
-    small = wl.B2B(2048, 256, 768, 768, act0=1, seed=21)
+    small = wl.B2B(256, 256, 768, 768, act0=1, seed=21)
     large = wl.B2B(128 * 400, 64, 256, 256, act0=1, seed=22)
     assert mp.mp_plan_b2b(handle(), small.M, small.N0, small.N1, small.K0).mode == mp.MP_B2B_TWO_LAUNCH
     assert mp.mp_plan_b2b(handle(), large.M, large.N0, large.N1, large.K0).mode == mp.MP_B2B_FUSED
