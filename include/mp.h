@@ -362,9 +362,9 @@ const char* mp_status_string(mp_status s);
  * elements.  D0 is never written to memory: each 128-row block of it stays
  * in the producing CTA's shared memory, rounded to bf16 (the type of the
  * second GEMM's operand), and feeds that CTA's second GEMM (the summary's
- * threadblock residence).  That needs N0 <= 256.  For shapes where two
- * launches are faster (few row blocks), D0 goes through a bf16 scratch
- * buffer instead (mp_set_b2b_mode).  act0 is MP_ACT_NONE,
+ * threadblock residence).  That needs N0 <= 256.  Where two launches are
+ * predicted clearly faster, and always for N0 > 256, D0 goes through a bf16
+ * scratch buffer instead (mp_set_b2b_mode).  act0 is MP_ACT_NONE,
  * MP_ACT_RELU or MP_ACT_GELU (the epilogue variants' activations).  C0 is not
  * read when beta0 == 0, nor C1 when beta1 == 0; C1 may be D1 (same pointer
  * and ld).  Asynchronous on `stream`, like mp_gemm.
@@ -372,10 +372,11 @@ const char* mp_status_string(mp_status s);
  * gives D1 = beta1 * C1.
  * Errors: MP_ERR_INVALID_ARG (negative size, NULL operand that is read, ld
  * too small, misaligned element, D1 overlapping an input other than an
- * identical C1, unknown act0); MP_ERR_UNSUPPORTED (N0 > 256, host-only
- * handle, or an A0, W0 or W1 whose base or row pitch is not 16-byte aligned
- * and that does not fit the staging area, where such operands are copied
- * with padded rows, as in mp_gemm); MP_ERR_CUDA (launch failure).
+ * identical C1, unknown act0); MP_ERR_UNSUPPORTED (N0 > 256 with the fused
+ * form forced, host-only handle, or an A0, W0 or W1 whose base or row pitch
+ * is not 16-byte aligned and that does not fit the staging area, where such
+ * operands are copied with padded rows, as in mp_gemm); MP_ERR_NO_MEMORY (the
+ * two-launch form's scratch buffer); MP_ERR_CUDA (launch failure).
  */
 mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, const void* A0, int64_t lda0,
                       const void* W0, int64_t ldw0, const float* C0, int64_t ldc0, const void* W1, int64_t ldw1,
@@ -407,13 +408,13 @@ mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0
 
 /*
  * Which form mp_gemm_b2b runs.  MP_B2B_FUSED: the fused kernel (D0 stays on
- * chip).  MP_B2B_TWO_LAUNCH: mp_gemm_ex writes D0 = act0(alpha0*A0*W0 +
- * beta0*C0) in bf16 (the same rounding as on chip) to a scratch buffer of the
- * handle, grown on first need, then mp_gemm runs the second GEMM.  With few
- * row blocks the fused kernel runs each block's first GEMM serially on one
- * SM and the two launches are faster.  MP_B2B_AUTO (the default) picks
- * per shape, comparing the two forms' cost models (mp_plan_b2b reports the
- * choice).  Errors: MP_ERR_INVALID_ARG (unknown mode).
+ * chip; N0 <= 256).  MP_B2B_TWO_LAUNCH: mp_gemm_ex writes D0 =
+ * act0(alpha0*A0*W0 + beta0*C0) in bf16 (the same rounding as on chip) to a
+ * scratch buffer of the handle, grown on first need, then mp_gemm runs the
+ * second GEMM.  MP_B2B_AUTO (the default) keeps the fused kernel unless the
+ * two forms' cost models predict the two launches more than 10% faster, and
+ * runs N0 > 256 as two launches (mp_plan_b2b reports the choice).
+ * Errors: MP_ERR_INVALID_ARG (unknown mode).
  */
 #define MP_B2B_AUTO 0
 #define MP_B2B_FUSED 1

@@ -142,7 +142,6 @@ mp_status check_b2b(const mp::B2BArgs& a) {
     if (second && overlap(d, span_of(a.W1, N0, N1, a.ldw1, 2, 1, 0))) return MP_ERR_INVALID_ARG;
     if (read_c1 && !(a.C1 == a.D1 && a.ldc1 == a.ldd1) && overlap(d, span_of(a.C1, M, N1, a.ldc1, 4, 1, 0)))
         return MP_ERR_INVALID_ARG;
-    if (N0 > 256) return MP_ERR_UNSUPPORTED;
     return MP_OK;
 }
 
@@ -173,10 +172,19 @@ mp_status check_conv(const mp::ConvArgs& a) {
 // the GEMM planner's estimates of both GEMMs plus 7.7 us, the fused kernel
 // its own estimate plus 2.0 us: fixed costs the two models leave out (the
 // launches, fill and drain), fitted on GB300 to the measured workloads of
-// fused pairs (64 problems each) in both forms.
+// fused pairs (64 problems each) in both forms.  The fused kernel is kept
+// unless two launches are predicted faster by more than 10% (the models'
+// error on these workloads), and N0 > 256 (a D0 row too wide for one
+// accumulator) always runs as two launches.
 mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     mp_status st = mp::plan_b2b(h->hw, M, N0, N1, K0, out);
-    if (st != MP_OK) return st;
+    const bool wide = st == MP_ERR_UNSUPPORTED && N0 > 256;
+    if (wide) {
+        if (h->b2b_mode == MP_B2B_FUSED) return MP_ERR_UNSUPPORTED;
+        std::memset(out, 0, sizeof(*out));
+    } else if (st != MP_OK) {
+        return st;
+    }
     mp_plan_info p0, p1;
     const int64_t k0 = N0 > 0 ? K0 : 0;
     double two = 7.7;
@@ -187,10 +195,12 @@ mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t 
     if ((st = mp::plan_shape(h, 1, M, N1, N0, &p1)) != MP_OK) return st;
     two += p1.cost_us;
     out->two_launch_cost_us = two;
-    if (h->b2b_mode != MP_B2B_AUTO)
+    if (wide)
+        out->mode = MP_B2B_TWO_LAUNCH;
+    else if (h->b2b_mode != MP_B2B_AUTO)
         out->mode = h->b2b_mode;
     else
-        out->mode = (out->cost_us + 2.0 <= two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
+        out->mode = (out->cost_us + 2.0 <= 1.1 * two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
     return MP_OK;
 }
 

@@ -176,21 +176,26 @@ def test_b2b_argument_checks():
     assert g(K0=0, A0=None, W0=None) == mp.MP_ERR_UNSUPPORTED
     # In place: C1 is D1 (same pointer and ld).
     assert g(C1=D1) == mp.MP_ERR_UNSUPPORTED
-    # N0 past one accumulator: not supported.
+    # N0 past one accumulator: valid (two launches); still no device here.
     assert g(N0=257, ldw0=257, ldc0=257) == mp.MP_ERR_UNSUPPORTED
     h.close()
 
 
 def test_b2b_form_choice():
-    """Few row blocks: two launches; many: the fused kernel; a forced mode wins."""
+    """The fused kernel unless two launches are clearly faster; N0 > 256 as
+    two launches; a forced mode wins (and a forced fused form refuses
+    N0 > 256)."""
     h = _host()
-    assert mp.mp_plan_b2b(h, 256, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_FUSED
+    assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_FUSED
+    assert mp.mp_plan_b2b(h, 2048, 384, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
     for M in (1, 512, 4096, 100352):
         p = mp.mp_plan_b2b(h, M, 64, 256, 256)
         assert p.two_launch_cost_us > 0 and p.cost_us > 0
     mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
     assert mp.mp_plan_b2b(h, 256, 256, 768, 768).mode == mp.MP_B2B_FUSED
+    with pytest.raises(mp.MPError):
+        mp.mp_plan_b2b(h, 2048, 384, 768, 768)
     mp.mp_set_b2b_mode(h, mp.MP_B2B_TWO_LAUNCH)
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_TWO_LAUNCH
     with pytest.raises(mp.MPError):
@@ -219,8 +224,8 @@ def test_b2b_plan_rules():
     # One row block, many chunks, a cheap first GEMM: chunks spread over SMs.
     p = mp.mp_plan_b2b(h, 128, 128, 8192, 64)
     assert p.cpg < p.chunks and p.units > 1
-    with pytest.raises(mp.MPError):
-        mp.mp_plan_b2b(h, 10, 257, 10, 10)
+    p = mp.mp_plan_b2b(h, 10, 257, 10, 10)  # wider than one accumulator: two launches
+    assert p.mode == mp.MP_B2B_TWO_LAUNCH and p.units == 0
     with pytest.raises(mp.MPError):
         mp.mp_plan_b2b(h, -1, 64, 10, 10)
     h.close()
