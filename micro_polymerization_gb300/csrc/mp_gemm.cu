@@ -27,6 +27,11 @@ namespace dev {
 __global__ void k_repack_bf16(const uint16_t* __restrict__ src, long long ld_src, long long stride_src,
                               uint16_t* __restrict__ dst, long long ld_dst, long long stride_dst, int rows,
                               int cols, int batch) {
+    // Launched as a programmatic dependent: wait until the previous kernel
+    // on the stream (which may still read the staging area) has finished;
+    // the GEMM that reads this copy may start its own set-up meanwhile.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long chunks = ld_dst / 8;
     const long long total = (long long)batch * rows * chunks;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -49,6 +54,22 @@ __global__ void k_repack_bf16(const uint16_t* __restrict__ src, long long ld_src
 }
 
 }  // namespace dev
+
+// One repack launch, as a programmatic dependent of the previous kernel.
+cudaError_t launch_repack(cudaStream_t stream, int blocks, const void* src, long long ld_src, long long stride_src,
+                          uint16_t* dst, long long ld_dst, long long stride_dst, int rows, int cols, int batch) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dev::k_repack_bf16, reinterpret_cast<const uint16_t*>(src), ld_src, stride_src,
+                              dst, ld_dst, stride_dst, rows, cols, batch);
+}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -463,9 +484,8 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
             const int64_t chunks = bA * M * (ld2 / 8);
             const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
-            dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(A), lda, sA, dst, ld2,
-                                                           st2, (int)M, (int)K, (int)bA);
-            if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+            if (launch_repack(stream, blocks, A, lda, sA, dst, ld2, st2, (int)M, (int)K, (int)bA) != cudaSuccess)
+                return MP_ERR_CUDA;
             A = dst;
             lda = ld2;
             sA = st2;
@@ -478,9 +498,8 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
             const int64_t chunks = bB * K * (ld2 / 8);
             const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
-            dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(B), ldb, sB, dst, ld2,
-                                                           st2, (int)K, (int)N, (int)bB);
-            if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+            if (launch_repack(stream, blocks, B, ldb, sB, dst, ld2, st2, (int)K, (int)N, (int)bB) != cudaSuccess)
+                return MP_ERR_CUDA;
             B = dst;
             ldb = ld2;
             sB = st2;
@@ -704,9 +723,8 @@ mp_status stage_if_unaligned(DeviceState* s, cudaStream_t stream, const void*& P
     if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
     uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
     const int blocks = (int)std::min<int64_t>(cdiv(rows * (ld2 / 8), 256), 4096);
-    dev::k_repack_bf16<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint16_t*>(P), ld, 0, dst, ld2, 0,
-                                                   (int)rows, (int)cols, 1);
-    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_repack(stream, blocks, P, ld, 0, dst, ld2, 0, (int)rows, (int)cols, 1) != cudaSuccess)
+        return MP_ERR_CUDA;
     P = dst;
     ld = ld2;
     used += bytes;
