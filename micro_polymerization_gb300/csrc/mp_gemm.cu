@@ -21,45 +21,70 @@
 namespace mp {
 namespace dev {
 
-// Copy a (batch x rows x cols) bf16 operand whose rows are not 16-byte
-// aligned into a staging buffer with rows padded to a multiple of 8 elements
-// (zero-filled), so that TMA can address it.
-__global__ void k_repack_bf16(const uint16_t* __restrict__ src, long long ld_src, long long stride_src,
-                              uint16_t* __restrict__ dst, long long ld_dst, long long stride_dst, int rows,
-                              int cols, int batch) {
+// One operand to stage: a (batch x rows x cols) bf16 matrix whose rows are
+// not 16-byte aligned, copied with rows padded to ld_dst (a multiple of 8
+// elements, zero-filled) so that TMA can address it.
+struct RepackJob {
+    const uint16_t* src;
+    long long ld_src, stride_src;
+    uint16_t* dst;
+    long long ld_dst, stride_dst;
+    int rows, cols, batch;
+};
+
+__device__ __forceinline__ long long repack_chunks(const RepackJob& j) {
+    return (long long)j.batch * j.rows * (j.ld_dst / 8);
+}
+
+// Up to two operands (A and B of one GEMM) in one launch: 16 bytes of the
+// destination per thread and step, the first operand's chunks first.
+__global__ void k_repack_bf16(const RepackJob j0, const RepackJob j1, int njobs) {
     // Launched as a programmatic dependent: wait until the previous kernel
     // on the stream (which may still read the staging area) has finished;
     // the GEMM that reads this copy may start its own set-up meanwhile.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long long chunks = ld_dst / 8;
-    const long long total = (long long)batch * rows * chunks;
+    const long long t0 = repack_chunks(j0);
+    const long long total = t0 + (njobs > 1 ? repack_chunks(j1) : 0);
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
-        const long long ch = i % chunks;
-        const long long rb = i / chunks;
-        const int r = (int)(rb % rows);
-        const int b = (int)(rb / rows);
-        const uint16_t* s = src + b * stride_src + r * ld_src + ch * 8;
+        const bool second = i >= t0;
+        const RepackJob& j = second ? j1 : j0;
+        const long long k = second ? i - t0 : i;
+        const long long chunks = j.ld_dst / 8;
+        const long long ch = k % chunks;
+        const long long rb = k / chunks;
+        const int r = (int)(rb % j.rows);
+        const int b = (int)(rb / j.rows);
+        const uint16_t* s = j.src + b * j.stride_src + r * j.ld_src + ch * 8;
         uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const long long c0 = ch * 8 + 2 * j;
-            const uint32_t lo = c0 < cols ? s[2 * j] : 0u;
-            const uint32_t hi = c0 + 1 < cols ? s[2 * j + 1] : 0u;
-            w[j] = lo | (hi << 16);
+        for (int e = 0; e < 4; e++) {
+            const long long c0 = ch * 8 + 2 * e;
+            const uint32_t lo = c0 < j.cols ? s[2 * e] : 0u;
+            const uint32_t hi = c0 + 1 < j.cols ? s[2 * e + 1] : 0u;
+            w[e] = lo | (hi << 16);
         }
-        *reinterpret_cast<uint4*>(dst + b * stride_dst + r * ld_dst + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(j.dst + b * j.stride_dst + r * j.ld_dst + ch * 8) =
+            make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 }  // namespace dev
 
-// One repack launch, as a programmatic dependent of the previous kernel.
-cudaError_t launch_repack(cudaStream_t stream, int blocks, const void* src, long long ld_src, long long stride_src,
-                          uint16_t* dst, long long ld_dst, long long stride_dst, int rows, int cols, int batch) {
+dev::RepackJob repack_job(const void* src, long long ld_src, long long stride_src, uint16_t* dst, long long ld_dst,
+                          long long stride_dst, int rows, int cols, int batch) {
+    return dev::RepackJob{reinterpret_cast<const uint16_t*>(src), ld_src, stride_src, dst, ld_dst, stride_dst,
+                          rows, cols, batch};
+}
+
+// One repack launch for `n` (1 or 2) operands, as a programmatic dependent of
+// the previous kernel.
+cudaError_t launch_repack(cudaStream_t stream, const dev::RepackJob* jobs, int n) {
+    long long chunks = 0;
+    for (int i = 0; i < n; i++) chunks += (long long)jobs[i].batch * jobs[i].rows * (jobs[i].ld_dst / 8);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>((chunks + 255) / 256, 4096)));
     cfg.blockDim = dim3(256);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -67,8 +92,7 @@ cudaError_t launch_repack(cudaStream_t stream, int blocks, const void* src, long
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dev::k_repack_bf16, reinterpret_cast<const uint16_t*>(src), ld_src, stride_src,
-                              dst, ld_dst, stride_dst, rows, cols, batch);
+    return cudaLaunchKernelEx(&cfg, dev::k_repack_bf16, jobs[0], n > 1 ? jobs[1] : jobs[0], n);
 }
 
 // ---------------------------------------------------------------------------
@@ -477,15 +501,14 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     int64_t bB = (batch > 1 && a.strideB != 0) ? batch : 1;
     if (K > 0) {
         int64_t used = 0;
+        dev::RepackJob jobs[2];
+        int njobs = 0;
         if (!tma_ok(A, lda, batch, sA)) {
             const int64_t ld2 = round_up(K, 8), st2 = M * ld2;
             const int64_t bytes = round_up(2 * bA * st2, 256);
             if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
             uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
-            const int64_t chunks = bA * M * (ld2 / 8);
-            const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
-            if (launch_repack(stream, blocks, A, lda, sA, dst, ld2, st2, (int)M, (int)K, (int)bA) != cudaSuccess)
-                return MP_ERR_CUDA;
+            jobs[njobs++] = repack_job(A, lda, sA, dst, ld2, st2, (int)M, (int)K, (int)bA);
             A = dst;
             lda = ld2;
             sA = st2;
@@ -496,15 +519,14 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             const int64_t bytes = round_up(2 * bB * st2, 256);
             if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
             uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
-            const int64_t chunks = bB * K * (ld2 / 8);
-            const int blocks = (int)std::min<int64_t>(cdiv(chunks, 256), 4096);
-            if (launch_repack(stream, blocks, B, ldb, sB, dst, ld2, st2, (int)K, (int)N, (int)bB) != cudaSuccess)
-                return MP_ERR_CUDA;
+            jobs[njobs++] = repack_job(B, ldb, sB, dst, ld2, st2, (int)K, (int)N, (int)bB);
             B = dst;
             ldb = ld2;
             sB = st2;
             used += bytes;
         }
+        // Both operands' copies in one launch.
+        if (njobs > 0 && launch_repack(stream, jobs, njobs) != cudaSuccess) return MP_ERR_CUDA;
         // Box shapes the plan's regions use: rows per A box of swapped tiles
         // (the smallest swapped bn divides the others: all are powers of 2),
         // and the numbers of 64-column blocks a B copy covers.
@@ -722,9 +744,8 @@ mp_status stage_if_unaligned(DeviceState* s, cudaStream_t stream, const void*& P
     const int64_t bytes = round_up(2 * rows * ld2, 256);
     if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
     uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
-    const int blocks = (int)std::min<int64_t>(cdiv(rows * (ld2 / 8), 256), 4096);
-    if (launch_repack(stream, blocks, P, ld, 0, dst, ld2, 0, (int)rows, (int)cols, 1) != cudaSuccess)
-        return MP_ERR_CUDA;
+    const dev::RepackJob job = repack_job(P, ld, 0, dst, ld2, 0, (int)rows, (int)cols, 1);
+    if (launch_repack(stream, &job, 1) != cudaSuccess) return MP_ERR_CUDA;
     P = dst;
     ld = ld2;
     used += bytes;
