@@ -32,41 +32,60 @@ struct RepackJob {
     int rows, cols, batch;
 };
 
-__device__ __forceinline__ long long repack_chunks(const RepackJob& j) {
-    return (long long)j.batch * j.rows * (j.ld_dst / 8);
-}
-
 // Up to two operands (A and B of one GEMM) in one launch: 16 bytes of the
-// destination per thread and step, the first operand's chunks first.
+// destination per thread and step, the first operand's chunks first.  Chunk
+// indices stay below 2^31 (the staging area bounds them), so the index
+// arithmetic is 32-bit.  The source is read in aligned 32-bit words: a row
+// that starts 2 bytes past a word boundary takes each output pair from the
+// high half of one word and the low half of the next.  Only words that hold
+// at least one element of the row are read.
 __global__ void k_repack_bf16(const RepackJob j0, const RepackJob j1, int njobs) {
     // Launched as a programmatic dependent: wait until the previous kernel
     // on the stream (which may still read the staging area) has finished;
     // the GEMM that reads this copy may start its own set-up meanwhile.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long long t0 = repack_chunks(j0);
-    const long long total = t0 + (njobs > 1 ? repack_chunks(j1) : 0);
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t c0 = (uint32_t)(j0.ld_dst / 8), c1 = njobs > 1 ? (uint32_t)(j1.ld_dst / 8) : 1u;
+    const uint32_t t0 = (uint32_t)j0.batch * (uint32_t)j0.rows * c0;
+    const uint32_t total = t0 + (njobs > 1 ? (uint32_t)j1.batch * (uint32_t)j1.rows * c1 : 0u);
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         const bool second = i >= t0;
         const RepackJob& j = second ? j1 : j0;
-        const long long k = second ? i - t0 : i;
-        const long long chunks = j.ld_dst / 8;
-        const long long ch = k % chunks;
-        const long long rb = k / chunks;
-        const int r = (int)(rb % j.rows);
-        const int b = (int)(rb / j.rows);
-        const uint16_t* s = j.src + b * j.stride_src + r * j.ld_src + ch * 8;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const long long c0 = ch * 8 + 2 * e;
-            const uint32_t lo = c0 < j.cols ? s[2 * e] : 0u;
-            const uint32_t hi = c0 + 1 < j.cols ? s[2 * e + 1] : 0u;
-            w[e] = lo | (hi << 16);
+        const uint32_t chunks = second ? c1 : c0;
+        const uint32_t k = second ? i - t0 : i;
+        const uint32_t rb = k / chunks;
+        const uint32_t ch = k - rb * chunks;
+        uint32_t b = 0, r = rb;
+        if (j.batch > 1) {
+            b = rb / (uint32_t)j.rows;
+            r = rb - b * (uint32_t)j.rows;
         }
-        *reinterpret_cast<uint4*>(j.dst + b * j.stride_dst + r * j.ld_dst + ch * 8) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        const uint16_t* srow = j.src + (long long)b * j.stride_src + (long long)r * j.ld_src;
+        const int e0 = (int)ch * 8;
+        const int nvalid = min(8, j.cols - e0);  // >= 1: the padding never fills a whole chunk
+        const bool odd = (reinterpret_cast<uintptr_t>(srow) & 2u) != 0;
+        const uint32_t* wp =
+            reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(srow) & ~uintptr_t(3)) + e0 / 2;
+        uint32_t o[4];
+        if (!odd) {
+            // word k holds elements e0 + 2k (low half) and e0 + 2k + 1
+#pragma unroll
+            for (int q = 0; q < 4; q++) o[q] = 2 * q < nvalid ? __ldg(wp + q) : 0u;
+        } else {
+            // word k holds elements e0 + 2k - 1 (low half) and e0 + 2k
+            uint32_t x[5];
+#pragma unroll
+            for (int q = 0; q < 5; q++) x[q] = 2 * q <= nvalid ? __ldg(wp + q) : 0u;
+#pragma unroll
+            for (int q = 0; q < 4; q++) o[q] = (x[q] >> 16) | (x[q + 1] << 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (2 * q >= nvalid) o[q] = 0u;
+            else if (2 * q + 1 >= nvalid) o[q] &= 0xffffu;
+        }
+        *reinterpret_cast<uint4*>(j.dst + (long long)b * j.stride_dst + (long long)r * j.ld_dst + e0) =
+            make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -83,6 +102,7 @@ dev::RepackJob repack_job(const void* src, long long ld_src, long long stride_sr
 cudaError_t launch_repack(cudaStream_t stream, const dev::RepackJob* jobs, int n) {
     long long chunks = 0;
     for (int i = 0; i < n; i++) chunks += (long long)jobs[i].batch * jobs[i].rows * (jobs[i].ld_dst / 8);
+    if (chunks >= (1ll << 31)) return cudaErrorInvalidValue;  // 32-bit chunk indices
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>((chunks + 255) / 256, 4096)));
     cfg.blockDim = dim3(256);
