@@ -377,6 +377,49 @@ def test_batched_equals_loop(seq):
     assert torch.equal(Db[0].cpu(), single) and torch.equal(Db[1].cpu(), -single)
 
 
+@pytest.mark.parametrize("M,N,K", [(37, 45, 77), (130, 9, 263)])
+def test_batched_unaligned_rows_are_repacked(M, N, K):
+    """Batched operands whose rows and batch strides are not 16-byte
+    aligned (odd K and N): both are staged in one copy, and a broadcast A
+    (batch stride 0) is staged once."""
+    dev = torch.device("cuda", 0)
+    g = wl.Gemm(M, N, K, batch=5, beta=0.5, seed=M + K)
+    A, B, C = wl.make_operands(g)
+    D = torch.empty(5, M, N, device=dev)
+    mp.mp_gemm_batched(handle(), A.to(dev), B.to(dev), C.to(dev), D, 1.5, 0.5)
+    torch.cuda.synchronize()
+    D = D.cpu()
+    for b in range(5):
+        assert_parity(D[b], A[b], B[b], C[b], 1.5, 0.5, what=f"unaligned batch {b} {(M, N, K)}")
+    D2 = torch.empty(5, M, N, device=dev)
+    mp.mp_gemm_batched(handle(), A[:1].to(dev), B.to(dev), None, D2, 1.0, 0.0)
+    torch.cuda.synchronize()
+    D2 = D2.cpu()
+    for b in range(5):
+        assert_parity(D2[b], A[0], B[b], None, 1.0, 0.0, what=f"broadcast A, batch {b}")
+
+
+@pytest.mark.parametrize("lda_extra,ldb_extra", [(0, 0), (1, 3)])
+def test_operands_two_bytes_past_a_word(lda_extra, ldb_extra):
+    """A and B start 2 bytes past a 4-byte boundary: with an even row pitch
+    every row starts there, with an odd one every other row does."""
+    dev = torch.device("cuda", 0)
+    M, N, K = 67, 90, 150
+    A, B, C = rand_problem(M, N, K, seed=9, beta=0.5)
+    lda, ldb = K + lda_extra, N + ldb_extra
+    Abuf = torch.zeros(1 + M * lda + 8, dtype=torch.bfloat16, device=dev)
+    Bbuf = torch.zeros(1 + K * ldb + 8, dtype=torch.bfloat16, device=dev)
+    Av = Abuf[1:1 + M * lda].view(M, lda)[:, :K]
+    Bv = Bbuf[1:1 + K * ldb].view(K, ldb)[:, :N]
+    Av.copy_(A.to(dev))
+    Bv.copy_(B.to(dev))
+    assert Av.data_ptr() % 4 == 2 and Bv.data_ptr() % 4 == 2
+    D = torch.empty(M, N, device=dev)
+    mp.mp_gemm(handle(), Av, Bv, C.to(dev), D, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert_parity(D.cpu(), A, B, C, 1.5, 0.5, what=f"2-byte offset, ld +{lda_extra}/+{ldb_extra}")
+
+
 def test_batched_shared_operand_stride_zero():
     dev = torch.device("cuda", 0)
     A, B, _ = rand_problem(64, 80, 96, seed=4)
