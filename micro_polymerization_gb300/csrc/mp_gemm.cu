@@ -755,20 +755,33 @@ void drop_unavailable_kernels(mp_handle h) {
 // ---------------------------------------------------------------------------
 // Back-to-back GEMMs: tensor maps and the launch of k_b2b_gemm
 // ---------------------------------------------------------------------------
-// A bf16 matrix whose base or row pitch TMA cannot address is copied into
-// the staging area with rows padded to a multiple of 8 elements.
-mp_status stage_if_unaligned(DeviceState* s, cudaStream_t stream, const void*& P, int64_t& ld, int64_t rows,
-                             int64_t cols, int64_t& used) {
-    if (tma_ok(P, ld, 1, 0)) return MP_OK;
-    const int64_t ld2 = round_up(cols, 8);
-    const int64_t bytes = round_up(2 * rows * ld2, 256);
-    if (used + bytes > s->staging_bytes) return MP_ERR_UNSUPPORTED;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
-    const dev::RepackJob job = repack_job(P, ld, 0, dst, ld2, 0, (int)rows, (int)cols, 1);
-    if (launch_repack(stream, &job, 1) != cudaSuccess) return MP_ERR_CUDA;
-    P = dst;
-    ld = ld2;
-    used += bytes;
+// The bf16 operands of one launch whose base or row pitch TMA cannot address
+// (at most three) are redirected to copies in the staging area with rows
+// padded to a multiple of 8 elements; the copies go out two per launch.
+struct StageOperand {
+    const void** P;
+    int64_t* ld;
+    int64_t rows, cols;
+};
+
+mp_status stage_unaligned(DeviceState* s, cudaStream_t stream, const StageOperand* ops, int n, int64_t& used) {
+    dev::RepackJob jobs[3];
+    int nj = 0;
+    for (int i = 0; i < n; i++) {
+        const StageOperand& o = ops[i];
+        if (tma_ok(*o.P, *o.ld, 1, 0)) continue;
+        const int64_t ld2 = round_up(o.cols, 8);
+        const int64_t bytes = round_up(2 * o.rows * ld2, 256);
+        if (used + bytes > s->staging_bytes || nj == 3) return MP_ERR_UNSUPPORTED;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(s->staging + used);
+        jobs[nj++] = repack_job(*o.P, *o.ld, 0, dst, ld2, 0, (int)o.rows, (int)o.cols, 1);
+        *o.P = dst;
+        *o.ld = ld2;
+        used += bytes;
+    }
+    // The copy kernel takes two operands per launch.
+    for (int i = 0; i < nj; i += 2)
+        if (launch_repack(stream, jobs + i, std::min(2, nj - i)) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 
@@ -782,16 +795,23 @@ mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     cudaStream_t stream = (cudaStream_t)a.stream;
     const void *A0 = a.A0, *W0 = a.W0, *W1 = a.W1;
     int64_t lda0 = a.lda0, ldw0 = a.ldw0, ldw1 = a.ldw1, used = 0;
-    mp_status st = MP_OK;
+    {
+        StageOperand ops[3];
+        int n = 0;
+        if (K0 > 0) {
+            ops[n++] = StageOperand{&A0, &lda0, M, K0};
+            ops[n++] = StageOperand{&W0, &ldw0, K0, N0};
+        }
+        if (N0 > 0) ops[n++] = StageOperand{&W1, &ldw1, N0, N1};
+        const mp_status st = stage_unaligned(s, stream, ops, n, used);
+        if (st != MP_OK) return st;
+    }
     if (K0 > 0) {
-        if ((st = stage_if_unaligned(s, stream, A0, lda0, M, K0, used)) != MP_OK) return st;
-        if ((st = stage_if_unaligned(s, stream, W0, ldw0, K0, N0, used)) != MP_OK) return st;
         if (!encode_3d(s, &p.tmA0, A0, K0, M, 1, lda0 * 2, round_up(M * lda0 * 2, 16), 64, 128) ||
             !encode_3d(s, &p.tmW0, W0, N0, K0, 1, ldw0 * 2, round_up(K0 * ldw0 * 2, 16), 64, 64))
             return MP_ERR_CUDA;
     }
     if (N0 > 0) {
-        if ((st = stage_if_unaligned(s, stream, W1, ldw1, N0, N1, used)) != MP_OK) return st;
         if (!encode_3d(s, &p.tmW1, W1, N1, N0, 1, ldw1 * 2, round_up(N0 * ldw1 * 2, 16), 64, 64))
             return MP_ERR_CUDA;
     }
@@ -899,9 +919,9 @@ mp_status device_run_conv(mp_handle h, const mp_conv_plan& pl, const ConvArgs& a
         const void* X = a.X;
         const void* F = a.F;
         int64_t ldx = C, ldf = K, used = 0;
-        mp_status st = stage_if_unaligned(s, stream, X, ldx, N * H * W, C, used);
+        const StageOperand ops[2] = {{&X, &ldx, N * H * W, C}, {&F, &ldf, R * S * C, K}};
+        const mp_status st = stage_unaligned(s, stream, ops, 2, used);
         if (st != MP_OK) return st;
-        if ((st = stage_if_unaligned(s, stream, F, ldf, R * S * C, K, used)) != MP_OK) return st;
         const uint64_t xd[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
         const uint64_t xs[3] = {(uint64_t)ldx * 2, (uint64_t)(W * ldx * 2), (uint64_t)(H * W * ldx * 2)};
         const uint32_t xb[4] = {64, (uint32_t)pl.wb, (uint32_t)pl.hb, (uint32_t)pl.nb};
@@ -1008,8 +1028,8 @@ mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& pl, int32_t cou
             const void* B = a.B;
             int64_t lda = a.lda, ldb = a.ldb;
             if (a.K > 0) {
-                if ((st = stage_if_unaligned(s, stream, A, lda, a.M, a.K, used)) != MP_OK) break;
-                if ((st = stage_if_unaligned(s, stream, B, ldb, a.K, a.N, used)) != MP_OK) break;
+                const StageOperand ops[2] = {{&A, &lda, a.M, a.K}, {&B, &ldb, a.K, a.N}};
+                if ((st = stage_unaligned(s, stream, ops, 2, used)) != MP_OK) break;
                 if (!encode_3d(s, &q.tmA, A, a.K, a.M, 1, lda * 2, round_up(a.M * lda * 2, 16), 64, 128) ||
                     !encode_3d(s, &q.tmB, B, a.N, a.K, 1, ldb * 2, round_up(a.K * ldb * 2, 16), 64, 64)) {
                     st = MP_ERR_CUDA;
