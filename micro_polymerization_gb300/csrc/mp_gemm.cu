@@ -91,6 +91,8 @@ __global__ void k_repack_bf16(const RepackJob j0, const RepackJob j1, int njobs)
 
 }  // namespace dev
 
+namespace {
+
 dev::RepackJob repack_job(const void* src, long long ld_src, long long stride_src, uint16_t* dst, long long ld_dst,
                           long long stride_dst, int rows, int cols, int batch) {
     return dev::RepackJob{reinterpret_cast<const uint16_t*>(src), ld_src, stride_src, dst, ld_dst, stride_dst,
@@ -114,6 +116,8 @@ cudaError_t launch_repack(cudaStream_t stream, const dev::RepackJob* jobs, int n
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dev::k_repack_bf16, jobs[0], n > 1 ? jobs[1] : jobs[0], n);
 }
+
+}  // namespace
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -755,6 +759,8 @@ void drop_unavailable_kernels(mp_handle h) {
 // ---------------------------------------------------------------------------
 // Back-to-back GEMMs: tensor maps and the launch of k_b2b_gemm
 // ---------------------------------------------------------------------------
+namespace {
+
 // The bf16 operands of one launch whose base or row pitch TMA cannot address
 // (at most three) are redirected to copies in the staging area with rows
 // padded to a multiple of 8 elements; the copies go out two per launch.
@@ -784,6 +790,8 @@ mp_status stage_unaligned(DeviceState* s, cudaStream_t stream, const StageOperan
         if (launch_repack(stream, jobs + i, std::min(2, nj - i)) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
+
+}  // namespace
 
 mp_status device_run_b2b(mp_handle h, const mp_b2b_plan& pl, const B2BArgs& a) {
     DeviceState* s = h->dev;
