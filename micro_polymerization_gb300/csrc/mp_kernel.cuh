@@ -212,6 +212,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Untiled bulk copy global -> shared memory (both 16-byte aligned, `bytes` a
+// multiple of 16), completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -960,6 +968,105 @@ __device__ __forceinline__ void reduce_rows(const Params& p, const Work& w, cons
     }
 }
 
+// o[0..3] = alpha * sum + beta * C at D[m][n..n+3] (columns past the region
+// clipped): activation, then the store.
+template <int EPI>
+__device__ __forceinline__ void put4_clipped(const Params& p, const Work& w, int m, int n, const float* o) {
+    if (n >= w.n_end) return;
+    uint8_t* d = d_ptr<EPI>(p, (long long)w.b * p.strideD + (long long)m * p.ldd + n);
+    if (p.vec_d && n + 3 < w.n_end) {
+        put_out4<EPI>(p, d, act_fn<EPI>(o[0]), act_fn<EPI>(o[1]), act_fn<EPI>(o[2]), act_fn<EPI>(o[3]));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; e++)
+            if (n + e < w.n_end) put_out<EPI>(p, d + e * d_esize<EPI>(p), act_fn<EPI>(o[e]));
+    }
+}
+
+// Shared memory the ring reduction needs for rows [r0, r1) of a split tile:
+// the S partial slices, and C's rows when they are copied too.
+__device__ __forceinline__ bool ring_c_rows(const Params& p, const Work& w) {
+    const int L = w.swap ? 128 : w.bn;
+    return p.beta != 0.0f && p.vec_c && w.n_t0 + L <= w.n_end;
+}
+__device__ __forceinline__ uint32_t ring_reduce_bytes(const Params& p, const Work& w, int r0, int r1) {
+    const uint32_t slice = (uint32_t)(r1 - r0) * (uint32_t)(w.swap ? 128 : w.bn) * 4u;
+    return slice * (uint32_t)(w.splits + (ring_c_rows(p, w) ? 1 : 0));
+}
+
+// Rows [r0, r1) of a split tile, when the operand ring is idle (every MMA of
+// this CTA has completed): one warp bulk-copies the S partial slices (each
+// (r1 - r0) x L contiguous floats) and, where C's rows lie whole inside D
+// and are 16-byte aligned, those rows of C into the ring under one mbarrier;
+// then the 128 epilogue threads add the partials in split order from shared
+// memory (the same order, hence the same bits, as reduce_rows) and write D.
+// Only one memory round trip, instead of one per group of outputs.  Returns
+// false when the wait for the copies gave up (the status word is set).
+template <int EPI>
+__device__ __forceinline__ bool reduce_rows_ring(const Params& p, const Work& w, const float* tile_ws, int r0,
+                                                 int r1, int tid, uint32_t ring, const uint8_t* ring_g,
+                                                 uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 uint64_t limit) {
+    const int L = w.swap ? 128 : w.bn;
+    const int L4 = L / 4;
+    const int S = w.splits;
+    const long long part_floats = 128ll * w.bn;
+    const int rows = r1 - r0;
+    const uint32_t slice = (uint32_t)rows * (uint32_t)L * 4u;
+    const bool c_ring = ring_c_rows(p, w);
+    const int rows_c = c_ring ? max(0, min(r1, w.m_end - w.m_t0) - r0) : 0;
+    const uint32_t c_off = (uint32_t)S * slice;
+    if (tid < 32) {
+        if (tid == 0) mbar_arrive_expect_tx(bar, (uint32_t)S * slice + (uint32_t)rows_c * (uint32_t)L * 4u);
+        __syncwarp();
+        for (int s = tid; s < S; s += 32)
+            bulk_load(ring + (uint32_t)s * slice, tile_ws + s * part_floats + (long long)r0 * L, slice, bar);
+        const float* c0 = p.C + (long long)w.b * p.strideC + (long long)(w.m_t0 + r0) * p.ldc + w.n_t0;
+        for (int r = tid; r < rows_c; r += 32)
+            bulk_load(ring + c_off + (uint32_t)(r * L * 4), c0 + (long long)r * p.ldc, (uint32_t)L * 4u, bar);
+    }
+    int ok = 1;
+    if ((tid & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, p.err, kErrWaitSplits, limit, true) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+        // Let this CTA's copies land before it leaves.
+        if (tid == 0) wait_bounded(bar, parity, abort_flag, p.err, kErrDrain, limit, false);
+        __syncwarp();
+        return false;
+    }
+    const float* sm = reinterpret_cast<const float*>(ring_g);
+    const float alpha = p.alpha, beta = p.beta;
+    const int total = rows * L4;
+    for (int i = tid; i < total; i += 128) {
+        const int rr = i / L4, g = i - rr * L4;
+        const int m = w.m_t0 + r0 + rr;
+        if (m >= w.m_end) continue;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < S; sp++) {
+            const float4 x = *reinterpret_cast<const float4*>(sm + (size_t)sp * (slice / 4) + rr * L + 4 * g);
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+        }
+        float o[4] = {alpha * a.x, alpha * a.y, alpha * a.z, alpha * a.w};
+        const int n = w.n_t0 + 4 * g;
+        if (beta != 0.0f) {
+            if (c_ring) {
+                const float4 cv = *reinterpret_cast<const float4*>(sm + c_off / 4 + rr * L + 4 * g);
+                o[0] = fmaf(beta, cv.x, o[0]);
+                o[1] = fmaf(beta, cv.y, o[1]);
+                o[2] = fmaf(beta, cv.z, o[2]);
+                o[3] = fmaf(beta, cv.w, o[3]);
+            } else {
+                const float* cp = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc + n;
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    if (n + e < w.n_end) o[e] = fmaf(beta, cp[e], o[e]);
+            }
+        }
+        put4_clipped<EPI>(p, w, m, n, o);
+    }
+    return true;
+}
+
 // Wait until the previous kernel on the stream (programmatic dependent
 // launch) has completed and its memory operations are visible; returns at
 // once when there is none.
@@ -1023,14 +1130,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     const uint32_t epi0 = base + kRingBytes;
     const uint32_t bar0 = epi0 + kStageBytesEpi;
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + (bar0 - base));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
     volatile int* epi_abort = reinterpret_cast<volatile int*>(tmem_slot + 3);
     // Region table copy: 512 bytes into the 1 KB barrier area (barriers and
     // flags use the first ~250 bytes).
     static_assert(sizeof(Region) * MP_MAX_REGIONS <= kBarBytes - 512, "region table does not fit");
-    static_assert((2 * kMaxStages + 5) * 8 + 16 <= 512, "barriers do not fit");
+    static_assert((2 * kMaxStages + 6) * 8 + 16 <= 512, "barriers do not fit");
     Region* regs_s = reinterpret_cast<Region*>(gbase + (bar0 - base) + 512);
 
     const int nst = p.num_stages;
@@ -1042,6 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     auto accf = [&](int b) { return bar0 + 8u * (2 * kMaxStages + b); };
     auto acce = [&](int b) { return bar0 + 8u * (2 * kMaxStages + 2 + b); };
     const uint32_t done_bar = bar0 + 8u * (2 * kMaxStages + 4);
+    const uint32_t red_bar = bar0 + 8u * (2 * kMaxStages + 5);  // split-K sums staged in the idle ring
     const uint64_t limit = p.wait_limit_ns;
 
     const int warp = threadIdx.x >> 5;
@@ -1066,6 +1174,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             mbar_init(acce(b), kPair ? 8 : 4);
         }
         mbar_init(done_bar, 1);
+        mbar_init(red_bar, 1);
         *abort_flag = 0;
         *s_last = 0;
         *epi_abort = 0;
@@ -1311,6 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t slab = 0;  // running slab index of this warp's bulk stores
         int acc = 0;
         uint32_t aph = 0;
+        uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
             if (p.beta != 0.0f && w.splits == 1 && !w.swap) {
@@ -1570,13 +1680,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     named_bar_sync(1, 128);
                     const int arrived = *s_last;
                     named_bar_sync(1, 128);
+                    bool reduced = true;
                     if (arrived) {
                         __threadfence();
                         const int R = w.swap ? w.bn : 128;
                         const int r0 = (int)((long long)R * w.split / w.splits);
                         const int r1 = (int)((long long)R * (w.split + 1) / w.splits);
-                        reduce_rows<EPI>(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
+                        // The ring is idle once this is the CTA's last unit:
+                        // every copy it loaded has been consumed by MMAs that
+                        // have completed.
+                        if (r1 > r0 && u + ustep >= p.total_units &&
+                            ring_reduce_bytes(p, w, r0, r1) <= (uint32_t)kRingBytes) {
+                            // The partials were written by other CTAs' generic or
+                            // bulk stores; the copies read them through the async proxy.
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            reduced = reduce_rows_ring<EPI>(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64,
+                                                            ring0, gbase, red_bar, red_ph, abort_flag, limit);
+                            red_ph ^= 1u;
+                        } else {
+                            reduce_rows<EPI>(p, w, p.ws + w.ws_tile, r0, r1, threadIdx.x - 64);
+                        }
                         named_bar_sync(1, 128);
+                    }
+                    if (arrived && reduced) {
                         if (threadIdx.x == 64) {
                             // The last split to leave resets the counter for the next launch.
                             const unsigned old = atomicAdd(p.cnt + w.cnt, 1u);
