@@ -292,17 +292,24 @@ mp_status mp_gemm_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
  * that own all device memory, processes that reserve device memory up front,
  * and latency-critical loops where an allocation may synchronize the device.
  *
- * Same operands, layout rules and errors as mp_gemm (one problem, on the
- * current device).  Its scratch is a fixed array inside the library, about
- * 48 MiB on every GPU that loads the library, held until the process exits:
+ * Same operands, layout rules and argument errors as mp_gemm (one problem, on
+ * the current device).  A kernel that gives up on a bounded wait records it
+ * in a status word of the fixed array; mp_check_noalloc reads it back (there
+ * is no handle for mp_check).  Its scratch is a fixed array inside the
+ * library, about 48 MiB per GPU, held until the process exits:
  * 16 MiB of split-K partials (the planner never asks for more), 4096 tile
  * counters, a status word, and a 32 MiB staging area for operands whose rows
  * are not 16-byte aligned.  A request that would need more than that -- an
  * unaligned operand above 32 MiB after padding its rows to 8 elements -- is
  * rejected with MP_ERR_UNSUPPORTED before anything runs.
  *
- * The first call on a device finds the array's address and clears it with a
- * synchronous cudaMemset; make that first call before any stream capture.
+ * The array's device memory is committed when the library's device code
+ * loads on a GPU: under CUDA's default lazy module loading that is the first
+ * call on the device (with CUDA_MODULE_LOADING=EAGER, when the library
+ * loads).  A caller that reserves nearly all device memory for its own pool
+ * should make one call before reserving it.  The first call on a device also
+ * finds the array's address and clears it with a synchronous cudaMemset;
+ * make that first call before any stream capture.
  * Every call shares the array and starts from what the previous call left:
  * the counters a call needs are cleared on `stream` before its kernel.  Calls
  * whose kernels overlap on the GPU (other streams, other host threads) race
@@ -315,6 +322,22 @@ mp_status mp_gemm_noalloc(int64_t M, int64_t N, int64_t K,
                           const float* C, int64_t ldc,
                           float* D, int64_t ldd,
                           float alpha, float beta, mp_stream stream);
+
+/*
+ * mp_check for mp_gemm_noalloc on the current device: synchronize `stream`
+ * and read the fixed array's status word.  MP_OK (also when no call has run
+ * on this device), MP_ERR_DEVICE_TIMEOUT if one of its kernels gave up on a
+ * bounded wait since the last check (the word and the array's tile counters
+ * are then cleared), or MP_ERR_CUDA.  Allocates nothing.  No counterpart on
+ * the pages, like mp_gemm_noalloc itself.
+ */
+mp_status mp_check_noalloc(mp_stream stream);
+
+/*
+ * Test hook: mp_inject_wait_timeout for the next mp_gemm_noalloc launch on
+ * the current device (the same `enable` modes and limit).
+ */
+mp_status mp_noalloc_inject_wait_timeout(int32_t enable, int64_t limit_ns);
 
 /*
  * Synchronize `stream` and read the device status word: MP_OK, or
@@ -330,13 +353,16 @@ mp_status mp_check(mp_handle h, mp_stream stream);
 mp_status mp_force_plan(mp_handle h, int32_t kernel, int32_t splits);
 
 /*
- * Test hook for failure detection: with enable != 0 the next launch on this
+ * Test hook for failure detection: with enable = 1 the next launch on this
  * handle (of any kernel: GEMM, fused pair, convolution, grouped GEMM)
  * withholds one shared-memory stage of its first work unit, so the
  * consumer's bounded wait runs out after limit_ns nanoseconds (0 keeps the
  * handle's limit, 1 s by default; a positive value also becomes the limit of
- * later launches).  The kernel then stops cleanly and mp_check reports
- * MP_ERR_DEVICE_TIMEOUT.  Nothing faults, traps or hangs.
+ * later launches).  With enable = 2 the GEMM kernel instead makes the
+ * split-K sums it stages in its idle operand ring wait for 16 bytes more
+ * than it copies (the other kernels treat 2 as 1).  The kernel then stops
+ * cleanly and mp_check reports MP_ERR_DEVICE_TIMEOUT.  Nothing faults, traps
+ * or hangs.  0 clears a pending injection; other values: MP_ERR_INVALID_ARG.
  */
 mp_status mp_inject_wait_timeout(mp_handle h, int32_t enable, int64_t limit_ns);
 

@@ -19,6 +19,7 @@ __all__ = [
     "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched",
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
     "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
+    "mp_check_noalloc", "mp_noalloc_inject_wait_timeout",
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
     "MpHw", "MpKernelDesc", "MpRegionInfo", "MpPlanInfo", "MP_MAX_REGIONS", "MP_MAX_KERNELS",
@@ -151,6 +152,8 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_gemm_noalloc": ([_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                                      _f, _f, _vp], ctypes.c_int),
                 "mp_check": ([_vp, _vp], ctypes.c_int),
+                "mp_check_noalloc": ([_vp], ctypes.c_int),
+                "mp_noalloc_inject_wait_timeout": ([_i32, _i64], ctypes.c_int),
                 "mp_force_plan": ([_vp, _i32, _i32], ctypes.c_int),
                 "mp_get_hw": ([_vp, ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
                                ctypes.POINTER(_i32)], ctypes.c_int),
@@ -550,6 +553,19 @@ def mp_set_kernel_model(h: Handle, k: int, fixed_us: float, per_step_us: float) 
     _check(library().mp_set_kernel_model(h.ptr, k, fixed_us, per_step_us), "mp_set_kernel_model")
 
 
-def mp_inject_wait_timeout(h: Handle, enable: bool = True, limit_ns: int = 0) -> None:
-    _check(library().mp_inject_wait_timeout(h.ptr, 1 if enable else 0, int(limit_ns)),
+def mp_inject_wait_timeout(h: Handle, enable=True, limit_ns: int = 0) -> None:
+    """enable: True or 1 withholds a pipeline stage of the next launch; 2 makes
+    the GEMM kernel's ring-staged split-K sums wait for bytes that never come;
+    False or 0 clears it."""
+    _check(library().mp_inject_wait_timeout(h.ptr, int(enable), int(limit_ns)),
            "mp_inject_wait_timeout")
+
+
+def mp_check_noalloc(stream=None) -> int:
+    """mp_check for mp_gemm_noalloc on the current device (no handle)."""
+    return int(library().mp_check_noalloc(_stream_ptr(stream)))
+
+
+def mp_noalloc_inject_wait_timeout(enable=True, limit_ns: int = 0) -> None:
+    _check(library().mp_noalloc_inject_wait_timeout(int(enable), int(limit_ns)),
+           "mp_noalloc_inject_wait_timeout")

@@ -158,6 +158,7 @@ struct DeviceState {
     EncodeTiledFn encode = nullptr;
     bool log = false;
     int inject_timeout = 0;
+    int64_t num_counters = kMaxCounters;  // split-K tile counters at `cnt`
     uint64_t wait_limit_ns = 1000000000ull;  // 1 s
     // Tensor-map cache (only for handles, which serve one host thread).
     TmEntry* tm_cache = nullptr;
@@ -302,11 +303,12 @@ bool encode_tiled(DeviceState* s, CUtensorMap* m, CUtensorMapDataType dt, uint32
 }
 
 bool encode_3d(DeviceState* s, CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
-               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     const uint64_t dims[3] = {d0, d1, d2};
     const uint64_t strides[2] = {stride1_bytes, stride2_bytes};
     const uint32_t box[3] = {box0, box1, 1};
-    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box);
+    return encode_tiled(s, m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, swz);
 }
 
 // fp32 output view [d2][d1][d0] for bulk tensor stores, box {box0, box1, 1}.
@@ -410,7 +412,7 @@ mp_status device_init(mp_handle h, int device) {
 // library image), so nothing is allocated here.  One state per device,
 // kept in static storage; call with `device` current.
 mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_floats, unsigned int* cnt,
-                              int* err, uint8_t* staging, int64_t staging_bytes) {
+                              int64_t num_counters, int* err, uint8_t* staging, int64_t staging_bytes) {
     static DeviceState fixed_states[kMaxFixedDevices];
     if (device < 0 || device >= kMaxFixedDevices) return MP_ERR_UNSUPPORTED;
     cudaDeviceProp prop;
@@ -421,6 +423,7 @@ mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_flo
     s->num_sms = prop.multiProcessorCount;
     s->ws = ws;
     s->cnt = cnt;
+    s->num_counters = num_counters;
     s->err = err;
     s->staging = staging;
     s->staging_bytes = staging_bytes;
@@ -476,7 +479,7 @@ mp_status device_check(mp_handle h, void* stream) {
     if (e != 0) {
         // An aborted launch may leave split-K counters mid-count: clear them.
         cudaMemset(s->err, 0, sizeof(int));
-        cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)kMaxCounters);
+        cudaMemset(s->cnt, 0, sizeof(unsigned) * (size_t)s->num_counters);
         if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
         return MP_ERR_DEVICE_TIMEOUT;
     }
@@ -556,11 +559,14 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         // and the numbers of 64-column blocks a B copy covers.
         int as_rows = 128;
         bool need_b4[4] = {false, false, false, false};
+        bool need_bs = false;
         for (int i = 0; i < plan.num_regions; i++) {
             const mp_region_info& r = plan.region[i];
             if (r.swap) {
                 as_rows = std::min(as_rows, (int)r.um);
                 need_b4[1] = true;
+            } else if (r.pair && r.un == 192) {
+                need_bs = true;  // 96-column halves: 32-column boxes, 64-byte swizzle
             } else if (r.un >= 64 && r.un <= 256) {
                 const int nblk = (int)(r.un / 64);
                 if (r.pair) {  // each CTA of a pair holds half of the blocks
@@ -577,6 +583,11 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             !encode_3d(s, &p.tmAs, A, K, M, bA, lda * 2, a_s2, 64, (uint32_t)as_rows) ||
             !encode_3d(s, &p.tmB, B, N, K, bB, ldb * 2, b_s2, 64, 64))
             return MP_ERR_CUDA;
+        if (need_bs) {
+            if (!encode_3d(s, &p.tmBs, B, N, K, bB, ldb * 2, b_s2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+                return MP_ERR_CUDA;
+            p.bs_ok = 1;
+        }
         // Whole-tile B copies: B as [batch][N/64][K][64] (block stride 128 B).
         // Only full 64-column blocks are addressable, so nothing past a row
         // end is ever read; tiles reaching past the last full block load per
@@ -654,7 +665,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
         const int bn = r.swap ? r.um : r.un;
         if (r.uk != kUk || bn < 16 || bn > kMaxBn || bn % 16 != 0 || (r.pair != 0) != (pair != 0) ||
             (!r.swap && !r.pair && (r.um != 128 || bn % 64 != 0)) || (r.swap && (r.un != 128 || r.pair)) ||
-            (r.pair && (r.um != 256 || (bn != 128 && bn != 256) || r.splits != 1)))
+            (r.pair && (r.um != 256 || (bn != 128 && bn != 192 && bn != 256) || r.splits != 1)))
             return MP_ERR_PLAN;
         d.m0 = (int)r.m0;
         d.n0 = (int)r.n0;
@@ -706,12 +717,13 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     int bn_max = 16;
     for (int i = 0; i < p.num_regions; i++) bn_max = std::max(bn_max, p.reg[i].bn);
     // The single MMA-issuing thread pays a fixed cost per stage (barrier
-    // wait, fence, commit) on top of each MMA; two K steps per stage halve
-    // that cost per MMA wherever the ring still holds at least three stages.
-    // CTA pairs issue one MMA for two SMs, so there the deeper ring of
-    // single K steps hides more latency (measured: 6 x 32 KB beats 3 x 64 KB).
+    // check, fence, commit: about 350 cycles measured on GB300) on top of
+    // about 70 cycles per MMA; two K steps per stage halve that cost per MMA
+    // wherever the ring still holds at least three stages.  Measured on CTA
+    // pairs with a 3072-deep K loop: 256 x 128 units 17.8 -> 12.9 us, 256 x 192
+    // 17.8 -> 16.6 us; 256 x 256 within 3% either way.
     p.sub_bytes = dev::kXBytes + (pair ? bn_max / 2 : bn_max) * 128;  // a pair's CTA holds half of B
-    p.kg = (!pair && 3 * 2 * p.sub_bytes <= dev::kRingBytes) ? 2 : 1;
+    p.kg = (3 * 2 * p.sub_bytes <= dev::kRingBytes) ? 2 : 1;
     p.stage_bytes = p.kg * p.sub_bytes;
     p.num_stages = std::min(dev::kMaxStages, dev::kRingBytes / p.stage_bytes);
 
@@ -1094,12 +1106,13 @@ mp_status device_run_grouped(mp_handle h, const mp_grouped_plan& pl, int32_t cou
 
 }  // namespace mp
 
-// Test hook for the bounded waits: the next launch withholds one stage so
-// that the consumer's wait runs out after `limit_ns`; mp_check then reports
+// Test hook for the bounded waits: the next launch withholds one stage (1),
+// or makes the ring-staged split-K sums wait for bytes that never come (2),
+// so that a bounded wait runs out after `limit_ns`; mp_check then reports
 // MP_ERR_DEVICE_TIMEOUT.  limit_ns == 0 keeps the current limit.
 extern "C" mp_status mp_inject_wait_timeout(mp_handle h, int32_t enable, int64_t limit_ns) {
-    if (!h || !h->dev || limit_ns < 0) return MP_ERR_INVALID_ARG;
-    h->dev->inject_timeout = enable ? 1 : 0;
+    if (!h || !h->dev || limit_ns < 0 || enable < 0 || enable > 2) return MP_ERR_INVALID_ARG;
+    h->dev->inject_timeout = enable;
     if (limit_ns > 0) h->dev->wait_limit_ns = (uint64_t)limit_ns;
     return MP_OK;
 }

@@ -102,7 +102,7 @@ mp_status device_check(mp_handle h, void* stream);
 // Remove micro-kernels the handle's device cannot run (CTA pairs).
 void drop_unavailable_kernels(mp_handle h);
 mp_status device_attach_fixed(mp_handle h, int device, float* ws, int64_t ws_floats, unsigned int* cnt,
-                              int* err, uint8_t* staging, int64_t staging_bytes);
+                              int64_t num_counters, int* err, uint8_t* staging, int64_t staging_bytes);
 // Argument rules of mp_gemm (mp_api.cpp).
 mp_status validate_args(const GemmArgs& a);
 

@@ -93,6 +93,10 @@ struct alignas(128) Params {
     // B viewed as [batch][N/64 full blocks][K][64]: box {64, 64 (K), j+1 blocks}
     // fetches j+1 adjacent 64-column blocks in one copy (encoded when used).
     CUtensorMap tmB4[4];
+    // B with the 64-byte swizzle, box {32 (N), 64 rows of K}: the 96-column
+    // halves of 256 x 192 pair tiles, in atoms of 32 columns (encoded when used).
+    CUtensorMap tmBs;
+    int bs_ok;           // 1: tmBs is encoded
     int nb_full;         // floor(N / 64): blocks tmB4 may address
     int b4_mask;         // bit j: tmB4[j] is encoded (prefetched at set-up)
     int as_rows;         // rows per A box of swapped tiles (divides every swapped bn)
@@ -104,7 +108,8 @@ struct alignas(128) Params {
     int a_bstep, b_bstep;
     int total_units;
     int num_regions;
-    int inject_timeout;  // test hook: withhold the first stage of the first unit
+    int inject_timeout;  // test hook: 1 withholds the first stage of the first unit; 2 makes the
+                         // ring-staged split-K sums wait for 16 bytes that never come
     int vec_c, vec_d;    // C / D rows allow 16-byte (fp32 D) or 8-byte (bf16 D) vector access
     int act;             // activation on alpha*acc + beta*C: 0 none, 1 ReLU, 2 GELU (erf form)
     int out_bf16;        // 1: D is bf16 (round to nearest even), else fp32
@@ -508,14 +513,15 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
-// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// stride byte offsets (16-byte units), descriptor version 1, and the swizzle
+// mode (2: 128-byte, 4: 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz = 2) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)swz << 61;
     return d;
 }
 
@@ -530,6 +536,13 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kstep) {
 // UMMA K step (16 rows) advances 2048 B.
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kstep) {
     return smem_desc(tile + 2048u * kstep, 8192u, 1024u);
+}
+
+// MN-major operand with the 64-byte swizzle: atoms of 32 MN elements x 8 K
+// rows (512 B); K groups of 8 rows 512 B apart, 32-wide MN blocks 4096 B
+// apart (one TMA box each); one UMMA K step (16 rows) advances 1024 B.
+__device__ __forceinline__ uint64_t desc_mnmajor64(uint32_t tile, int kstep) {
+    return smem_desc(tile + 1024u * kstep, 4096u, 512u, 4u);
 }
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, M = m (128, or
@@ -1017,7 +1030,11 @@ __device__ __forceinline__ bool reduce_rows_ring(const Params& p, const Work& w,
     const int rows_c = c_ring ? max(0, min(r1, w.m_end - w.m_t0) - r0) : 0;
     const uint32_t c_off = (uint32_t)S * slice;
     if (tid < 32) {
-        if (tid == 0) mbar_arrive_expect_tx(bar, (uint32_t)S * slice + (uint32_t)rows_c * (uint32_t)L * 4u);
+        // (Test hook 2: expect 16 bytes more than are copied, so that the
+        // bounded wait below runs out.)
+        if (tid == 0)
+            mbar_arrive_expect_tx(bar, (uint32_t)S * slice + (uint32_t)rows_c * (uint32_t)L * 4u +
+                                           (p.inject_timeout == 2 ? 16u : 0u));
         __syncwarp();
         for (int s = tid; s < S; s += 32)
             bulk_load(ring + (uint32_t)s * slice, tile_ws + s * part_floats + (long long)r0 * L, slice, bar);
@@ -1187,6 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         for (int j = 0; j < 4; j++)
             if (p.b4_mask & (1 << j)) tma_prefetch_map(&p.tmB4[j]);
         if (p.tma_d) tma_prefetch_map(&p.tmD);
+        if (p.bs_ok) tma_prefetch_map(&p.tmBs);
         for (int i = 0; i < MP_MAX_REGIONS; i++)
             if (p.w_mask & (1 << i)) tma_prefetch_map(&p.tmW[i]);
     }
@@ -1233,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         const uint32_t pid = warp == 0 ? 0u : 1u;
         uint32_t g = 0;
         uint32_t armed_mask = 0, armed_ph = 0;
-        bool withhold = pid == 0 && p.inject_timeout != 0;
+        bool withhold = pid == 0 && p.inject_timeout == 1;
         bool dep_done = false;
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
@@ -1264,7 +1282,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                             // This CTA's 128 rows of A and its half of B's
                             // 64-column blocks (rank r: blocks [r h, r h + h)).
                             const int h = nblk >> 1, first = rank * h;
-                            if (leader) {
+                            if (w.bn == 192) {
+                                // 96 columns per CTA: three 32-column boxes
+                                // (64-byte swizzle) from lanes 1..3.
+                                const int x = w.n_t0 + 96 * rank + 32 * (lane - 1);
+                                if (leader) {
+                                    if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
+                                    else if (lane <= 3) tma_load_3d(ys + (lane - 1) * 4096, &p.tmBs, fb, x, kc, bb);
+                                } else {
+                                    if (lane == 0) tma_load_3d_pair(xs, &p.tmA, fb, kc, w.m_t0, ab);
+                                    else if (lane <= 3) tma_load_3d_pair(ys + (lane - 1) * 4096, &p.tmBs, fb, x, kc, bb);
+                                }
+                            } else if (leader) {
                                 if (lane == 0) tma_load_3d(xs, &p.tmA, fb, kc, w.m_t0, ab);
                                 if (whole_b) {
                                     if (lane == 1) tma_load_4d(ys, &p.tmB4[h - 1], fb, 0, kc, blk0 + first, bb);
@@ -1355,9 +1384,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             // shared addresses stay below 2^18, so the sums never carry out of
             // the field): one 64-bit add per operand.
             const uint64_t dx0 = w.swap ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
-            const uint64_t dy0 = w.swap ? desc_kmajor(ring0 + kXBytes, 0) : desc_mnmajor(ring0 + kXBytes, 0);
+            // Pairs of 192-wide tiles hold B with the 64-byte swizzle.
+            const bool b64 = kPair && w.bn == 192;
+            const uint64_t dy0 = w.swap ? desc_kmajor(ring0 + kXBytes, 0)
+                                 : b64  ? desc_mnmajor64(ring0 + kXBytes, 0)
+                                        : desc_mnmajor(ring0 + kXBytes, 0);
             const uint32_t kx = w.swap ? (2048u >> 4) : (32u >> 4);
-            const uint32_t ky = w.swap ? (32u >> 4) : (2048u >> 4);
+            const uint32_t ky = w.swap ? (32u >> 4) : b64 ? (1024u >> 4) : (2048u >> 4);
             const uint32_t sstep = stage_bytes >> 4, jstep = sub_bytes >> 4;
             // One wait and one commit per stage of kg (1 or 2) K steps.
             for (int kb = w.kb0; kb < w.kb1; kb += kg) {

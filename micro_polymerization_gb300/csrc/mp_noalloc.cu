@@ -11,8 +11,12 @@
 // mp_gemm needs an mp_handle, and mp_init allocates the handle's split-K
 // workspace, tile counters, status word and staging area with cudaMalloc.
 // This entry point needs no handle: its scratch is one fixed array that is
-// part of the library image (kScratchBytes below, about 48 MiB), placed on
-// every GPU that loads the library and held until the process exits.
+// part of the library image (kScratchBytes below, about 48 MiB).  Its device
+// memory is committed when the library's device code is loaded on a GPU: at
+// the first call on that device under CUDA's default lazy module loading (or
+// when the library loads, with CUDA_MODULE_LOADING=EAGER), and it is held
+// until the process exits.  A caller that reserves nearly all device memory
+// up front should make one call first.
 //
 // Layout of the array: split-K partials (16 MiB of fp32), tile counters (4096
 // x 32 bit), the device status word, and a 32 MiB staging area for operands
@@ -69,7 +73,8 @@ mp_status setup(int device, PerDevice** out) {
         uint8_t* staging = p + kPartialBytes + kCounterBytes + kStatusBytes;
         if (cudaMemset(counters, 0, kCounterBytes + kStatusBytes) != cudaSuccess) return MP_ERR_CUDA;
         mp_status st = mp::device_attach_fixed(&d.handle, device, partials, (int64_t)(kPartialBytes / sizeof(float)),
-                                               counters, status, staging, (int64_t)kStagingBytes);
+                                               counters, (int64_t)kCounterCount, status, staging,
+                                               (int64_t)kStagingBytes);
         if (st != MP_OK) return st;
         mp::default_gb300_kernels(d.handle.hw, d.handle.kernels, &d.handle.num_kernels);
         mp::drop_unavailable_kernels(&d.handle);
@@ -112,4 +117,32 @@ extern "C" mp_status mp_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void
         return MP_ERR_CUDA;
     // Operands needing more than the 32 MiB staging area give MP_ERR_UNSUPPORTED here.
     return mp::device_run(&d->handle, plan, a);
+}
+
+// The fixed status word of the current device: a kernel of mp_gemm_noalloc
+// that gave up on a bounded wait left a nonzero code there.  Synchronize
+// `stream`, read the word, and on a nonzero code clear it and the tile
+// counters (an aborted split may leave them mid-count).  Copies and memsets
+// only: nothing is allocated.
+extern "C" mp_status mp_check_noalloc(mp_stream stream) {
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return MP_ERR_CUDA;
+    if (device < 0 || device >= mp::kMaxFixedDevices) return MP_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        if (!g_devices[device].ready) return MP_OK;  // nothing has run on this device
+    }
+    return mp_check(&g_devices[device].handle, stream);
+}
+
+// Test hook for the bounded waits of mp_gemm_noalloc on the current device
+// (the same modes as mp_inject_wait_timeout).  Sets the device up first when
+// no call has done so yet.
+extern "C" mp_status mp_noalloc_inject_wait_timeout(int32_t enable, int64_t limit_ns) {
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return MP_ERR_CUDA;
+    PerDevice* d = nullptr;
+    mp_status st = setup(device, &d);
+    if (st != MP_OK) return st;
+    return mp_inject_wait_timeout(&d->handle, enable, limit_ns);
 }

@@ -28,6 +28,7 @@
 #include <vector>
 #include <chrono>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "mp_internal.h"
@@ -562,22 +563,31 @@ mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_
 // D^T = B^T A^T: the UMMA M = 128 runs over N and the short M becomes the
 // UMMA N (16..128), so a skinny M wastes no tensor-core rows.  Pair kernels
 // put a 256-row tile on two SMs (pair MMA): each SM loads 128 rows of A and
-// half of B's columns, so operand bytes per MMA fall by a third (256 wide) or
-// a quarter (128 wide); a task holds two SMs, and the cluster set-up and
-// exit cost a fixed extra.
+// half of B's columns, so operand bytes per MMA fall by a third (256 wide),
+// by 30% (192 wide) or by a quarter (128 wide); a task holds two SMs, and the
+// cluster set-up and exit cost a fixed extra.
 void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
     struct G { int um, un, swap, pair; };
     static const G kSet[] = {
         {128, 256, 0, 0}, {128, 192, 0, 0}, {128, 128, 0, 0}, {128, 64, 0, 0},
         {16, 128, 1, 0},  {32, 128, 1, 0},  {64, 128, 1, 0},  {128, 128, 1, 0},
-        {256, 256, 0, 1}, {256, 128, 0, 1},
+        {256, 256, 0, 1}, {256, 128, 0, 1}, {256, 192, 0, 1},
     };
     const double pe = std::max(1, hw.num_pe);
     const double mma_pe = hw.mma_tflops > 0 ? hw.mma_tflops / pe : 13.0;   // TFLOP/s per PE
     const double l2_pe = hw.l2_gbs > 0 ? hw.l2_gbs / pe : 120.0;          // GB/s per PE
     const double hbm_pe = hw.hbm_gbs > 0 ? hw.hbm_gbs / pe : 45.0;
+    // The 256 x 192 pair joins the set only with MP_PAIR192=1.  Measured on
+    // GB300 against the set without it (the same box, back to back): it runs
+    // its K loop about 10% faster than the one-CTA 128 x 192 tile on the
+    // (3520..4032, 768, 3072) GEMMs that the model gives it, yet the
+    // dynamic-sequence step is 2% slower with it (0.887 against 0.869 ms), and
+    // the stress and merged workloads are even.
+    const char* p192 = std::getenv("MP_PAIR192");
+    const bool with_192 = p192 && p192[0] == '1';
     int32_t c = 0;
     for (const G& g : kSet) {
+        if (g.pair && g.un == 192 && !with_192) continue;
         mp_kernel_desc& d = out[c++];
         d.um = g.um;
         d.un = g.un;

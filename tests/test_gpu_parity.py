@@ -27,7 +27,7 @@ def rand_problem(M, N, K, seed, beta=0.0):
 # --------------------------------------------------------------------------
 # small shapes: brute force over every combination of tiny sizes
 # --------------------------------------------------------------------------
-TINY = [1, 2, 3, 5, 8, 9]
+TINY = list(range(1, 10))  # every combination of sizes 1..9
 
 
 def test_tiny_shapes_bruteforce():
@@ -113,22 +113,55 @@ def test_pair_kernels_match_single_cta_kernels_and_oracle(M, N, K):
     CTA each compute: the same MMAs per output row, so the outputs agree bit
     for bit.  Odd tile-row counts leave the second half of the last pair past
     the end of D."""
-    h = handle()
-    ks = _kernels()
-    pairs = [(k, d) for k, d in enumerate(ks) if d.pair]
-    assert {(d.um, d.un) for _, d in pairs} == {(256, 256), (256, 128)}
+    h = _handle_with_pair192()
     try:
+        _, ks = mp.mp_get_hw(h)
+        pairs = [(k, d) for k, d in enumerate(ks) if d.pair]
+        assert {(d.um, d.un) for _, d in pairs} == {(256, 256), (256, 192), (256, 128)}
         for k, d in pairs:
             single = next(i for i, e in enumerate(ks) if not e.pair and not e.swap and e.un == d.un)
             A, B, C = rand_problem(M, N, K, seed=k * 7 + M, beta=0.5)
             mp.mp_force_plan(h, single, 1)
-            D1 = run_gemm(A, B, C, 1.25, 0.5)
+            D1 = run_gemm(A, B, C, 1.25, 0.5, h=h)
             mp.mp_force_plan(h, k, 1)
-            D2 = run_gemm(A, B, C, 1.25, 0.5)
+            D2 = run_gemm(A, B, C, 1.25, 0.5, h=h)
             assert torch.equal(D1, D2), f"pair kernel {k} ({d.um}x{d.un}) {(M, N, K)}"
             assert_parity(D2, A, B, C, 1.25, 0.5, what=f"pair kernel {k} {(M, N, K)}")
     finally:
-        mp.mp_force_plan(h, -1, 0)
+        h.close()
+
+
+def _handle_with_pair192():
+    """A handle whose set includes the 256 x 192 pair (opt-in: MP_PAIR192=1)."""
+    import os
+    os.environ["MP_PAIR192"] = "1"
+    try:
+        return mp.mp_init(0)
+    finally:
+        del os.environ["MP_PAIR192"]
+
+
+def test_pair192_is_opt_in_and_matches_oracle_on_every_edge():
+    """The 256 x 192 pair (each CTA holding 96 columns of B with the 64-byte
+    swizzle) is left out of the default set and joins it with MP_PAIR192=1,
+    after the other kernels.  Ragged rows and columns (a last pair half past M,
+    a CTA's 96 columns past N, wholly or partly), beta * C, and a K loop not a
+    multiple of 64."""
+    ks_default = _kernels()
+    assert not any(d.pair and d.un == 192 for d in ks_default)
+    h = _handle_with_pair192()
+    try:
+        _, ks = mp.mp_get_hw(h)
+        assert [(d.um, d.un, d.swap, d.pair) for d in ks[:len(ks_default)]] == \
+               [(d.um, d.un, d.swap, d.pair) for d in ks_default]
+        k = next(i for i, d in enumerate(ks) if d.pair and d.un == 192)
+        for (M, N, K) in [(300, 520, 700), (129, 97, 65), (700, 192 * 3, 1000), (513, 1000, 333)]:
+            mp.mp_force_plan(h, k, 1)
+            A, B, C = rand_problem(M, N, K, seed=M + N, beta=0.5)
+            D = run_gemm(A, B, C, 1.5, 0.5, h=h)
+            assert_parity(D, A, B, C, 1.5, 0.5, what=f"pair 256x192 {(M, N, K)}")
+    finally:
+        h.close()
 
 
 def test_pair_kernel_launches_as_cluster(capfd):
@@ -652,3 +685,100 @@ def test_bounded_waits_of_the_other_kernels_report_and_recover():
     finally:
         mp.mp_set_b2b_mode(h, mp.MP_B2B_AUTO)
         mp.mp_inject_wait_timeout(h, False, 1_000_000_000)
+
+
+# --------------------------------------------------------------------------
+# split-K sums staged in the idle operand ring (a CTA's last unit)
+# --------------------------------------------------------------------------
+def _ring_kernels():
+    ks = _kernels()
+    normal = next(i for i, d in enumerate(ks) if not d.pair and not d.swap and d.un == 128)
+    swapped = next(i for i, d in enumerate(ks) if d.swap and d.um == 32)
+    return normal, swapped
+
+
+@pytest.mark.parametrize("c_offset", [0, 1])
+def test_ring_staged_split_sums(c_offset):
+    """Twelve splits (more than a cluster holds on chip) of a few tiles: every
+    CTA's only unit is a split, so its 1/S of the tile's rows are summed from
+    partials bulk-copied into the idle ring.  Normal and swapped tiles, a
+    ragged last row tile, beta * C with C's rows 16-byte aligned (copied into
+    the ring too) and offset by 4 bytes (read directly), against the oracle."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    normal, swapped = _ring_kernels()
+    try:
+        for k, (M, N, K) in [(normal, (200, 300, 2000)), (normal, (130, 256, 1500)),
+                             (swapped, (50, 300, 2000)), (swapped, (77, 128, 1300))]:
+            mp.mp_force_plan(h, k, 12)
+            p = mp.mp_plan(h, M, N, K)
+            assert p.total_tasks <= mp.mp_get_hw(h)[0].num_pe, "one unit per CTA"
+            A, B, C = rand_problem(M, N, K, seed=M + K + c_offset, beta=0.5)
+            # C stored with row pitch N + 4 starting c_offset floats into its buffer.
+            store = torch.zeros(M * (N + 4) + 4, dtype=torch.float32, device=dev)
+            Cv = store[c_offset:c_offset + M * (N + 4)].view(M, N + 4)[:, :N]
+            Cv.copy_(C.to(dev))
+            D = torch.full((M, N), float("nan"), device=dev)
+            mp.mp_gemm(h, A.to(dev), B.to(dev), Cv, D, 1.5, 0.5)
+            torch.cuda.synchronize()
+            assert_parity(D.cpu(), A, B, C, 1.5, 0.5, what=f"ring sums kernel {k} {(M, N, K)} C+{4 * c_offset}B")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
+def test_ring_staged_split_sums_timeout_reports_and_recovers():
+    """Hook mode 2: the ring-staged sums wait for 16 bytes more than are
+    copied; the bounded wait runs out, mp_check reports it, and the next call
+    is correct."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    normal, _ = _ring_kernels()
+    A, B, C = rand_problem(200, 300, 2000, seed=77, beta=0.5)
+    try:
+        mp.mp_force_plan(h, normal, 12)
+        D = torch.empty(200, 300, device=dev)
+        mp.mp_inject_wait_timeout(h, 2, 50_000_000)  # 50 ms
+        mp.mp_gemm(h, A.to(dev), B.to(dev), C.to(dev), D, 1.0, 0.5)
+        assert mp.mp_check(h) == mp.MP_ERR_DEVICE_TIMEOUT
+        mp.mp_inject_wait_timeout(h, 0, 1_000_000_000)
+        assert mp.mp_check(h) == mp.MP_OK
+        assert_parity(run_gemm(A, B, C, 1.0, 0.5), A, B, C, 1.0, 0.5, what="after ring timeout")
+    finally:
+        mp.mp_inject_wait_timeout(h, 0, 1_000_000_000)
+        mp.mp_force_plan(h, -1, 0)
+
+
+# --------------------------------------------------------------------------
+# the stress sweep: one GEMM of every plan class the polymerizer produces
+# --------------------------------------------------------------------------
+def _split_class(s):
+    return "none" if s == 1 else ("on-chip-size" if s <= 8 else "wide")
+
+
+def test_stress_every_plan_class():
+    """The 1001 stress shapes (alpha 1.5, beta 0.5) fall into classes by
+    (pattern, per region the micro-kernel and its split-K -- none, up to 8
+    ways, more --, and whether A's, B's and D's rows are 16-byte aligned).
+    The smallest shape of every class runs: the full oracle up to 2^30
+    multiply-adds, else every entry of the edge tiles, 4096 random entries
+    and a Freivalds probe of the whole product."""
+    h = handle()
+    gs = wl.workload("stress")
+    classes = {}
+    for g in gs:
+        p = mp.mp_plan(h, g.M, g.N, g.K)
+        key = (p.pattern, tuple((r.kernel, _split_class(r.splits)) for r in p.regions()),
+               (2 * g.K) % 16 == 0, (2 * g.N) % 16 == 0, (4 * g.N) % 16 == 0)
+        classes.setdefault(key, []).append(g)
+    assert sum(len(v) for v in classes.values()) == len(gs) == 1001
+    assert len(classes) >= 20, len(classes)
+    rng = np.random.default_rng(11)
+    for key in sorted(classes, key=str):
+        g = min(classes[key], key=lambda x: x.flops)
+        A, B, C = wl.make_operands(g)
+        D = run_gemm(A, B, C, g.alpha, g.beta)
+        what = f"stress class {key} via {(g.M, g.N, g.K)}"
+        if g.M * g.N * g.K <= 2 ** 30:
+            assert_parity(D, A, B, C, g.alpha, g.beta, what=what)
+        else:
+            assert_sampled_parity(D, A, B, C, g.alpha, g.beta, rng, what=what)
