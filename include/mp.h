@@ -166,6 +166,19 @@ mp_status mp_plan_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
                           mp_plan_info* out);
 
 /*
+ * Plan `count` shapes in one call: mnk holds (M, N, K) triples, host memory,
+ * read only; `out` (nullable) receives count plans, as mp_plan would.  Meant
+ * for planning a set of shape buckets ahead of time, and for timing the
+ * polymerizer itself without a language binding in the loop (MikPoly summary,
+ * section 5, cost model overhead: microseconds per shape).  Shapes already in
+ * the handle's plan cache are looked up, not searched; a handle made with
+ * MP_PLAN_CACHE=0 in the environment keeps no cache, so every call searches.
+ * Returns the first error (MP_ERR_INVALID_ARG for a negative or oversized
+ * dimension); plans before it are filled in.
+ */
+mp_status mp_plan_many(mp_handle h, int32_t count, const int64_t* mnk, mp_plan_info* out);
+
+/*
  * Cost of a given strategy under the handle's model [MP section 3, cost
  * model]: the caller fills num_regions and, per region, kernel, m0, n0,
  * m_ext, n_ext and splits; the call fills every other field and cost_us.

@@ -16,7 +16,7 @@ from typing import Optional
 from . import _build
 
 __all__ = [
-    "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched",
+    "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched", "mp_plan_many",
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
     "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
     "mp_check_noalloc", "mp_noalloc_inject_wait_timeout",
@@ -144,6 +144,7 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_destroy": ([_vp], ctypes.c_int),
                 "mp_plan": ([_vp, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
                 "mp_plan_batched": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
+                "mp_plan_many": ([_vp, _i32, ctypes.POINTER(_i64), ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
                 "mp_evaluate_plan": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo)], ctypes.c_int),
                 "mp_gemm": ([_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _i64,
                              _f, _f, _vp], ctypes.c_int),
@@ -253,6 +254,16 @@ def mp_plan_batched(h: Handle, batch: int, M: int, N: int, K: int) -> MpPlanInfo
     info = MpPlanInfo()
     _check(library().mp_plan_batched(h.ptr, batch, M, N, K, ctypes.byref(info)), "mp_plan_batched")
     return info
+
+
+def mp_plan_many(h: Handle, shapes, want_plans: bool = True):
+    """Plan a list of (M, N, K) in one library call; returns the plans (or
+    None when want_plans is False, which only runs the searches)."""
+    n = len(shapes)
+    flat = (_i64 * (3 * n))(*[int(x) for s in shapes for x in s])
+    out = (MpPlanInfo * max(1, n))() if want_plans else None
+    _check(library().mp_plan_many(h.ptr, n, flat, out), "mp_plan_many")
+    return [out[i] for i in range(n)] if want_plans else None
 
 
 def mp_evaluate_plan(h: Handle, batch: int, M: int, N: int, K: int, regions) -> MpPlanInfo:

@@ -53,8 +53,10 @@ void load_calibration(mp_handle h, const char* path) {
 mp_handle new_handle() {
     mp_handle h = new (std::nothrow) mp_handle_s();
     if (!h) return nullptr;
+    // MP_PLAN_CACHE=0: no plan cache, so that every call runs the search.
+    const char* pc = std::getenv("MP_PLAN_CACHE");
     try {
-        h->cache.resize(4096);
+        if (!(pc && pc[0] == '0')) h->cache.resize(4096);
     } catch (...) {
         delete h;
         return nullptr;
@@ -289,6 +291,18 @@ mp_status mp_plan_batched(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
     if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || batch >= kMaxDim) return MP_ERR_INVALID_ARG;
     mp_plan_info tmp;
     return mp::plan_shape(h, batch, M, N, K, out ? out : &tmp);
+}
+
+mp_status mp_plan_many(mp_handle h, int32_t count, const int64_t* mnk, mp_plan_info* out) {
+    if (!h || count < 0 || (count > 0 && !mnk)) return MP_ERR_INVALID_ARG;
+    mp_plan_info tmp;
+    for (int32_t i = 0; i < count; i++) {
+        const int64_t M = mnk[3 * i], N = mnk[3 * i + 1], K = mnk[3 * i + 2];
+        if (M < 0 || N < 0 || K < 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return MP_ERR_INVALID_ARG;
+        const mp_status st = mp::plan_shape(h, 1, M, N, K, out ? out + i : &tmp);
+        if (st != MP_OK) return st;
+    }
+    return MP_OK;
 }
 
 mp_status mp_evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,

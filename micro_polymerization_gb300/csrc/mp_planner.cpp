@@ -287,11 +287,18 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
 
     // ---- Pattern II: two regions cut along M or along N ----------------------
     // First-region kernels: the three best single-kernel choices.
-    int32_t order[MP_MAX_KERNELS];
-    for (int32_t k = 0; k < h->num_kernels; k++) order[k] = k;
-    std::sort(order, order + h->num_kernels,
-              [&](int32_t a, int32_t b) { return single_cost[a] < single_cost[b]; });
+    // (A stable selection of the three cheapest: ties keep kernel order.)
+    int32_t order[3];
     const int n_first = std::min<int32_t>(3, h->num_kernels);
+    for (int i = 0; i < n_first; i++) {
+        int32_t pick = -1;
+        for (int32_t k = 0; k < h->num_kernels; k++) {
+            bool taken = false;
+            for (int j = 0; j < i; j++) taken |= order[j] == k;
+            if (!taken && (pick < 0 || single_cost[k] < single_cost[pick])) pick = k;
+        }
+        order[i] = pick;
+    }
 
     for (int dir = 0; dir < 2; dir++) {  // 0: cut along M, 1: cut along N
         const int64_t along = dir == 0 ? M : N;

@@ -247,3 +247,37 @@ def test_wave_and_pipe_cost_models():
 
 def _key(p):
     return [(r.kernel, r.m0, r.n0, r.m_ext, r.n_ext, r.splits) for r in p.regions()]
+
+
+def _gb300_host_handle():
+    hw = mp.MpHw(num_pe=152, warps_per_wave=152 * 6, local_mem_bytes=232448, shared_mem_bytes=132644864,
+                 hbm_gbs=6684.0, l2_gbs=20000.0, mma_tflops=1974.0)
+    return mp.mp_init_host(hw)
+
+
+def test_plan_many_equals_one_plan_per_call():
+    """mp_plan_many gives, shape by shape, the plan mp_plan gives (with and
+    without a plan cache), and rejects bad dimensions."""
+    shapes = [(g.M, g.N, g.K) for g in wl.workload("dynamic_sequence")] + [(1, 1, 1), (105, 1024, 12544),
+                                                                           (5, 7, 0)]
+    h = _gb300_host_handle()
+    os.environ["MP_PLAN_CACHE"] = "0"
+    try:
+        h0 = _gb300_host_handle()
+    finally:
+        del os.environ["MP_PLAN_CACHE"]
+    try:
+        for hh in (h, h0):
+            many = mp.mp_plan_many(hh, shapes)
+            for s, p in zip(shapes, many):
+                one = mp.mp_plan(hh, *s)
+                assert ctypes.string_at(ctypes.addressof(p), ctypes.sizeof(p)) == \
+                    ctypes.string_at(ctypes.addressof(one), ctypes.sizeof(one)), s
+        assert mp.mp_plan_many(h, shapes, want_plans=False) is None
+        bad = (ctypes.c_int64 * 3)(4, -1, 4)
+        assert mp.library().mp_plan_many(h.ptr, 1, bad, None) == mp.MP_ERR_INVALID_ARG
+        assert mp.library().mp_plan_many(h.ptr, -1, bad, None) == mp.MP_ERR_INVALID_ARG
+        assert mp.library().mp_plan_many(h.ptr, 0, None, None) == mp.MP_OK
+    finally:
+        h.close()
+        h0.close()
