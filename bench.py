@@ -35,10 +35,12 @@ import numpy as np  # noqa: E402
 METRIC = "dynamic-shape GEMM TFLOPS (device-timed, incl. planning) and % of per-shape roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of the persistent kernel from one ncu capture (bytes per
-# algorithmic byte, i.e. dram read+write / (2MK+2KN+4MN)), valid only for the
-# kernel source it was taken on; see profiles/.
-TRAFFIC_RECORD = {"kernel_sha1": "79d49ea1b6e9f20aa1f80216128d08d22399d8a2", "dram_bytes_per_alg_byte": 0.384}
+# DRAM traffic of the persistent kernel from one ncu capture of a small case
+# (profiles/k_poly_gemm_traffic_dynamic_sequence.md), valid only for the
+# kernel source it was taken on: dram__bytes_read.sum over the algorithmic
+# operand bytes (2MK + 2KN), and dram__bytes_write.sum over the algorithmic
+# output bytes (4MN), summed over the captured launches.
+TRAFFIC_RECORD = {"kernel_sha1": None, "read_per_alg_read": None, "write_per_alg_write": None}
 
 
 # --epilogue: (activation, bf16 D) of mp_gemm_ex.
@@ -55,6 +57,25 @@ def load_peaks():
                 "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
     except Exception:
         return dict(PEAKS_FALLBACK), "fallback"
+
+
+def traffic_fields(gs, sel, epi):
+    """roofline.traffic (DRAM bytes per launch of the selected launches) and
+    its read and write parts, from TRAFFIC_RECORD scaled by each launch's
+    algorithmic bytes; all null when the record belongs to other kernel
+    source."""
+    rec = TRAFFIC_RECORD
+    ok = rec["kernel_sha1"] == kernel_sha1() and not epi and rec["read_per_alg_read"] is not None
+    note = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture, as ratios to the "
+            "algorithmic operand bytes (2MK+2KN) and output bytes (4MN), scaled to these launches; much of "
+            "D's fp32 write-back leaves L2 after a launch ends, so traffic_write undercounts D")
+    if not ok:
+        return {"traffic": None, "traffic_read": None, "traffic_write": None,
+                "traffic_note": "no ncu record for this kernel source"}
+    rd = sum(2.0 * gs[i].M * gs[i].K + 2.0 * gs[i].K * gs[i].N for i in sel) / max(1, len(sel))
+    wr = sum(4.0 * gs[i].M * gs[i].N for i in sel) / max(1, len(sel))
+    r, w = rec["read_per_alg_read"] * rd, rec["write_per_alg_write"] * wr
+    return {"traffic": round(r + w), "traffic_read": round(r), "traffic_write": round(w), "traffic_note": note}
 
 
 def kernel_sha1():
@@ -76,10 +97,14 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    _count = 0
+
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join("/tmp", f"mp_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1
+        self.path = os.path.join("/tmp", f"mp_clocks_{os.getpid()}_{ClockSampler._count}.csv")
+        self._summary = None
 
     def __enter__(self):
         try:
@@ -101,6 +126,11 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
+        if self._summary is None:
+            self._summary = self._read()
+        return self._summary
+
+    def _read(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -171,6 +201,128 @@ def needs_repack(ptr: int, ld: int) -> bool:
 
 
 # ---------------------------------------------------------------------------
+# call building and timing helpers
+# ---------------------------------------------------------------------------
+def gemm_call(lib, h, g, A, B, C, D, sp, epi=0):
+    """Pre-marshalled C-ABI arguments of one GEMM (the call itself plans and
+    launches)."""
+    cp = C.data_ptr() if C is not None else None
+    if g.batch > 1:
+        return (lib.mp_gemm_batched, (h.ptr, g.batch, g.M, g.N, g.K, A.data_ptr(), g.K, g.M * g.K,
+                                      B.data_ptr(), g.N, g.K * g.N, cp, g.N, g.M * g.N,
+                                      D.data_ptr(), g.N, g.M * g.N, g.alpha, g.beta, sp))
+    if epi:
+        return (lib.mp_gemm_ex, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
+                                 cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, epi, sp))
+    return (lib.mp_gemm, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
+                          cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, sp))
+
+
+def new_output(g, dev, out_bf16=False):
+    import torch
+    return torch.empty((g.batch, g.M, g.N) if g.batch > 1 else (g.M, g.N), device=dev,
+                       dtype=torch.bfloat16 if out_bf16 else torch.float32)
+
+
+def run_calls(calls):
+    import micro_polymerization_gb300 as mp
+    for fn, a in calls:
+        st = fn(*a)
+        if st != 0:
+            raise mp.MPError(st, "GEMM call")
+
+
+def operand_bytes(ops_i):
+    return sum(t.numel() * t.element_size() for t in ops_i if t is not None)
+
+
+def per_shape_back_to_back(lib, h, gs, ops, sp, stream, epi=0, reps=3):
+    """Device time per call of each GEMM when it is called back to back, as in
+    a step, with cold operands: the calls cycle over copies of the GEMM's
+    operands and outputs that together exceed twice L2 (at most 128 copies and
+    about 4 GiB), so every call reads operands L2 no longer holds, except for
+    GEMMs so small that 128 copies still fit.  The GPU is held by a sleep
+    kernel while the calls are queued, so host issue time is not measured;
+    events bracket the whole run of calls, not each call (an event between
+    two calls costs about 5 us of device time here: it ends the programmatic
+    overlap of one launch with the next).  Planning is inside every call (a
+    plan-cache hit after the first)."""
+    import torch
+    out = []
+    for g, o in zip(gs, ops):
+        nbytes = operand_bytes(o)
+        copies = int(min(128, max(2, math.ceil(2 * L2_BYTES / max(1, nbytes)))))
+        copies = max(2, min(copies, int((4 << 30) // max(1, nbytes))))
+        A, B, C, D = o
+        sets = [o] + [(A.clone(), B.clone(), C.clone() if C is not None else None, torch.empty_like(D))
+                      for _ in range(copies - 1)]
+        calls = [gemm_call(lib, h, g, a, b, c, d, sp, epi) for a, b, c, d in sets]
+        run_calls(calls)
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda._sleep(20_000_000)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run_calls(calls)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e3 / len(calls))
+        out.append(best)
+        del sets, calls
+    return np.array(out)
+
+
+def flop_weighted_frac(gs, t_us, peaks, d_bytes=4):
+    troof = np.array([roofline_us(g, peaks, d_bytes)[0] for g in gs])
+    flops = np.array([g.flops for g in gs], dtype=np.float64)
+    return float(np.sum(flops * troof / t_us) / np.sum(flops)), float(troof.sum() / t_us.sum())
+
+
+CONFIG_RECORDS = ["single_skinny", "dynamic_resolution", "merged_qkv", "merged_batched", "stress"]
+
+
+def config_record(name, args, lib, h, dev, sp, stream, peaks, local):
+    """One line per further workload of the metric: the whole workload as one
+    step of back-to-back calls (TFLOP/s, clocks sampled meanwhile) and the
+    FLOP-weighted per-shape roofline fraction over at most 128 of its GEMMs
+    (a seeded sample; the stress sweep keeps 4096^3)."""
+    import torch
+    from micro_polymerization_gb300 import workloads as wl
+    gs = wl.workload(name)
+    ops = []
+    for g in gs:
+        A, B, C = wl.make_operands(g, device=dev)
+        ops.append((A, B, C, new_output(g, dev)))
+    calls = [gemm_call(lib, h, g, *o, sp) for g, o in zip(gs, ops)]
+    for _ in range(3):
+        run_calls(calls)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(steps):
+            run_calls(calls)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = sum(g.flops for g in gs)
+    idx = list(range(len(gs)))
+    if len(gs) > 128:
+        idx = sorted(np.random.default_rng(7).choice(len(gs) - 1, 127, replace=False).tolist()) + [len(gs) - 1]
+    sub_g = [gs[i] for i in idx]
+    t = per_shape_back_to_back(lib, h, sub_g, [ops[i] for i in idx], sp, stream)
+    fw, ratio = flop_weighted_frac(sub_g, t, peaks)
+    del ops, calls
+    torch.cuda.empty_cache()
+    return {"workload": workload_desc(name), "gemms": len(gs), "value": round(flops / (ms * 1e-3) / 1e12, 3),
+            "unit": "TFLOPS", "ms_per_step": round(ms, 4), "steps": steps,
+            "per_shape_roofline": {"flop_weighted_frac": round(fw, 4), "sum_troof_over_sum_t": round(ratio, 4),
+                                   "gemms": len(sub_g)},
+            "clocks": clocks.summary()}
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
 def run_mp(args):
@@ -195,6 +347,8 @@ def run_mp(args):
     sp = stream.cuda_stream
 
     gs = rank_workload(args.workload, rank)
+    if args.limit:
+        gs = gs[:args.limit]
     act, out_bf16 = EPILOGUES[args.epilogue]
     epi = act | (mp.MP_EPI_OUT_BF16 if out_bf16 else 0)
     d_bytes = 2 if out_bf16 else 4
@@ -211,19 +365,7 @@ def run_mp(args):
     torch.cuda.synchronize()
 
     # Pre-marshalled C-ABI argument tuples (the call itself plans and launches).
-    calls = []
-    for g, A, B, C, D in ops:
-        cp = C.data_ptr() if C is not None else None
-        if g.batch > 1:
-            calls.append((lib.mp_gemm_batched, (h.ptr, g.batch, g.M, g.N, g.K, A.data_ptr(), g.K, g.M * g.K,
-                                                B.data_ptr(), g.N, g.K * g.N, cp, g.N, g.M * g.N,
-                                                D.data_ptr(), g.N, g.M * g.N, g.alpha, g.beta, sp)))
-        elif epi:
-            calls.append((lib.mp_gemm_ex, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
-                                           cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, epi, sp)))
-        else:
-            calls.append((lib.mp_gemm, (h.ptr, g.M, g.N, g.K, A.data_ptr(), g.K, B.data_ptr(), g.N,
-                                        cp, g.N, D.data_ptr(), g.N, g.alpha, g.beta, sp)))
+    calls = [gemm_call(lib, h, g, A, B, C, D, sp, epi) for g, A, B, C, D in ops]
 
     def step(evs=None):
         for i, (fn, a) in enumerate(calls):
@@ -305,13 +447,16 @@ def run_mp(args):
         if mp.mp_check(h) != 0:
             raise RuntimeError("device status word set by the grouped submission")
 
-    # Per-shape roofline fractions (from the per-launch times).
+    # Per-shape roofline fractions.  The per-shape time is the device time per
+    # call with the GEMM called back to back on cold operands (see
+    # per_shape_back_to_back); the event-bracketed times of the calls inside a
+    # step (per_launch above) are reported beside it.
+    b2b = per_shape_back_to_back(lib, h, gs, [o[1:] for o in ops], sp, stream, epi=epi)
     troof = np.array([roofline_us(g, peaks, d_bytes)[0] for g in gs])
     bounds = [roofline_us(g, peaks, d_bytes)[1] for g in gs]
     flops = np.array([g.flops for g in gs], dtype=np.float64)
-    frac_shape = troof / per_launch
-    flop_weighted = float(np.sum(flops * frac_shape) / np.sum(flops))
-    time_ratio = float(troof.sum() / per_launch.sum())
+    flop_weighted, time_ratio = flop_weighted_frac(gs, b2b, peaks, d_bytes)
+    fw_events, ratio_events = flop_weighted_frac(gs, per_launch, peaks, d_bytes)
 
     # Dominant kernel: the persistent GEMM kernel (one launch per GEMM).  Its
     # bound is the one that dominates the summed roofline time.
@@ -320,19 +465,16 @@ def run_mp(args):
     if t_hbm >= t_ten:
         sel = [i for i, b in enumerate(bounds) if b == "hbm"]
         work = sum(gs[i].min_bytes(d_bytes) for i in sel)
-        achieved = work / (per_launch[sel].sum() * 1e-6) / 1e9
+        achieved = work / (b2b[sel].sum() * 1e-6) / 1e9
         peak = peaks["hbm_gbs"]
         unit, bound = "GB/s", "hbm"
     else:
         sel = [i for i, b in enumerate(bounds) if b == "tensor"]
         work = sum(gs[i].flops for i in sel)
-        achieved = work / (per_launch[sel].sum() * 1e-6) / 1e12
+        achieved = work / (b2b[sel].sum() * 1e-6) / 1e12
         peak = peaks["bf16_tflops"]
         unit, bound = "TFLOP/s", "tensor"
-    traffic = None
-    if TRAFFIC_RECORD["kernel_sha1"] == kernel_sha1() and TRAFFIC_RECORD["dram_bytes_per_alg_byte"] and not epi:
-        alg = sum(gs[i].min_bytes() for i in sel) / max(1, len(sel))
-        traffic = TRAFFIC_RECORD["dram_bytes_per_alg_byte"] * alg
+    traffic = traffic_fields(gs, sel, epi)
 
     # End to end: pinned host inputs copied in, outputs read back, every step.
     e2e = None
@@ -398,16 +540,58 @@ def run_mp(args):
         e2e = {"value": round(flops_step * world * e2e_steps / t_e2e / 1e12, 3), "unit": "TFLOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
-    # Planner latency on the host (search, cache bypassed by fresh shapes).
+    # Planner latency: one mp_plan_many call over the workload's shapes on a
+    # handle without a plan cache, so that every shape is searched; timed
+    # around the single library call (no binding in the loop).
     plan_us = None
     if rank == 0:
-        h2 = mp.mp_init_host(mp.mp_get_hw(h)[0])
-        shapes = [(g.M + 1, g.N, g.K) for g in gs]
-        t0 = time.perf_counter()
-        for s in shapes:
-            mp.mp_plan(h2, *s)
-        plan_us = (time.perf_counter() - t0) / len(shapes) * 1e6
+        os.environ["MP_PLAN_CACHE"] = "0"
+        try:
+            h2 = mp.mp_init_host(mp.mp_get_hw(h)[0])
+        finally:
+            del os.environ["MP_PLAN_CACHE"]
+        shapes = [(g.M, g.N, g.K) for g in gs if g.batch == 1]
+        if shapes:
+            mp.mp_plan_many(h2, shapes, want_plans=False)
+            best = float("inf")
+            for _ in range(20):
+                t0 = time.perf_counter()
+                mp.mp_plan_many(h2, shapes, want_plans=False)
+                best = min(best, time.perf_counter() - t0)
+            plan_us = best / len(shapes) * 1e6
         h2.close()
+
+    # Informational: the same step on a handle without a plan cache, so that
+    # every call runs the polymerizer's search before its launch.
+    no_cache = None
+    if not epi and rank == 0 and not args.no_group:
+        os.environ["MP_PLAN_CACHE"] = "0"
+        try:
+            h3 = mp.mp_init(local, calib)
+        finally:
+            del os.environ["MP_PLAN_CACHE"]
+        calls3 = [gemm_call(lib, h3, g, A, B, C, D, sp) for g, A, B, C, D in ops]
+        for _ in range(3):
+            run_calls(calls3)
+        torch.cuda.synchronize()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        for _ in range(args.steps):
+            run_calls(calls3)
+        n1.record(stream)
+        torch.cuda.synchronize()
+        ms_nc = n0.elapsed_time(n1) / args.steps
+        no_cache = {"ms_per_step": round(ms_nc, 4), "value": round(flops_step / (ms_nc * 1e-3) / 1e12, 3),
+                    "note": "the same step on a handle made with MP_PLAN_CACHE=0: every call searches"}
+        if mp.mp_check(h3) != 0:
+            raise RuntimeError("device status word set by the no-cache step")
+        h3.close()
+
+    # The other workloads of the metric, one record each.
+    configs = None
+    if rank == 0 and args.workload == "dynamic_sequence" and not epi and not args.no_configs and not args.limit:
+        configs = {name: config_record(name, args, lib, h, dev, sp, stream, peaks, local)
+                   for name in CONFIG_RECORDS}
 
     if args.dump and rank == 0:
         with open(args.dump, "w") as f:
@@ -432,18 +616,23 @@ def run_mp(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": workload_desc(args.workload), "gemms_per_step": len(gs),
-                       "flops_per_step": int(flops_step), "l2": l2_note(gs), "epilogue": args.epilogue,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": run_config(args, gs, world),
             "per_shape_roofline": {"flop_weighted_frac": round(flop_weighted, 4),
                                    "sum_troof_over_sum_t": round(time_ratio, 4),
+                                   "timing": "each GEMM called back to back on cold operands, events around "
+                                             "the run of calls",
+                                   "events_around_each_call": {"flop_weighted_frac": round(fw_events, 4),
+                                                               "sum_troof_over_sum_t": round(ratio_events, 4)},
                                    "peaks": peak_src},
-            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "launches": len(sel), "kernel": "k_poly_gemm", "peak_source": peak_src},
+            "roofline": dict({"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                              "frac": round(achieved / peak, 4)}, **traffic,
+                             launches=len(sel), kernel="k_poly_gemm", peak_source=peak_src),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "as_one_group": as_group,
             "plan_us": round(plan_us, 3) if plan_us is not None else None,
+            "plan_how": "one mp_plan_many call over the workload's shapes, no plan cache, best of 20",
+            "no_plan_cache": no_cache,
+            "configs": configs,
             "cost_model": "calibrated" if calib else "analytic",
             "clocks": clocks.summary(), "impl": "mp",
         }
@@ -455,6 +644,13 @@ def run_mp(args):
 
 
 L2_BYTES = 126 * 2 ** 20
+
+
+def run_config(args, gs, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": workload_desc(args.workload), "gemms_per_step": len(gs),
+            "flops_per_step": int(sum(g.flops for g in gs)), "l2": l2_note(gs), "epilogue": args.epilogue,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def l2_note(gs):
@@ -567,6 +763,7 @@ def cpu_baseline(args, gs, budget_s=None, act=0, out_bf16=False):
         if t_total >= budget_s:
             break
     return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(used), "kind": "oracle",
+            "seconds": round(t_total, 4),
             "sample": f"first min(M, 256) rows of each of the first {done} GEMMs of the workload "
                       f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64, OpenMP)"}
 
@@ -627,7 +824,7 @@ def cpu_baseline_b2b(args, bs, budget_s=None):
         done += 1
         if t_total >= budget_s:
             break
-    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(oracle.max_threads()),
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "seconds": round(t_total, 4), "cores": int(oracle.max_threads()),
             "kind": "oracle",
             "sample": f"first min(M, 256) rows of each of the first {done} problems of the workload "
                       f"({flops / 1e9:.1f} GFLOP in {t_total:.1f} s, fp64)"}
@@ -834,7 +1031,7 @@ def cpu_baseline_conv(args, cs, budget_s=None):
         if t_total >= budget_s:
             break
     import os as _os
-    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "cores": int(_os.cpu_count() or 1),
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOPS", "seconds": round(t_total, 4), "cores": int(_os.cpu_count() or 1),
             "kind": "oracle",
             "sample": f"first image of each of the first {done} layers ({flops / 1e9:.1f} GFLOP in "
                       f"{t_total:.1f} s, fp64, numpy products per filter tap)"}
@@ -1179,6 +1376,7 @@ def run_reference(args):
     from micro_polymerization_gb300 import workloads as wl
     import oracle  # noqa: F401
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    config = {"workload": workload_desc(args.workload), "epilogue": args.epilogue}
     if is_conv(args.workload):
         cs = conv_workload(args.workload)
         for _ in range(args.warmup):
@@ -1195,12 +1393,16 @@ def run_reference(args):
             cpu_baseline(args, gs[:1], budget_s=0.01)
         act, out_bf16 = EPILOGUES[args.epilogue]
         vals = [cpu_baseline(args, gs, budget_s=per_step, act=act, out_bf16=out_bf16) for _ in range(args.steps)]
+        config = run_config(args, gs, world)
     v = statistics.median(x["value"] for x in vals)
+    # A step of this arm is a bounded sample of the workload: its time is the
+    # sample's wall time.
+    ms_step = statistics.median(x["seconds"] for x in vals) * 1e3
     line = {
         "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload), "epilogue": args.epilogue},
+        "config": config,
         "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": vals[0]["cores"], "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1225,6 +1427,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-group", action="store_true", help="skip the informational grouped submission")
     ap.add_argument("--no-calib", action="store_true", help="plan with the analytic cost model")
+    ap.add_argument("--no-configs", action="store_true", help="skip the records of the other workloads")
+    ap.add_argument("--limit", type=int, default=0, help="only the first N GEMMs of the workload (profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
