@@ -403,7 +403,9 @@ const char* mp_status_string(mp_status s);
  * second GEMM's operand), and feeds that CTA's second GEMM (the summary's
  * threadblock residence).  That needs N0 <= 256.  Where two launches are
  * predicted clearly faster, and always for N0 > 256, D0 goes through a bf16
- * scratch buffer instead (mp_set_b2b_mode).  act0 is MP_ACT_NONE,
+ * buffer instead (mp_set_b2b_mode): the end of the handle's staging area
+ * (allocated at mp_init, 1 GiB by default), so mp_gemm_b2b never allocates;
+ * that form needs M * round8(N0) * 2 bytes <= half of the area.  act0 is MP_ACT_NONE,
  * MP_ACT_RELU or MP_ACT_GELU (the epilogue variants' activations).  C0 is not
  * read when beta0 == 0, nor C1 when beta1 == 0; C1 may be D1 (same pointer
  * and ld).  Asynchronous on `stream`, like mp_gemm.
@@ -414,8 +416,8 @@ const char* mp_status_string(mp_status s);
  * identical C1, unknown act0); MP_ERR_UNSUPPORTED (N0 > 256 with the fused
  * form forced, host-only handle, or an A0, W0 or W1 whose base or row pitch
  * is not 16-byte aligned and that does not fit the staging area, where such
- * operands are copied with padded rows, as in mp_gemm); MP_ERR_NO_MEMORY (the
- * two-launch form's scratch buffer); MP_ERR_CUDA (launch failure).
+ * operands are copied with padded rows, as in mp_gemm, or a two-launch D0
+ * larger than half of the staging area); MP_ERR_CUDA (launch failure).
  */
 mp_status mp_gemm_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, const void* A0, int64_t lda0,
                       const void* W0, int64_t ldw0, const float* C0, int64_t ldc0, const void* W1, int64_t ldw1,
@@ -448,9 +450,8 @@ mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0
 /*
  * Which form mp_gemm_b2b runs.  MP_B2B_FUSED: the fused kernel (D0 stays on
  * chip; N0 <= 256).  MP_B2B_TWO_LAUNCH: mp_gemm_ex writes D0 =
- * act0(alpha0*A0*W0 + beta0*C0) in bf16 (the same rounding as on chip) to a
- * scratch buffer of the handle, grown on first need, then mp_gemm runs the
- * second GEMM.  MP_B2B_AUTO (the default) keeps the fused kernel unless the
+ * act0(alpha0*A0*W0 + beta0*C0) in bf16 (the same rounding as on chip) to
+ * the end of the handle's staging area, then mp_gemm runs the second GEMM.  MP_B2B_AUTO (the default) keeps the fused kernel unless the
  * two forms' cost models predict the two launches more than 10% faster, and
  * runs N0 > 256 as two launches (mp_plan_b2b reports the choice).
  * Errors: MP_ERR_INVALID_ARG (unknown mode).

@@ -165,9 +165,6 @@ struct DeviceState {
     // Clusters of two CTAs of k_poly_gemm that can be resident at once (0:
     // paired launches disabled).
     int max_pairs = 0;
-    // bf16 D0 of the two-launch form of mp_gemm_b2b (grown on first need).
-    void* b2b_scratch = nullptr;
-    size_t b2b_scratch_bytes = 0;
 };
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
@@ -462,7 +459,6 @@ void device_destroy(mp_handle h) {
         cudaFree(s->cnt);
         cudaFree(s->err);
         cudaFree(s->staging);
-        cudaFree(s->b2b_scratch);
     }
     delete[] s->tm_cache;
     delete s;
@@ -895,30 +891,34 @@ mp_status device_run_b2b_two(mp_handle h, const B2BArgs& a) {
     if (!s) return MP_ERR_UNSUPPORTED;
     DeviceGuard g(s->device);
     const int64_t ld0 = round_up(std::max<int64_t>(a.N0, 1), 8);
-    const size_t bytes = (size_t)(a.M * ld0 * 2);
-    if (bytes > s->b2b_scratch_bytes) {
-        // cudaFree waits for the device, so no launch still reads the old buffer.
-        cudaFree(s->b2b_scratch);
-        s->b2b_scratch = nullptr;
-        s->b2b_scratch_bytes = 0;
-        if (cudaMalloc(&s->b2b_scratch, bytes) != cudaSuccess) return MP_ERR_NO_MEMORY;
-        s->b2b_scratch_bytes = bytes;
-    }
+    const int64_t bytes = round_up(a.M * ld0 * 2, 256);
+    // D0 (bf16, rows of ld0) lives at the end of the handle's staging area,
+    // allocated at mp_init, so that this form allocates nothing; the two
+    // launches stage their unaligned operands in the part before it.  D0 may
+    // take at most half of the area.
+    const int64_t full = s->staging_bytes;
+    if (bytes > full / 2) return MP_ERR_UNSUPPORTED;
+    void* d0 = s->staging + (full - bytes);
+    s->staging_bytes = full - bytes;
     mp_status st = MP_OK;
     if (a.N0 > 0) {
         GemmArgs g0{1, a.M, a.N0, a.K0, a.A0, a.lda0, 0, a.W0, a.ldw0, 0, a.C0, a.ldc0, 0,
-                    static_cast<float*>(s->b2b_scratch), ld0, 0, a.alpha0, a.beta0, a.stream,
+                    static_cast<float*>(d0), ld0, 0, a.alpha0, a.beta0, a.stream,
                     a.act0 | MP_EPI_OUT_BF16};
         mp_plan_info p0;
         if ((st = validate_args(g0)) != MP_OK || (st = plan_shape(h, 1, a.M, a.N0, a.K0, &p0)) != MP_OK ||
-            (st = device_run(h, p0, g0)) != MP_OK)
+            (st = device_run(h, p0, g0)) != MP_OK) {
+            s->staging_bytes = full;
             return st;
+        }
     }
-    GemmArgs g1{1, a.M, a.N1, a.N0, s->b2b_scratch, ld0, 0, a.W1, a.ldw1, 0, a.C1, a.ldc1, 0, a.D1, a.ldd1, 0,
+    GemmArgs g1{1, a.M, a.N1, a.N0, d0, ld0, 0, a.W1, a.ldw1, 0, a.C1, a.ldc1, 0, a.D1, a.ldd1, 0,
                 a.alpha1, a.beta1, a.stream, 0};
     mp_plan_info p1;
-    if ((st = validate_args(g1)) != MP_OK || (st = plan_shape(h, 1, a.M, a.N1, a.N0, &p1)) != MP_OK) return st;
-    return device_run(h, p1, g1);
+    if ((st = validate_args(g1)) == MP_OK && (st = plan_shape(h, 1, a.M, a.N1, a.N0, &p1)) == MP_OK)
+        st = device_run(h, p1, g1);
+    s->staging_bytes = full;
+    return st;
 }
 
 // ---------------------------------------------------------------------------

@@ -175,3 +175,26 @@ def test_b2b_auto_choice_runs_the_planned_form():
     got, ref, bound = run_b2b(large, rows=rows)
     ok, worst = oracle.within_b2b(got, ref, bound)
     assert ok, worst
+
+
+def test_b2b_two_launch_form_allocates_nothing():
+    """The two-launch form keeps D0 at the end of the handle's staging area:
+    a call with unaligned A0, W0 and W1 (staged in front of D0) meets the
+    bound, and repeating it leaves the device's free memory unchanged."""
+    mp.mp_set_b2b_mode(handle(), mp.MP_B2B_TWO_LAUNCH)
+    b = wl.B2B(300, 100, 77, 130, alpha0=1.0, beta0=0.5, alpha1=1.0, beta1=0.5, act0=1, seed=31)
+    A0, W0, C0, W1, C1 = wl.make_b2b_operands(b)
+    d = [t.to(DEV) for t in (A0, W0, C0, W1, C1)]
+    D1 = torch.empty(b.M, b.N1, device=DEV)
+    for call in range(2):
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info(0)[0]
+        mp.mp_gemm_b2b(handle(), d[0], d[1], d[2], d[3], d[4], D1, b.alpha0, b.beta0, b.alpha1, b.beta1,
+                       b.act0)
+        torch.cuda.synchronize()
+        assert mp.mp_check(handle()) == 0
+        assert torch.cuda.mem_get_info(0)[0] == free0, f"call {call + 1} changed free device memory"
+    args = (_bits(A0), _bits(W0), C0.numpy(), _bits(W1), C1.numpy(), b.alpha0, b.beta0, b.alpha1, b.beta1)
+    ref, d0 = oracle.b2b(*args, b.act0)
+    ok, worst = oracle.within_b2b(D1.cpu().numpy(), ref, oracle.b2b_bound(*args, b.act0, d0))
+    assert ok, worst
