@@ -81,6 +81,11 @@ typedef struct {
  * [MP section 3, "micro-kernel generation"], and its performance model
  * g_predict(t) = fixed_us + per_step_us * t for a pipeline task of t
  * micro-kernel instances [MP section 3, "micro-kernel performance model"].
+ * That section's task runs in three overlapped stages (load, compute, write
+ * back); on a PE that runs tasks back to back, a task's write-back overlaps
+ * the next task's load and compute, so only the last wave's write-back adds
+ * to the time: tail_us, charged once per plan (with the launch and pipeline
+ * fill), keeps it out of g_predict.
  * swap = 1 marks the transposed form (D^T = B^T A^T) used for short M.
  * pair = 1 marks a tile computed by a cluster of two CTAs on two SMs with the
  * pair MMA (each CTA holds half of the tile's rows of A and D and half of its
@@ -94,6 +99,9 @@ typedef struct {
     int32_t pair;
     double fixed_us;           /* per-task time that does not scale with t     */
     double per_step_us;        /* time per micro-kernel instance (one uk step) */
+    double tail_us;            /* time added once per plan after the last wave:
+                                  its write-back (stage 3), not hidden behind a
+                                  next task, plus launch and pipeline fill     */
 } mp_kernel_desc;
 
 /* One region R_i of a plan and its cost terms [MP section 3, cost model]. */
@@ -383,10 +391,12 @@ mp_status mp_inject_wait_timeout(mp_handle h, int32_t enable, int64_t limit_ns);
 mp_status mp_get_hw(mp_handle h, mp_hw* hw, mp_kernel_desc* kernels, int32_t* num_kernels);
 
 /*
- * Replace micro-kernel k's performance model (g_predict) with measured
- * values; used by calibration.  The plan cache is cleared.
+ * Replace micro-kernel k's performance model (g_predict and its tail) with
+ * measured values; used by calibration.  The plan cache is cleared.
+ * Errors: MP_ERR_INVALID_ARG (no such kernel, negative fixed or tail time,
+ * per-step time not positive).
  */
-mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us);
+mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us, double tail_us);
 
 /* Static text for a status code. */
 const char* mp_status_string(mp_status s);

@@ -59,7 +59,7 @@ class MpHw(ctypes.Structure):
 class MpKernelDesc(ctypes.Structure):
     _fields_ = [("um", ctypes.c_int32), ("un", ctypes.c_int32), ("uk", ctypes.c_int32),
                 ("warps", ctypes.c_int32), ("swap", ctypes.c_int32), ("pair", ctypes.c_int32),
-                ("fixed_us", ctypes.c_double), ("per_step_us", ctypes.c_double)]
+                ("fixed_us", ctypes.c_double), ("per_step_us", ctypes.c_double), ("tail_us", ctypes.c_double)]
 
 
 class MpRegionInfo(ctypes.Structure):
@@ -158,7 +158,7 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_force_plan": ([_vp, _i32, _i32], ctypes.c_int),
                 "mp_get_hw": ([_vp, ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
                                ctypes.POINTER(_i32)], ctypes.c_int),
-                "mp_set_kernel_model": ([_vp, _i32, ctypes.c_double, ctypes.c_double], ctypes.c_int),
+                "mp_set_kernel_model": ([_vp, _i32, ctypes.c_double, ctypes.c_double, ctypes.c_double], ctypes.c_int),
                 "mp_inject_wait_timeout": ([_vp, _i32, _i64], ctypes.c_int),
                 "mp_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "mp_enumerate_plans": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo), _i32,
@@ -560,8 +560,8 @@ def mp_get_hw(h: Handle):
     return hw, [ks[i] for i in range(n.value)]
 
 
-def mp_set_kernel_model(h: Handle, k: int, fixed_us: float, per_step_us: float) -> None:
-    _check(library().mp_set_kernel_model(h.ptr, k, fixed_us, per_step_us), "mp_set_kernel_model")
+def mp_set_kernel_model(h: Handle, k: int, fixed_us: float, per_step_us: float, tail_us: float = 0.0) -> None:
+    _check(library().mp_set_kernel_model(h.ptr, k, fixed_us, per_step_us, tail_us), "mp_set_kernel_model")
 
 
 def mp_inject_wait_timeout(h: Handle, enable=True, limit_ns: int = 0) -> None:

@@ -26,7 +26,8 @@ double env_double(const char* name, double dflt) {
     return (end && end != v && x > 0) ? x : dflt;
 }
 
-// Calibration table: "um un uk swap fixed_us per_step_us" per line.
+// Calibration table: "um un uk swap fixed_us per_step_us [tail_us]" per line
+// (a line without tail_us keeps the kernel's tail).
 void load_calibration(mp_handle h, const char* path) {
     if (!path || !*path) return;
     FILE* f = std::fopen(path, "r");
@@ -36,14 +37,16 @@ void load_calibration(mp_handle h, const char* path) {
         char* hash = std::strchr(line, '#');
         if (hash) *hash = 0;
         int um, un, uk, swap;
-        double fixed, step;
-        if (std::sscanf(line, "%d %d %d %d %lf %lf", &um, &un, &uk, &swap, &fixed, &step) != 6) continue;
+        double fixed, step, tail = -1.0;
+        const int got = std::sscanf(line, "%d %d %d %d %lf %lf %lf", &um, &un, &uk, &swap, &fixed, &step, &tail);
+        if (got < 6) continue;
         if (!(fixed >= 0) || !(step > 0)) continue;
         for (int k = 0; k < h->num_kernels; k++) {
             mp_kernel_desc& d = h->kernels[k];
             if (d.um == um && d.un == un && d.uk == uk && d.swap == swap) {
                 d.fixed_us = fixed;
                 d.per_step_us = step;
+                if (got == 7 && tail >= 0) d.tail_us = tail;
             }
         }
     }
@@ -257,7 +260,8 @@ mp_status mp_init_host(mp_handle* out, const mp_hw* hw, const mp_kernel_desc* ke
         return MP_ERR_INVALID_ARG;
     for (int32_t k = 0; k < num_kernels; k++) {
         const mp_kernel_desc& d = kernels[k];
-        if (d.um < 1 || d.un < 1 || d.uk < 1 || d.warps < 1 || d.fixed_us < 0 || d.per_step_us < 0)
+        if (d.um < 1 || d.un < 1 || d.uk < 1 || d.warps < 1 || d.fixed_us < 0 || d.per_step_us < 0 ||
+            !(d.tail_us >= 0))
             return MP_ERR_INVALID_ARG;
     }
     mp_handle h = new_handle();
@@ -508,11 +512,12 @@ mp_status mp_get_hw(mp_handle h, mp_hw* hw, mp_kernel_desc* kernels, int32_t* nu
     return MP_OK;
 }
 
-mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us) {
-    if (!h || k < 0 || k >= h->num_kernels || !(fixed_us >= 0) || !(per_step_us > 0))
+mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us, double tail_us) {
+    if (!h || k < 0 || k >= h->num_kernels || !(fixed_us >= 0) || !(per_step_us > 0) || !(tail_us >= 0))
         return MP_ERR_INVALID_ARG;
     h->kernels[k].fixed_us = fixed_us;
     h->kernels[k].per_step_us = per_step_us;
+    h->kernels[k].tail_us = tail_us;
     mp::clear_plan_cache(h);
     return MP_OK;
 }

@@ -2,9 +2,16 @@
 // factors under the cost model of the MikPoly summary, section 3
 // ("polymerization cost model", "heuristic search").
 //
-//   Cost(S, H) = sum over regions (R_i, K~_i) of  f_wave * f_pipe
+//   Cost(S, H) = sum over regions (R_i, K~_i) of  f_wave * f_pipe  (+ tail)
 //   f_wave     = ceil(f_parallel(R_i, K~_i) / |P_multi|)
 //   f_pipe     = g_predict(f_num(R_i, K~_i))
+//
+// The tail is the section's three-stage pipeline taken at its word: a PE runs
+// its tasks back to back, each task's write-back (stage 3) overlapping the
+// next task's load and compute, so only the last wave's write-back is not
+// hidden.  It is charged once per strategy (the largest tail among its
+// regions' micro-kernels, with the launch and the pipeline fill), and
+// g_predict keeps only what every task pays.
 //
 // f_parallel is the number of pipeline tasks of region i (its tiles times its
 // split-K factor), |P_multi| the number of tasks the machine runs at once
@@ -69,6 +76,7 @@ struct RegionEval {
     int64_t f_wave = 0;
     double f_pipe = 0.0;
     double cost = 0.0;
+    double tail = 0.0;
     int64_t ws_floats = 0;
     bool ok = false;
 };
@@ -120,6 +128,7 @@ RegionEval eval_region(const mp_handle_s* h, int32_t k, int64_t m_ext, int64_t n
     r.f_wave = cdiv(r.f_parallel, slots_for(h, u));
     r.f_pipe = f_pipe_of(h, u, f_num, splits, r.f_parallel);
     r.cost = (double)r.f_wave * r.f_pipe;
+    r.tail = u.tail_us;
     r.ws_floats = splits > 1 ? tiles * splits * (int64_t)u.um * u.un : 0;
     r.ok = splits == 1 || (!u.pair && r.ws_floats <= h->workspace_floats && tiles <= kMaxCounters);
     return r;
@@ -157,9 +166,19 @@ struct Strategy {
     int32_t nreg = 0;
     int64_t m0[2], n0[2], m_ext[2], n_ext[2];
     RegionEval ev[2];
-    double sum = 0.0;   // sum of f_wave * f_pipe
+    double sum = 0.0;   // sum of f_wave * f_pipe, plus the tail
     double cost = 0.0;  // max(sum, HBM floor)
 };
+
+// Sum of f_wave * f_pipe over the regions, plus the strategy's tail.
+inline double strategy_sum(const Strategy& s) {
+    double sum = 0.0, tail = 0.0;
+    for (int i = 0; i < s.nreg; i++) {
+        sum += s.ev[i].cost;
+        tail = std::max(tail, s.ev[i].tail);
+    }
+    return sum + tail;
+}
 
 inline double tile_area(const mp_handle_s* h, const Strategy& s) {
     double a = 0.0;
@@ -245,8 +264,7 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
     // Pruning compares partial MikPoly costs, so it runs under that model only.
     const bool prune = h->plan_mode == MP_PLAN_MIKPOLY;
     auto finish = [&](Strategy& s) {
-        s.sum = 0.0;
-        for (int i = 0; i < s.nreg; i++) s.sum += s.ev[i].cost;
+        s.sum = strategy_sum(s);
         s.cost = strategy_cost(h, s, floor_us);
         evaluated++;
         if (better(h, s, best)) best = s;
@@ -276,7 +294,7 @@ mp_status search(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K, mp
             s.m0[0] = 0; s.n0[0] = 0; s.m_ext[0] = M; s.n_ext[0] = N;
             s.ev[0] = e;
             finish(s);
-            single_cost[k] = std::min(single_cost[k], e.cost);
+            single_cost[k] = std::min(single_cost[k], e.cost + e.tail);
         }
     }
     if (h->force_kernel >= 0 || h->force_splits > 0) {
@@ -394,8 +412,7 @@ mp_status enumerate_plans(mp_handle h, int64_t batch, int64_t M, int64_t N, int6
     const double floor_us = hbm_floor_us(h, batch, M, N, K, false);
     std::vector<Strategy> all;
     auto add = [&](Strategy& st) {
-        st.sum = 0.0;
-        for (int i = 0; i < st.nreg; i++) st.sum += st.ev[i].cost;
+        st.sum = strategy_sum(st);
         st.cost = strategy_cost(h, st, floor_us);
         all.push_back(st);
     };
@@ -541,7 +558,7 @@ mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_
                         mp_plan_info* p) {
     if (!h || !p || batch < 1 || M < 1 || N < 1 || K < 0) return MP_ERR_INVALID_ARG;
     if (p->num_regions < 1 || p->num_regions > MP_MAX_REGIONS) return MP_ERR_INVALID_ARG;
-    double sum = 0.0;
+    double sum = 0.0, tail = 0.0;
     p->total_tasks = 0;
     p->workspace_bytes = 0;
     for (int i = 0; i < p->num_regions; i++) {
@@ -556,10 +573,11 @@ mp_status evaluate_plan(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_
         r.f_wave = e.f_wave;
         r.f_pipe_us = e.f_pipe;
         sum += e.cost;
+        tail = std::max(tail, e.tail);
         p->total_tasks += e.f_parallel;
         p->workspace_bytes += 4 * e.ws_floats;
     }
-    p->cost_us = std::max(sum, hbm_floor_us(h, batch, M, N, K, false));
+    p->cost_us = std::max(sum + tail, hbm_floor_us(h, batch, M, N, K, false));
     if (p->pattern == 0) p->pattern = p->num_regions == 1 ? 1 : 2;
     return validate_plan(*p, M, N, K);
 }
@@ -611,8 +629,14 @@ void default_gb300_kernels(const mp_hw& hw, mp_kernel_desc* out, int32_t* n) {
         d.per_step_us = std::max(std::max(mma_us, load_us), kStepFloorUs);
         // Epilogue: the tile's fp32 output at the SM's share of HBM; the
         // swapped form stores straight from registers at about half the rate.
+        // It is charged in every task, not once as a tail: measured on
+        // GB300, a second wave costs its K loop plus most of an epilogue
+        // (the first wave's stores slow the second wave's operand loads), and
+        // planning with the epilogue as a once-per-plan tail made the
+        // dynamic-sequence, merged-QKV and stress steps 0-5% slower.
         const double epi_bytes = 4.0 * kUmmaM * (g.swap ? g.um : g.un);  // per SM
         d.fixed_us = 0.6 + (g.swap ? 2.0 : 1.0) * epi_bytes / (hbm_pe * 1e3) + (g.pair ? kPairFixedUs : 0.0);
+        d.tail_us = 0.0;
     }
     *n = c;
 }

@@ -281,3 +281,25 @@ def test_plan_many_equals_one_plan_per_call():
     finally:
         h.close()
         h0.close()
+
+
+def test_tail_is_charged_once_per_plan():
+    """A micro-kernel's tail_us enters Cost(S, H) once, not once per wave:
+    cost = f_wave * g_predict(f_num) + tail (one region, no HBM floor)."""
+    hw = mp.MpHw(num_pe=4, warps_per_wave=16, local_mem_bytes=1 << 17, shared_mem_bytes=1 << 22,
+                 hbm_gbs=0.0, l2_gbs=0.0, mma_tflops=0.0)
+    k = mp.MpKernelDesc(um=64, un=64, uk=64, warps=4, swap=0, fixed_us=1.0, per_step_us=0.5, tail_us=0.0)
+    h = mp.mp_init_host(hw, [k])
+    try:
+        M, N, K = 64 * 8, 64, 64 * 10          # 8 tasks on 4 slots: 2 waves of 10 steps
+        base = mp.mp_evaluate_plan(h, 1, M, N, K, [dict(kernel=0, m0=0, n0=0, m_ext=M, n_ext=N)])
+        assert base.region[0].f_wave == 2
+        assert base.cost_us == pytest.approx(2 * (1.0 + 0.5 * 10))
+        mp.mp_set_kernel_model(h, 0, 1.0, 0.5, 3.0)
+        with_tail = mp.mp_evaluate_plan(h, 1, M, N, K, [dict(kernel=0, m0=0, n0=0, m_ext=M, n_ext=N)])
+        assert with_tail.cost_us == pytest.approx(base.cost_us + 3.0)
+        assert mp.mp_plan(h, M, N, K).cost_us == pytest.approx(base.cost_us + 3.0)
+        with pytest.raises(mp.MPError):
+            mp.mp_set_kernel_model(h, 0, 1.0, 0.5, -1.0)
+    finally:
+        h.close()
