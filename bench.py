@@ -298,7 +298,15 @@ def config_record(name, args, lib, h, dev, sp, stream, peaks, local):
     for _ in range(3):
         run_calls(calls)
     torch.cuda.synchronize()
-    steps = max(3, min(args.steps, 20))
+    # Enough steps for the clock sampler (100 ms period) to see the region:
+    # at least about 0.25 s, at least 3 steps.
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    run_calls(calls)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = max(1e-3, w0.elapsed_time(w1))
+    steps = int(max(3, min(20000, math.ceil(250.0 / est_ms))))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         e0.record(stream)
