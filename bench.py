@@ -49,6 +49,15 @@ EPILOGUES = {"none": (0, False), "relu": (1, False), "gelu": (2, False), "bf16":
              "relu+bf16": (1, True), "gelu+bf16": (2, True)}
 
 
+CALIB_TABLE = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
+
+
+def calib_arg(args):
+    """mp_init's calib_path: the shipped GB300 table ("" -- the analytic model
+    -- with --no-calib or when the table is missing)."""
+    return CALIB_TABLE if (os.path.exists(CALIB_TABLE) and not args.no_calib) else ""
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -346,10 +355,10 @@ def run_mp(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    # The planner's g_predict table, measured once per machine by
-    # micro_polymerization_gb300/calibrate.py (analytic defaults if absent).
-    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
-    calib = calib if (os.path.exists(calib) and not args.no_calib) else None
+    # The planner's performance model: the table measured on GB300 by
+    # micro_polymerization_gb300/calibrate.py and shipped with the package
+    # (mp_init's default), or with --no-calib the analytic model.
+    calib = calib_arg(args)
     h = mp.mp_init(local, calib)
     lib = mp.library()
     stream = torch.cuda.current_stream()
@@ -643,6 +652,7 @@ def run_mp(args):
             "no_plan_cache": no_cache,
             "configs": configs,
             "cost_model": "calibrated" if calib else "analytic",
+            "cost_model_table": os.path.relpath(calib, ROOT) if calib else None,
             "clocks": clocks.summary(), "impl": "mp",
         }
         print(json.dumps(line), flush=True)
@@ -1062,8 +1072,7 @@ def run_conv(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
-    h = mp.mp_init(local, calib if (os.path.exists(calib) and not args.no_calib) else None)
+    h = mp.mp_init(local, calib_arg(args))
     lib = mp.library()
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -1249,8 +1258,7 @@ def run_grouped(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    calib = os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt")
-    h = mp.mp_init(local, calib if (os.path.exists(calib) and not args.no_calib) else None)
+    h = mp.mp_init(local, calib_arg(args))
     lib = mp.library()
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream

@@ -133,16 +133,24 @@ typedef struct {
 /*
  * Create a handle on CUDA device `device` (must be an sm_103 GB300-class
  * GPU).  Reads the device's SM count and memory sizes into H, allocates the
- * library-owned device memory, and loads a micro-kernel timing table from
- * `calib_path` when it is non-NULL and readable; otherwise the analytic
- * default model is used.  The table is plain text, one micro-kernel per line:
- * "um un uk swap fixed_us per_step_us" ('#' starts a comment); lines that
- * name no kernel of the set are ignored.  The rates in H default to GB300
- * figures and can be overridden with the environment variables MP_HBM_GBS,
- * MP_L2_GBS and MP_MMA_TFLOPS.  The set holds the CTA-pair micro-kernels
- * only when the device can keep two-CTA clusters of the kernel resident and
- * MP_PAIR is not "0"; they come last, so the other kernels' indices do not
- * depend on them.
+ * library-owned device memory, and sets the micro-kernels' performance model
+ * (g_predict, its tail, the split-K reduction terms):
+ *   calib_path NULL: the table measured on GB300 that ships with the library
+ *       (<package>/calib/gb300.txt beside <package>/_lib/libmp.so), when it
+ *       is readable; otherwise the analytic model;
+ *   calib_path "": the analytic model (hand-fitted GB300 constants);
+ *   otherwise: the table at calib_path when readable, else the analytic model.
+ * A table is plain text, one micro-kernel per line:
+ * "um un uk swap fixed_us per_step_us [tail_us]", plus lines
+ * "split on_chip sync_us bytes_factor [S]" for the split-K reduction (see
+ * mp_set_split_model; without S, on_chip 1 sets every cluster size); '#'
+ * starts a comment, and lines that name no kernel of the set are ignored.
+ * micro_polymerization_gb300/calibrate.py writes such tables.  The rates in
+ * H default to GB300 figures and can be overridden with the environment
+ * variables MP_HBM_GBS, MP_L2_GBS and MP_MMA_TFLOPS.  The set holds the
+ * CTA-pair micro-kernels only when the device can keep two-CTA clusters of
+ * the kernel resident and MP_PAIR is not "0"; they come last, so the other
+ * kernels' indices do not depend on them.
  * Errors: MP_ERR_INVALID_ARG (out NULL or bad device), MP_ERR_UNSUPPORTED
  * (not sm_103), MP_ERR_NO_MEMORY, MP_ERR_CUDA.
  */
@@ -397,6 +405,34 @@ mp_status mp_get_hw(mp_handle h, mp_hw* hw, mp_kernel_desc* kernels, int32_t* nu
  * per-step time not positive).
  */
 mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double per_step_us, double tail_us);
+
+/*
+ * Replace the cost model of the split-K reduction (MikPoly summary, section 3:
+ * a split tile's tasks each run g_predict(f_num) K steps and then combine
+ * their partial sums).  A task of a tile split S > 1 ways costs
+ *     g_predict(f_num) + sync_us + bytes_factor * 4 um un / (l2_gbs / num_pe)
+ * microseconds (the last term: the tile's fp32 partial at one PE's share of
+ * L2 bandwidth).  on_chip = 0 (S = 0) sets the reduction through L2;
+ * on_chip = 1 the one through distributed shared memory in clusters of S
+ * CTAs, for S in [2, 8], or for every such S when S = 0.  The plan cache is
+ * cleared.  Errors: MP_ERR_INVALID_ARG (h NULL, on_chip or S out of range, a
+ * negative or NaN term).
+ */
+mp_status mp_set_split_model(mp_handle h, int32_t on_chip, int32_t S, double sync_us, double bytes_factor);
+
+/*
+ * Read one split-K cost entry: (on_chip 0, S 0) or (on_chip 1, S in [2, 8]).
+ * Either output pointer may be NULL.  Errors: MP_ERR_INVALID_ARG.
+ */
+mp_status mp_get_split_model(mp_handle h, int32_t on_chip, int32_t S, double* sync_us, double* bytes_factor);
+
+/*
+ * Apply a calibration table (the text format mp_init reads) to a handle:
+ * the lines that name a micro-kernel of its set and the "split" lines
+ * replace those terms; the rest of the model is kept.  The plan cache is
+ * cleared.  Errors: MP_ERR_INVALID_ARG (h or path NULL, file unreadable).
+ */
+mp_status mp_load_calibration(mp_handle h, const char* path);
 
 /* Static text for a status code. */
 const char* mp_status_string(mp_status s);

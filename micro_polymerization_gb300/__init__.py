@@ -18,7 +18,7 @@ from . import _build
 __all__ = [
     "MPError", "mp_init", "mp_init_host", "mp_destroy", "mp_plan", "mp_plan_batched", "mp_plan_many",
     "mp_evaluate_plan", "mp_gemm", "mp_gemm_batched", "mp_check", "mp_force_plan", "mp_get_hw",
-    "mp_set_kernel_model", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
+    "mp_set_kernel_model", "mp_set_split_model", "mp_get_split_model", "mp_load_calibration", "mp_inject_wait_timeout", "mp_status_string", "library", "mp_gemm_noalloc",
     "mp_check_noalloc", "mp_noalloc_inject_wait_timeout",
     "mp_enumerate_plans", "mp_gemm_with_plan", "mp_set_plan_mode", "MP_PLAN_MIKPOLY", "MP_PLAN_WAVE",
     "MP_PLAN_PIPE", "mp_gemm_ex", "MP_ACT_NONE", "MP_ACT_RELU", "MP_ACT_GELU", "MP_EPI_OUT_BF16",
@@ -159,6 +159,10 @@ def library(build: bool = True) -> ctypes.CDLL:
                 "mp_get_hw": ([_vp, ctypes.POINTER(MpHw), ctypes.POINTER(MpKernelDesc),
                                ctypes.POINTER(_i32)], ctypes.c_int),
                 "mp_set_kernel_model": ([_vp, _i32, ctypes.c_double, ctypes.c_double, ctypes.c_double], ctypes.c_int),
+                "mp_set_split_model": ([_vp, _i32, _i32, ctypes.c_double, ctypes.c_double], ctypes.c_int),
+                "mp_load_calibration": ([_vp, ctypes.c_char_p], ctypes.c_int),
+                "mp_get_split_model": ([_vp, _i32, _i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+                                       ctypes.c_int),
                 "mp_inject_wait_timeout": ([_vp, _i32, _i64], ctypes.c_int),
                 "mp_status_string": ([ctypes.c_int], ctypes.c_char_p),
                 "mp_enumerate_plans": ([_vp, _i64, _i64, _i64, _i64, ctypes.POINTER(MpPlanInfo), _i32,
@@ -223,9 +227,11 @@ class Handle:
 
 
 def mp_init(device: int = 0, calib_path: Optional[str] = None) -> Handle:
+    """calib_path None: the measured GB300 table shipped in calib/gb300.txt;
+    "": the analytic model; otherwise the table at that path."""
     out = _vp()
     _check(library().mp_init(ctypes.byref(out), int(device),
-                             calib_path.encode() if calib_path else None), "mp_init")
+                             os.fsencode(calib_path) if calib_path is not None else None), "mp_init")
     return Handle(out.value, device)
 
 
@@ -562,6 +568,25 @@ def mp_get_hw(h: Handle):
 
 def mp_set_kernel_model(h: Handle, k: int, fixed_us: float, per_step_us: float, tail_us: float = 0.0) -> None:
     _check(library().mp_set_kernel_model(h.ptr, k, fixed_us, per_step_us, tail_us), "mp_set_kernel_model")
+
+
+def mp_set_split_model(h: Handle, on_chip: int, sync_us: float, bytes_factor: float, S: int = 0) -> None:
+    """on_chip 0: the reduction through L2 (S 0); 1: on chip in clusters of S
+    (2..8), or every cluster size when S is 0."""
+    _check(library().mp_set_split_model(h.ptr, int(on_chip), int(S), sync_us, bytes_factor), "mp_set_split_model")
+
+
+def mp_load_calibration(h: Handle, path: str) -> None:
+    _check(library().mp_load_calibration(h.ptr, os.fsencode(path)), "mp_load_calibration")
+
+
+def mp_get_split_model(h: Handle, on_chip: int, S: int = 0):
+    """(sync_us, bytes_factor) of the split-K reduction: on_chip 0 (S 0)
+    through L2, on_chip 1 on chip in clusters of S (2..8)."""
+    s, f = ctypes.c_double(), ctypes.c_double()
+    _check(library().mp_get_split_model(h.ptr, int(on_chip), int(S), ctypes.byref(s), ctypes.byref(f)),
+           "mp_get_split_model")
+    return s.value, f.value
 
 
 def mp_inject_wait_timeout(h: Handle, enable=True, limit_ns: int = 0) -> None:

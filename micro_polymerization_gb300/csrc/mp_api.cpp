@@ -3,6 +3,8 @@
 // throws across the boundary or falls back to host arithmetic.
 #include <cerrno>
 #include <cstdio>
+#include <dlfcn.h>
+#include <string>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -26,16 +28,45 @@ double env_double(const char* name, double dflt) {
     return (end && end != v && x > 0) ? x : dflt;
 }
 
-// Calibration table: "um un uk swap fixed_us per_step_us [tail_us]" per line
-// (a line without tail_us keeps the kernel's tail).
-void load_calibration(mp_handle h, const char* path) {
-    if (!path || !*path) return;
+// Calibration table: "um un uk swap fixed_us per_step_us [tail_us]" per
+// micro-kernel (a line without tail_us keeps the kernel's tail), and
+// "split on_chip sync_us bytes_factor [S]" for the split-K reduction (on_chip
+// 0: through L2; 1: on chip, for cluster size S or, without S, every size).
+// One split-K cost entry (see mp_set_split_model); false if out of range.
+bool set_split_model(mp_handle h, int on_chip, int S, double sync_us, double factor) {
+    if (!(sync_us >= 0) || !(factor >= 0)) return false;
+    if (on_chip == 0 && S == 0) {
+        h->split_sync_us[0] = sync_us;
+        h->split_bytes_factor[0] = factor;
+        return true;
+    }
+    if (on_chip != 1 || (S != 0 && (S < 2 || S > mp::kClusterSplitMaxS))) return false;
+    for (int s = 2; s <= mp::kClusterSplitMaxS; s++) {
+        if (S == 0 || s == S) {
+            h->split_sync_us[s] = sync_us;
+            h->split_bytes_factor[s] = factor;
+        }
+    }
+    return true;
+}
+
+// Returns false when the file cannot be opened.
+bool load_calibration(mp_handle h, const char* path) {
+    if (!path || !*path) return false;
     FILE* f = std::fopen(path, "r");
-    if (!f) return;
+    if (!f) return false;
     char line[512];
     while (std::fgets(line, sizeof line, f)) {
         char* hash = std::strchr(line, '#');
         if (hash) *hash = 0;
+        int on_chip, S = 0;
+        double sync_us, factor;
+        const int sg = std::sscanf(line, " split %d %lf %lf %d", &on_chip, &sync_us, &factor, &S);
+        if (sg >= 3) {
+            if (sg == 3) S = 0;
+            set_split_model(h, on_chip, S, sync_us, factor);
+            continue;
+        }
         int um, un, uk, swap;
         double fixed, step, tail = -1.0;
         const int got = std::sscanf(line, "%d %d %d %d %lf %lf %lf", &um, &un, &uk, &swap, &fixed, &step, &tail);
@@ -51,6 +82,23 @@ void load_calibration(mp_handle h, const char* path) {
         }
     }
     std::fclose(f);
+    mp::clear_plan_cache(h);
+    return true;
+}
+
+// The measured table shipped with the library: the library is
+// <package>/_lib/libmp.so and the table <package>/calib/gb300.txt.  Empty if
+// the library's own path cannot be found.
+std::string shipped_calibration() {
+    Dl_info info;
+    if (!dladdr(reinterpret_cast<void*>(&mp_init), &info) || !info.dli_fname) return {};
+    std::string p = info.dli_fname;
+    for (int up = 0; up < 2; up++) {
+        const size_t cut = p.find_last_of('/');
+        if (cut == std::string::npos) return {};
+        p.resize(cut);
+    }
+    return p + "/calib/gb300.txt";
 }
 
 mp_handle new_handle() {
@@ -246,7 +294,12 @@ mp_status mp_init(mp_handle* out, int device, const char* calib_path) {
     h->hw.mma_tflops = env_double("MP_MMA_TFLOPS", h->hw.mma_tflops);
     mp::default_gb300_kernels(h->hw, h->kernels, &h->num_kernels);
     mp::drop_unavailable_kernels(h);
-    load_calibration(h, calib_path);
+    if (calib_path) {
+        load_calibration(h, calib_path);  // "" keeps the analytic model
+    } else {
+        const std::string shipped = shipped_calibration();
+        if (!shipped.empty()) load_calibration(h, shipped.c_str());
+    }
     *out = h;
     return MP_OK;
 }
@@ -519,6 +572,31 @@ mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double pe
     h->kernels[k].per_step_us = per_step_us;
     h->kernels[k].tail_us = tail_us;
     mp::clear_plan_cache(h);
+    return MP_OK;
+}
+
+mp_status mp_load_calibration(mp_handle h, const char* path) {
+    if (!h || !path) return MP_ERR_INVALID_ARG;
+    return load_calibration(h, path) ? MP_OK : MP_ERR_INVALID_ARG;
+}
+
+mp_status mp_set_split_model(mp_handle h, int32_t on_chip, int32_t S, double sync_us, double bytes_factor) {
+    if (!h || !set_split_model(h, on_chip, S, sync_us, bytes_factor)) return MP_ERR_INVALID_ARG;
+    mp::clear_plan_cache(h);
+    return MP_OK;
+}
+
+mp_status mp_get_split_model(mp_handle h, int32_t on_chip, int32_t S, double* sync_us, double* bytes_factor) {
+    if (!h) return MP_ERR_INVALID_ARG;
+    int i;
+    if (on_chip == 0 && S == 0)
+        i = 0;
+    else if (on_chip == 1 && S >= 2 && S <= mp::kClusterSplitMaxS)
+        i = S;
+    else
+        return MP_ERR_INVALID_ARG;
+    if (sync_us) *sync_us = h->split_sync_us[i];
+    if (bytes_factor) *bytes_factor = h->split_bytes_factor[i];
     return MP_OK;
 }
 

@@ -511,7 +511,7 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
             ok = r.splits == S && R * (L + 4) * 4 <= dev::kRingBytes;
             tasks += cdiv(r.m_ext, r.um) * cdiv(r.n_ext, r.un) * batch * S;
         }
-        if (ok && tasks <= h->cluster_ctas[S]) csplit = S;
+        if (ok && tasks <= mp::cluster_split_room(h, S)) csplit = S;
     }
     p.csplit = csplit;
     p.pair = pair;

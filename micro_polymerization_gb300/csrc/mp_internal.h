@@ -26,6 +26,18 @@ constexpr int64_t kDefaultWorkspaceFloats = 16ll << 20;  // 64 MiB of fp32 parti
 constexpr int64_t kDefaultStagingBytes = 1ll << 30;      // repack area for unaligned operands
 constexpr int kMaxFixedDevices = 64;                      // devices served by the no-allocation entry point
 
+// Split-K reduction cost beyond g_predict(f_num), per task: sync_us plus
+// bytes_factor passes of the tile's fp32 partial at one PE's share of L2
+// bandwidth.  Through L2: park the partial, a counter round trip, sum 1/S of
+// every partial.  On chip (clusters of S <= 8 CTAs): two cluster barriers and
+// the sum through distributed shared memory, with terms per S (measured on
+// GB300 the sum costs more at S = 2 and 3, where each CTA sums and stores a
+// larger slice).  Defaults fitted on GB300 from timestamped kernel copies; a
+// calibration table's "split" lines replace them with measured values.
+constexpr int kClusterSplitMaxS = 8;
+constexpr double kDefaultSplitSyncUs[2] = {4.0, 2.5};        // [0] through L2, [1] on chip
+constexpr double kDefaultSplitBytesFactor[2] = {4.0, 1.0};
+
 struct PlanKey {
     int64_t batch, M, N, K;
     bool operator==(const PlanKey& o) const {
@@ -65,10 +77,33 @@ struct mp_handle_s {
     int32_t cluster_split_max = 0;
     int32_t cluster_ctas[17] = {};
 
+    // Split-K cost model (mp_set_split_model): index 0 through L2, index S
+    // (2..8) on chip in clusters of S CTAs; index 1 is unused.
+    double split_sync_us[mp::kClusterSplitMaxS + 1];
+    double split_bytes_factor[mp::kClusterSplitMaxS + 1];
+    mp_handle_s() {
+        for (int s = 0; s <= mp::kClusterSplitMaxS; s++) {
+            split_sync_us[s] = mp::kDefaultSplitSyncUs[s == 0 ? 0 : 1];
+            split_bytes_factor[s] = mp::kDefaultSplitBytesFactor[s == 0 ? 0 : 1];
+        }
+    }
+
     mp::DeviceState* dev = nullptr;
 };
 
 namespace mp {
+
+// Tasks a split-K launch on chip (clusters of S CTAs) may have: the clusters
+// the device keeps resident, less one for odd S.  Measured on GB300 in a
+// stream of different GEMMs, clusters of 3 and 5 that took every cluster slot
+// cost 3-5 us more than with one slot free (odd clusters straddle the
+// two-SM TPCs, and the last ones wait until the previous kernel's CTAs leave
+// the SMs they need); at full occupancy clusters of 2, 4, 6 and 8 did not,
+// and back to back, one shape after itself, none did.
+inline int64_t cluster_split_room(const mp_handle_s* h, int S) {
+    const int64_t cap = h->cluster_ctas[S];
+    return (S & 1) ? (cap > S ? cap - S : 0) : cap;
+}
 
 // Planner (mp_planner.cpp).
 mp_status plan_shape(mp_handle h, int64_t batch, int64_t M, int64_t N, int64_t K,

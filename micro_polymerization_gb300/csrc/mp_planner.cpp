@@ -48,19 +48,11 @@ namespace {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Split-K: every split parks its fp32 partial, waits for the tile's other
-// splits (a counter round trip through L2) and sums 1/S of all partials.
-// Measured on GB300: about 6 us beyond the K loop for a 128 x 128 tile.
-constexpr double kSplitSyncUs = 4.0;
-constexpr double kSplitBytesFactor = 4.0;  // tile bytes moved, in L2 passes
-// On chip (clusters of S CTAs, one task each): the partial goes TMEM ->
-// shared memory, one cluster barrier, 1/S of the rows summed over S partials
-// through distributed shared memory, a second barrier before exit.  Measured
-// on GB300: 2-3 us cheaper than through L2 for S <= 8; past 8 (non-portable
-// cluster sizes) no cheaper, so only S <= 8 runs on chip.
-constexpr int kClusterSplitMax = 8;
-constexpr double kClusterSplitUs = 2.5;
-constexpr double kClusterSplitBytesFactor = 1.0;
+// Split-K on chip runs in clusters of S CTAs, one task each.  Measured on
+// GB300: 2-3 us cheaper than through L2 for S <= 8; past 8 (non-portable
+// cluster sizes) no cheaper, so only S <= 8 runs on chip.  The reduction's
+// cost terms live in the handle (split_sync_us, split_bytes_factor).
+constexpr int kClusterSplitMax = kClusterSplitMaxS;
 // Floor of one uk step of any micro-kernel: the single MMA-issuing thread's
 // per-instruction and per-stage cost (measured on GB300 with tiny tiles).
 constexpr double kStepFloorUs = 0.21;
@@ -87,10 +79,10 @@ inline int64_t slots_for(const mp_handle_s* h, const mp_kernel_desc& u) {
 }
 
 // Split-K runs on chip when the handle's device can hold clusters of S CTAs
-// and all `tasks` fit one wave of them.
+// and all `tasks` fit one wave of them (cluster_split_room).
 inline bool split_on_chip(const mp_handle_s* h, const mp_kernel_desc& u, int64_t splits, int64_t tasks) {
     return !u.pair && splits >= 2 && splits <= h->cluster_split_max && splits <= kClusterSplitMax &&
-           tasks <= h->cluster_ctas[splits];
+           tasks <= cluster_split_room(h, (int)splits);
 }
 
 // g_predict(f_num) plus the split-K reduction: every task of a split tile
@@ -102,10 +94,8 @@ inline double f_pipe_of(const mp_handle_s* h, const mp_kernel_desc& u, int64_t f
     if (splits > 1 && h->hw.l2_gbs > 0 && h->hw.num_pe > 0) {
         double tile_bytes = 4.0 * u.um * u.un;
         double pe_gbs = h->hw.l2_gbs / h->hw.num_pe;
-        if (split_on_chip(h, u, splits, tasks))
-            t += kClusterSplitUs + kClusterSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);
-        else
-            t += kSplitSyncUs + kSplitBytesFactor * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
+        const int c = split_on_chip(h, u, splits, tasks) ? (int)splits : 0;
+        t += h->split_sync_us[c] + h->split_bytes_factor[c] * tile_bytes / (pe_gbs * 1e3);  // bytes / (GB/s) -> us
     }
     return t;
 }
@@ -153,7 +143,7 @@ int split_candidates(const mp_handle_s* h, const mp_kernel_desc& u, int64_t tile
     if (fill > 1) out[n++] = (int32_t)fill;
     // The largest on-chip split that one wave of clusters holds.
     for (int32_t s = std::min<int32_t>(kClusterSplitMax, h->cluster_split_max); s >= 2; s--) {
-        if (s <= kb && tiles * s <= h->cluster_ctas[s]) {
+        if (s <= kb && tiles * s <= cluster_split_room(h, s)) {
             out[n++] = s;
             break;
         }

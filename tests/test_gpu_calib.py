@@ -1,0 +1,40 @@
+"""The measured GB300 table is the planner's default model on the GPU."""
+import os
+
+import pytest
+
+import micro_polymerization_gb300 as mp
+
+TABLE = os.path.join(os.path.dirname(mp.__file__), "calib", "gb300.txt")
+
+
+def _kernel_lines(path):
+    out = {}
+    for line in open(path):
+        f = line.split("#")[0].split()
+        if len(f) >= 6 and f[0] != "split":
+            out[(int(f[0]), int(f[1]), int(f[3]))] = tuple(float(x) for x in f[4:7])
+    return out
+
+
+@pytest.mark.gpu
+def test_mp_init_loads_the_shipped_table_by_default():
+    assert os.path.exists(TABLE)
+    want = _kernel_lines(TABLE)
+    h, ha = mp.mp_init(0), mp.mp_init(0, "")
+    try:
+        _, ks = mp.mp_get_hw(h)
+        _, ka = mp.mp_get_hw(ha)
+        seen = 0
+        for d, a in zip(ks, ka):
+            key = (d.um, d.un, d.swap)
+            if key in want:
+                seen += 1
+                assert (d.fixed_us, d.per_step_us, d.tail_us) == pytest.approx(want[key], abs=1e-4)
+        assert seen >= 8
+        # "" keeps the analytic model, which differs from the table.
+        assert any(abs(d.fixed_us - a.fixed_us) > 1e-3 for d, a in zip(ks, ka))
+        assert mp.mp_get_split_model(h, 0) != mp.mp_get_split_model(ha, 0)
+    finally:
+        h.close()
+        ha.close()

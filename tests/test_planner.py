@@ -303,3 +303,145 @@ def test_tail_is_charged_once_per_plan():
             mp.mp_set_kernel_model(h, 0, 1.0, 0.5, -1.0)
     finally:
         h.close()
+
+
+def _split_handle():
+    """4 PEs at 1000 GB/s of L2 (250 GB/s each), one 64 x 64 micro-kernel."""
+    hw = mp.MpHw(num_pe=4, warps_per_wave=16, local_mem_bytes=1 << 17, shared_mem_bytes=1 << 22,
+                 hbm_gbs=0.0, l2_gbs=1000.0, mma_tflops=0.0)
+    k = mp.MpKernelDesc(um=64, un=64, uk=64, warps=4, swap=0, fixed_us=1.0, per_step_us=0.5, tail_us=0.0)
+    return mp.mp_init_host(hw, [k])
+
+
+def test_split_model_enters_each_split_task():
+    """A tile split S ways costs g_predict(f_num) + sync_us + bytes_factor *
+    (4 um un bytes at one PE's share of L2) per task; a host handle has no
+    clusters, so the split goes through L2 (on_chip = 0)."""
+    h = _split_handle()
+    try:
+        M, N, K = 64, 64, 64 * 12            # one tile, 12 K steps
+        region = [dict(kernel=0, m0=0, n0=0, m_ext=M, n_ext=N, splits=4)]
+        d_sync, d_factor = mp.mp_get_split_model(h, 0)
+        pass_us = 4.0 * 64 * 64 / (250.0 * 1e3)
+        p = mp.mp_evaluate_plan(h, 1, M, N, K, region)
+        r = p.region[0]
+        assert (r.splits, r.f_num, r.f_parallel, r.f_wave) == (4, 3, 4, 1)
+        assert p.cost_us == pytest.approx(1.0 + 0.5 * 3 + d_sync + d_factor * pass_us)
+        mp.mp_set_split_model(h, 0, 7.0, 2.0)
+        assert mp.mp_get_split_model(h, 0) == (7.0, 2.0)
+        assert mp.mp_get_split_model(h, 1, S=2) != (7.0, 2.0)     # the on-chip terms are apart
+        p2 = mp.mp_evaluate_plan(h, 1, M, N, K, region)
+        assert p2.cost_us == pytest.approx(1.0 + 0.5 * 3 + 7.0 + 2.0 * pass_us)
+        # An unsplit plan does not see the split terms.
+        one = [dict(kernel=0, m0=0, n0=0, m_ext=M, n_ext=N)]
+        assert mp.mp_evaluate_plan(h, 1, M, N, K, one).cost_us == pytest.approx(1.0 + 0.5 * 12)
+        # A cheap enough reduction makes the search split; a dear one does not.
+        mp.mp_set_split_model(h, 0, 0.0, 0.0)
+        assert mp.mp_plan(h, M, N, K).region[0].splits > 1
+        mp.mp_set_split_model(h, 0, 100.0, 0.0)
+        assert mp.mp_plan(h, M, N, K).region[0].splits == 1
+        for bad in [(2, 1.0, 1.0, 0), (0, -1.0, 1.0, 0), (0, 1.0, float("nan"), 0), (0, 1.0, 1.0, 4),
+                    (1, 1.0, 1.0, 1), (1, 1.0, 1.0, 9)]:
+            with pytest.raises(mp.MPError):
+                mp.mp_set_split_model(h, *bad[:3], S=bad[3])
+        for on_chip, S in [(1, 0), (0, 3), (1, 9)]:
+            with pytest.raises(mp.MPError):
+                mp.mp_get_split_model(h, on_chip, S)
+        # On chip: one cluster size, or every size at once.
+        mp.mp_set_split_model(h, 1, 1.5, 0.5)
+        assert all(mp.mp_get_split_model(h, 1, S) == (1.5, 0.5) for S in range(2, 9))
+        mp.mp_set_split_model(h, 1, 6.0, 3.0, S=3)
+        assert mp.mp_get_split_model(h, 1, 3) == (6.0, 3.0)
+        assert mp.mp_get_split_model(h, 1, 4) == (1.5, 0.5)
+    finally:
+        h.close()
+
+
+def test_calibration_table_is_parsed(tmp_path):
+    """The table's kernel lines replace g_predict and its tail, its split lines
+    the reduction terms; comments and lines naming no kernel are ignored."""
+    h = _split_handle()
+    try:
+        path = tmp_path / "table.txt"
+        path.write_text("# um un uk swap fixed_us per_step_us tail_us\n"
+                        "64 64 64 0 2.5 0.25 0.75   # measured\n"
+                        "128 256 64 0 9.0 9.0 9.0\n"
+                        "split 0 3.25 1.5\n"
+                        "split 1 0.5 0.125\n"
+                        "split 1 2.75 0.625 2\n"
+                        "split 1 9.0 9.0 9\n"
+                        "split 2 9.0 9.0\n")
+        mp.mp_load_calibration(h, str(path))
+        _, ks = mp.mp_get_hw(h)
+        assert (ks[0].fixed_us, ks[0].per_step_us, ks[0].tail_us) == (2.5, 0.25, 0.75)
+        assert mp.mp_get_split_model(h, 0) == (3.25, 1.5)
+        assert mp.mp_get_split_model(h, 1, 2) == (2.75, 0.625)
+        assert all(mp.mp_get_split_model(h, 1, S) == (0.5, 0.125) for S in range(3, 9))
+        # The plan cache does not keep costs of the replaced model.
+        assert mp.mp_plan(h, 64, 64, 64 * 4).cost_us == pytest.approx(2.5 + 0.25 * 4 + 0.75)
+        with pytest.raises(mp.MPError):
+            mp.mp_load_calibration(h, str(tmp_path / "missing.txt"))
+    finally:
+        h.close()
+
+
+def test_calibration_writer_round_trips_through_the_parser(tmp_path):
+    """calibrate.write_table's text (both forms, with split lines) is what
+    mp_load_calibration reads back: g_predict, tail and the split terms."""
+    from micro_polymerization_gb300 import calibrate as cal
+    assert cal.fit_line([1, 2, 3], [5.0, 7.0, 9.0]) == pytest.approx((3.0, 2.0))
+    assert cal.fit_line([1, 2, 3], [9.0, 7.0, 5.0]) == pytest.approx((7.0, 0.0))  # slope clamped at 0
+    hw = mp.MpHw(num_pe=152, warps_per_wave=912, local_mem_bytes=1 << 17, shared_mem_bytes=1 << 27,
+                 hbm_gbs=6800.0, l2_gbs=20000.0, mma_tflops=1890.0)
+    h = mp.mp_init_host(hw)
+    try:
+        _, ks = mp.mp_get_hw(h)
+        rows = [(d, 1.0 + i, 0.25 + 0.01 * i, 4.0 + i, 5.0 + i, 0.5 + 0.01 * i, [(4, 9.0, 12.0)], (1, 1), (2, 1))
+                for i, d in enumerate(ks)]
+        split = {0: (4.25, 2.5, [(128, 256, 0, 12, 4, 14.5)]), 3: (2.125, 5.5, []), 8: (2.5, 2.75, [])}
+        for form in ("waves", "one-wave"):
+            path = tmp_path / f"{form}.txt"
+            cal.write_table(str(path), hw, rows, form, split)
+            h2 = mp.mp_init_host(hw)
+            try:
+                mp.mp_load_calibration(h2, str(path))
+                _, k2 = mp.mp_get_hw(h2)
+                for i, d in enumerate(k2):
+                    want = (1.0 + i, 0.25 + 0.01 * i, 4.0 + i) if form == "waves" else (5.0 + i, 0.5 + 0.01 * i, 0.0)
+                    assert (d.fixed_us, d.per_step_us, d.tail_us) == pytest.approx(want, abs=1e-4)
+                assert mp.mp_get_split_model(h2, 0) == pytest.approx((4.25, 2.5))
+                assert mp.mp_get_split_model(h2, 1, 3) == pytest.approx((2.125, 5.5))
+                assert mp.mp_get_split_model(h2, 1, 8) == pytest.approx((2.5, 2.75))
+            finally:
+                h2.close()
+    finally:
+        h.close()
+
+
+def test_waves_fit_and_refit(tmp_path):
+    """fit_kernel on exact lines T1 = 6 + 0.5 t, T2 - T1 = 2 + 0.25 t: a later
+    wave costs 2 us plus the one-wave rate, the first the whole T1 line
+    (tail 4); --refit rewrites a table from its recorded points."""
+    from micro_polymerization_gb300 import calibrate as cal
+    pts = [(t, 6 + 0.5 * t, (6 + 0.5 * t) + (2 + 0.25 * t)) for t in (4, 12, 24)]
+    assert cal.fit_kernel(pts) == pytest.approx((2.0, 0.5, 4.0, 6.0, 0.5))
+    hw = mp.MpHw(num_pe=152, warps_per_wave=912, local_mem_bytes=1 << 17, shared_mem_bytes=1 << 27,
+                 hbm_gbs=6800.0, l2_gbs=20000.0, mma_tflops=1890.0)
+    h = mp.mp_init_host(hw)
+    try:
+        _, ks = mp.mp_get_hw(h)
+        rows = [(d,) + cal.fit_kernel(pts) + (pts, (128, 256), (256, 256)) for d in ks]
+        src = tmp_path / "waves.txt"
+        cal.write_table(str(src), hw, rows, "waves", {0: (4.0, 2.0, [(128, 256, 0, 12, 4, 14.5)])})
+        dst = tmp_path / "one.txt"
+        cal.refit(str(src), str(dst), "one-wave")
+        mp.mp_load_calibration(h, str(dst))
+        _, k1 = mp.mp_get_hw(h)
+        assert all((d.fixed_us, d.per_step_us, d.tail_us) == pytest.approx((6.0, 0.5, 0.0), abs=1e-4) for d in k1)
+        assert mp.mp_get_split_model(h, 0) == pytest.approx((4.0, 2.0))
+        cal.refit(str(dst), str(tmp_path / "back.txt"), "waves")
+        mp.mp_load_calibration(h, str(tmp_path / "back.txt"))
+        _, kw = mp.mp_get_hw(h)
+        assert all((d.fixed_us, d.per_step_us, d.tail_us) == pytest.approx((2.0, 0.5, 4.0), abs=1e-4) for d in kw)
+    finally:
+        h.close()
