@@ -629,41 +629,36 @@ __device__ __forceinline__ void put_out4(const Params& p, uint8_t* d, float x0, 
     }
 }
 
+// Swapped tile: TMEM lane tl is column n_t0 + tl of D, and the 16 values
+// are rows m_t0 + c .. + 15 (a warp's stores of one row cover 128
+// contiguous bytes).  All 16 values of C are loaded before the first store:
+// C may be D itself (in place), so a load after a store could not be moved
+// ahead of it and the loads would wait for each other; each element of D
+// depends only on its own element of C, so reading them all first gives the
+// same result.
 template <int EPI>
 __device__ __forceinline__ void store16(const Params& p, const Work& w, int tl, int c, const float* v) {
     const float alpha = p.alpha, beta = p.beta;
-    if (!w.swap) {
-        // lane = row of D, columns = columns of D
-        const int m = w.m_t0 + tl;
-        if (m >= w.m_end) return;
-        uint8_t* d = d_ptr<EPI>(p, (long long)w.b * p.strideD + (long long)m * p.ldd);
-        const int es = d_esize<EPI>(p);
-        const float* cr = p.C + (long long)w.b * p.strideC + (long long)m * p.ldc;
-        const int n0 = w.n_t0 + c;
-#pragma unroll
-        for (int j = 0; j < 16; j++) {
-            const int n = n0 + j;
-            if (n < w.n_end) {
-                float r = alpha * v[j];
-                if (beta != 0.0f) r = fmaf(beta, cr[n], r);
-                put_out<EPI>(p, d + (long long)n * es, act_fn<EPI>(r));
-            }
-        }
-    } else {
-        // lane = column of D, columns = rows of D
-        const int n = w.n_t0 + tl;
-        if (n >= w.n_end) return;
-        uint8_t* bd = d_ptr<EPI>(p, (long long)w.b * p.strideD + n);
-        const long long ldd_b = p.ldd * d_esize<EPI>(p);
-        const long long bc = (long long)w.b * p.strideC + n;
+    const int n = w.n_t0 + tl;
+    if (n >= w.n_end) return;
+    uint8_t* bd = d_ptr<EPI>(p, (long long)w.b * p.strideD + n);
+    const long long ldd_b = p.ldd * d_esize<EPI>(p);
+    const long long bc = (long long)w.b * p.strideC + n;
+    float cv[16];
+    if (beta != 0.0f) {
 #pragma unroll
         for (int j = 0; j < 16; j++) {
             const int m = w.m_t0 + c + j;
-            if (m < w.m_end) {
-                float r = alpha * v[j];
-                if (beta != 0.0f) r = fmaf(beta, p.C[bc + (long long)m * p.ldc], r);
-                put_out<EPI>(p, bd + (long long)m * ldd_b, act_fn<EPI>(r));
-            }
+            cv[j] = m < w.m_end ? p.C[bc + (long long)m * p.ldc] : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        const int m = w.m_t0 + c + j;
+        if (m < w.m_end) {
+            float r = alpha * v[j];
+            if (beta != 0.0f) r = fmaf(beta, cv[j], r);
+            put_out<EPI>(p, bd + (long long)m * ldd_b, act_fn<EPI>(r));
         }
     }
 }
@@ -841,6 +836,18 @@ __device__ __forceinline__ void load_c(const Params& p, const Work& w, int lane,
 
 __device__ __forceinline__ void load_c32(const Params& p, const Work& w, int lane, int m0, int n0, float* c) {
     load_c<32>(p, w, lane, m0, n0, c);
+}
+
+// Swapped tile: ask L2 for the block of C its epilogue will read before the
+// accumulator is ready.  Warp quarter q stores D columns n_t0 + 32 q .. + 31
+// (one 128-byte line of a row); lane l asks for rows l, l + 32, ... of the
+// tile's w.bn rows.
+__device__ __forceinline__ void prefetch_c_swapped(const Params& p, const Work& w, int q, int lane) {
+    const int n = w.n_t0 + 32 * q;
+    if (n >= w.n_end) return;
+    const float* cb = p.C + (long long)w.b * p.strideC + n;
+    for (int r = lane; r < w.bn && w.m_t0 + r < w.m_end; r += 32)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(cb + (long long)(w.m_t0 + r) * p.ldc));
 }
 
 // Ask L2 for this lane's row of C over the whole tile (one 128-byte line per
@@ -1456,8 +1463,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (p.beta != 0.0f && w.splits == 1 && !w.swap) {
-                if (p.tma_d)
+            if (p.beta != 0.0f && w.splits == 1) {
+                if (w.swap)
+                    prefetch_c_swapped(p, w, q, lane);
+                else if (p.tma_d)
                     prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
                 else
                     prefetch_c_tile_row(p, w, w.m_t0 + q * 32 + lane);
