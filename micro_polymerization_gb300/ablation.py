@@ -20,7 +20,10 @@ Every plan is timed back to back with CUDA events through
 over the workload, together with the host planning time of the heuristic and
 of the enumeration.
 
-    python -m micro_polymerization_gb300.ablation [--workload dynamic_sequence] [--top 24] [--count 64]
+    python -m micro_polymerization_gb300.ablation [--workload dynamic_sequence] [--top 24] [--count 64] [--analytic]
+
+The cost model is the handle's default (the measured table shipped with the
+package); --analytic plans with the analytic model instead.
 """
 from __future__ import annotations
 
@@ -56,14 +59,15 @@ def _key(p):
     return tuple((r.kernel, r.m0, r.n0, r.m_ext, r.n_ext, r.splits) for r in p.regions())
 
 
-def run(workload: str = "dynamic_sequence", top: int = 24, count: int = 64, reps: int = 20, device: int = 0):
+def run(workload: str = "dynamic_sequence", top: int = 24, count: int = 64, reps: int = 20, device: int = 0,
+        analytic: bool = False):
     import torch
     import micro_polymerization_gb300 as mp
     from micro_polymerization_gb300 import workloads as wl
 
     dev = torch.device("cuda", device)
     torch.cuda.set_device(dev)
-    h = mp.mp_init(device)
+    h = mp.mp_init(device, "" if analytic else None)
     lib = mp.library()
     gs = [g for g in wl.workload(workload) if g.batch == 1][:count]
     tot = {"oracle": 0.0, "mikpoly": 0.0, "wave": 0.0, "pipe": 0.0}
@@ -102,7 +106,7 @@ def run(workload: str = "dynamic_sequence", top: int = 24, count: int = 64, reps
         h.close()
     n = max(1, len(gs))
     return {
-        "workload": workload, "gemms": len(gs), "top": top,
+        "workload": workload, "gemms": len(gs), "top": top, "cost_model": "analytic" if analytic else "default",
         "speed_vs_oracle": {k: round(tot["oracle"] / v, 4) for k, v in tot.items() if v > 0},
         "sum_us": {k: round(v, 1) for k, v in tot.items()},
         "plan_us_heuristic": round(plan_us / n, 2), "plan_us_enumeration": round(enum_us / n, 1),
@@ -118,8 +122,9 @@ def main(argv=None) -> int:
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--device", type=int, default=0)
     ap.add_argument("--per-shape", action="store_true", help="include every shape's times")
+    ap.add_argument("--analytic", action="store_true", help="plan with the analytic cost model")
     args = ap.parse_args(argv)
-    res = run(args.workload, args.top, args.count, args.reps, args.device)
+    res = run(args.workload, args.top, args.count, args.reps, args.device, args.analytic)
     if not args.per_shape:
         res.pop("per_shape")
     sys.stdout.write(json.dumps(res) + "\n")
