@@ -38,3 +38,31 @@ def test_mp_init_loads_the_shipped_table_by_default():
     finally:
         h.close()
         ha.close()
+
+
+@pytest.mark.gpu
+def test_calibrate_writes_a_table_the_library_loads(tmp_path, monkeypatch):
+    """calibrate.py end to end on a reduced grid (two K depths, one cluster
+    size on chip, one split through L2): every micro-kernel gets a line with a
+    positive rate, the split lines parse, and a handle planning with the
+    table still produces valid plans."""
+    from micro_polymerization_gb300 import calibrate as cal
+    monkeypatch.setattr(cal, "STEPS", (4, 12))
+    monkeypatch.setattr(cal, "SPLIT_STEPS", (4,))
+    monkeypatch.setattr(cal, "SPLIT_ON_CHIP", (4,))
+    monkeypatch.setattr(cal, "SPLIT_THROUGH_L2", (12,))
+    out = tmp_path / "gb300.txt"
+    assert cal.main(["--out", str(out)]) == 0
+    lines = _kernel_lines(str(out))
+    h = mp.mp_init(0, str(out))
+    try:
+        _, ks = mp.mp_get_hw(h)
+        assert all((k.um, k.un, k.swap) in lines for k in ks)
+        assert all(k.per_step_us > 0 and k.fixed_us >= 0 and k.tail_us >= 0 for k in ks)
+        sync, factor = mp.mp_get_split_model(h, 0)
+        assert sync >= 0 and factor >= 0
+        for M, N, K in [(105, 1024, 12544), (2088, 2304, 768), (4096, 4096, 4096), (7, 9, 5)]:
+            p = mp.mp_plan(h, M, N, K)
+            assert p.num_regions >= 1 and p.cost_us > 0
+    finally:
+        h.close()
