@@ -348,6 +348,29 @@ def test_in_place_c_equals_d():
     assert_parity(CD.cpu(), A, B, C, 1.5, 0.5, what="in place")
 
 
+@pytest.mark.parametrize("splits", [1, 3])
+def test_in_place_every_micro_kernel(splits):
+    """C = D in place with every micro-kernel forced: each epilogue path reads
+    an element of C before it writes that element of D (the swapped tiles
+    read a column's 16 values of C before their 16 stores)."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    try:
+        for k, desc in enumerate(_kernels()):
+            if desc.pair and splits > 1:
+                continue
+            for (M, N, K) in [(37, 520, 130), (130, 129, 64), (19, 200, 300)]:
+                mp.mp_force_plan(h, k, splits)
+                A, B, C = rand_problem(M, N, K, seed=k * 17 + N, beta=0.5)
+                CD = C.to(dev).clone()
+                mp.mp_gemm(h, A.to(dev), B.to(dev), CD, CD, 1.5, 0.5)
+                torch.cuda.synchronize()
+                assert_parity(CD.cpu(), A, B, C, 1.5, 0.5,
+                              what=f"in place, kernel {k} ({desc.um}x{desc.un} swap={desc.swap}) splits={splits} {(M, N, K)}")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
 def test_k_zero_and_empty():
     dev = torch.device("cuda", 0)
     C = torch.randn(33, 65)
