@@ -35,6 +35,14 @@ def test_mp_init_loads_the_shipped_table_by_default():
         # "" keeps the analytic model, which differs from the table.
         assert any(abs(d.fixed_us - a.fixed_us) > 1e-3 for d, a in zip(ks, ka))
         assert mp.mp_get_split_model(h, 0) != mp.mp_get_split_model(ha, 0)
+        # A table that cannot be read leaves the analytic model.
+        hm = mp.mp_init(0, os.path.join(os.path.dirname(TABLE), "no-such-table.txt"))
+        try:
+            _, km = mp.mp_get_hw(hm)
+            assert [(k.fixed_us, k.per_step_us, k.tail_us) for k in km] == \
+                [(k.fixed_us, k.per_step_us, k.tail_us) for k in ka]
+        finally:
+            hm.close()
     finally:
         h.close()
         ha.close()
