@@ -465,6 +465,40 @@ def run_mp(args):
         if mp.mp_check(h) != 0:
             raise RuntimeError("device status word set by the grouped submission")
 
+    # The same calls captured once in a CUDA graph and replayed: informational.
+    # A replay runs the plans and operand addresses of the capture, so no
+    # planning is inside it; the headline times the calls themselves.
+    as_graph = None
+    if not args.no_group:
+        cs = torch.cuda.Stream(device=dev)
+        gcalls = [gemm_call(lib, h, g, A, B, C, D, cs.cuda_stream, epi) for g, A, B, C, D in ops]
+        with torch.cuda.stream(cs):
+            run_calls(gcalls)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            run_calls(gcalls)
+        with torch.cuda.stream(cs):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            r0.record(cs)
+            for _ in range(args.steps):
+                graph.replay()
+            r1.record(cs)
+        torch.cuda.synchronize()
+        ms_graph = r0.elapsed_time(r1) / args.steps
+        if mp.mp_check(h) != 0:
+            raise RuntimeError("device status word set by the graph replays")
+        as_graph = {"ms_per_step": round(ms_graph, 4),
+                    "value": round(flops_step / (ms_graph * 1e-3) / 1e12, 3),
+                    "note": "the same mp_gemm calls captured once in a CUDA graph and replayed; a replay "
+                            "runs the plans and operand addresses of the capture (no planning inside); "
+                            "not the headline"}
+        del graph
+
     # Per-shape roofline fractions.  The per-shape time is the device time per
     # call with the GEMM called back to back on cold operands (see
     # per_shape_back_to_back); the event-bracketed times of the calls inside a
@@ -647,6 +681,7 @@ def run_mp(args):
                              launches=len(sel), kernel="k_poly_gemm", peak_source=peak_src),
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "as_one_group": as_group,
+            "as_graph": as_graph,
             "plan_us": round(plan_us, 3) if plan_us is not None else None,
             "plan_how": "one mp_plan_many call over the workload's shapes, no plan cache, best of 20",
             "no_plan_cache": no_cache,
@@ -1442,7 +1477,8 @@ def main(argv=None):
     ap.add_argument("--dump", default=None, help="write per-GEMM time, roofline and plan (JSON lines)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--no-group", action="store_true", help="skip the informational grouped submission")
+    ap.add_argument("--no-group", action="store_true",
+                    help="skip the informational grouped submission and CUDA-graph replay")
     ap.add_argument("--no-calib", action="store_true", help="plan with the analytic cost model")
     ap.add_argument("--no-configs", action="store_true", help="skip the records of the other workloads")
     ap.add_argument("--limit", type=int, default=0, help="only the first N GEMMs of the workload (profiling)")

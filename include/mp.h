@@ -268,7 +268,11 @@ mp_status mp_set_plan_mode(mp_handle h, int32_t mode);
  * K == 0 gives D = beta * C.  D may equal C only with ldc == ldd; any other
  * overlap of D with A, B or C is MP_ERR_INVALID_ARG.  Repeated calls with the
  * same plan give bitwise-identical D (split-K partials are reduced in a fixed
- * order).
+ * order).  A call may be recorded by CUDA stream capture into a graph: each
+ * replay runs the plan and the operand addresses of the capture (no planning
+ * on replay), on the data then in those buffers.  The handle's workspace,
+ * tile counters and staging area serve replays as they serve calls, so
+ * replays and calls of one handle must not overlap on the GPU.
  * Errors: MP_ERR_INVALID_ARG, MP_ERR_UNSUPPORTED (host-only handle or size
  * beyond the staging area), MP_ERR_PLAN, MP_ERR_CUDA (launch failure).
  */
