@@ -725,14 +725,32 @@ __device__ __forceinline__ void transpose16(int lane, const float* v, float4* st
     __syncwarp();
 }
 
+// beta * C for a normal tile's 32-column chunk c: lane = column n_t0 + c +
+// lane, cv[r] = row m_t0 + 32 q + r (0 outside the region).  All 32 loads are
+// issued before any is used, and the caller issues them before the chunk's
+// TMEM load: one memory round trip per chunk.
+__device__ __forceinline__ void load_c_cols(const Params& p, const Work& w, int q, int lane, int c, float* cv) {
+    const int n = w.n_t0 + c + lane;
+    const int mb = w.m_t0 + q * 32;
+    const int rows = min(32, w.m_end - mb);
+    const float* cr = p.C + (long long)w.b * p.strideC + (long long)mb * p.ldc + n;
+    const bool in_n = n < w.n_end;
+#pragma unroll
+    for (int r = 0; r < 32; r++) {
+        cv[r] = (in_n && r < rows) ? *cr : 0.0f;
+        cr += p.ldc;
+    }
+}
+
 // Normal tile whose D rows are not 16-byte aligned (no tensor map; any
 // alignment): the warp's 32 rows x 32 columns go through its shared-memory
 // slab (128-byte swizzle, conflict-free both ways) and come back one row at
 // a time with lane = column, so that every store instruction covers 128
-// contiguous bytes of one row of D.  Same arithmetic as the other paths.
+// contiguous bytes of one row of D.  cv: the chunk's beta * C operand
+// (load_c_cols), unused when beta == 0.  Same arithmetic as the other paths.
 template <int EPI>
 __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int q, int lane, int c, const float* v,
-                                            uint8_t* slab) {
+                                            const float* cv, uint8_t* slab) {
     const float a = p.alpha, bt = p.beta;
     const int n = w.n_t0 + c + lane;
     const bool in_n = n < w.n_end;
@@ -745,37 +763,19 @@ __device__ __forceinline__ void emit32_rows(const Params& p, const Work& w, int 
         *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     __syncwarp();
-    // Rows in two halves of 16; beta * C for a half is loaded first, all in
-    // flight at once (coalesced along each row; the values of the tile are
-    // in the slab by now).  Row pointers advance by the leading dimensions.
     const uint8_t* src = slab + (lane & 3) * 4;
     uint8_t* dp = d_ptr<EPI>(p, (long long)w.b * p.strideD + (long long)mb * p.ldd + n);
     const long long ldd_b = p.ldd * d_esize<EPI>(p);
-    const float* cp = p.C + (long long)w.b * p.strideC + (long long)mb * p.ldc + n;
-#pragma unroll 1
-    for (int h0 = 0; h0 < rows; h0 += 16) {
-        float cv[16];
-        if (bt != 0.0f) {
-            const float* cr = cp;
 #pragma unroll
-            for (int r = 0; r < 16; r++) {
-                cv[r] = (in_n && h0 + r < rows) ? *cr : 0.0f;
-                cr += p.ldc;
-            }
+    for (int r = 0; r < 32; r++) {
+        if (r >= rows) break;
+        const float x = *reinterpret_cast<const float*>(src + r * 128 + (((lane >> 2) ^ (r & 7)) << 4));
+        if (in_n) {
+            float o = a * x;
+            if (bt != 0.0f) o = fmaf(bt, cv[r], o);
+            put_out<EPI>(p, dp, act_fn<EPI>(o));
         }
-#pragma unroll
-        for (int r = 0; r < 16; r++) {
-            if (h0 + r >= rows) break;
-            const int rr = h0 + r;
-            const float x = *reinterpret_cast<const float*>(src + rr * 128 + (((lane >> 2) ^ (rr & 7)) << 4));
-            if (in_n) {
-                float o = a * x;
-                if (bt != 0.0f) o = fmaf(bt, cv[r], o);
-                put_out<EPI>(p, dp, act_fn<EPI>(o));
-            }
-            dp += ldd_b;
-        }
-        cp += 16 * p.ldc;
+        dp += ldd_b;
     }
 }
 
@@ -1574,6 +1574,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 // The slab area may still be read by an earlier tile's bulk stores.
                 if (lane == 0) bulk_wait_read_all();
                 for (int c = 0; c < w.bn; c += 32) {
+                    float cv[32];
+                    load_c_cols(p, w, q, lane, c, cv);
                     float v[32];
                     if (has_k) {
                         tmem_ld32(t + c, v);
@@ -1581,7 +1583,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 #pragma unroll
                         for (int j = 0; j < 32; j++) v[j] = 0.0f;
                     }
-                    emit32_rows<EPI>(p, w, q, lane, c, v, epi_g);
+                    emit32_rows<EPI>(p, w, q, lane, c, v, cv, epi_g);
                 }
                 tc_fence_before();
                 __syncwarp();
