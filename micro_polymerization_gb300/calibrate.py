@@ -32,7 +32,7 @@ runs each, two calibrations on two boxes): waves tables timed in the mixed
 stream planned the dynamic-sequence step 0.3-0.8% faster, dynamic resolution
 0.4-0.5% and merged QKV 0.6-0.9% faster, the batched merge 0-1.5% slower and
 the skinny GEMM even.  On the stress sweep (alpha 1.5, beta 0.5) the table
-came out 1.7% slower on the final kernel: it is calibrated with beta = 0,
+planned 1.7% slower: it is calibrated with beta = 0,
 and with beta * C a partly filled 128-row tile's epilogue leaves most of its
 warps idle, where the swapped tiles the analytic model picks for small M do
 not.  Charging later waves the
