@@ -25,22 +25,21 @@ Two forms of table can be written, in the text format mp_init reads
       intercept;
   one-wave: the least-squares line through the one-wave times; launch, fill
       and the write-back are inside fixed_us, charged in every wave, and
-      tail_us is 0 -- the structure of the analytic default model.
+      tail_us is 0 -- the structure of the analytic model.
 
 Measured on GB300 against the analytic model (bench.py, the same box, three
 runs each, two calibrations on two boxes): waves tables timed in the mixed
 stream planned the dynamic-sequence step 0.3-0.8% faster, dynamic resolution
 0.4-0.5% and merged QKV 0.6-0.9% faster, the batched merge 0-1.5% slower and
 the skinny GEMM even.  On the stress sweep (alpha 1.5, beta 0.5) the table
-planned 1.7% slower: it is calibrated with beta = 0,
-and with beta * C a partly filled 128-row tile's epilogue leaves most of its
-warps idle, where the swapped tiles the analytic model picks for small M do
-not.  Charging later waves the
-two-wave increment's own slope instead let one-wave CTA-pair plans of
-(3520..4032, 768, 3072) look cheap and made the step 3% slower; the one-wave
-form charges a pair's launch cost in every wave and moved a 29-wave GEMM of
-the stress sample off CTA pairs; tables timed back to back made the steps
-1-7% slower.
+planned 1.7% slower: it is calibrated with beta = 0, and with beta * C a
+partly filled 128-row tile's epilogue leaves most of its warps idle, where
+the swapped tiles the analytic model picks for small M do not.  Charging
+later waves the two-wave increment's own slope instead let one-wave CTA-pair
+plans of (3520..4032, 768, 3072) look cheap and made the step 3% slower; the
+one-wave form charges a pair's launch cost in every wave and moved a 29-wave
+GEMM of the stress sample off CTA pairs; tables timed back to back made the
+steps 1-7% slower.
 
 The split-K reduction is measured the same way: one-CTA micro-kernels forced
 to split K S ways (S = 2..8 reduce on chip in clusters of S CTAs; S = 12, 16
