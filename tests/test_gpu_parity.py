@@ -771,6 +771,29 @@ def test_ring_staged_split_sums_timeout_reports_and_recovers():
         mp.mp_force_plan(h, -1, 0)
 
 
+@pytest.mark.parametrize("kernel_un", [64, 128, 192, 256])
+def test_aligned_d_beta_c_every_width(kernel_un):
+    """beta * C with 16-byte aligned rows of C and D (the bulk-store epilogue,
+    C read a 32-column chunk at a time): one-wave and multi-wave plans,
+    ragged last row tiles, tiles past N, in place and not, every normal tile
+    width, against the oracle."""
+    h = handle()
+    dev = torch.device("cuda", 0)
+    k = [i for i, d in enumerate(_kernels()) if (d.um, d.un, d.swap, d.pair) == (128, kernel_un, 0, 0)][0]
+    try:
+        mp.mp_force_plan(h, k, 1)
+        for (M, N, K) in [(300, 1024, 200), (1000, 2048, 128), (37, 512, 64), (5000, 768, 96)]:
+            A, B, C = rand_problem(M, N, K, seed=kernel_un + M, beta=0.5)
+            D = run_gemm(A, B, C, 1.5, 0.5, h=h)
+            assert_parity(D, A, B, C, 1.5, 0.5, what=f"aligned beta*C, 128x{kernel_un} {(M, N, K)}")
+            CD = C.to(dev).clone()
+            mp.mp_gemm(h, A.to(dev), B.to(dev), CD, CD, 1.5, 0.5)
+            torch.cuda.synchronize()
+            assert_parity(CD.cpu(), A, B, C, 1.5, 0.5, what=f"aligned beta*C in place, 128x{kernel_un} {(M, N, K)}")
+    finally:
+        mp.mp_force_plan(h, -1, 0)
+
+
 # --------------------------------------------------------------------------
 # the stress sweep: one GEMM of every plan class the polymerizer produces
 # --------------------------------------------------------------------------
