@@ -866,7 +866,7 @@ __device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int l
     __syncwarp();
     const float a = p.alpha, bt = p.beta;
     uint8_t* row = slab + lane * 128;
-    if (bt == 0.0f && epi_act<EPI>() == 0) {
+    if ((EPI & 8) != 0 || (bt == 0.0f && epi_act<EPI>() == 0)) {
 #pragma unroll
         for (int j = 0; j < 8; j++)
             *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
@@ -1146,6 +1146,10 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
 template <int CG, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
     constexpr bool kPair = CG == 2;
+    // EPI bit 3: the lean instantiation for plans of one-CTA tiles with no
+    // split and no swapped region, 16-byte aligned D and beta = 0 (the
+    // launch picks it); the paths it cannot take are folded away.
+    constexpr bool kLean = (EPI & 8) != 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1264,7 +1268,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const Work w = decode(p, regs_s, u, rank);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
             const int blk0 = w.n_t0 >> 6;
-            const int nblk = w.swap ? 2 : (w.bn >> 6);
+            const int nblk = (!kLean && w.swap) ? 2 : (w.bn >> 6);
             const bool whole_b = blk0 + nblk <= p.nb_full;
             for (int kb = w.kb0; kb < w.kb1; kb += kg, ++g) {
                 if ((g & 1u) != pid) continue;
@@ -1284,7 +1288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     for (int j = 0; j < nsub; j++) {
                     const uint32_t xs = ring0 + stage * stage_bytes + j * sub_bytes, ys = xs + kXBytes;
                     const int kc = (kb + j) * 64;
-                    if (!w.swap) {
+                    if (kLean || !w.swap) {
                         if constexpr (kPair) {
                             // This CTA's 128 rows of A and its half of B's
                             // 64-column blocks (rank r: blocks [r h, r h + h)).
@@ -1385,19 +1389,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
             const uint32_t idesc =
-                w.swap ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
+                (!kLean && w.swap) ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
             // Descriptors of stage 0, K step 0.  Every later stage and K step
             // only moves the start address (bits 0..13, in 16-byte units;
             // shared addresses stay below 2^18, so the sums never carry out of
             // the field): one 64-bit add per operand.
-            const uint64_t dx0 = w.swap ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
+            const bool swp = !kLean && w.swap;
+            const uint64_t dx0 = swp ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
             // Pairs of 192-wide tiles hold B with the 64-byte swizzle.
             const bool b64 = kPair && w.bn == 192;
-            const uint64_t dy0 = w.swap ? desc_kmajor(ring0 + kXBytes, 0)
+            const uint64_t dy0 = swp ? desc_kmajor(ring0 + kXBytes, 0)
                                  : b64  ? desc_mnmajor64(ring0 + kXBytes, 0)
                                         : desc_mnmajor(ring0 + kXBytes, 0);
-            const uint32_t kx = w.swap ? (2048u >> 4) : (32u >> 4);
-            const uint32_t ky = w.swap ? (32u >> 4) : b64 ? (1024u >> 4) : (2048u >> 4);
+            const uint32_t kx = swp ? (2048u >> 4) : (32u >> 4);
+            const uint32_t ky = swp ? (32u >> 4) : b64 ? (1024u >> 4) : (2048u >> 4);
             const uint32_t sstep = stage_bytes >> 4, jstep = sub_bytes >> 4;
             // One wait and one commit per stage of kg (1 or 2) K steps.
             for (int kb = w.kb0; kb < w.kb1; kb += kg) {
@@ -1463,7 +1468,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (p.beta != 0.0f && w.splits == 1) {
+            if (!kLean && p.beta != 0.0f && w.splits == 1) {
                 if (w.swap)
                     prefetch_c_swapped(p, w, q, lane);
                 else if (p.tma_d)
@@ -1543,8 +1548,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (!epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap) {
-                const bool with_c = p.beta != 0.0f;
+            } else if (kLean || (!epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap)) {
+                const bool with_c = !kLean && p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
                     float cv[32];
@@ -1767,7 +1772,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 
     grid_dep_wait();
     __syncthreads();
-    if constexpr (!kPair) {
+    if constexpr (!kPair && !kLean) {
         if (p.csplit) {
             // Every partial of this CTA's tile is now in its cluster's shared
             // memory; sum this CTA's slice; leave only when no CTA of the
