@@ -749,12 +749,12 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // threads, shared memory and launch bounds).
     const int epi = p.act | (p.out_bf16 ? 4 : 0);
     // The lean instantiation (EPI bit 3) when the plan needs none of the
-    // paths it leaves out: one-CTA tiles, no split, no swapped region,
-    // 16-byte aligned D, beta = 0, the plain epilogue.
-    bool lean = epi == 0 && !pair && !csplit && p.tma_d && p.beta == 0.0f;
+    // paths it leaves out: no split, no swapped region, 16-byte aligned D,
+    // beta = 0, the plain epilogue (one-CTA tiles or CTA pairs).
+    bool lean = epi == 0 && !csplit && p.tma_d && p.beta == 0.0f;
     for (int i = 0; i < plan.num_regions && lean; i++)
         lean = plan.region[i].splits == 1 && !plan.region[i].swap;
-    const cudaError_t e = lean ? launch_poly_gemm<8>(cfg, false, p)
+    const cudaError_t e = lean ? launch_poly_gemm<8>(cfg, pair, p)
                           : epi == 0 ? launch_poly_gemm<0>(cfg, pair, p)
                           : p.out_bf16 ? launch_poly_gemm_bf16(cfg, pair, epi, p)
                                        : launch_poly_gemm_act_f32(cfg, pair, epi, p);

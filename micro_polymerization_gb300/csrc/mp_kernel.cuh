@@ -1146,9 +1146,9 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
 template <int CG, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
     constexpr bool kPair = CG == 2;
-    // EPI bit 3: the lean instantiation for plans of one-CTA tiles with no
-    // split and no swapped region, 16-byte aligned D and beta = 0 (the
-    // launch picks it); the paths it cannot take are folded away.
+    // EPI bit 3: the lean instantiation for plans with no split and no
+    // swapped region, 16-byte aligned D and beta = 0 (the launch picks it);
+    // the paths it cannot take are folded away.
     constexpr bool kLean = (EPI & 8) != 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
