@@ -169,7 +169,7 @@ struct DeviceState {
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
 bool set_kernel_smem() {
-    return set_poly_gemm_smem<0>() && set_poly_gemm_smem<8>() && set_poly_gemm_smem_act_f32() &&
+    return set_poly_gemm_smem<0>() && set_poly_gemm_smem<8>() && set_poly_gemm_smem<16>() && set_poly_gemm_smem_act_f32() &&
            set_poly_gemm_smem_bf16() && b2b::set_smem() &&
            conv::set_smem() && grp::set_smem();
 }
@@ -748,13 +748,15 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // bit 2 (the occupancy queries above hold for all of them: the same
     // threads, shared memory and launch bounds).
     const int epi = p.act | (p.out_bf16 ? 4 : 0);
-    // The lean instantiation (EPI bit 3) when the plan needs none of the
-    // paths it leaves out: no split, no swapped region, 16-byte aligned D,
-    // beta = 0, the plain epilogue (one-CTA tiles or CTA pairs).
-    bool lean = epi == 0 && !csplit && p.tma_d && p.beta == 0.0f;
-    for (int i = 0; i < plan.num_regions && lean; i++)
-        lean = plan.region[i].splits == 1 && !plan.region[i].swap;
+    // The lean instantiations of the plain epilogue when the plan needs none
+    // of the paths they leave out: EPI 16 for no split and no swapped
+    // region, EPI 8 for that with 16-byte aligned D and beta = 0 as well.
+    bool plain = epi == 0 && !csplit;
+    for (int i = 0; i < plan.num_regions && plain; i++)
+        plain = plan.region[i].splits == 1 && !plan.region[i].swap;
+    const bool lean = plain && p.tma_d && p.beta == 0.0f;
     const cudaError_t e = lean ? launch_poly_gemm<8>(cfg, pair, p)
+                          : plain ? launch_poly_gemm<16>(cfg, pair, p)
                           : epi == 0 ? launch_poly_gemm<0>(cfg, pair, p)
                           : p.out_bf16 ? launch_poly_gemm_bf16(cfg, pair, epi, p)
                                        : launch_poly_gemm_act_f32(cfg, pair, epi, p);

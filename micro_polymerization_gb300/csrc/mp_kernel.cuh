@@ -791,7 +791,7 @@ __device__ __forceinline__ void prefetch_c_tile_row(const Params& p, const Work&
 template <int EPI>
 __device__ __forceinline__ void emit16(const Params& p, const Work& w, int q, int lane, int c, const float* v,
                                        float4* stage) {
-    if (w.swap) {
+    if ((EPI & 24) == 0 && w.swap) {  // the lean instantiations have no swapped tiles
         store16<EPI>(p, w, q * 32 + lane, c, v);
         return;
     }
@@ -1146,10 +1146,11 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* ptr) {
 template <int CG, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant__ Params p) {
     constexpr bool kPair = CG == 2;
-    // EPI bit 3: the lean instantiation for plans with no split and no
-    // swapped region, 16-byte aligned D and beta = 0 (the launch picks it);
-    // the paths it cannot take are folded away.
+    // Lean instantiations (the launch picks them; the paths they cannot
+    // take are folded away).  EPI bit 4: plans with no split and no swapped
+    // region.  Bit 3: the same with 16-byte aligned D and beta = 0 as well.
     constexpr bool kLean = (EPI & 8) != 0;
+    constexpr bool kPlain = (EPI & 24) != 0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1268,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const Work w = decode(p, regs_s, u, rank);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
             const int blk0 = w.n_t0 >> 6;
-            const int nblk = (!kLean && w.swap) ? 2 : (w.bn >> 6);
+            const int nblk = (!kPlain && w.swap) ? 2 : (w.bn >> 6);
             const bool whole_b = blk0 + nblk <= p.nb_full;
             for (int kb = w.kb0; kb < w.kb1; kb += kg, ++g) {
                 if ((g & 1u) != pid) continue;
@@ -1288,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     for (int j = 0; j < nsub; j++) {
                     const uint32_t xs = ring0 + stage * stage_bytes + j * sub_bytes, ys = xs + kXBytes;
                     const int kc = (kb + j) * 64;
-                    if (kLean || !w.swap) {
+                    if (kPlain || !w.swap) {
                         if constexpr (kPair) {
                             // This CTA's 128 rows of A and its half of B's
                             // 64-column blocks (rank r: blocks [r h, r h + h)).
@@ -1389,12 +1390,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
             const uint32_t idesc =
-                (!kLean && w.swap) ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
+                (!kPlain && w.swap) ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
             // Descriptors of stage 0, K step 0.  Every later stage and K step
             // only moves the start address (bits 0..13, in 16-byte units;
             // shared addresses stay below 2^18, so the sums never carry out of
             // the field): one 64-bit add per operand.
-            const bool swp = !kLean && w.swap;
+            const bool swp = !kPlain && w.swap;
             const uint64_t dx0 = swp ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
             // Pairs of 192-wide tiles hold B with the 64-byte swizzle.
             const bool b64 = kPair && w.bn == 192;
@@ -1468,8 +1469,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (!kLean && p.beta != 0.0f && w.splits == 1) {
-                if (w.swap)
+            if (!kLean && p.beta != 0.0f && (kPlain || w.splits == 1)) {
+                if (!kPlain && w.swap)
                     prefetch_c_swapped(p, w, q, lane);
                 else if (p.tma_d)
                     prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
@@ -1548,7 +1549,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (kLean || (!epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap)) {
+            } else if (kLean || (!epi_bf16<EPI>() && (kPlain || (w.splits == 1 && !w.swap)) && p.tma_d)) {
                 const bool with_c = !kLean && p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
@@ -1573,7 +1574,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (w.splits == 1 && !w.swap && p.beta != 0.0f) {
+            } else if ((kPlain || (w.splits == 1 && !w.swap)) && p.beta != 0.0f) {
                 // Unaligned D with beta * C (measured: faster than the
                 // transposed stores below once C has to be read).
                 // The slab area may still be read by an earlier tile's bulk stores.
@@ -1593,7 +1594,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (w.splits == 1) {
+            } else if (kPlain || w.splits == 1) {
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
                     if (has_k) {
@@ -1772,7 +1773,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
 
     grid_dep_wait();
     __syncthreads();
-    if constexpr (!kPair && !kLean) {
+    if constexpr (!kPair && !kPlain) {
         if (p.csplit) {
             // Every partial of this CTA's tile is now in its cluster's shared
             // memory; sum this CTA's slice; leave only when no CTA of the
