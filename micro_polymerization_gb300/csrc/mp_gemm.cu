@@ -169,7 +169,8 @@ struct DeviceState {
 
 // The dynamic shared memory of every instantiation of the persistent kernel.
 bool set_kernel_smem() {
-    return set_poly_gemm_smem<0>() && set_poly_gemm_smem<8>() && set_poly_gemm_smem<16>() && set_poly_gemm_smem_act_f32() &&
+    return set_poly_gemm_smem<0>() && set_poly_gemm_smem<8>() && set_poly_gemm_smem<16>() && set_poly_gemm_smem<32>() &&
+           set_poly_gemm_smem_act_f32() &&
            set_poly_gemm_smem_bf16() && b2b::set_smem() &&
            conv::set_smem() && grp::set_smem();
 }
@@ -755,8 +756,13 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     for (int i = 0; i < plan.num_regions && plain; i++)
         plain = plan.region[i].splits == 1 && !plan.region[i].swap;
     const bool lean = plain && p.tma_d && p.beta == 0.0f;
+    // EPI 32: every region split, none swapped.
+    bool split_only = epi == 0 && !pair && plan.num_regions > 0;
+    for (int i = 0; i < plan.num_regions && split_only; i++)
+        split_only = plan.region[i].splits > 1 && !plan.region[i].swap;
     const cudaError_t e = lean ? launch_poly_gemm<8>(cfg, pair, p)
                           : plain ? launch_poly_gemm<16>(cfg, pair, p)
+                          : split_only ? launch_poly_gemm<32>(cfg, false, p)
                           : epi == 0 ? launch_poly_gemm<0>(cfg, pair, p)
                           : p.out_bf16 ? launch_poly_gemm_bf16(cfg, pair, epi, p)
                                        : launch_poly_gemm_act_f32(cfg, pair, epi, p);

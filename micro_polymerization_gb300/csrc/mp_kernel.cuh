@@ -1151,6 +1151,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
     // region.  Bit 3: the same with 16-byte aligned D and beta = 0 as well.
     constexpr bool kLean = (EPI & 8) != 0;
     constexpr bool kPlain = (EPI & 24) != 0;
+    // EPI bit 5: plans whose regions are all split and none swapped.
+    constexpr bool kSplitOnly = (EPI & 32) != 0;
+    constexpr bool kNoSwap = kPlain || kSplitOnly;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1269,7 +1272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             const Work w = decode(p, regs_s, u, rank);
             const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
             const int blk0 = w.n_t0 >> 6;
-            const int nblk = (!kPlain && w.swap) ? 2 : (w.bn >> 6);
+            const int nblk = (!kNoSwap && w.swap) ? 2 : (w.bn >> 6);
             const bool whole_b = blk0 + nblk <= p.nb_full;
             for (int kb = w.kb0; kb < w.kb1; kb += kg, ++g) {
                 if ((g & 1u) != pid) continue;
@@ -1289,7 +1292,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     for (int j = 0; j < nsub; j++) {
                     const uint32_t xs = ring0 + stage * stage_bytes + j * sub_bytes, ys = xs + kXBytes;
                     const int kc = (kb + j) * 64;
-                    if (kPlain || !w.swap) {
+                    if (kNoSwap || !w.swap) {
                         if constexpr (kPair) {
                             // This CTA's 128 rows of A and its half of B's
                             // 64-column blocks (rank r: blocks [r h, r h + h)).
@@ -1390,12 +1393,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * kAccStride);
             const uint32_t idesc =
-                (!kPlain && w.swap) ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
+                (!kNoSwap && w.swap) ? idesc_bf16(w.bn, true, false) : idesc_bf16(w.bn, false, true, kPair ? 256 : 128);
             // Descriptors of stage 0, K step 0.  Every later stage and K step
             // only moves the start address (bits 0..13, in 16-byte units;
             // shared addresses stay below 2^18, so the sums never carry out of
             // the field): one 64-bit add per operand.
-            const bool swp = !kPlain && w.swap;
+            const bool swp = !kNoSwap && w.swap;
             const uint64_t dx0 = swp ? desc_mnmajor(ring0, 0) : desc_kmajor(ring0, 0);
             // Pairs of 192-wide tiles hold B with the 64-byte swizzle.
             const bool b64 = kPair && w.bn == 192;
@@ -1469,7 +1472,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (!kLean && p.beta != 0.0f && (kPlain || w.splits == 1)) {
+            if (!kLean && !kSplitOnly && p.beta != 0.0f && (kPlain || w.splits == 1)) {
                 if (!kPlain && w.swap)
                     prefetch_c_swapped(p, w, q, lane);
                 else if (p.tma_d)
@@ -1493,7 +1496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
-            if (epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap) {
+            if (!kSplitOnly && epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap) {
                 // bf16 D: 64-column chunks, so that a lane's row of the slab is
                 // 128 bytes (the 128-byte swizzle); two TMEM loads per chunk.
                 const bool with_c = p.beta != 0.0f;
@@ -1549,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (kLean || (!epi_bf16<EPI>() && (kPlain || (w.splits == 1 && !w.swap)) && p.tma_d)) {
+            } else if (kLean || (!kSplitOnly && !epi_bf16<EPI>() && (kPlain || (w.splits == 1 && !w.swap)) && p.tma_d)) {
                 const bool with_c = !kLean && p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
@@ -1574,7 +1577,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if ((kPlain || (w.splits == 1 && !w.swap)) && p.beta != 0.0f) {
+            } else if (!kSplitOnly && (kPlain || (w.splits == 1 && !w.swap)) && p.beta != 0.0f) {
                 // Unaligned D with beta * C (measured: faster than the
                 // transposed stores below once C has to be read).
                 // The slab area may still be read by an earlier tile's bulk stores.
@@ -1594,7 +1597,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (kPlain || w.splits == 1) {
+            } else if (!kSplitOnly && (kPlain || w.splits == 1)) {
                 for (int c = 0; c < w.bn; c += 16) {
                     float v[16];
                     if (has_k) {
@@ -1619,8 +1622,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     // (the ring is idle: one task per CTA, all MMAs done); the
                     // cluster sums it at the end of the kernel.
                     float* ps = reinterpret_cast<float*>(gbase);
-                    const int P = (w.swap ? 128 : w.bn) + 4;
-                    if (!w.swap) {
+                    const int P = ((!kNoSwap && w.swap) ? 128 : w.bn) + 4;
+                    if (kNoSwap || !w.swap) {
                         float* prow = ps + (q * 32 + lane) * P;
                         for (int c = 0; c < w.bn; c += 32) {
                             float v[32];
@@ -1652,7 +1655,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) release_acc(acc);
-                } else if (w.swap) {
+                } else if (!kNoSwap && w.swap) {
                     // lane = buffer column: every store covers 128 contiguous bytes.
                     for (int c = 0; c < w.bn; c += 16) {
                         float v[16];
