@@ -749,23 +749,24 @@ mp_status device_run(mp_handle h, const mp_plan_info& plan, const GemmArgs& a) {
     // bit 2 (the occupancy queries above hold for all of them: the same
     // threads, shared memory and launch bounds).
     const int epi = p.act | (p.out_bf16 ? 4 : 0);
-    // The lean instantiations of the plain epilogue when the plan needs none
-    // of the paths they leave out: EPI 16 for no split and no swapped
-    // region, EPI 8 for that with 16-byte aligned D and beta = 0 as well.
-    bool plain = epi == 0 && !csplit;
-    for (int i = 0; i < plan.num_regions && plain; i++)
-        plain = plan.region[i].splits == 1 && !plan.region[i].swap;
-    const bool lean = plain && p.tma_d && p.beta == 0.0f;
-    // EPI 32: every region split, none swapped.
+    // Lean instantiations when the plan needs none of the paths they leave
+    // out.  EPI bit 3 (any epilogue): no split, no swapped region, 16-byte
+    // aligned D, beta = 0.  For the plain epilogue also bit 4 (no split, no
+    // swapped region) and bit 5 (every region split, none swapped).
+    bool nsns = !csplit;  // no split, no swapped region
+    for (int i = 0; i < plan.num_regions && nsns; i++)
+        nsns = plan.region[i].splits == 1 && !plan.region[i].swap;
+    const bool lean = nsns && p.tma_d && p.beta == 0.0f;
     bool split_only = epi == 0 && !pair && plan.num_regions > 0;
     for (int i = 0; i < plan.num_regions && split_only; i++)
         split_only = plan.region[i].splits > 1 && !plan.region[i].swap;
-    const cudaError_t e = lean ? launch_poly_gemm<8>(cfg, pair, p)
-                          : plain ? launch_poly_gemm<16>(cfg, pair, p)
-                          : split_only ? launch_poly_gemm<32>(cfg, false, p)
-                          : epi == 0 ? launch_poly_gemm<0>(cfg, pair, p)
-                          : p.out_bf16 ? launch_poly_gemm_bf16(cfg, pair, epi, p)
-                                       : launch_poly_gemm_act_f32(cfg, pair, epi, p);
+    const int epi_l = lean ? (epi | 8) : epi;
+    const cudaError_t e = epi == 0 ? (lean ? launch_poly_gemm<8>(cfg, pair, p)
+                                      : nsns ? launch_poly_gemm<16>(cfg, pair, p)
+                                      : split_only ? launch_poly_gemm<32>(cfg, false, p)
+                                                   : launch_poly_gemm<0>(cfg, pair, p))
+                          : p.out_bf16 ? launch_poly_gemm_bf16(cfg, pair, epi_l, p)
+                                       : launch_poly_gemm_act_f32(cfg, pair, epi_l, p);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }

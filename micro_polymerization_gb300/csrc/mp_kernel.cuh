@@ -866,7 +866,7 @@ __device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int l
     __syncwarp();
     const float a = p.alpha, bt = p.beta;
     uint8_t* row = slab + lane * 128;
-    if ((EPI & 8) != 0 || (bt == 0.0f && epi_act<EPI>() == 0)) {
+    if (epi_act<EPI>() == 0 && ((EPI & 8) != 0 || bt == 0.0f)) {
 #pragma unroll
         for (int j = 0; j < 8; j++)
             *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
@@ -880,7 +880,8 @@ __device__ __forceinline__ void emit32_tma(const Params& p, const Work& w, int l
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 o[e] = a * v[4 * j + e];
-                if (EPI == 0 || bt != 0.0f) o[e] = fmaf(bt, c[4 * j + e], o[e]);  // EPI 0: bt != 0 here
+                if ((EPI & 8) == 0 && (EPI == 0 || bt != 0.0f))  // EPI 0 (not lean): bt != 0 here
+                    o[e] = fmaf(bt, c[4 * j + e], o[e]);
                 o[e] = act_fn<EPI>(o[e]);
             }
             *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
@@ -1496,10 +1497,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
             tc_fence_after();
             const uint32_t t = tmem + (uint32_t)(acc * kAccStride) + ((uint32_t)(q * 32) << 16);
             const bool has_k = w.kb1 > w.kb0;
-            if (!kSplitOnly && epi_bf16<EPI>() && w.splits == 1 && p.tma_d && !w.swap) {
+            if (!kSplitOnly && epi_bf16<EPI>() && (kLean || (w.splits == 1 && p.tma_d && !w.swap))) {
                 // bf16 D: 64-column chunks, so that a lane's row of the slab is
                 // 128 bytes (the 128-byte swizzle); two TMEM loads per chunk.
-                const bool with_c = p.beta != 0.0f;
+                const bool with_c = !kLean && p.beta != 0.0f;
                 const float a = p.alpha, bt = p.beta;
                 for (int c = 0; c < w.bn; c += 64) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;
@@ -1552,7 +1553,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(acc);
-            } else if (kLean || (!kSplitOnly && !epi_bf16<EPI>() && (kPlain || (w.splits == 1 && !w.swap)) && p.tma_d)) {
+            } else if ((kLean && !epi_bf16<EPI>()) ||
+                       (!kSplitOnly && !epi_bf16<EPI>() && (kPlain || (w.splits == 1 && !w.swap)) && p.tma_d)) {
                 const bool with_c = !kLean && p.beta != 0.0f;
                 for (int c = 0; c < w.bn; c += 32) {
                     const int m0 = w.m_t0 + q * 32, n0 = w.n_t0 + c;

@@ -572,7 +572,8 @@ def test_explicit_plans_and_ablation_models_match_oracle(M, N, K):
     assert e.value.status == mp.MP_ERR_PLAN
 
 
-@pytest.mark.parametrize("M,N,K,beta", [(300, 520, 700, 0.5), (300, 517, 450, 0.5), (130, 517, 200, 0.0)])
+@pytest.mark.parametrize("M,N,K,beta", [(300, 520, 700, 0.5), (300, 517, 450, 0.5), (130, 517, 200, 0.0),
+                                        (300, 520, 700, 0.0)])
 def test_epilogue_variants_every_kernel(M, N, K, beta):
     """mp_gemm_ex: ReLU / GELU on alpha*A*B + beta*C and fp32 / bf16 D, for
     every micro-kernel with and without split-K, on aligned and odd-pitch D:
