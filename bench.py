@@ -36,11 +36,11 @@ METRIC = "dynamic-shape GEMM TFLOPS (device-timed, incl. planning) and % of per-
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic of the persistent kernel from one ncu capture of a small case
-# (profiles/k_poly_gemm_traffic_dynamic_sequence.md), valid only for the
+# (profiles/k_poly_gemm_launches_dynamic_sequence.md), valid only for the
 # kernel source it was taken on: dram__bytes_read.sum over the algorithmic
 # operand bytes (2MK + 2KN), and dram__bytes_write.sum over the algorithmic
 # output bytes (4MN), summed over the captured launches.
-TRAFFIC_RECORD = {"kernel_sha1": "97c1a37a68be2b093a7093678d8385222439dcae", "read_per_alg_read": 1.0049,
+TRAFFIC_RECORD = {"kernel_sha1": "50f020f607d8c6e4a1e361d82d2b8a4101395891", "read_per_alg_read": 1.0056,
                   "write_per_alg_write": 0.0}
 
 

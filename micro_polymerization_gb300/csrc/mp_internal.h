@@ -16,6 +16,9 @@ namespace mp {
 constexpr int kUmmaM = 128;
 constexpr int kUk = 64;
 constexpr int kMaxBn = 256;
+// K steps of A and B a one-CTA launch prefetches into L2 before waiting for
+// the previous kernel on the stream (plans that qualify: mp_gemm.cu).
+constexpr int kL2PrefetchSteps = 3;
 // Warps per task in the wave model of the GB300 kernel set (one CTA per SM,
 // so warps_per_wave = SMs * kModelWarpsPerTask gives one task slot per SM).
 constexpr int kModelWarpsPerTask = 6;

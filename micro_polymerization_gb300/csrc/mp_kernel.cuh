@@ -132,6 +132,10 @@ struct alignas(128) Params {
     // (rank r takes tile row 2 t + r) that share their B tile, each CTA
     // multicasting half of B's 64-column blocks into both shared memories.
     int pair;
+    // One-CTA launches: the first epilogue warp prefetches into L2 the first
+    // l2_pf K steps of A and B of its CTA's first unit before waiting for the
+    // previous kernel (0: no prefetch).
+    int l2_pf;
     unsigned long long wait_limit_ns;
     Region reg[MP_MAX_REGIONS];
     float* ws;
@@ -361,6 +365,22 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// L2 prefetch of one tensor box (the coordinates a load of the same box
+// would take); nothing reaches shared memory and nothing is waited for.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
 }
 
 // TMEM allocation.  CG = 1: one warp of the CTA; CG = 2: one warp of each
@@ -1454,6 +1474,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         }
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        // While the previous kernel may still run, warm L2 with the leading K
+        // steps of this CTA's first unit (one K step per lane, the boxes the
+        // producers will load).  A prefetch hands no data to the SM, so it
+        // may precede the dependency wait; the producers' own copies follow it.
+        if constexpr (!kPair) {
+            if (warp == 2 && p.l2_pf > 0 && u0 < p.total_units) {
+                const Work w = decode(p, regs_s, u0, 0);
+                if (kNoSwap || !w.swap) {
+                    const int nk = min(p.l2_pf, w.kb1 - w.kb0);
+                    const int ab = w.b * p.a_bstep, bb = w.b * p.b_bstep;
+                    const int blk0 = w.n_t0 >> 6, nblk = w.bn >> 6;
+                    const bool whole_b = blk0 + nblk <= p.nb_full;
+                    for (int j = lane; j < nk; j += 32) {
+                        const int kc = (w.kb0 + j) * 64;
+                        tma_prefetch_l2_3d(&p.tmA, kc, w.m_t0, ab);
+                        if (whole_b)
+                            tma_prefetch_l2_4d(&p.tmB4[nblk - 1], 0, kc, blk0, bb);
+                        else
+                            for (int c = 0; c < nblk; c++) tma_prefetch_l2_3d(&p.tmB, w.n_t0 + 64 * c, kc, bb);
+                    }
+                }
+            }
+        }
         grid_dep_wait();
         // The accumulator buffer goes back to the MMA issuer: the leader's
         // barrier, from both CTAs of a pair.
