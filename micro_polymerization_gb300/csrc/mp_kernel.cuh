@@ -1497,6 +1497,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                 }
             }
         }
+        // The same for the C block of that unit's epilogue, when beta*C is
+        // read (one-CTA plans; later units ask for theirs after the wait).
+        bool c_early = false;
+        if constexpr (!kLean && !kSplitOnly && !kPair) {
+            if (p.beta != 0.0f && u0 < p.total_units) {
+                const Work w = decode(p, regs_s, u0, 0);
+                if (kPlain || w.splits == 1) {
+                    const int q = warp & 3;
+                    if (!kPlain && w.swap)
+                        prefetch_c_swapped(p, w, q, lane);
+                    else if (p.tma_d)
+                        prefetch_c_row(p, w, w.m_t0 + q * 32 + lane);
+                    else
+                        prefetch_c_tile_row(p, w, w.m_t0 + q * 32 + lane);
+                    c_early = true;
+                }
+            }
+        }
         grid_dep_wait();
         // The accumulator buffer goes back to the MMA issuer: the leader's
         // barrier, from both CTAs of a pair.
@@ -1516,7 +1534,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
         uint32_t red_ph = 0;  // phase of red_bar
         for (int u = u0; u < p.total_units; u += ustep) {
             const Work w = decode(p, regs_s, u, rank);
-            if (!kLean && !kSplitOnly && p.beta != 0.0f && (kPlain || w.splits == 1)) {
+            if (!kLean && !kSplitOnly && p.beta != 0.0f && (kPlain || w.splits == 1) && !(c_early && u == u0)) {
                 if (!kPlain && w.swap)
                     prefetch_c_swapped(p, w, q, lane);
                 else if (p.tma_d)
