@@ -501,9 +501,11 @@ mp_status mp_plan_b2b(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0
  * Which form mp_gemm_b2b runs.  MP_B2B_FUSED: the fused kernel (D0 stays on
  * chip; N0 <= 256).  MP_B2B_TWO_LAUNCH: mp_gemm_ex writes D0 =
  * act0(alpha0*A0*W0 + beta0*C0) in bf16 (the same rounding as on chip) to
- * the end of the handle's staging area, then mp_gemm runs the second GEMM.  MP_B2B_AUTO (the default) keeps the fused kernel unless the
- * two forms' cost models predict the two launches more than 10% faster, and
- * runs N0 > 256 as two launches (mp_plan_b2b reports the choice).
+ * the end of the handle's staging area, then mp_gemm runs the second GEMM.
+ * MP_B2B_AUTO (the default) keeps the fused kernel unless the two forms'
+ * cost models predict the two launches faster, by more than 5% when the
+ * handle plans with a measured table (10% with the analytic model), and runs
+ * N0 > 256 as two launches (mp_plan_b2b reports the choice).
  * Errors: MP_ERR_INVALID_ARG (unknown mode).
  */
 #define MP_B2B_AUTO 0

@@ -78,6 +78,7 @@ bool load_calibration(mp_handle h, const char* path) {
                 d.fixed_us = fixed;
                 d.per_step_us = step;
                 if (got == 7 && tail >= 0) d.tail_us = tail;
+                h->calibrated = true;
             }
         }
     }
@@ -221,14 +222,27 @@ mp_status check_conv(const mp::ConvArgs& a) {
     return MP_OK;
 }
 
-// The fused plan and the form mp_gemm_b2b runs.  The two-launch form costs
-// the GEMM planner's estimates of both GEMMs plus 7.7 us, the fused kernel
-// its own estimate plus 2.0 us: fixed costs the two models leave out (the
-// launches, fill and drain), fitted on GB300 to the measured workloads of
-// fused pairs (64 problems each) in both forms.  The fused kernel is kept
-// unless two launches are predicted faster by more than 10% (the models'
-// error on these workloads), and N0 > 256 (a D0 row too wide for one
-// accumulator) always runs as two launches.
+// The fused plan and the form mp_gemm_b2b runs.  The fused kernel costs its
+// own estimate plus 2.0 us (launch, fill and drain, which its model leaves
+// out).  The two-launch form costs the GEMM planner's estimates of both GEMMs
+// plus what they leave out, which depends on the GEMM model:
+//   - measured table (the default): less 1.5 us (the second launch's set-up
+//     overlaps the first), plus D0's write and read (4 M N0 bytes) at
+//     1.87 TB/s, which a single GEMM's estimate does not see.  Fitted on GB300
+//     to every problem of the two fused-pair workloads (128 problems), each
+//     timed in both forms on cold operands: rms error of the two-launch
+//     estimate 0.46 us, of the fused one 0.91 us.  Fused unless two launches
+//     are predicted faster by more than 5%.
+//   - analytic model (no launch costs in the GEMM estimates): plus 7.7 us,
+//     fitted to the same two workloads' step times; fused unless two launches
+//     are predicted faster by more than 10%.
+// N0 > 256 (a D0 row too wide for one accumulator) always runs as two
+// launches.
+constexpr double kB2BFusedFixedUs = 2.0;
+constexpr double kB2BTwoLaunchFixedUs[2] = {7.7, -1.5};     // analytic, measured
+constexpr double kB2BD0RoundTripGBs = 1870.0;               // measured table only
+constexpr double kB2BMargin[2] = {1.10, 1.05};
+
 mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t K0, mp_b2b_plan* out) {
     mp_status st = mp::plan_b2b(h->hw, M, N0, N1, K0, out);
     const bool wide = st == MP_ERR_UNSUPPORTED && N0 > 256;
@@ -240,7 +254,9 @@ mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t 
     }
     mp_plan_info p0, p1;
     const int64_t k0 = N0 > 0 ? K0 : 0;
-    double two = 7.7;
+    const int cal = h->calibrated ? 1 : 0;
+    double two = kB2BTwoLaunchFixedUs[cal];
+    if (cal) two += 4.0 * (double)M * (double)N0 / (kB2BD0RoundTripGBs * 1e3);
     if (N0 > 0) {
         if ((st = mp::plan_shape(h, 1, M, N0, k0, &p0)) != MP_OK) return st;
         two += p0.cost_us;
@@ -253,7 +269,7 @@ mp_status plan_b2b_mode(mp_handle h, int64_t M, int64_t N0, int64_t N1, int64_t 
     else if (h->b2b_mode != MP_B2B_AUTO)
         out->mode = h->b2b_mode;
     else
-        out->mode = (out->cost_us + 2.0 <= 1.1 * two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
+        out->mode = (out->cost_us + kB2BFusedFixedUs <= kB2BMargin[cal] * two) ? MP_B2B_FUSED : MP_B2B_TWO_LAUNCH;
     return MP_OK;
 }
 
@@ -571,6 +587,7 @@ mp_status mp_set_kernel_model(mp_handle h, int32_t k, double fixed_us, double pe
     h->kernels[k].fixed_us = fixed_us;
     h->kernels[k].per_step_us = per_step_us;
     h->kernels[k].tail_us = tail_us;
+    h->calibrated = true;
     mp::clear_plan_cache(h);
     return MP_OK;
 }

@@ -402,6 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_b2b_gemm(const __grid_constant_
         __syncwarp();
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        // While the previous kernel may still run, warm L2 with the first
+        // GEMM's leading K steps of this CTA's first unit (one K step per
+        // lane: the A0 box and the W0 boxes that start inside N0).  A
+        // prefetch hands no data to the SM, so it may precede the wait.
+        if (warp == 2 && p.l2_pf > 0 && nk0 > 0 && (int)blockIdx.x < p.units) {
+            const int m0 = ((int)blockIdx.x / groups) * 128;
+            const int nk = min(p.l2_pf, nk0);
+            for (int j = lane; j < nk; j += 32) {
+                tma_prefetch_l2_3d(&p.tmA0, j * 64, m0, 0);
+                for (int b = 0; b < nk1 && 64 * b < p.N0; b++) tma_prefetch_l2_3d(&p.tmW0, 64 * b, j * 64, 0);
+            }
+        }
         grid_dep_wait();
         const int q = warp & 3;  // TMEM lane quarter = rows 32q..32q+31 of the tile
         uint8_t* slab = gbase + (epi0 - base) + q * kEpiSlabBytes;

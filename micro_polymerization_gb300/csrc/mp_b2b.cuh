@@ -53,6 +53,9 @@ struct alignas(128) Params {
     int* err;            // the handle's status word
     unsigned long long wait_limit_ns;
     int inject_timeout;  // test hook: producer warp 0 withholds its first stage
+    // K steps of A0 and W0 the first epilogue warp prefetches into L2 for its
+    // CTA's first unit before waiting for the previous kernel (0: none).
+    int l2_pf;
 };
 
 // Dynamic shared memory of a launch: operand ring, D0 operand (128 rows of

@@ -295,6 +295,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_conv_igemm(const __grid_constan
         __syncwarp();
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        // While the previous kernel may still run, warm L2 with the leading K
+        // steps of this CTA's first unit (one K step per lane): the X box and
+        // the filter boxes its producers will load.  A prefetch hands no data
+        // to the SM, so it may precede the dependency wait.  Its coordinates
+        // are clamped into X, and filter boxes past K are left out: every
+        // prefetch starts inside its tensor.
+        if (warp == 2 && p.l2_pf > 0 && p.ksteps > 0 && (int)blockIdx.x < p.units) {
+            const Tile t = decode_tile(p, (int)blockIdx.x / p.splits);
+            int kb0, kb1;
+            split_range(p, (int)blockIdx.x % p.splits, kb0, kb1);
+            const int nk = min(p.l2_pf, kb1 - kb0);
+            for (int j = lane; j < nk; j += 32) {
+                const int kb = kb0 + j;
+                const int tap = kb / p.cblocks, cb = kb - tap * p.cblocks;
+                const int r = tap / p.S, s = tap - r * p.S;
+                const int qx = min(max(t.q0 + s - p.pad_w, 0), p.W - 1);
+                const int py = min(max(t.p0 + r - p.pad_h, 0), p.H - 1);
+                tma_prefetch_l2_4d(&p.tmX, cb * 64, qx, py, t.n0);
+                for (int b = 0; b < nbox && t.k0 + 64 * b < p.K; b++)
+                    tma_prefetch_l2_3d(&p.tmF, t.k0 + 64 * b, tap * p.C + cb * 64, 0);
+            }
+        }
         grid_dep_wait();
         const int q = warp & 3;
         uint8_t* slab = gbase + (epi0 - base) + q * kEpiSlabBytes;

@@ -80,6 +80,10 @@ struct mp_handle_s {
     int32_t cluster_split_max = 0;
     int32_t cluster_ctas[17] = {};
 
+    // true once a calibration table has set a micro-kernel's g_predict (the
+    // GEMM estimates then include each launch's fixed costs).
+    bool calibrated = false;
+
     // Split-K cost model (mp_set_split_model): index 0 through L2, index S
     // (2..8) on chip in clusters of S CTAs; index 1 is unused.
     double split_sync_us[mp::kClusterSplitMaxS + 1];

@@ -1491,8 +1491,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_poly_gemm(const __grid_constant
                         tma_prefetch_l2_3d(&p.tmA, kc, w.m_t0, ab);
                         if (whole_b)
                             tma_prefetch_l2_4d(&p.tmB4[nblk - 1], 0, kc, blk0, bb);
-                        else
-                            for (int c = 0; c < nblk; c++) tma_prefetch_l2_3d(&p.tmB, w.n_t0 + 64 * c, kc, bb);
+                        else  // the blocks that start inside N
+                            for (int c = 0; c < nblk && w.n_t0 + 64 * c < w.n_end; c++)
+                                tma_prefetch_l2_3d(&p.tmB, w.n_t0 + 64 * c, kc, bb);
                     }
                 }
             }

@@ -184,8 +184,19 @@ def test_b2b_argument_checks():
 def test_b2b_form_choice():
     """The fused kernel unless two launches are clearly faster; N0 > 256 as
     two launches; a forced mode wins (and a forced fused form refuses
-    N0 > 256)."""
-    h = _host()
+    N0 > 256).  With the measured table (the default) the choice follows
+    what GB300 measured on cold operands: 256 -> 64 -> 256 pairs ran faster
+    fused at every M (M = 1000: 7.5 against 8.9 us; M = 75264: 27.3 against
+    30.8 us), 768 -> 256 -> 768 pairs faster as two launches (M = 2136: 13.0
+    against 14.4 us)."""
+    cal = _host()
+    mp.mp_load_calibration(cal, os.path.join(ROOT, "micro_polymerization_gb300", "calib", "gb300.txt"))
+    for M in (1000, 100352):
+        assert mp.mp_plan_b2b(cal, M, 64, 256, 256).mode == mp.MP_B2B_FUSED
+    for M in (256, 2048):
+        assert mp.mp_plan_b2b(cal, M, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
+    cal.close()
+    h = _host()  # the analytic model
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_FUSED
     assert mp.mp_plan_b2b(h, 2048, 256, 768, 768).mode == mp.MP_B2B_FUSED
     assert mp.mp_plan_b2b(h, 2048, 384, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH

@@ -129,3 +129,53 @@ def test_in_place_c_is_the_previous_calls_output():
         mp.mp_gemm(h, A2, B2, D, D, 1.0, 0.5)
         torch.cuda.synchronize()
         assert_exact(D, want2, "in-place chain")
+
+
+def test_conv_input_is_the_previous_calls_output():
+    """mp_conv2d whose X (NHWC) the previous call wrote as a bf16 GEMM output."""
+    import oracle
+    h = handle()
+    N, H, W, C, K, R, S = 4, 20, 20, 64, 128, 3, 3
+    A1, B1 = ints(N * H * W, 200, 15), ints(200, C, 16)
+    F = ints(R * S * C, K, 17).reshape(R, S, C, K)
+    Xbuf = torch.empty(N * H * W, C, device=DEV, dtype=torch.bfloat16)
+    D = torch.empty(N, H, W, K, device=DEV)
+    want_x = ref_bf16(A1.cpu(), B1.cpu())
+    want = oracle.conv2d_nhwc(bits(want_x.reshape(N, H, W, C)), bits(F.cpu()), None, 1.0, 0.0, 1, 1)
+    for _ in range(3):
+        Xbuf.fill_(float("nan"))
+        D.fill_(float("nan"))
+        mp.mp_gemm_ex(h, A1, B1, None, Xbuf, 1.0, 0.0)
+        mp.mp_conv2d(h, Xbuf.view(N, H, W, C), F, None, D, 1.0, 0.0, 1, 1)
+        torch.cuda.synchronize()
+        assert mp.mp_check(h) == 0
+        assert_exact(D.reshape(-1, K), want.reshape(-1, K), "conv chain")
+
+
+def test_fused_pair_input_is_the_previous_calls_output():
+    """mp_gemm_b2b (fused form) whose A0 the previous call wrote as a bf16
+    GEMM output; entries of A0 in {-1, 0, 1} keep the on-chip bf16 D0 exact."""
+    import oracle
+    h = handle()
+    M, K0, N0, N1 = 1000, 192, 256, 768
+    A1 = ints(M, 8, 18)
+    B1 = torch.zeros(8, K0, dtype=torch.bfloat16)
+    B1[0] = ints(1, K0, 19).cpu()[0]
+    B1 = B1.to(DEV)
+    W0, W1 = ints(K0, N0, 20), ints(N0, N1, 21)
+    A0 = torch.empty(M, K0, device=DEV, dtype=torch.bfloat16)
+    D1 = torch.empty(M, N1, device=DEV)
+    want_a0 = ref_bf16(A1.cpu(), B1.cpu())
+    want, _ = oracle.b2b(bits(want_a0), bits(W0.cpu()), None, bits(W1.cpu()), None, 1.0, 0.0, 1.0, 0.0, 1)
+    mp.mp_set_b2b_mode(h, mp.MP_B2B_FUSED)
+    try:
+        for _ in range(3):
+            A0.fill_(float("nan"))
+            D1.fill_(float("nan"))
+            mp.mp_gemm_ex(h, A1, B1, None, A0, 1.0, 0.0)
+            mp.mp_gemm_b2b(h, A0, W0, None, W1, None, D1, 1.0, 0.0, 1.0, 0.0, 1)
+            torch.cuda.synchronize()
+            assert mp.mp_check(h) == 0
+            assert_exact(D1, want, "fused pair chain")
+    finally:
+        mp.mp_set_b2b_mode(h, mp.MP_B2B_AUTO)
