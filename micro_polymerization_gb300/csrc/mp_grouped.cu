@@ -229,6 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_grouped(const __grid_const
         __syncwarp();
     } else {
         // ------------------------------ epilogue (128 threads) ----------------
+        // While the previous kernel may still run, warm L2 with the leading K
+        // steps of this CTA's first tile (one K step per lane: the A box and
+        // the B boxes that start inside N), unless that problem reads C.  A
+        // prefetch hands no data to the SM, so it may precede the wait.
+        if (warp == 2 && p.l2_pf > 0 && (int)blockIdx.x < p.units) {
+            const Tile t = decode(p, (int)blockIdx.x);
+            const Problem& q = p.prob[t.i];
+            if (q.beta == 0.0f) {
+                const int nk = min(p.l2_pf, t.nk);
+                for (int j = lane; j < nk; j += 32) {
+                    tma_prefetch_l2_3d(&q.tmA, j * 64, t.m0, 0);
+                    for (int b = 0; b < nbox && t.n0 + 64 * b < q.N; b++)
+                        tma_prefetch_l2_3d(&q.tmB, t.n0 + 64 * b, j * 64, 0);
+                }
+            }
+        }
         grid_dep_wait();
         const int wq = warp & 3;
         uint8_t* slab = gbase + (epi0 - base) + wq * kEpiSlabBytes;

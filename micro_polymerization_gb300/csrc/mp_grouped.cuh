@@ -49,6 +49,10 @@ struct alignas(128) Params {
     int* err;
     unsigned long long wait_limit_ns;
     int inject_timeout;  // test hook: producer warp 0 withholds its first stage
+    // K steps of A and B the first epilogue warp prefetches into L2 for its
+    // CTA's first tile (when that problem reads no C) before waiting for the
+    // previous kernel (0: none).
+    int l2_pf;
 };
 
 inline int smem_bytes(int num_stages, int stage_bytes) {
