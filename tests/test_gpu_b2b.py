@@ -163,14 +163,19 @@ def test_b2b_two_launch_form(shape):
 
 
 def test_b2b_auto_choice_runs_the_planned_form():
-    """AUTO takes the form mp_plan_b2b reports: the fused kernel, and two
-    launches for a D0 wider than one accumulator; both within the bound."""
+    """AUTO takes the form mp_plan_b2b reports: the fused kernel for a
+    256 -> 64 -> 256 pair, two launches for a 768 -> 256 -> 768 pair of
+    small M (measured faster that way) and for a D0 wider than one
+    accumulator; each within the bound."""
     mp.mp_set_b2b_mode(handle(), mp.MP_B2B_AUTO)
     wide = wl.B2B(300, 384, 200, 160, alpha0=1.0, beta0=0.5, alpha1=1.0, beta1=0.5, act0=2, seed=21)
     large = wl.B2B(128 * 400, 64, 256, 256, act0=1, seed=22)
+    adapter = wl.B2B(2048, 256, 768, 768, act0=1, seed=23)
     assert mp.mp_plan_b2b(handle(), wide.M, wide.N0, wide.N1, wide.K0).mode == mp.MP_B2B_TWO_LAUNCH
     assert mp.mp_plan_b2b(handle(), large.M, large.N0, large.N1, large.K0).mode == mp.MP_B2B_FUSED
+    assert mp.mp_plan_b2b(handle(), adapter.M, adapter.N0, adapter.N1, adapter.K0).mode == mp.MP_B2B_TWO_LAUNCH
     check(wide)
+    check(adapter)
     rows = np.arange(0, large.M, 331)
     got, ref, bound = run_b2b(large, rows=rows)
     ok, worst = oracle.within_b2b(got, ref, bound)
