@@ -299,11 +299,12 @@ def test_unaligned_rows_are_repacked(M, N, K):
     assert_parity(D, A, B, C, 1.5, 0.5, what=f"unaligned {(M, N, K)}")
 
 
+@pytest.mark.parametrize("beta", [0.5, 0.0])
 @pytest.mark.parametrize("splits", [1, 3])
-def test_unaligned_d_rows_every_kernel(splits):
+def test_unaligned_d_rows_every_kernel(splits, beta):
     """D whose row pitch is not 16-byte aligned (odd leading dimension): the
     row-wise epilogue and split-K reduction, for every micro-kernel, with
-    beta * C fused and canaries in the padding of each row."""
+    and without beta * C, and canaries in the padding of each row."""
     dev = torch.device("cuda", 0)
     h = handle()
     M, N, K, ldd = 300, 517, 200, 523
@@ -315,12 +316,13 @@ def test_unaligned_d_rows_every_kernel(splits):
             mp.mp_force_plan(h, k, splits)
             buf = torch.full((M * ldd,), -777.0, device=dev)
             D = buf.view(M, ldd)[:, :N]
-            mp.mp_gemm(h, A.to(dev), B.to(dev), C.to(dev), D, 1.5, 0.5)
+            mp.mp_gemm(h, A.to(dev), B.to(dev), C.to(dev), D, 1.5, beta)
             torch.cuda.synchronize()
             full = buf.view(M, ldd).cpu()
             assert torch.all(full[:, N:] == -777.0), f"kernel {k}: write past the row end"
-            assert_parity(full[:, :N].contiguous(), A, B, C, 1.5, 0.5,
-                          what=f"unaligned D kernel {k} ({desc.um}x{desc.un} swap={desc.swap}) splits={splits}")
+            assert_parity(full[:, :N].contiguous(), A, B, C, 1.5, beta,
+                          what=f"unaligned D kernel {k} ({desc.um}x{desc.un} swap={desc.swap}) "
+                               f"splits={splits} beta={beta}")
     finally:
         mp.mp_force_plan(h, -1, 0)
 
