@@ -195,6 +195,13 @@ def test_b2b_form_choice():
         assert mp.mp_plan_b2b(cal, M, 64, 256, 256).mode == mp.MP_B2B_FUSED
     for M in (256, 2048):
         assert mp.mp_plan_b2b(cal, M, 256, 768, 768).mode == mp.MP_B2B_TWO_LAUNCH
+    # Every problem of the two fused-pair workloads takes the form its
+    # workload ran faster in as a whole (0.750 ms all fused against 0.846 ms
+    # as two launches; 0.813 ms as two launches against 0.936 ms fused).
+    from micro_polymerization_gb300 import workloads as wl
+    for name, mode in (("b2b_1x1", mp.MP_B2B_FUSED), ("b2b_adapter", mp.MP_B2B_TWO_LAUNCH)):
+        for b in wl.B2B_WORKLOADS[name]():
+            assert mp.mp_plan_b2b(cal, b.M, b.N0, b.N1, b.K0).mode == mode, (name, b.M)
     cal.close()
     h = _host()  # the analytic model
     assert mp.mp_plan_b2b(h, 100352, 64, 256, 256).mode == mp.MP_B2B_FUSED
